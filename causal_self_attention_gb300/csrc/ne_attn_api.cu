@@ -1,0 +1,472 @@
+// ne_attn_api.cu -- the C ABI (include/ne_attn.h, include/ne_attn_debug.h):
+// host-side argument checks, TMA tensor-map encoding, the per-device RoPE
+// cos/sin table cache, the device status word, backward workspace handling,
+// and the launches.  No arithmetic of the method runs here except building the
+// RoPE table (on the host, in double).
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/ne_attn.h"
+#include "../../include/ne_attn_debug.h"
+#include "ne_common.cuh"
+
+namespace ne {
+cudaError_t launch_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                       const FwdParams& p, int n_qtiles, cudaStream_t stream);
+cudaError_t launch_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                       const CUtensorMap& tmDO, const BwdParams& p, int n_tiles,
+                       cudaStream_t stream);
+cudaError_t launch_debug_tile(const CUtensorMap& tm, int h, int row0, int rotate, int pos0,
+                              RopeTable rope, void* dst_raw, __nv_bfloat16* dst_rows,
+                              int* status, cudaStream_t stream);
+cudaError_t launch_debug_umma(int form, const __nv_bfloat16* a, const __nv_bfloat16* b, float* d,
+                              int* status, cudaStream_t stream);
+}  // namespace ne
+
+namespace {
+
+using ne::RopeTable;
+
+__device__ int g_device_status = 0;
+
+constexpr int kMaxDevices = 64;
+
+struct RopeEntry {
+  float base = 0.f;
+  int capacity = 0;
+  float2* dev = nullptr;
+};
+
+struct DeviceState {
+  bool ready = false;
+  int* status = nullptr;  // device address of g_device_status on this device
+  bool supported = false;
+  std::vector<RopeEntry> tables;
+  std::vector<float2*> retired;  // replaced tables, freed by ne_attn_release
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+int g_last_code = 0;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+ne_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return NE_OK;
+  if (e == cudaErrorMemoryAllocation) return NE_ERR_OOM;
+  return NE_ERR_CUDA;
+}
+
+// Per-device set-up (caller holds g_mutex).
+ne_status device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return NE_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return NE_ERR_UNSUPPORTED;
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return NE_ERR_CUDA;
+    st.supported = (major == 10 && minor == 3);
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return NE_ERR_CUDA;
+    st.status = static_cast<int*>(p);
+    st.ready = true;
+  }
+  if (!st.supported) return NE_ERR_UNSUPPORTED;
+  *out = &st;
+  return NE_OK;
+}
+
+ne_status get_encoder() {
+  if (g_encode) return NE_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return NE_ERR_CUDA;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return NE_OK;
+}
+
+// RoPE table for (base, D = 64) covering at least `positions` positions:
+// cs[p * 32 + i] = ((float)cos(p * theta_i), (float)sin(p * theta_i)),
+// theta_i = base^(-(2i)/64), all in double before the final fp32 rounding.
+ne_status rope_table(DeviceState& st, float base, int positions, RopeTable* out) {
+  for (auto& e : st.tables)
+    if (e.base == base && e.capacity >= positions) {
+      *out = RopeTable{e.dev, e.capacity};
+      return NE_OK;
+    }
+  int cap = 4096;
+  while (cap < positions) cap *= 2;
+  std::vector<float2> host(static_cast<size_t>(cap) * 32);
+  for (int i = 0; i < 32; ++i) {
+    const double theta = std::pow(static_cast<double>(base), -(2.0 * i) / 64.0);
+    for (int pos = 0; pos < cap; ++pos) {
+      const double a = static_cast<double>(pos) * theta;
+      host[static_cast<size_t>(pos) * 32 + i] =
+          make_float2(static_cast<float>(std::cos(a)), static_cast<float>(std::sin(a)));
+    }
+  }
+  float2* dev = nullptr;
+  cudaError_t e = cudaMalloc(&dev, host.size() * sizeof(float2));
+  if (e != cudaSuccess) return cuda_status(e);
+  e = cudaMemcpy(dev, host.data(), host.size() * sizeof(float2), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    cudaFree(dev);
+    return cuda_status(e);
+  }
+  for (auto& t : st.tables)
+    if (t.base == base) {
+      // Kernels already enqueued may still read the old table: retire it.
+      st.retired.push_back(t.dev);
+      t.dev = dev;
+      t.capacity = cap;
+      *out = RopeTable{dev, cap};
+      return NE_OK;
+    }
+  st.tables.push_back(RopeEntry{base, cap, dev});
+  *out = RopeTable{dev, cap};
+  return NE_OK;
+}
+
+// 3-d tensor map over [n_rows, H, 64] bf16, box 64 x 1 x 128, 128-byte swizzle.
+ne_status encode_rows(CUtensorMap* map, const void* base, int n_rows, int H) {
+  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(n_rows)};
+  cuuint64_t strides[2] = {64 * 2, static_cast<cuuint64_t>(H) * 64 * 2};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NE_OK : NE_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+struct Shape {
+  const int* cu = nullptr;
+  int nseq = 0, n_tot = 0, max_len = 0, H = 0, D = 0;
+  bool fixed = true;
+};
+
+ne_status check_shape(const Shape& s) {
+  if (s.D != 64) return NE_ERR_UNSUPPORTED;
+  if (s.H <= 0 || s.nseq <= 0 || s.max_len <= 0 || s.n_tot <= 0) return NE_ERR_INVALID_ARG;
+  if (!s.fixed && !s.cu) return NE_ERR_INVALID_ARG;
+  const long long rows = s.fixed ? static_cast<long long>(s.nseq) * s.max_len : s.n_tot;
+  if (rows > (1LL << 31) - 1 - 256) return NE_ERR_INVALID_ARG;
+  if (static_cast<long long>(s.nseq) * s.H > (1LL << 31) - 1) return NE_ERR_INVALID_ARG;
+  if ((s.max_len + 127) / 128 > 65535) return NE_ERR_INVALID_ARG;
+  if (static_cast<long long>(rows) * s.H * 64 > (1LL << 40)) return NE_ERR_INVALID_ARG;
+  return NE_OK;
+}
+
+ne::Problem make_problem(const Shape& s) {
+  ne::Problem pb;
+  pb.cu_seqlens = s.fixed ? nullptr : s.cu;
+  pb.nseq = s.nseq;
+  pb.max_len = s.max_len;
+  pb.H = s.H;
+  pb.n_tot = s.n_tot;
+  pb.lse_fixed = s.fixed ? 1 : 0;
+  return pb;
+}
+
+ne_status run_fwd(const Shape& s, const void* q, const void* k, const void* v, float rope_base,
+                  float scale, void* out, int out_f32, float* lse, void* stream) {
+  if (!q || !k || !v || !out || !lse) return NE_ERR_INVALID_ARG;
+  ne_status rc = check_shape(s);
+  if (rc != NE_OK) return rc;
+  if (!std::isfinite(scale) || !std::isfinite(rope_base) || rope_base <= 0.f)
+    return NE_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned4(lse))
+    return NE_ERR_MISALIGNED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState* st = nullptr;
+  if ((rc = device_state(&st)) != NE_OK) return rc;
+  if ((rc = get_encoder()) != NE_OK) return rc;
+  const int n_qtiles = (s.max_len + 127) / 128;
+  ne::FwdParams p;
+  p.pb = make_problem(s);
+  p.out = out;
+  p.out_f32 = out_f32;
+  p.lse = lse;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = st->status;
+  if ((rc = rope_table(*st, rope_base, n_qtiles * 128, &p.rope)) != NE_OK) return rc;
+  CUtensorMap tq, tk, tv;
+  if ((rc = encode_rows(&tq, q, s.n_tot, s.H)) != NE_OK) return rc;
+  if ((rc = encode_rows(&tk, k, s.n_tot, s.H)) != NE_OK) return rc;
+  if ((rc = encode_rows(&tv, v, s.n_tot, s.H)) != NE_OK) return rc;
+  return cuda_status(ne::launch_fwd(tq, tk, tv, p, n_qtiles, static_cast<cudaStream_t>(stream)));
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+ne_status run_bwd(const Shape& s, const void* q, const void* k, const void* v, const void* out,
+                  const void* dout, const float* lse, float rope_base, float scale, void* dq,
+                  void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return NE_ERR_INVALID_ARG;
+  ne_status rc = check_shape(s);
+  if (rc != NE_OK) return rc;
+  if (!std::isfinite(scale) || !std::isfinite(rope_base) || rope_base <= 0.f)
+    return NE_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
+      !aligned4(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return NE_ERR_MISALIGNED;
+  const size_t need = ne_attn_bwd_workspace_bytes(s.n_tot, s.H, s.D);
+  if (workspace && workspace_bytes < need) return NE_ERR_INVALID_ARG;
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return NE_ERR_MISALIGNED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState* st = nullptr;
+  if ((rc = device_state(&st)) != NE_OK) return rc;
+  if ((rc = get_encoder()) != NE_OK) return rc;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const int n_tiles = (s.max_len + 127) / 128;
+  ne::BwdParams p;
+  p.pb = make_problem(s);
+  p.out = static_cast<const __nv_bfloat16*>(out);
+  p.dout = static_cast<const __nv_bfloat16*>(dout);
+  p.lse = lse;
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = st->status;
+  if ((rc = rope_table(*st, rope_base, n_tiles * 128, &p.rope)) != NE_OK) return rc;
+  CUtensorMap tq, tk, tv, tdo;
+  if ((rc = encode_rows(&tq, q, s.n_tot, s.H)) != NE_OK) return rc;
+  if ((rc = encode_rows(&tk, k, s.n_tot, s.H)) != NE_OK) return rc;
+  if ((rc = encode_rows(&tv, v, s.n_tot, s.H)) != NE_OK) return rc;
+  if ((rc = encode_rows(&tdo, dout, s.n_tot, s.H)) != NE_OK) return rc;
+  void* ws = workspace;
+  bool owned = false;
+  if (!ws) {
+    cudaError_t e = cudaMallocAsync(&ws, need, cs);
+    if (e != cudaSuccess) return cuda_status(e);
+    owned = true;
+  }
+  const size_t acc_bytes = align256(static_cast<size_t>(s.n_tot) * s.H * 64 * sizeof(float));
+  p.dq_acc = static_cast<float*>(ws);
+  p.delta = reinterpret_cast<float*>(static_cast<char*>(ws) + acc_bytes);
+  cudaError_t e = ne::launch_bwd(tq, tk, tv, tdo, p, n_tiles, cs);
+  if (owned) {
+    cudaError_t e2 = cudaFreeAsync(ws, cs);
+    if (e == cudaSuccess) e = e2;
+  }
+  return cuda_status(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ne_status_string(ne_status s) {
+  switch (s) {
+    case NE_OK: return "NE_OK";
+    case NE_ERR_INVALID_ARG: return "NE_ERR_INVALID_ARG";
+    case NE_ERR_UNSUPPORTED: return "NE_ERR_UNSUPPORTED";
+    case NE_ERR_MISALIGNED: return "NE_ERR_MISALIGNED";
+    case NE_ERR_CUDA: return "NE_ERR_CUDA";
+    case NE_ERR_TIMEOUT: return "NE_ERR_TIMEOUT";
+    case NE_ERR_OOM: return "NE_ERR_OOM";
+    case NE_ERR_BAD_SEQLEN: return "NE_ERR_BAD_SEQLEN";
+    default: return "NE_ERR_UNKNOWN";
+  }
+}
+
+size_t ne_attn_bwd_workspace_bytes(int n_tot, int H, int D) {
+  if (n_tot <= 0 || H <= 0 || D != 64) return 0;
+  return align256(static_cast<size_t>(n_tot) * H * 64 * sizeof(float)) +
+         align256(static_cast<size_t>(n_tot) * H * sizeof(float));
+}
+
+ne_status ne_attn_fwd(const ne_bf16* q, const ne_bf16* k, const ne_bf16* v, int B, int H, int T,
+                      int D, float rope_base, float scale, ne_bf16* out, float* lse,
+                      void* stream) {
+  Shape s;
+  s.nseq = B;
+  s.max_len = T;
+  s.n_tot = (B > 0 && T > 0) ? B * T : 0;
+  s.H = H;
+  s.D = D;
+  if (B > 0 && T > 0 && static_cast<long long>(B) * T > (1LL << 31) - 1) return NE_ERR_INVALID_ARG;
+  return run_fwd(s, q, k, v, rope_base, scale, out, 0, lse, stream);
+}
+
+ne_status ne_attn_fwd_f32out(const ne_bf16* q, const ne_bf16* k, const ne_bf16* v, int B, int H,
+                             int T, int D, float rope_base, float scale, float* out, float* lse,
+                             void* stream) {
+  Shape s;
+  s.nseq = B;
+  s.max_len = T;
+  s.n_tot = (B > 0 && T > 0) ? B * T : 0;
+  s.H = H;
+  s.D = D;
+  if (B > 0 && T > 0 && static_cast<long long>(B) * T > (1LL << 31) - 1) return NE_ERR_INVALID_ARG;
+  return run_fwd(s, q, k, v, rope_base, scale, out, 1, lse, stream);
+}
+
+ne_status ne_attn_varlen_fwd(const ne_bf16* q, const ne_bf16* k, const ne_bf16* v,
+                             const int* cu_seqlens, int nseq, int n_tot, int max_seqlen, int H,
+                             int D, float rope_base, float scale, ne_bf16* out, float* lse,
+                             void* stream) {
+  Shape s;
+  s.cu = cu_seqlens;
+  s.fixed = false;
+  s.nseq = nseq;
+  s.n_tot = n_tot;
+  s.max_len = max_seqlen;
+  s.H = H;
+  s.D = D;
+  return run_fwd(s, q, k, v, rope_base, scale, out, 0, lse, stream);
+}
+
+ne_status ne_attn_varlen_fwd_f32out(const ne_bf16* q, const ne_bf16* k, const ne_bf16* v,
+                                    const int* cu_seqlens, int nseq, int n_tot, int max_seqlen,
+                                    int H, int D, float rope_base, float scale, float* out,
+                                    float* lse, void* stream) {
+  Shape s;
+  s.cu = cu_seqlens;
+  s.fixed = false;
+  s.nseq = nseq;
+  s.n_tot = n_tot;
+  s.max_len = max_seqlen;
+  s.H = H;
+  s.D = D;
+  return run_fwd(s, q, k, v, rope_base, scale, out, 1, lse, stream);
+}
+
+ne_status ne_attn_bwd(const ne_bf16* q, const ne_bf16* k, const ne_bf16* v, const ne_bf16* out,
+                      const ne_bf16* dout, const float* lse, int B, int H, int T, int D,
+                      float rope_base, float scale, ne_bf16* dq, ne_bf16* dk, ne_bf16* dv,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  Shape s;
+  s.nseq = B;
+  s.max_len = T;
+  s.n_tot = (B > 0 && T > 0) ? B * T : 0;
+  s.H = H;
+  s.D = D;
+  if (B > 0 && T > 0 && static_cast<long long>(B) * T > (1LL << 31) - 1) return NE_ERR_INVALID_ARG;
+  return run_bwd(s, q, k, v, out, dout, lse, rope_base, scale, dq, dk, dv, workspace,
+                 workspace_bytes, stream);
+}
+
+ne_status ne_attn_varlen_bwd(const ne_bf16* q, const ne_bf16* k, const ne_bf16* v,
+                             const ne_bf16* out, const ne_bf16* dout, const float* lse,
+                             const int* cu_seqlens, int nseq, int n_tot, int max_seqlen, int H,
+                             int D, float rope_base, float scale, ne_bf16* dq, ne_bf16* dk,
+                             ne_bf16* dv, void* workspace, size_t workspace_bytes, void* stream) {
+  Shape s;
+  s.cu = cu_seqlens;
+  s.fixed = false;
+  s.nseq = nseq;
+  s.n_tot = n_tot;
+  s.max_len = max_seqlen;
+  s.H = H;
+  s.D = D;
+  return run_bwd(s, q, k, v, out, dout, lse, rope_base, scale, dq, dk, dv, workspace,
+                 workspace_bytes, stream);
+}
+
+ne_status ne_attn_get_device_status(void* stream) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState* st = nullptr;
+  ne_status rc = device_state(&st);
+  if (rc != NE_OK) return rc;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return NE_ERR_CUDA;
+  int code = 0;
+  if (cudaMemcpyFromSymbol(&code, g_device_status, sizeof(int)) != cudaSuccess) return NE_ERR_CUDA;
+  const int zero = 0;
+  if (code != 0 && cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess)
+    return NE_ERR_CUDA;
+  g_last_code = code;
+  if (code == ne::NE_DEV_OK) return NE_OK;
+  if (code == ne::NE_DEV_BAD_SEQLEN) return NE_ERR_BAD_SEQLEN;
+  if (code >= ne::NE_DEV_TIMEOUT_BASE) return NE_ERR_TIMEOUT;
+  return NE_ERR_CUDA;
+}
+
+int ne_attn_last_device_code(void) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  return g_last_code;
+}
+
+void ne_attn_release(void) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int cur = 0;
+  cudaGetDevice(&cur);
+  for (int d = 0; d < kMaxDevices; ++d) {
+    DeviceState& st = g_dev[d];
+    if (st.tables.empty() && st.retired.empty()) continue;
+    cudaSetDevice(d);
+    for (auto& t : st.tables) cudaFree(t.dev);
+    for (auto* p : st.retired) cudaFree(p);
+    st.tables.clear();
+    st.retired.clear();
+  }
+  cudaSetDevice(cur);
+}
+
+// ------------------------------------------------------------ debug entries --
+
+ne_status ne_debug_tma_tile(const ne_bf16* src, int n_rows, int H, int h, int row0,
+                            void* dst_raw, void* stream) {
+  if (!src || !dst_raw || n_rows <= 0 || H <= 0 || h < 0 || h >= H) return NE_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(dst_raw)) return NE_ERR_MISALIGNED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState* st = nullptr;
+  ne_status rc = device_state(&st);
+  if (rc != NE_OK) return rc;
+  if ((rc = get_encoder()) != NE_OK) return rc;
+  CUtensorMap tm;
+  if ((rc = encode_rows(&tm, src, n_rows, H)) != NE_OK) return rc;
+  return cuda_status(ne::launch_debug_tile(tm, h, row0, 0, 0, RopeTable{nullptr, 0}, dst_raw,
+                                           nullptr, st->status,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+ne_status ne_debug_rope_tile(const ne_bf16* src, int n_rows, int H, int h, int row0, int pos0,
+                             float rope_base, ne_bf16* dst, void* stream) {
+  if (!src || !dst || n_rows <= 0 || H <= 0 || h < 0 || h >= H || pos0 < 0)
+    return NE_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(dst)) return NE_ERR_MISALIGNED;
+  if (!std::isfinite(rope_base) || rope_base <= 0.f) return NE_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState* st = nullptr;
+  ne_status rc = device_state(&st);
+  if (rc != NE_OK) return rc;
+  if ((rc = get_encoder()) != NE_OK) return rc;
+  RopeTable rt;
+  if ((rc = rope_table(*st, rope_base, pos0 + 128, &rt)) != NE_OK) return rc;
+  CUtensorMap tm;
+  if ((rc = encode_rows(&tm, src, n_rows, H)) != NE_OK) return rc;
+  return cuda_status(ne::launch_debug_tile(tm, h, row0, 1, pos0, rt, nullptr,
+                                           reinterpret_cast<__nv_bfloat16*>(dst), st->status,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+ne_status ne_debug_umma(int form, const ne_bf16* a, const ne_bf16* b, float* d, void* stream) {
+  if (form < 0 || form > 2 || !a || !b || !d) return NE_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(d)) return NE_ERR_MISALIGNED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState* st = nullptr;
+  ne_status rc = device_state(&st);
+  if (rc != NE_OK) return rc;
+  return cuda_status(ne::launch_debug_umma(form, reinterpret_cast<const __nv_bfloat16*>(a),
+                                           reinterpret_cast<const __nv_bfloat16*>(b), d,
+                                           st->status, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,508 @@
+// ne_attn_bwd.cu -- backward of causal self-attention with fused RoPE, sm_103a.
+//
+// Three kernels on one stream (gradients hand-derived, no autograd, as the
+// NanoEuler Show HN page, paragraph 2, describes for its engine):
+//   1. preprocess: D_m = dO_m . O_m (fp32, [H, N_tot]) and zero the fp32 dQ'
+//      accumulator;
+//   2. main: one CTA per (128-key tile j, head, sequence) walks the query
+//      tiles i >= j, recomputing P from the saved LSE:
+//        S^T  = K' Q'^T,  P^T = exp(scale S^T - LSE),  dP^T = V dO^T,
+//        dS^T = P^T o (dP^T - D),
+//        dV  += P^T dO,   dK' += dS^T Q',   dQ'_i = dS K'  (-> fp32 atomics),
+//      and at the end writes dV and dK = scale * R(n)^T dK' (bf16);
+//   3. postprocess: dQ = scale * R(m)^T dQ' (bf16).
+// q' = R(m) q and k' = R(n) k are rotated in shared memory right after their
+// TMA loads, as in the forward.
+//
+// Main-kernel warp roles (448 threads):
+//   warps 0-3   rotate: K_j once; every Q_i tile; stage LSE_i and D_i in smem
+//   warps 4-7   softmax: thread t owns key row t (TMEM lane t): P^T, dS^T rows
+//               to smem; epilogue of dK, dV
+//   warp 8      MMA: allocates TMEM; lane 0 issues the five MMAs per tile
+//   warp 9      TMA: lane 0 loads K_j, V_j once and Q_i, dO_i (2 stages)
+//   warps 10-13 dQ: thread owns query row; TMEM dQ' -> red.global.add.v4.f32
+// TMEM columns: S^T 0-127, dP^T 128-255, dV 256-319, dK' 320-383, dQ' 384-447.
+#include "ne_rope.cuh"
+#include "ne_sm100.cuh"
+
+namespace ne {
+
+namespace bwd {
+
+constexpr int kThreads = 448;
+constexpr int OFF_K = 0;
+constexpr int OFF_V = OFF_K + kTileBytes;
+constexpr int OFF_Q = OFF_V + kTileBytes;        // 2 stages
+constexpr int OFF_DO = OFF_Q + 2 * kTileBytes;   // 2 stages
+constexpr int OFF_PT = OFF_DO + 2 * kTileBytes;  // P^T: 2 blocks of 64 queries
+constexpr int OFF_DST = OFF_PT + 2 * kTileBytes; // dS^T: same layout
+constexpr int OFF_LSE = OFF_DST + 2 * kTileBytes;  // 2 stages x 128 fp32 (log2 units)
+constexpr int OFF_DEL = OFF_LSE + 2 * 128 * 4;     // 2 stages x 128 fp32
+constexpr int OFF_BAR = OFF_DEL + 2 * 128 * 4;
+constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
+
+enum Bar {
+  B_KV_FULL = 0,
+  B_K_ROT,
+  B_QDO_FULL,                     // 2
+  B_Q_ROT = B_QDO_FULL + 2,       // 2
+  B_QDO_EMPTY = B_Q_ROT + 2,      // 2
+  B_S_FULL = B_QDO_EMPTY + 2,
+  B_S_FREE,
+  B_DS_FULL,
+  B_PDS_FREE,
+  B_DQ_FULL,
+  B_DQ_FREE,
+  B_MMA_DONE,
+  B_COUNT
+};
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384;
+
+constexpr uint32_t kIdescNN = make_idesc_bf16(128, 128, false, false);  // S^T, dP^T
+constexpr uint32_t kIdescKM = make_idesc_bf16(128, 64, false, true);    // dV, dK
+constexpr uint32_t kIdescMM = make_idesc_bf16(128, 64, true, true);     // dQ
+
+}  // namespace bwd
+
+// ---------------------------------------------------------------------------
+// 1. preprocess: delta[h, row] = sum_d dO . O ; zero dq_acc.  8 threads per
+//    (row, head) pair, each on 8 of the 64 elements.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256)
+    ne_attn_bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ out,
+                                  const __nv_bfloat16* __restrict__ dout, float* __restrict__ delta,
+                                  float* __restrict__ dq_acc, long long n_pairs, int H,
+                                  int n_tot) {
+  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long pair = t >> 3;  // row * H + h
+  const int part = static_cast<int>(t & 7);
+  float acc = 0.f;
+  if (pair < n_pairs) {
+    const uint4 o = __ldg(reinterpret_cast<const uint4*>(out + pair * 64) + part);
+    const uint4 g = __ldg(reinterpret_cast<const uint4*>(dout + pair * 64) + part);
+    const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+    const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      acc = __fmaf_rn(bf16lo_to_f32(ow[w]), bf16lo_to_f32(gw[w]), acc);
+      acc = __fmaf_rn(bf16hi_to_f32(ow[w]), bf16hi_to_f32(gw[w]), acc);
+    }
+    float4* z = reinterpret_cast<float4*>(dq_acc + pair * 64) + part * 2;
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+  if (pair < n_pairs && part == 0) {
+    const long long row = pair / H;
+    const int h = static_cast<int>(pair - row * H);
+    delta[static_cast<long long>(h) * n_tot + row] = acc;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 2. main kernel
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(bwd::kThreads, 1)
+    ne_attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ,
+                       const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ CUtensorMap tmDO, const BwdParams p) {
+  using namespace bwd;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + 8 * B_COUNT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_BAR + 8 * B_COUNT + 4);
+
+  const int H = p.pb.H;
+  const int seq = blockIdx.x / H;
+  const int h = blockIdx.x % H;
+  const int kt = blockIdx.y;  // key tile; tile 0 has the most query tiles: launched first
+  int start, len;
+  if (!seq_bounds(p.pb, seq, start, len, nullptr)) return;
+  if (kt * kBN >= len) return;
+  const int n_qt = (len + kBM - 1) / kBM;
+  const int n_it = n_qt - kt;  // query tiles kt .. n_qt-1
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[B_KV_FULL], 1);
+    mbar_init(&bars[B_K_ROT], 128);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars[B_QDO_FULL + s], 1);
+      mbar_init(&bars[B_Q_ROT + s], 128);
+      mbar_init(&bars[B_QDO_EMPTY + s], 1);
+    }
+    mbar_init(&bars[B_S_FULL], 1);
+    mbar_init(&bars[B_S_FREE], 128);
+    mbar_init(&bars[B_DS_FULL], 128);
+    mbar_init(&bars[B_PDS_FREE], 1);
+    mbar_init(&bars[B_DQ_FULL], 1);
+    mbar_init(&bars[B_DQ_FREE], 128);
+    mbar_init(&bars[B_MMA_DONE], 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  uint8_t* sK = smem + OFF_K;
+  uint8_t* sV = smem + OFF_V;
+  uint8_t* sQ = smem + OFF_Q;
+  uint8_t* sDO = smem + OFF_DO;
+  uint8_t* sPT = smem + OFF_PT;
+  uint8_t* sDST = smem + OFF_DST;
+  float* sLSE = reinterpret_cast<float*>(smem + OFF_LSE);
+  float* sDEL = reinterpret_cast<float*>(smem + OFF_DEL);
+
+  if (warp == 9) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmDO);
+      mbar_arrive_expect_tx(&bars[B_KV_FULL], 2 * kTileBytes);
+      tma_load_3d(sK, &tmK, &bars[B_KV_FULL], 0, h, start + kt * kBN);
+      tma_load_3d(sV, &tmV, &bars[B_KV_FULL], 0, h, start + kt * kBN);
+      int last_issued[2] = {-1, -1};
+      for (int it = 0; it < n_it; ++it) {
+        const int s = it & 1;
+        if (it >= 2 &&
+            !mbar_wait(&bars[B_QDO_EMPTY + s], ((it - 2) >> 1) & 1, abort_flag, p.status, 31))
+          break;
+        const int qrow = start + (kt + it) * kBM;
+        mbar_arrive_expect_tx(&bars[B_QDO_FULL + s], 2 * kTileBytes);
+        tma_load_3d(sQ + s * kTileBytes, &tmQ, &bars[B_QDO_FULL + s], 0, h, qrow);
+        tma_load_3d(sDO + s * kTileBytes, &tmDO, &bars[B_QDO_FULL + s], 0, h, qrow);
+        last_issued[s] = it;
+      }
+      if (*abort_flag) {
+        mbar_wait(&bars[B_KV_FULL], 0, abort_flag, nullptr, 0);
+        for (int s = 0; s < 2; ++s)
+          if (last_issued[s] >= 0) {
+            const long long t0 = clock64();
+            while (!mbar_try_wait(&bars[B_QDO_FULL + s], (last_issued[s] >> 1) & 1) &&
+                   clock64() - t0 < NE_WAIT_LIMIT_CYCLES) {
+            }
+          }
+      }
+    }
+  } else if (warp == 8) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
+      const uint32_t aPT = smem_u32(sPT), aDST = smem_u32(sDST);
+      bool ok = mbar_wait(&bars[B_K_ROT], 0, abort_flag, p.status, 32);
+      // S^T = K' Q'^T and dP^T = V dO^T for query tile `it`.
+      auto issue_s_dp = [&](int it) -> bool {
+        const int s = it & 1;
+        if (!mbar_wait(&bars[B_Q_ROT + s], (it >> 1) & 1, abort_flag, p.status, 33)) return false;
+        if (it >= 1 && !mbar_wait(&bars[B_S_FREE], (it - 1) & 1, abort_flag, p.status, 34))
+          return false;
+        tc_fence_after();
+        const uint32_t aQ = smem_u32(sQ + s * kTileBytes), aDO = smem_u32(sDO + s * kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16_ss(tmem + kColS, make_sdesc_sw128(aK + kk * 32, 16, 1024),
+                       make_sdesc_sw128(aQ + kk * 32, 16, 1024), kIdescNN, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16_ss(tmem + kColDP, make_sdesc_sw128(aV + kk * 32, 16, 1024),
+                       make_sdesc_sw128(aDO + kk * 32, 16, 1024), kIdescNN, kk > 0 ? 1u : 0u);
+        umma_commit(&bars[B_S_FULL]);
+        return true;
+      };
+      if (ok) ok = issue_s_dp(0);
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int s = it & 1;
+        if (it + 1 < n_it && !issue_s_dp(it + 1)) { ok = false; break; }
+        if (!mbar_wait(&bars[B_DS_FULL], it & 1, abort_flag, p.status, 35)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t aQ = smem_u32(sQ + s * kTileBytes), aDO = smem_u32(sDO + s * kTileBytes);
+        // dV += P^T dO  (A: P^T K-major over queries; B: dO MN-major)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16_ss(tmem + kColDV,
+                       make_sdesc_sw128(aPT + (kk >> 2) * kTileBytes + (kk & 3) * 32, 16, 1024),
+                       make_sdesc_sw128(aDO + kk * 2048, kTileBytes, 1024), kIdescKM,
+                       (it > 0 || kk > 0) ? 1u : 0u);
+        // dK' += dS^T Q'
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16_ss(tmem + kColDK,
+                       make_sdesc_sw128(aDST + (kk >> 2) * kTileBytes + (kk & 3) * 32, 16, 1024),
+                       make_sdesc_sw128(aQ + kk * 2048, kTileBytes, 1024), kIdescKM,
+                       (it > 0 || kk > 0) ? 1u : 0u);
+        // dQ'_i = dS K'  (A: dS^T read MN-major, i.e. as dS; B: K' MN-major)
+        if (it >= 1 && !mbar_wait(&bars[B_DQ_FREE], (it - 1) & 1, abort_flag, p.status, 36)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16_ss(tmem + kColDQ, make_sdesc_sw128(aDST + kk * 2048, kTileBytes, 1024),
+                       make_sdesc_sw128(aK + kk * 2048, kTileBytes, 1024), kIdescMM,
+                       kk > 0 ? 1u : 0u);
+        umma_commit(&bars[B_DQ_FULL]);
+        umma_commit(&bars[B_PDS_FREE]);
+        umma_commit(&bars[B_QDO_EMPTY + s]);
+      }
+      umma_commit(&bars[B_MMA_DONE]);
+      const long long t0 = clock64();
+      while (!mbar_try_wait(&bars[B_MMA_DONE], 0) && clock64() - t0 < NE_WAIT_LIMIT_CYCLES) {
+      }
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------- RoPE + LSE/D staging
+    const int r = threadIdx.x;
+    if (mbar_wait(&bars[B_KV_FULL], 0, abort_flag, p.status, 37)) {
+      rope_rotate_row(sK, r, kt * kBN + r, p.rope);
+      fence_proxy_async_smem();
+      mbar_arrive(&bars[B_K_ROT]);
+      for (int it = 0; it < n_it; ++it) {
+        const int s = it & 1;
+        if (!mbar_wait(&bars[B_QDO_FULL + s], (it >> 1) & 1, abort_flag, p.status, 38)) break;
+        const int qpos = (kt + it) * kBM + r;
+        rope_rotate_row(sQ + s * kTileBytes, r, qpos, p.rope);
+        float l2 = INFINITY, dl = 0.f;  // query rows past the sequence get P = 0
+        if (qpos < len) {
+          l2 = __ldg(p.lse + lse_index(p.pb, h, seq, start, qpos)) * 1.4426950408889634f;
+          dl = __ldg(p.delta + static_cast<long long>(h) * p.pb.n_tot + start + qpos);
+        }
+        sLSE[s * 128 + r] = l2;
+        sDEL[s * 128 + r] = dl;
+        fence_proxy_async_smem();
+        mbar_arrive(&bars[B_Q_ROT + s]);
+      }
+    }
+  } else if (warp < 8) {
+    // --------------------------------------------------------- softmax warps
+    const int wq = warp - 4;
+    const int r = wq * 32 + lane;  // key row in tile
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int s = it & 1;
+      if (!mbar_wait_warp(&bars[B_S_FULL], it & 1, abort_flag, p.status, 39)) { ok = false; break; }
+      // LSE/D of this query tile were staged before Q_ROT[s] completed.
+      if (!mbar_wait_warp(&bars[B_Q_ROT + s], (it >> 1) & 1, abort_flag, p.status, 40)) {
+        ok = false;
+        break;
+      }
+      // P^T / dS^T buffers: free once the MMAs of the previous tile are done.
+      if (it >= 1 && !mbar_wait_warp(&bars[B_PDS_FREE], (it - 1) & 1, abort_flag, p.status, 41)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const bool diag = (it == 0);  // query tile == key tile: mask query < key
+      const float* lse2 = sLSE + s * 128;
+      const float* del = sDEL + s * 128;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {  // 32 query columns at a time
+        uint32_t sr[32], dpr[32];
+        tmem_ld_x32(tmem + lane_base + kColS + c * 32, sr);
+        tmem_ld_x32(tmem + lane_base + kColDP + c * 32, dpr);
+        tmem_ld_wait(sr);
+        tmem_ld_wait(dpr);
+        if (c == 3) {
+          tc_fence_before();
+          mbar_arrive(&bars[B_S_FREE]);
+        }
+        uint32_t pw[16], dw[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float pv[2], dsv[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int col = c * 32 + e + u;
+            float pe = ex2_approx(__uint_as_float(sr[e + u]) * p.scale_log2 - lse2[col]);
+            if (diag && col < r) pe = 0.f;
+            pv[u] = pe;
+            dsv[u] = pe * (__uint_as_float(dpr[e + u]) - del[col]);
+          }
+          pw[e / 2] = pack_bf16x2(pv[0], pv[1]);
+          dw[e / 2] = pack_bf16x2(dsv[0], dsv[1]);
+        }
+        // Row r, columns c*32 .. c*32+31: block c/2, 16-byte chunks (c%2)*4 .. +3.
+        const int blk = c >> 1;
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const uint32_t off = blk * kTileBytes + sw128_offset(r, (c & 1) * 4 + k4);
+          *reinterpret_cast<uint4*>(sPT + off) =
+              make_uint4(pw[4 * k4], pw[4 * k4 + 1], pw[4 * k4 + 2], pw[4 * k4 + 3]);
+          *reinterpret_cast<uint4*>(sDST + off) =
+              make_uint4(dw[4 * k4], dw[4 * k4 + 1], dw[4 * k4 + 2], dw[4 * k4 + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars[B_DS_FULL]);
+    }
+    // ---- epilogue: dV and dK = scale * R^T dK' for keys inside the sequence
+    if (ok && mbar_wait_warp(&bars[B_MMA_DONE], 0, abort_flag, p.status, 42)) {
+      tc_fence_after();
+      uint32_t dvr[64], dkr[64];
+      tmem_ld_x32(tmem + lane_base + kColDV, dvr);
+      tmem_ld_x32(tmem + lane_base + kColDV + 32, dvr + 32);
+      tmem_ld_wait(dvr);
+      tmem_ld_wait(dvr + 32);
+      tmem_ld_x32(tmem + lane_base + kColDK, dkr);
+      tmem_ld_x32(tmem + lane_base + kColDK + 32, dkr + 32);
+      tmem_ld_wait(dkr);
+      tmem_ld_wait(dkr + 32);
+      const int kpos = kt * kBN + r;
+      if (kpos < len) {
+        const long long orow = (static_cast<long long>(start + kpos) * H + h) * kHD;
+        uint4* dvd = reinterpret_cast<uint4*>(p.dv + orow);
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          dvd[c] = make_uint4(
+              pack_bf16x2(__uint_as_float(dvr[8 * c + 0]), __uint_as_float(dvr[8 * c + 1])),
+              pack_bf16x2(__uint_as_float(dvr[8 * c + 2]), __uint_as_float(dvr[8 * c + 3])),
+              pack_bf16x2(__uint_as_float(dvr[8 * c + 4]), __uint_as_float(dvr[8 * c + 5])),
+              pack_bf16x2(__uint_as_float(dvr[8 * c + 6]), __uint_as_float(dvr[8 * c + 7])));
+        const float2* cs = p.rope.cs + static_cast<long long>(kpos) * 32;
+        float g[64];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float2 t = __ldg(cs + i);
+          const float a = __uint_as_float(dkr[i]) * p.scale;
+          const float b = __uint_as_float(dkr[i + 32]) * p.scale;
+          g[i] = a * t.x + b * t.y;
+          g[i + 32] = b * t.x - a * t.y;
+        }
+        uint4* dkd = reinterpret_cast<uint4*>(p.dk + orow);
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          dkd[c] = make_uint4(pack_bf16x2(g[8 * c + 0], g[8 * c + 1]),
+                              pack_bf16x2(g[8 * c + 2], g[8 * c + 3]),
+                              pack_bf16x2(g[8 * c + 4], g[8 * c + 5]),
+                              pack_bf16x2(g[8 * c + 6], g[8 * c + 7]));
+      }
+    }
+  } else {
+    // -------------------------------------------------- dQ' accumulation
+    const int wq = warp & 3;  // warps 10,11,12,13 -> TMEM lane quarters 2,3,0,1
+    const int r = wq * 32 + lane;  // query row in tile
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    for (int it = 0; it < n_it; ++it) {
+      if (!mbar_wait_warp(&bars[B_DQ_FULL], it & 1, abort_flag, p.status, 43)) break;
+      tc_fence_after();
+      uint32_t a[64];
+      tmem_ld_x32(tmem + lane_base + kColDQ, a);
+      tmem_ld_x32(tmem + lane_base + kColDQ + 32, a + 32);
+      tmem_ld_wait(a);
+      tmem_ld_wait(a + 32);
+      tc_fence_before();
+      mbar_arrive(&bars[B_DQ_FREE]);
+      const int qpos = (kt + it) * kBM + r;
+      if (qpos < len) {
+        float* dst = p.dq_acc + (static_cast<long long>(start + qpos) * H + h) * kHD;
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 4 * c),
+                       "f"(__uint_as_float(a[4 * c])), "f"(__uint_as_float(a[4 * c + 1])),
+                       "f"(__uint_as_float(a[4 * c + 2])), "f"(__uint_as_float(a[4 * c + 3]))
+                       : "memory");
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 3. postprocess: dq = bf16(scale * R(m)^T dq_acc).  Grid (tiles, sequences);
+//    4 threads per (row, head): thread part c rotates chunk c (dims 8c..8c+7)
+//    against chunk c + 4.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256)
+    ne_attn_dq_postprocess_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq,
+                                  const Problem pb, RopeTable rope, float scale) {
+  const int seq = blockIdx.y;
+  int start, len;
+  if (!seq_bounds(pb, seq, start, len, nullptr)) return;
+  const int t0 = blockIdx.x * kBM;
+  if (t0 >= len) return;
+  const int H = pb.H;
+  const int rows = min(kBM, len - t0);
+  const int items = rows * H * 4;
+  for (int w = threadIdx.x; w < items; w += blockDim.x) {
+    const int part = w & 3;
+    const int rh = w >> 2;
+    const int rr = rh / H, h = rh - rr * H;
+    const int pos = t0 + rr;
+    const float* src = dq_acc + (static_cast<long long>(start + pos) * H + h) * kHD;
+    const float4* lo4 = reinterpret_cast<const float4*>(src + part * 8);
+    const float4* hi4 = reinterpret_cast<const float4*>(src + 32 + part * 8);
+    const float4 l0 = lo4[0], l1 = lo4[1], h0 = hi4[0], h1 = hi4[1];
+    const float lo[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+    const float hi[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+    const float2* cs = rope.cs + static_cast<long long>(pos) * 32 + part * 8;
+    float go[8], gh[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float2 t = __ldg(cs + i);
+      const float a = lo[i] * scale, b = hi[i] * scale;
+      go[i] = a * t.x + b * t.y;
+      gh[i] = b * t.x - a * t.y;
+    }
+    __nv_bfloat16* d = dq + (static_cast<long long>(start + pos) * H + h) * kHD;
+    *reinterpret_cast<uint4*>(d + part * 8) =
+        make_uint4(pack_bf16x2(go[0], go[1]), pack_bf16x2(go[2], go[3]),
+                   pack_bf16x2(go[4], go[5]), pack_bf16x2(go[6], go[7]));
+    *reinterpret_cast<uint4*>(d + 32 + part * 8) =
+        make_uint4(pack_bf16x2(gh[0], gh[1]), pack_bf16x2(gh[2], gh[3]),
+                   pack_bf16x2(gh[4], gh[5]), pack_bf16x2(gh[6], gh[7]));
+  }
+}
+
+cudaError_t launch_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                       const CUtensorMap& tmDO, const BwdParams& p, int n_tiles,
+                       cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(ne_attn_bwd_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         bwd::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const long long n_pairs = static_cast<long long>(p.pb.n_tot) * p.pb.H;
+  const long long threads = n_pairs * 8;
+  const int blocks = static_cast<int>((threads + 255) / 256);
+  ne_attn_bwd_preprocess_kernel<<<blocks, 256, 0, stream>>>(p.out, p.dout, p.delta, p.dq_acc,
+                                                            n_pairs, p.pb.H, p.pb.n_tot);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.pb.nseq * p.pb.H, n_tiles);
+  ne_attn_bwd_kernel<<<grid, bwd::kThreads, bwd::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, tmDO, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dim3 pgrid(n_tiles, p.pb.nseq);
+  ne_attn_dq_postprocess_kernel<<<pgrid, 256, 0, stream>>>(p.dq_acc, p.dq, p.pb, p.rope, p.scale);
+  return cudaGetLastError();
+}
+
+}  // namespace ne

@@ -1,0 +1,97 @@
+// ne_common.cuh -- shared definitions of the attention kernels: tile sizes,
+// launch parameter blocks, and the device-side status codes.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace ne {
+
+// Tile geometry: 128 query rows x 128 key columns, head dimension 64 (one
+// 128-byte bf16 row per token and head, exactly one 128-byte swizzle atom).
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+constexpr int kHD = 64;
+constexpr int kTileBytes = kBM * kHD * 2;  // 16 KiB: one 128 x 64 bf16 tile
+
+// Device status word values (ne_attn_get_device_status maps them to ne_status).
+constexpr int NE_DEV_OK = 0;
+constexpr int NE_DEV_BAD_SEQLEN = 1;        // a sequence longer than max_seqlen, or
+                                            // cu_seqlens outside [0, n_tot]
+constexpr int NE_DEV_TIMEOUT_BASE = 0x100;  // + wait site id
+
+// RoPE table: for position p and frequency i < 32, rope[p * 32 + i] = (cos, sin)
+// of p * theta_i in fp32, each the fp32 rounding of the double value.
+struct RopeTable {
+  const float2* cs;
+  int capacity;  // number of positions
+};
+
+// One attention problem in the packed form: tokens are rows of [N_tot, H, 64];
+// sequence s spans rows cu[s] .. cu[s+1]-1.  A fixed-length batch [B, T, H, 64]
+// is the packed form with cu = {0, T, 2T, ...}, given implicitly (cu == nullptr).
+struct Problem {
+  const int* cu_seqlens;  // device, nseq + 1 entries, or nullptr for fixed length
+  int nseq;               // B for fixed length
+  int max_len;            // T for fixed length; max_seqlen for varlen
+  int H;
+  int n_tot;              // total rows
+  int lse_fixed;          // 1: LSE is [B, H, T]; 0: LSE is [H, N_tot]
+};
+
+struct FwdParams {
+  Problem pb;
+  void* out;         // bf16 or fp32 [N_tot, H, 64]
+  int out_f32;
+  float* lse;
+  float scale_log2;  // softmax scale * log2(e)
+  RopeTable rope;
+  int* status;
+};
+
+struct BwdParams {
+  Problem pb;
+  const __nv_bfloat16* out;
+  const __nv_bfloat16* dout;
+  const float* lse;
+  float* delta;     // [H, N_tot] fp32 workspace: D_m = dO_m . O_m
+  float* dq_acc;    // [N_tot, H, 64] fp32 workspace (rotated-frame dQ', unscaled)
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  float scale;
+  float scale_log2;
+  RopeTable rope;
+  int* status;
+};
+
+// Sequence bounds of sequence s.  Returns false (and raises the device status)
+// if cu_seqlens puts the sequence outside [0, n_tot] or makes it longer than
+// max_len; the caller then skips the sequence.
+__device__ __forceinline__ bool seq_bounds(const Problem& pb, int s, int& start, int& len,
+                                           int* status) {
+  if (pb.cu_seqlens) {
+    start = __ldg(pb.cu_seqlens + s);
+    const int end = __ldg(pb.cu_seqlens + s + 1);
+    len = end - start;
+    if (start < 0 || end > pb.n_tot || len < 0 || len > pb.max_len) {
+      if (status) atomicCAS(status, 0, NE_DEV_BAD_SEQLEN);
+      return false;
+    }
+  } else {
+    start = s * pb.max_len;
+    len = pb.max_len;
+  }
+  return true;
+}
+
+// Index of LSE / delta element (head h, sequence s starting at row `start`,
+// position t within the sequence).
+__device__ __forceinline__ long long lse_index(const Problem& pb, int h, int s, int start, int t) {
+  if (pb.lse_fixed) return (static_cast<long long>(s) * pb.H + h) * pb.max_len + t;
+  return static_cast<long long>(h) * pb.n_tot + start + t;
+}
+
+}  // namespace ne

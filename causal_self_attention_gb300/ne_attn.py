@@ -1,0 +1,232 @@
+"""ctypes binding of ``libne_attn.so`` (C ABI: include/ne_attn.h, include/ne_attn_debug.h).
+
+Argument marshalling only: every step of the computation runs in the
+library's CUDA kernels.  Torch supplies device memory and streams.  Each
+function keeps the C name; tensors replace raw pointers and the sizes are read
+from their shapes.  A nonzero status raises :class:`NeAttnError`.  There is no
+fallback: if the library is missing, or the device is not an sm_103 GPU, the
+call fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+_lib = None
+
+NE_OK = 0
+STATUS_NAMES = {0: "NE_OK", 1: "NE_ERR_INVALID_ARG", 2: "NE_ERR_UNSUPPORTED",
+                3: "NE_ERR_MISALIGNED", 4: "NE_ERR_CUDA", 5: "NE_ERR_TIMEOUT", 6: "NE_ERR_OOM",
+                7: "NE_ERR_BAD_SEQLEN"}
+
+EXPORTED = ("ne_attn_fwd", "ne_attn_fwd_f32out", "ne_attn_bwd", "ne_attn_bwd_workspace_bytes",
+            "ne_attn_varlen_fwd", "ne_attn_varlen_fwd_f32out", "ne_attn_varlen_bwd",
+            "ne_attn_get_device_status", "ne_attn_last_device_code", "ne_status_string",
+            "ne_attn_release", "ne_debug_tma_tile", "ne_debug_rope_tile", "ne_debug_umma")
+
+
+class NeAttnError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(status, status)}")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib():
+    """Load the library (built in-tree by ``causal_self_attention_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with "
+                           "`python -m causal_self_attention_gb300.build`")
+    L = ctypes.CDLL(path)
+    P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    sig = {
+        "ne_attn_fwd": [P, P, P, I, I, I, I, F, F, P, P, P],
+        "ne_attn_fwd_f32out": [P, P, P, I, I, I, I, F, F, P, P, P],
+        "ne_attn_bwd": [P, P, P, P, P, P, I, I, I, I, F, F, P, P, P, P, Z, P],
+        "ne_attn_varlen_fwd": [P, P, P, P, I, I, I, I, I, F, F, P, P, P],
+        "ne_attn_varlen_fwd_f32out": [P, P, P, P, I, I, I, I, I, F, F, P, P, P],
+        "ne_attn_varlen_bwd": [P, P, P, P, P, P, P, I, I, I, I, I, F, F, P, P, P, P, Z, P],
+        "ne_attn_get_device_status": [P],
+        "ne_attn_last_device_code": [],
+        "ne_attn_release": [],
+        "ne_debug_tma_tile": [P, I, I, I, I, P, P],
+        "ne_debug_rope_tile": [P, I, I, I, I, I, F, P, P],
+        "ne_debug_umma": [I, P, P, P, P],
+    }
+    for name, args in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = None if name == "ne_attn_release" else I
+    L.ne_attn_bwd_workspace_bytes.argtypes = [I, I, I]
+    L.ne_attn_bwd_workspace_bytes.restype = Z
+    L.ne_status_string.argtypes = [I]
+    L.ne_status_string.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def _check(name, rc):
+    if rc != NE_OK:
+        raise NeAttnError(name, rc)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _need(t, dtype, name):
+    if not (t.is_cuda and t.dtype == dtype and t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+
+
+def ne_status_string(status: int) -> str:
+    return lib().ne_status_string(int(status)).decode()
+
+
+def ne_attn_bwd_workspace_bytes(n_tot: int, H: int, D: int = 64) -> int:
+    return int(lib().ne_attn_bwd_workspace_bytes(int(n_tot), int(H), int(D)))
+
+
+def ne_attn_fwd(q, k, v, rope_base=10000.0, scale=None, out=None, lse=None, out_f32=False,
+                stream=None):
+    """Forward on ``[B, T, H, 64]`` bf16 tensors.  Returns ``(out, lse)``;
+    ``lse`` is ``[B, H, T]`` fp32, ``out`` bf16 (fp32 with ``out_f32``)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, torch.bfloat16, n)
+    B, T, H, D = q.shape
+    scale = D ** -0.5 if scale is None else scale
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32 if out_f32 else torch.bfloat16,
+                          device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    fn = lib().ne_attn_fwd_f32out if out_f32 else lib().ne_attn_fwd
+    _check("ne_attn_fwd", fn(_ptr(q), _ptr(k), _ptr(v), B, H, T, D, float(rope_base),
+                             float(scale), _ptr(out), _ptr(lse), _stream(stream)))
+    return out, lse
+
+
+def ne_attn_bwd(q, k, v, out, dout, lse, rope_base=10000.0, scale=None, dq=None, dk=None,
+                dv=None, workspace=None, stream=None):
+    """Backward on ``[B, T, H, 64]`` tensors.  Returns ``(dq, dk, dv)`` (bf16).
+    ``workspace``: a CUDA uint8 tensor of ``ne_attn_bwd_workspace_bytes`` bytes,
+    or None (stream-ordered temporary inside the library)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        _need(t, torch.bfloat16, n)
+    _need(lse, torch.float32, "lse")
+    B, T, H, D = q.shape
+    scale = D ** -0.5 if scale is None else scale
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("ne_attn_bwd", lib().ne_attn_bwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), B, H, T, D,
+        float(rope_base), float(scale), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+        ws_bytes, _stream(stream)))
+    return dq, dk, dv
+
+
+def ne_attn_varlen_fwd(q, k, v, cu_seqlens, max_seqlen, rope_base=10000.0, scale=None,
+                       out=None, lse=None, out_f32=False, stream=None):
+    """Forward on packed ``[N_tot, H, 64]`` tensors; ``cu_seqlens`` int32 CUDA
+    ``[nseq + 1]``.  Returns ``(out, lse)`` with ``lse`` ``[H, N_tot]``."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, torch.bfloat16, n)
+    _need(cu_seqlens, torch.int32, "cu_seqlens")
+    N, H, D = q.shape
+    scale = D ** -0.5 if scale is None else scale
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32 if out_f32 else torch.bfloat16,
+                          device=q.device)
+    if lse is None:
+        lse = torch.empty((H, N), dtype=torch.float32, device=q.device)
+    fn = lib().ne_attn_varlen_fwd_f32out if out_f32 else lib().ne_attn_varlen_fwd
+    _check("ne_attn_varlen_fwd", fn(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens),
+                                    cu_seqlens.numel() - 1, N, int(max_seqlen), H, D,
+                                    float(rope_base), float(scale), _ptr(out), _ptr(lse),
+                                    _stream(stream)))
+    return out, lse
+
+
+def ne_attn_varlen_bwd(q, k, v, out, dout, lse, cu_seqlens, max_seqlen, rope_base=10000.0,
+                       scale=None, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward of :func:`ne_attn_varlen_fwd`.  Returns ``(dq, dk, dv)``."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        _need(t, torch.bfloat16, n)
+    _need(lse, torch.float32, "lse")
+    _need(cu_seqlens, torch.int32, "cu_seqlens")
+    N, H, D = q.shape
+    scale = D ** -0.5 if scale is None else scale
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("ne_attn_varlen_bwd", lib().ne_attn_varlen_bwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(cu_seqlens),
+        cu_seqlens.numel() - 1, N, int(max_seqlen), H, D, float(rope_base), float(scale),
+        _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), ws_bytes, _stream(stream)))
+    return dq, dk, dv
+
+
+def ne_attn_get_device_status(stream=None) -> int:
+    """Synchronize the stream; return (and clear) the device status code."""
+    return int(lib().ne_attn_get_device_status(_stream(stream)))
+
+
+def ne_attn_last_device_code() -> int:
+    return int(lib().ne_attn_last_device_code())
+
+
+def ne_attn_release() -> None:
+    lib().ne_attn_release()
+
+
+# ------------------------------------------------------------- bring-up entries
+
+def ne_debug_tma_tile(src, h, row0, stream=None):
+    """Raw 16 KiB shared-memory image of one TMA-loaded tile (uint8 CUDA tensor)."""
+    _need(src, torch.bfloat16, "src")
+    n, H, _ = src.shape
+    dst = torch.empty(16384, dtype=torch.uint8, device=src.device)
+    _check("ne_debug_tma_tile", lib().ne_debug_tma_tile(_ptr(src), n, H, h, row0, _ptr(dst),
+                                                        _stream(stream)))
+    return dst
+
+
+def ne_debug_rope_tile(src, h, row0, pos0, rope_base=10000.0, stream=None):
+    """The tile after the kernels' in-smem RoPE, un-swizzled: ``[128, 64]`` bf16."""
+    _need(src, torch.bfloat16, "src")
+    n, H, _ = src.shape
+    dst = torch.empty((128, 64), dtype=torch.bfloat16, device=src.device)
+    _check("ne_debug_rope_tile", lib().ne_debug_rope_tile(_ptr(src), n, H, h, row0, pos0,
+                                                          float(rope_base), _ptr(dst),
+                                                          _stream(stream)))
+    return dst
+
+
+def ne_debug_umma(form, a, b, stream=None):
+    """One tcgen05 MMA chain; see include/ne_attn_debug.h for the three forms."""
+    _need(a, torch.bfloat16, "a")
+    _need(b, torch.bfloat16, "b")
+    d = torch.empty((128, 128 if form == 0 else 64), dtype=torch.float32, device=a.device)
+    _check("ne_debug_umma", lib().ne_debug_umma(int(form), _ptr(a), _ptr(b), _ptr(d),
+                                                _stream(stream)))
+    return d

@@ -1,0 +1,144 @@
+/*
+ * ne_attn.h -- C ABI of the GB300 (sm_103a) causal self-attention library with
+ * rotary position embedding (RoPE), forward and backward.
+ *
+ * The operation (per sequence, per head, positions m, n = 0..L-1; the pages
+ * print no equations, so the standard definitions are restated here):
+ *   q'_m = R(m) q_m, k'_n = R(n) k_n        RoPE, rotate-half pairing (element
+ *                                           i with i + D/2), theta_i =
+ *                                           base^(-(2i)/D), angle m * theta_i
+ *   S_mn = scale * q'_m . k'_n              for n <= m (causal)
+ *   LSE_m = log sum_{n<=m} exp(S_mn)        natural log, scale included
+ *   O_m = sum_{n<=m} exp(S_mn - LSE_m) v_n
+ * and the backward returns dq, dk, dv with respect to the UN-rotated q and k
+ * (the rotation is inside the operation).
+ * Sources: causal self-attention with RoPE applied to the projections --
+ * "Tiny Hackable CUDA: C ve CUDA ile Sifirdan Dil Modeli Gelistirmek",
+ * section 3; a hand-written FlashAttention with RoPE in a CUDA engine whose
+ * analytic gradients (including through RoPE) are checked against a centred
+ * finite difference -- NanoEuler Show HN page, paragraph 2; 12 heads of width
+ * 64 (GPT-2 small) -- techinfos.ro NanoEuler article, section "Arhitectura si
+ * tehnologii folosite".  RoPE itself: RoFormer (Su et al. 2021).
+ *
+ * Conventions shared by every entry point:
+ *  - Head dimension D must be 64 (NE_ERR_UNSUPPORTED otherwise).
+ *  - q, k, v, out, dout, dq, dk, dv are bf16 (raw 16-bit words, type
+ *    ne_bf16), row-major [B, T, H, 64] for the fixed-length calls and
+ *    [N_tot, H, 64] for the varlen calls, 64 contiguous.  Every one of these
+ *    pointers must be 16-byte aligned (NE_ERR_MISALIGNED).
+ *  - lse is fp32 [B, H, T] (fixed length) or [H, N_tot] (varlen), 4-byte
+ *    aligned.
+ *  - Every pointer is DEVICE memory owned by the caller; the library keeps no
+ *    reference to it after the call returns.  The library owns only its RoPE
+ *    cos/sin tables (released by ne_attn_release) and, when a backward is
+ *    given no workspace, a stream-ordered temporary it frees itself.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
+ *    enqueued asynchronously on it; the call returns after the launch.
+ *  - Argument errors are detected on the host before anything is launched
+ *    and return a nonzero ne_status.  Errors found on the device (a varlen
+ *    sequence longer than max_seqlen, a pipeline wait that timed out) are
+ *    recorded in a device status word read by ne_attn_get_device_status.
+ *  - Nothing here calls exit, abort or traps the GPU.
+ *  - Calls are thread-safe; the RoPE table cache is per device.
+ */
+#ifndef NE_ATTN_H
+#define NE_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int ne_status;
+#define NE_OK 0
+#define NE_ERR_INVALID_ARG 1 /* null pointer, non-positive size, bad cu_seqlens count */
+#define NE_ERR_UNSUPPORTED 2 /* D != 64, or a device without sm_100-family tensor cores */
+#define NE_ERR_MISALIGNED 3  /* a tensor pointer not 16-byte aligned */
+#define NE_ERR_CUDA 4        /* a CUDA runtime / driver call failed */
+#define NE_ERR_TIMEOUT 5     /* a device pipeline wait expired (reported by get_device_status) */
+#define NE_ERR_OOM 6         /* allocation of a table or temporary failed */
+#define NE_ERR_BAD_SEQLEN 7  /* a varlen sequence was longer than max_seqlen (device-detected) */
+
+typedef uint16_t ne_bf16; /* raw bfloat16 bits */
+
+/* Forward, fixed length.  q, k, v: [B, T, H, 64] bf16.  out: [B, T, H, 64]
+ * bf16 (written).  lse: [B, H, T] fp32 (written), natural log.  scale is the
+ * softmax scale (1/sqrt(64) = 0.125 for the usual choice); rope_base is the
+ * RoPE theta base (10000 for the usual choice).  B, H, T >= 1. */
+ne_status ne_attn_fwd(const ne_bf16* q, const ne_bf16* k, const ne_bf16* v, int B, int H, int T,
+                      int D, float rope_base, float scale, ne_bf16* out, float* lse,
+                      void* stream);
+
+/* Same as ne_attn_fwd but writes O as fp32 (before any bf16 rounding). */
+ne_status ne_attn_fwd_f32out(const ne_bf16* q, const ne_bf16* k, const ne_bf16* v, int B, int H,
+                             int T, int D, float rope_base, float scale, float* out, float* lse,
+                             void* stream);
+
+/* Bytes of workspace ne_attn_bwd / ne_attn_varlen_bwd need for n_tot tokens
+ * (B*T for fixed length) and H heads: an fp32 dQ accumulator [n_tot, H, D]
+ * and the fp32 row terms D_m = dO_m . O_m [H, n_tot], each 256-byte aligned. */
+size_t ne_attn_bwd_workspace_bytes(int n_tot, int H, int D);
+
+/* Backward, fixed length.  q, k, v, out (the forward's O), dout: [B, T, H, 64]
+ * bf16; lse: the forward's [B, H, T] fp32.  dq, dk, dv: [B, T, H, 64] bf16
+ * (written), gradients w.r.t. the un-rotated q, k and v.  workspace: device
+ * memory of at least ne_attn_bwd_workspace_bytes(B*T, H, D) bytes, 256-byte
+ * aligned, or NULL to let the library allocate (and free) a temporary on
+ * `stream` with cudaMallocAsync.  dq is accumulated with fp32 atomics, so its
+ * last bits may differ from run to run; dk and dv are deterministic. */
+ne_status ne_attn_bwd(const ne_bf16* q, const ne_bf16* k, const ne_bf16* v, const ne_bf16* out,
+                      const ne_bf16* dout, const float* lse, int B, int H, int T, int D,
+                      float rope_base, float scale, ne_bf16* dq, ne_bf16* dk, ne_bf16* dv,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* Forward, packed variable-length batch.  Sequence s occupies rows
+ * cu_seqlens[s] .. cu_seqlens[s+1]-1 of q, k, v, out ([n_tot, H, 64] bf16);
+ * cu_seqlens is DEVICE int32 [nseq + 1], nondecreasing, cu_seqlens[0] = 0,
+ * cu_seqlens[nseq] = n_tot.  RoPE positions restart at 0 in every sequence and
+ * attention never crosses a sequence boundary.  max_seqlen must be >= every
+ * sequence length (a longer sequence is reported as NE_ERR_BAD_SEQLEN by
+ * ne_attn_get_device_status and its tail is not computed).  lse: [H, n_tot]
+ * fp32.  With equal lengths T this computes exactly what ne_attn_fwd computes
+ * on [B, T, H, 64] (LSE layout aside). */
+ne_status ne_attn_varlen_fwd(const ne_bf16* q, const ne_bf16* k, const ne_bf16* v,
+                             const int* cu_seqlens, int nseq, int n_tot, int max_seqlen, int H,
+                             int D, float rope_base, float scale, ne_bf16* out, float* lse,
+                             void* stream);
+
+/* Same as ne_attn_varlen_fwd but writes O as fp32. */
+ne_status ne_attn_varlen_fwd_f32out(const ne_bf16* q, const ne_bf16* k, const ne_bf16* v,
+                                    const int* cu_seqlens, int nseq, int n_tot, int max_seqlen,
+                                    int H, int D, float rope_base, float scale, float* out,
+                                    float* lse, void* stream);
+
+/* Backward of ne_attn_varlen_fwd; arguments as there and as in ne_attn_bwd.
+ * workspace: ne_attn_bwd_workspace_bytes(n_tot, H, D) bytes or NULL. */
+ne_status ne_attn_varlen_bwd(const ne_bf16* q, const ne_bf16* k, const ne_bf16* v,
+                             const ne_bf16* out, const ne_bf16* dout, const float* lse,
+                             const int* cu_seqlens, int nseq, int n_tot, int max_seqlen, int H,
+                             int D, float rope_base, float scale, ne_bf16* dq, ne_bf16* dk,
+                             ne_bf16* dv, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronize `stream`, then return and clear the device status word of the
+ * current device: NE_OK, NE_ERR_TIMEOUT or NE_ERR_BAD_SEQLEN (or NE_ERR_CUDA
+ * if the synchronization itself failed). */
+ne_status ne_attn_get_device_status(void* stream);
+
+/* Detail of the last device status read by ne_attn_get_device_status: the raw
+ * device code (for a timeout, 0x100 + the id of the wait that expired). */
+int ne_attn_last_device_code(void);
+
+/* Human-readable name of a status code (static string). */
+const char* ne_status_string(ne_status s);
+
+/* Free the RoPE tables cached for every device.  Call only when no launch
+ * that may read them is still pending. */
+void ne_attn_release(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NE_ATTN_H */

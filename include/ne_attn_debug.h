@@ -1,0 +1,46 @@
+/*
+ * ne_attn_debug.h -- bring-up entry points of the attention library, used by
+ * its GPU tests to check each hardware primitive on its own against plain
+ * host arithmetic: the TMA 128-byte-swizzled tile load, the in-smem RoPE of a
+ * tile, and the three tcgen05 MMA operand forms the attention kernels use.
+ * They follow the conventions of ne_attn.h (device pointers owned by the
+ * caller, asynchronous on `stream`, host-side argument checks).  The paper
+ * pages have no counterpart: these exist only to test the pieces.
+ */
+#ifndef NE_ATTN_DEBUG_H
+#define NE_ATTN_DEBUG_H
+
+#include "ne_attn.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* TMA-load the 128 x 64 tile at rows row0..row0+127, head h of src
+ * ([n_rows, H, 64] bf16; rows past n_rows read as zero) into shared memory
+ * with the 128-byte swizzle, and copy the 16384 raw shared-memory bytes to
+ * dst_raw (device, 16384 bytes). */
+ne_status ne_debug_tma_tile(const ne_bf16* src, int n_rows, int H, int h, int row0,
+                            void* dst_raw, void* stream);
+
+/* TMA-load the same tile, apply the kernels' in-smem RoPE to every row r at
+ * position pos0 + r with the library's cached table for rope_base, and write
+ * the rotated tile un-swizzled to dst ([128, 64] bf16). */
+ne_status ne_debug_rope_tile(const ne_bf16* src, int n_rows, int H, int h, int row0, int pos0,
+                             float rope_base, ne_bf16* dst, void* stream);
+
+/* One tcgen05 MMA chain (bf16 in, fp32 accumulate in TMEM), operands written
+ * to shared memory with the software 128-byte swizzle:
+ *   form 0: d[128,128] = a[128,64] . b[128,64]^T       (both K-major)
+ *   form 1: d[128,64]  = a[128,128] . b[128,64]        (a K-major; b is
+ *                                                     [K=128, N=64], MN-major)
+ *   form 2: d[128,64]  = a[128,128]^T . b[128,64]      (a is [K=128, M=128],
+ *                                                     MN-major; b as form 1)
+ * a, b: row-major bf16 as written above; d: row-major fp32. */
+ne_status ne_debug_umma(int form, const ne_bf16* a, const ne_bf16* b, float* d, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NE_ATTN_DEBUG_H */

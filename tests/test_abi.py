@@ -1,0 +1,73 @@
+"""CPU checks of the boundary: the library builds for sm_103a, loads, and
+exports every function include/*.h declares; host-side argument checks return
+their status codes before anything touches a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^[A-Za-z_][\w\s\*]*?\b(ne_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from causal_self_attention_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for must in ("ne_attn_fwd", "ne_attn_bwd", "ne_attn_varlen_fwd", "ne_attn_varlen_bwd",
+                 "ne_attn_bwd_workspace_bytes", "ne_attn_get_device_status", "ne_status_string",
+                 "ne_attn_release"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_every_declared_symbol():
+    from causal_self_attention_gb300 import ne_attn
+    assert set(_declared()) <= set(ne_attn.EXPORTED)
+
+
+def test_status_strings_and_workspace(lib):
+    lib.ne_status_string.restype = ctypes.c_char_p
+    assert lib.ne_status_string(0) == b"NE_OK"
+    assert lib.ne_status_string(5) == b"NE_ERR_TIMEOUT"
+    lib.ne_attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+    ws = lib.ne_attn_bwd_workspace_bytes(8192, 12, 64)
+    assert ws == 8192 * 12 * 64 * 4 + 8192 * 12 * 4
+    assert lib.ne_attn_bwd_workspace_bytes(8192, 12, 128) == 0
+
+
+def test_argument_errors_return_before_any_launch(lib):
+    P = ctypes.c_void_p
+    lib.ne_attn_fwd.argtypes = [P, P, P] + [ctypes.c_int] * 4 + [ctypes.c_float] * 2 + [P, P, P]
+    fake = P(0x10000)  # never dereferenced: every case below fails its host check first
+    # null pointer
+    assert lib.ne_attn_fwd(None, fake, fake, 1, 1, 64, 64, 10000.0, 0.125, fake, fake, None) == 1
+    # unsupported head dimension
+    assert lib.ne_attn_fwd(fake, fake, fake, 1, 1, 64, 128, 10000.0, 0.125, fake, fake, None) == 2
+    # non-positive size
+    assert lib.ne_attn_fwd(fake, fake, fake, 0, 1, 64, 64, 10000.0, 0.125, fake, fake, None) == 1
+    # misaligned tensor pointer
+    assert lib.ne_attn_fwd(P(0x10002), fake, fake, 1, 1, 64, 64, 10000.0, 0.125, fake, fake,
+                           None) == 3
+    # bad rope base
+    assert lib.ne_attn_fwd(fake, fake, fake, 1, 1, 64, 64, -1.0, 0.125, fake, fake, None) == 1
