@@ -1,0 +1,395 @@
+#!/usr/bin/env python
+"""Benchmark of causal RoPE self-attention forward + backward on GB300.
+
+One step = ne_attn_fwd + ne_attn_bwd (all kernels of the path) over one batch
+of the GPT-2-small training shape, B=8, H=12, T=1024, D=64, bf16 inputs drawn
+N(0,1) from a fixed seed, inputs resident in HBM.  The L2 is flushed (a 512 MiB
+write) between timed steps, outside the timed region.  Throughput counts the
+causal FLOPs: 2*B*H*T^2*D forward plus 2.5x that backward.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs N independent replicas (the operation needs no exchange between
+GPUs), one process per GPU under torch.distributed; value = all ranks' FLOPs /
+the slowest rank's time.  ``--impl reference`` times the CPU oracle (the
+plain double-precision C implementation) on a bounded sample of the same
+workload on this host's cores.  Prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "RoPE causal attention fwd+bwd TFLOP/s at B8 H12 T1024 D64; % of BF16 peak"
+UNIT = "TFLOP/s"
+WORKLOAD = "gpt2s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def flops_fwd_bwd(B, H, T, D):
+    fwd = 2.0 * B * H * T * T * D
+    return fwd, 2.5 * fwd
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def rank_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+# --------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock/throttle samples of one GPU while it runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.out = None
+        try:
+            self.out = open(f"/tmp/ne_clocks_{os.getpid()}.csv", "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(device_index), "-lms", "50"], stdout=self.out,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.out.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.out.name)
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": reasons, "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_sample(seconds_target, inp, fixed_T=None):
+    """Time the oracle (as it stands) on whole heads of the workload until about
+    `seconds_target` seconds have been spent; returns (flops, seconds, heads, T)."""
+    import oracle
+    B, T, H, D = inp["B"], inp["T"], inp["H"], inp["D"]
+    T = fixed_T or T
+    fwd, bwd = flops_fwd_bwd(1, 1, T, D)
+    heads = 0
+    t0 = time.perf_counter()
+    while True:
+        b, h = divmod(heads % (B * H), H)
+        q, k, v, do = (inp[n][b, :T, h:h + 1] for n in ("q", "k", "v", "dout"))
+        oracle.attention(q, k, v, do, [0, T], base=inp["rope_base"], scale=inp["scale"])
+        heads += 1
+        el = time.perf_counter() - t0
+        if el >= seconds_target or heads >= 4 * B * H:
+            break
+    return heads * (fwd + bwd), el, heads, T
+
+
+def run_reference(args):
+    rank, _, world = rank_env()
+    if world > 1 and rank != 0:
+        return 0
+    import oracle
+    from causal_self_attention_gb300.inputs import make_inputs
+    inp = make_inputs(WORKLOAD)
+    B, T, H, D = inp["B"], inp["T"], inp["H"], inp["D"]
+    # Calibrate one head, then size each step so the whole run stays within minutes.
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle_sample(0.0, inp)
+    t_head = time.perf_counter() - t0
+    budget = 150.0
+    Ts = T
+    while (args.steps + args.warmup) * t_head * (Ts / T) ** 2 > budget and Ts > 64:
+        Ts //= 2
+    for _ in range(args.warmup):
+        oracle_sample(0.0, inp, fixed_T=Ts)
+    total_flops, total_s = 0.0, 0.0
+    for _ in range(args.steps):
+        f, s, _, _ = oracle_sample(0.0, inp, fixed_T=Ts)
+        total_flops += f
+        total_s += s
+    value = total_flops / total_s / 1e12
+    sample = (f"one head (b, h) of the {WORKLOAD} workload per step, positions 0..{Ts - 1}, "
+              f"fwd+bwd in fp64, all of the oracle's OpenMP threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD}: B={B} H={H} T={T} D={D}, causal, RoPE base 10000, "
+                               "fwd+bwd", "sample_T": Ts},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# --------------------------------------------------------------------- ours
+def source_sha(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, or None
+    when the kernel source has changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel)
+    if not rec:
+        return None
+    if rec.get("source_sha") != source_sha(rec["sources"]):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from causal_self_attention_gb300 import build as nb
+    rank, local_rank, world = rank_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if rank == 0 or world == 1:
+        nb.build()
+    if world > 1:
+        dist.barrier()
+    from causal_self_attention_gb300 import ne_attn as na
+    from causal_self_attention_gb300.inputs import make_inputs
+
+    inp = make_inputs(WORKLOAD)
+    B, T, H, D = inp["B"], inp["T"], inp["H"], inp["D"]
+    base, scale = inp["rope_base"], inp["scale"]
+    f_fwd, f_bwd = flops_fwd_bwd(B, H, T, D)
+    f_step = f_fwd + f_bwd
+    q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "dout"))
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(na.ne_attn_bwd_workspace_bytes(B * T, H, D), dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        na.ne_attn_fwd(q, k, v, base, scale, out=out, lse=lse, stream=stream)
+        na.ne_attn_bwd(q, k, v, out, do, lse, base, scale, dq=dq, dk=dk, dv=dv, workspace=ws,
+                       stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert na.ne_attn_get_device_status() == 0
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    for e in ev:  # torch creates the CUDA event on first record: create them all now
+        for x in e:
+            x.record(stream)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    w0 = time.perf_counter()
+    for i in range(K):
+        e = ev[i]
+        flush.zero_()
+        na.ne_attn_set_bwd_phase_events(e[2], e[3])
+        e[0].record(stream)
+        na.ne_attn_fwd(q, k, v, base, scale, out=out, lse=lse, stream=stream)
+        e[1].record(stream)
+        na.ne_attn_bwd(q, k, v, out, do, lse, base, scale, dq=dq, dk=dk, dv=dv, workspace=ws,
+                       stream=stream)
+        e[4].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - w0
+    clk = clocks.stop()
+    na.ne_attn_set_bwd_phase_events(None, None)
+    status = na.ne_attn_get_device_status()
+    t_fwd = [e[0].elapsed_time(e[1]) for e in ev]
+    t_pre = [e[1].elapsed_time(e[2]) for e in ev]
+    t_main = [e[2].elapsed_time(e[3]) for e in ev]
+    t_post = [e[3].elapsed_time(e[4]) for e in ev]
+    t_step = [e[0].elapsed_time(e[4]) for e in ev]
+    total_ms = sum(t_step)
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    value = world * f_step * K / (total_ms * 1e-3) / 1e12
+
+    # ---- end to end through the public API with host buffers ------------------
+    pin = {n: inp[n].pin_memory() for n in ("q", "k", "v", "dout")}
+    h_out = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    h_grads = [torch.empty(q.shape, dtype=torch.bfloat16).pin_memory() for _ in range(3)]
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4 + sum(t.numel() * 2 for t in h_grads)
+    KE = args.e2e_steps
+    ee = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(KE)]
+    for i in range(KE + 2):
+        if i >= 2:
+            flush.zero_()
+            ee[i - 2][0].record(stream)
+        q.copy_(pin["q"], non_blocking=True)
+        k.copy_(pin["k"], non_blocking=True)
+        v.copy_(pin["v"], non_blocking=True)
+        do.copy_(pin["dout"], non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+        for hg, g in zip(h_grads, (dq, dk, dv)):
+            hg.copy_(g, non_blocking=True)
+        if i >= 2:
+            ee[i - 2][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ee)
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_value = world * f_step / (e2e_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_kind = load_peaks()
+    peak_tf = peaks["bf16_tflops"]
+    per_kernel = {
+        "ne_attn_fwd_kernel": statistics.mean(t_fwd),
+        "ne_attn_bwd_preprocess_kernel": statistics.mean(t_pre),
+        "ne_attn_bwd_kernel": statistics.mean(t_main),
+        "ne_attn_dq_postprocess_kernel": statistics.mean(t_post),
+    }
+    dom = max(per_kernel, key=per_kernel.get)
+    kernel_flops = {"ne_attn_fwd_kernel": f_fwd, "ne_attn_bwd_kernel": f_bwd}
+    achieved = kernel_flops.get(dom, 0.0) / (per_kernel[dom] * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_tf,
+                "unit": "TFLOP/s", "frac": achieved / peak_tf,
+                "peak_source": f"{peak_kind} bf16 burst (MEASURED_PEAKS.json)"
+                if peak_kind == "measured" else "fallback bf16 burst",
+                "traffic": recorded_traffic(dom)}
+    # HBM-bound helpers: algorithmic bytes / time.
+    n_el = B * T * H * D
+    pre_bytes = 2 * n_el * 2 + B * H * T * 4 + n_el * 4  # read O, dO; write D, zero dQ'
+    post_bytes = n_el * 4 + n_el * 2                      # read dQ', write dQ
+    kernels = {
+        "ne_attn_fwd_kernel": {"ms": per_kernel["ne_attn_fwd_kernel"],
+                               "tflops": f_fwd / (per_kernel["ne_attn_fwd_kernel"] * 1e-3) / 1e12},
+        "ne_attn_bwd_kernel": {"ms": per_kernel["ne_attn_bwd_kernel"],
+                               "tflops": f_bwd / (per_kernel["ne_attn_bwd_kernel"] * 1e-3) / 1e12},
+        "ne_attn_bwd_preprocess_kernel": {
+            "ms": per_kernel["ne_attn_bwd_preprocess_kernel"],
+            "gbs": pre_bytes / (per_kernel["ne_attn_bwd_preprocess_kernel"] * 1e-3) / 1e9},
+        "ne_attn_dq_postprocess_kernel": {
+            "ms": per_kernel["ne_attn_dq_postprocess_kernel"],
+            "gbs": post_bytes / (per_kernel["ne_attn_dq_postprocess_kernel"] * 1e-3) / 1e9},
+    }
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": max(args.warmup, 3), "ms_per_step": total_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD}: B={B} H={H} T={T} D={D}, causal, RoPE base 10000, "
+                               "fwd+bwd", "B": B, "H": H, "T": T, "D": D,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "flushed (512 MiB write) between timed steps"},
+        "pct_bf16_peak": 100.0 * value / (world * peak_tf),
+        "pct_bf16_peak_sustained": 100.0 * value / (world * peaks.get("bf16_tflops_sustained",
+                                                                      peak_tf)),
+        "roofline": roofline,
+        "kernels": kernels,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 4 * K,
+        "clocks": clk,
+        "wall_s": wall,
+        "device_status": status,
+    }
+    if not args.no_cpu_baseline and (world == 1 or rank == 0):
+        import oracle
+        oracle.build()
+        fl, s, heads, Ts = oracle_sample(args.cpu_seconds, inp)
+        line["cpu_baseline"] = {
+            "value": fl / s / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{heads} whole heads (b, h) of the {WORKLOAD} workload, T={Ts}, fwd+bwd "
+                      f"in fp64, {s:.1f} s"}
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -19,8 +19,8 @@ namespace ne {
 cudaError_t launch_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                        const FwdParams& p, int n_qtiles, cudaStream_t stream);
 cudaError_t launch_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                       const CUtensorMap& tmDO, const BwdParams& p, int n_tiles,
-                       cudaStream_t stream);
+                       const CUtensorMap& tmDO, const CUtensorMap& tmDQ, const BwdParams& p,
+                       int n_tiles, cudaStream_t stream, cudaEvent_t ev_pre, cudaEvent_t ev_main);
 cudaError_t launch_debug_tile(const CUtensorMap& tm, int h, int row0, int rotate, int pos0,
                               RopeTable rope, void* dst_raw, __nv_bfloat16* dst_rows,
                               int* status, cudaStream_t stream);
@@ -53,6 +53,7 @@ struct DeviceState {
 std::mutex g_mutex;
 DeviceState g_dev[kMaxDevices];
 int g_last_code = 0;
+cudaEvent_t g_ev_pre = nullptr, g_ev_main = nullptr;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 ne_status cuda_status(cudaError_t e) {
@@ -147,6 +148,19 @@ ne_status encode_rows(CUtensorMap* map, const void* base, int n_rows, int H) {
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NE_OK : NE_ERR_CUDA;
+}
+
+// 3-d tensor map over the fp32 dQ' accumulator [n_rows, H, 64], box 32 x 1 x 128
+// (128-byte rows), 128-byte swizzle: the target of the backward's bulk reduce-adds.
+ne_status encode_rows_f32(CUtensorMap* map, void* base, int n_rows, int H) {
+  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(n_rows)};
+  cuuint64_t strides[2] = {64 * 4, static_cast<cuuint64_t>(H) * 64 * 4};
+  cuuint32_t box[3] = {32, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? NE_OK : NE_ERR_CUDA;
 }
 
@@ -260,7 +274,11 @@ ne_status run_bwd(const Shape& s, const void* q, const void* k, const void* v, c
   const size_t acc_bytes = align256(static_cast<size_t>(s.n_tot) * s.H * 64 * sizeof(float));
   p.dq_acc = static_cast<float*>(ws);
   p.delta = reinterpret_cast<float*>(static_cast<char*>(ws) + acc_bytes);
-  cudaError_t e = ne::launch_bwd(tq, tk, tv, tdo, p, n_tiles, cs);
+  CUtensorMap tdq;
+  rc = encode_rows_f32(&tdq, p.dq_acc, s.n_tot, s.H);
+  cudaError_t e = rc == NE_OK ? ne::launch_bwd(tq, tk, tv, tdo, tdq, p, n_tiles, cs, g_ev_pre,
+                                                g_ev_main)
+                              : cudaErrorInvalidValue;
   if (owned) {
     cudaError_t e2 = cudaFreeAsync(ws, cs);
     if (e == cudaSuccess) e = e2;
@@ -378,6 +396,14 @@ ne_status ne_attn_varlen_bwd(const ne_bf16* q, const ne_bf16* k, const ne_bf16* 
   s.D = D;
   return run_bwd(s, q, k, v, out, dout, lse, rope_base, scale, dq, dk, dv, workspace,
                  workspace_bytes, stream);
+}
+
+ne_status ne_attn_set_bwd_phase_events(void* ev_after_preprocess, void* ev_after_main) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if ((ev_after_preprocess == nullptr) != (ev_after_main == nullptr)) return NE_ERR_INVALID_ARG;
+  g_ev_pre = static_cast<cudaEvent_t>(ev_after_preprocess);
+  g_ev_main = static_cast<cudaEvent_t>(ev_after_main);
+  return NE_OK;
 }
 
 ne_status ne_attn_get_device_status(void* stream) {

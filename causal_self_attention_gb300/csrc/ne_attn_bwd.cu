@@ -8,19 +8,20 @@
 //      tiles i >= j, recomputing P from the saved LSE:
 //        S^T  = K' Q'^T,  P^T = exp(scale S^T - LSE),  dP^T = V dO^T,
 //        dS^T = P^T o (dP^T - D),
-//        dV  += P^T dO,   dK' += dS^T Q',   dQ'_i = dS K'  (-> fp32 atomics),
+//        dV  += P^T dO,   dK' += dS^T Q',   dQ'_i = dS K'  (-> TMA reduce-add),
 //      and at the end writes dV and dK = scale * R(n)^T dK' (bf16);
 //   3. postprocess: dQ = scale * R(m)^T dQ' (bf16).
 // q' = R(m) q and k' = R(n) k are rotated in shared memory right after their
 // TMA loads, as in the forward.
 //
 // Main-kernel warp roles (448 threads):
-//   warps 0-3   rotate: K_j once; every Q_i tile; stage LSE_i and D_i in smem
-//   warps 4-7   softmax: thread t owns key row t (TMEM lane t): P^T, dS^T rows
-//               to smem; epilogue of dK, dV
-//   warp 8      MMA: allocates TMEM; lane 0 issues the five MMAs per tile
-//   warp 9      TMA: lane 0 loads K_j, V_j once and Q_i, dO_i (2 stages)
-//   warps 10-13 dQ: thread owns query row; TMEM dQ' -> red.global.add.v4.f32
+//   warps 0-3   rotate + dQ': K_j once, every Q_i, LSE_i/D_i staging (table
+//               rows and LSE/D prefetched one tile ahead); then TMEM dQ'_i ->
+//               swizzled fp32 smem -> two bulk tensor reduce-adds into dQ'
+//   warps 4-7   softmax, query columns 0-63 of the tile (thread t: key row t)
+//   warps 8-11  softmax, query columns 64-127
+//   warp 12     MMA: allocates TMEM; lane 0 issues the five MMAs per tile
+//   warp 13     TMA: lane 0 loads K_j, V_j once and Q_i, dO_i (2 stages)
 // TMEM columns: S^T 0-127, dP^T 128-255, dV 256-319, dK' 320-383, dQ' 384-447.
 #include "ne_rope.cuh"
 #include "ne_sm100.cuh"
@@ -32,11 +33,12 @@ namespace bwd {
 constexpr int kThreads = 448;
 constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + kTileBytes;
-constexpr int OFF_Q = OFF_V + kTileBytes;        // 2 stages
-constexpr int OFF_DO = OFF_Q + 2 * kTileBytes;   // 2 stages
-constexpr int OFF_PT = OFF_DO + 2 * kTileBytes;  // P^T: 2 blocks of 64 queries
-constexpr int OFF_DST = OFF_PT + 2 * kTileBytes; // dS^T: same layout
-constexpr int OFF_LSE = OFF_DST + 2 * kTileBytes;  // 2 stages x 128 fp32 (log2 units)
+constexpr int OFF_Q = OFF_V + kTileBytes;          // 2 stages
+constexpr int OFF_DO = OFF_Q + 2 * kTileBytes;     // 2 stages
+constexpr int OFF_PT = OFF_DO + 2 * kTileBytes;    // P^T: 2 blocks of 64 queries
+constexpr int OFF_DST = OFF_PT + 2 * kTileBytes;   // dS^T: same layout
+constexpr int OFF_DQ = OFF_DST + 2 * kTileBytes;   // dQ' staging: 2 x [128][32] fp32, SW128
+constexpr int OFF_LSE = OFF_DQ + 2 * kTileBytes;   // 2 stages x 128 fp32 (log2 units)
 constexpr int OFF_DEL = OFF_LSE + 2 * 128 * 4;     // 2 stages x 128 fp32
 constexpr int OFF_BAR = OFF_DEL + 2 * 128 * 4;
 constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
@@ -63,6 +65,8 @@ constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ =
 constexpr uint32_t kIdescNN = make_idesc_bf16(128, 128, false, false);  // S^T, dP^T
 constexpr uint32_t kIdescKM = make_idesc_bf16(128, 64, false, true);    // dV, dK
 constexpr uint32_t kIdescMM = make_idesc_bf16(128, 64, true, true);     // dQ
+
+constexpr int kPostRows = 16;  // rows per CTA of the dQ postprocess
 
 }  // namespace bwd
 
@@ -106,11 +110,12 @@ __global__ void __launch_bounds__(256)
 // ---------------------------------------------------------------------------
 // 2. main kernel
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(bwd::kThreads, 1)
+__global__ void __launch_bounds__(448, 1)
     ne_attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
-                       const __grid_constant__ CUtensorMap tmDO, const BwdParams p) {
+                       const __grid_constant__ CUtensorMap tmDO,
+                       const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   using namespace bwd;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -141,8 +146,8 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       mbar_init(&bars[B_QDO_EMPTY + s], 1);
     }
     mbar_init(&bars[B_S_FULL], 1);
-    mbar_init(&bars[B_S_FREE], 128);
-    mbar_init(&bars[B_DS_FULL], 128);
+    mbar_init(&bars[B_S_FREE], 256);
+    mbar_init(&bars[B_DS_FULL], 256);
     mbar_init(&bars[B_PDS_FREE], 1);
     mbar_init(&bars[B_DQ_FULL], 1);
     mbar_init(&bars[B_DQ_FREE], 128);
@@ -150,7 +155,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     *abort_flag = 0;
     mbar_fence_init();
   }
-  if (warp == 8) {
+  if (warp == 12) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
@@ -165,10 +170,11 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
   uint8_t* sDO = smem + OFF_DO;
   uint8_t* sPT = smem + OFF_PT;
   uint8_t* sDST = smem + OFF_DST;
+  uint8_t* sDQ = smem + OFF_DQ;
   float* sLSE = reinterpret_cast<float*>(smem + OFF_LSE);
   float* sDEL = reinterpret_cast<float*>(smem + OFF_DEL);
 
-  if (warp == 9) {
+  if (warp == 13) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
@@ -201,7 +207,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
           }
       }
     }
-  } else if (warp == 8) {
+  } else if (warp == 12) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
@@ -268,31 +274,87 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       }
     }
   } else if (warp < 4) {
-    // ------------------------------------------------- RoPE + LSE/D staging
-    const int r = threadIdx.x;
-    if (mbar_wait(&bars[B_KV_FULL], 0, abort_flag, p.status, 37)) {
-      rope_rotate_row(sK, r, kt * kBN + r, p.rope);
+    // ------------------------------------- RoPE, LSE/D staging, dQ' reduction
+    const int r = threadIdx.x;  // 0..127: tile row (key row for K, query row otherwise)
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    RopeRow tab;
+    rope_load_row(p.rope, kt * kBN + r, tab);
+    // LSE (log2 units) and D of query row r of tile `it`; rows past the
+    // sequence get LSE = +inf, hence P = 0.
+    auto load_rowstats = [&](int it, float& l2, float& dl) {
+      const int qpos = (kt + it) * kBM + r;
+      l2 = INFINITY;
+      dl = 0.f;
+      if (qpos < len) {
+        l2 = __ldg(p.lse + lse_index(p.pb, h, seq, start, qpos)) * 1.4426950408889634f;
+        dl = __ldg(p.delta + static_cast<long long>(h) * p.pb.n_tot + start + qpos);
+      }
+    };
+    // dQ'_it: TMEM -> swizzled fp32 staging -> two bulk reduce-adds (32 columns each).
+    auto reduce_dq = [&](int it) -> bool {
+      if (!mbar_wait_warp(&bars[B_DQ_FULL], it & 1, abort_flag, p.status, 43)) return false;
+      tc_fence_after();
+      uint32_t a[64];
+      tmem_ld_x32(tmem + lane_base + kColDQ, a);
+      tmem_ld_x32(tmem + lane_base + kColDQ + 32, a + 32);
+      tmem_ld_wait(a);
+      tmem_ld_wait(a + 32);
+      tc_fence_before();
+      mbar_arrive(&bars[B_DQ_FREE]);
+      if (r == 0) bulk_wait_group_read0();  // previous reduction has read the staging
+      named_bar_sync(1, 128);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        *reinterpret_cast<uint4*>(sDQ + sw128_offset(r, c)) =
+            make_uint4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
+        *reinterpret_cast<uint4*>(sDQ + kTileBytes + sw128_offset(r, c)) =
+            make_uint4(a[32 + 4 * c], a[33 + 4 * c], a[34 + 4 * c], a[35 + 4 * c]);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (r == 0) {
+        const int qrow = start + (kt + it) * kBM;
+        tma_reduce_add_3d(&tmDQ, sDQ, 0, h, qrow);
+        tma_reduce_add_3d(&tmDQ, sDQ + kTileBytes, 32, h, qrow);
+        bulk_commit_group();
+      }
+      return true;
+    };
+    bool ok = mbar_wait(&bars[B_KV_FULL], 0, abort_flag, p.status, 37);
+    if (ok) {
+      rope_rotate_row(sK, r, tab);
       fence_proxy_async_smem();
       mbar_arrive(&bars[B_K_ROT]);
+      float l2, dl;
+      rope_load_row(p.rope, kt * kBM + r, tab);
+      load_rowstats(0, l2, dl);
       for (int it = 0; it < n_it; ++it) {
         const int s = it & 1;
-        if (!mbar_wait(&bars[B_QDO_FULL + s], (it >> 1) & 1, abort_flag, p.status, 38)) break;
-        const int qpos = (kt + it) * kBM + r;
-        rope_rotate_row(sQ + s * kTileBytes, r, qpos, p.rope);
-        float l2 = INFINITY, dl = 0.f;  // query rows past the sequence get P = 0
-        if (qpos < len) {
-          l2 = __ldg(p.lse + lse_index(p.pb, h, seq, start, qpos)) * 1.4426950408889634f;
-          dl = __ldg(p.delta + static_cast<long long>(h) * p.pb.n_tot + start + qpos);
+        if (!mbar_wait(&bars[B_QDO_FULL + s], (it >> 1) & 1, abort_flag, p.status, 38)) {
+          ok = false;
+          break;
         }
+        rope_rotate_row(sQ + s * kTileBytes, r, tab);
         sLSE[s * 128 + r] = l2;
         sDEL[s * 128 + r] = dl;
         fence_proxy_async_smem();
         mbar_arrive(&bars[B_Q_ROT + s]);
+        if (it >= 1 && !reduce_dq(it - 1)) {
+          ok = false;
+          break;
+        }
+        if (it + 1 < n_it) {  // prefetch the next tile's table rows and row terms
+          rope_load_row(p.rope, (kt + it + 1) * kBM + r, tab);
+          load_rowstats(it + 1, l2, dl);
+        }
       }
+      if (ok) reduce_dq(n_it - 1);
     }
-  } else if (warp < 8) {
+    if (r == 0) bulk_wait_group0();
+  } else if (warp < 12) {
     // --------------------------------------------------------- softmax warps
-    const int wq = warp - 4;
+    const int half = (warp - 4) >> 2;  // query columns 64*half .. 64*half+63
+    const int wq = warp & 3;
     const int r = wq * 32 + lane;  // key row in tile
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     bool ok = true;
@@ -314,13 +376,14 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       const float* lse2 = sLSE + s * 128;
       const float* del = sDEL + s * 128;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {  // 32 query columns at a time
+      for (int cc = 0; cc < 2; ++cc) {  // 32 query columns at a time
+        const int c = 2 * half + cc;
         uint32_t sr[32], dpr[32];
         tmem_ld_x32(tmem + lane_base + kColS + c * 32, sr);
         tmem_ld_x32(tmem + lane_base + kColDP + c * 32, dpr);
         tmem_ld_wait(sr);
         tmem_ld_wait(dpr);
-        if (c == 3) {
+        if (cc == 1) {
           tc_fence_before();
           mbar_arrive(&bars[B_S_FREE]);
         }
@@ -340,10 +403,9 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
           dw[e / 2] = pack_bf16x2(dsv[0], dsv[1]);
         }
         // Row r, columns c*32 .. c*32+31: block c/2, 16-byte chunks (c%2)*4 .. +3.
-        const int blk = c >> 1;
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
-          const uint32_t off = blk * kTileBytes + sw128_offset(r, (c & 1) * 4 + k4);
+          const uint32_t off = half * kTileBytes + sw128_offset(r, (c & 1) * 4 + k4);
           *reinterpret_cast<uint4*>(sPT + off) =
               make_uint4(pw[4 * k4], pw[4 * k4 + 1], pw[4 * k4 + 2], pw[4 * k4 + 3]);
           *reinterpret_cast<uint4*>(sDST + off) =
@@ -353,79 +415,47 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       fence_proxy_async_smem();
       mbar_arrive(&bars[B_DS_FULL]);
     }
-    // ---- epilogue: dV and dK = scale * R^T dK' for keys inside the sequence
+    // ---- epilogue: dV (first half) and dK = scale * R^T dK' (second half) --
     if (ok && mbar_wait_warp(&bars[B_MMA_DONE], 0, abort_flag, p.status, 42)) {
       tc_fence_after();
-      uint32_t dvr[64], dkr[64];
-      tmem_ld_x32(tmem + lane_base + kColDV, dvr);
-      tmem_ld_x32(tmem + lane_base + kColDV + 32, dvr + 32);
-      tmem_ld_wait(dvr);
-      tmem_ld_wait(dvr + 32);
-      tmem_ld_x32(tmem + lane_base + kColDK, dkr);
-      tmem_ld_x32(tmem + lane_base + kColDK + 32, dkr + 32);
-      tmem_ld_wait(dkr);
-      tmem_ld_wait(dkr + 32);
+      uint32_t g[64];
+      const uint32_t col = half ? kColDK : kColDV;
+      tmem_ld_x32(tmem + lane_base + col, g);
+      tmem_ld_x32(tmem + lane_base + col + 32, g + 32);
+      tmem_ld_wait(g);
+      tmem_ld_wait(g + 32);
       const int kpos = kt * kBN + r;
       if (kpos < len) {
         const long long orow = (static_cast<long long>(start + kpos) * H + h) * kHD;
-        uint4* dvd = reinterpret_cast<uint4*>(p.dv + orow);
+        float v[64];
+        if (half == 0) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          dvd[c] = make_uint4(
-              pack_bf16x2(__uint_as_float(dvr[8 * c + 0]), __uint_as_float(dvr[8 * c + 1])),
-              pack_bf16x2(__uint_as_float(dvr[8 * c + 2]), __uint_as_float(dvr[8 * c + 3])),
-              pack_bf16x2(__uint_as_float(dvr[8 * c + 4]), __uint_as_float(dvr[8 * c + 5])),
-              pack_bf16x2(__uint_as_float(dvr[8 * c + 6]), __uint_as_float(dvr[8 * c + 7])));
-        const float2* cs = p.rope.cs + static_cast<long long>(kpos) * 32;
-        float g[64];
+          for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(g[i]);
+        } else {
+          const float2* cs = p.rope.cs + static_cast<long long>(kpos) * 32;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float2 t = __ldg(cs + i);
-          const float a = __uint_as_float(dkr[i]) * p.scale;
-          const float b = __uint_as_float(dkr[i + 32]) * p.scale;
-          g[i] = a * t.x + b * t.y;
-          g[i + 32] = b * t.x - a * t.y;
+          for (int i = 0; i < 32; ++i) {
+            const float2 t = __ldg(cs + i);
+            const float a = __uint_as_float(g[i]) * p.scale;
+            const float b = __uint_as_float(g[i + 32]) * p.scale;
+            v[i] = a * t.x + b * t.y;
+            v[i + 32] = b * t.x - a * t.y;
+          }
         }
-        uint4* dkd = reinterpret_cast<uint4*>(p.dk + orow);
+        uint4* dst = reinterpret_cast<uint4*>((half ? p.dk : p.dv) + orow);
 #pragma unroll
         for (int c = 0; c < 8; ++c)
-          dkd[c] = make_uint4(pack_bf16x2(g[8 * c + 0], g[8 * c + 1]),
-                              pack_bf16x2(g[8 * c + 2], g[8 * c + 3]),
-                              pack_bf16x2(g[8 * c + 4], g[8 * c + 5]),
-                              pack_bf16x2(g[8 * c + 6], g[8 * c + 7]));
-      }
-    }
-  } else {
-    // -------------------------------------------------- dQ' accumulation
-    const int wq = warp & 3;  // warps 10,11,12,13 -> TMEM lane quarters 2,3,0,1
-    const int r = wq * 32 + lane;  // query row in tile
-    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-    for (int it = 0; it < n_it; ++it) {
-      if (!mbar_wait_warp(&bars[B_DQ_FULL], it & 1, abort_flag, p.status, 43)) break;
-      tc_fence_after();
-      uint32_t a[64];
-      tmem_ld_x32(tmem + lane_base + kColDQ, a);
-      tmem_ld_x32(tmem + lane_base + kColDQ + 32, a + 32);
-      tmem_ld_wait(a);
-      tmem_ld_wait(a + 32);
-      tc_fence_before();
-      mbar_arrive(&bars[B_DQ_FREE]);
-      const int qpos = (kt + it) * kBM + r;
-      if (qpos < len) {
-        float* dst = p.dq_acc + (static_cast<long long>(start + qpos) * H + h) * kHD;
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 4 * c),
-                       "f"(__uint_as_float(a[4 * c])), "f"(__uint_as_float(a[4 * c + 1])),
-                       "f"(__uint_as_float(a[4 * c + 2])), "f"(__uint_as_float(a[4 * c + 3]))
-                       : "memory");
+          dst[c] = make_uint4(pack_bf16x2(v[8 * c + 0], v[8 * c + 1]),
+                              pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
+                              pack_bf16x2(v[8 * c + 4], v[8 * c + 5]),
+                              pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
       }
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == 12) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -433,9 +463,9 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// 3. postprocess: dq = bf16(scale * R(m)^T dq_acc).  Grid (tiles, sequences);
-//    4 threads per (row, head): thread part c rotates chunk c (dims 8c..8c+7)
-//    against chunk c + 4.
+// 3. postprocess: dq = bf16(scale * R(m)^T dq_acc).  Grid (row blocks of
+//    kPostRows, sequences); 4 threads per (row, head): thread part c rotates
+//    chunk c (dims 8c..8c+7) against chunk c + 4.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256)
     ne_attn_dq_postprocess_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq,
@@ -443,10 +473,10 @@ __global__ void __launch_bounds__(256)
   const int seq = blockIdx.y;
   int start, len;
   if (!seq_bounds(pb, seq, start, len, nullptr)) return;
-  const int t0 = blockIdx.x * kBM;
+  const int t0 = blockIdx.x * bwd::kPostRows;
   if (t0 >= len) return;
   const int H = pb.H;
-  const int rows = min(kBM, len - t0);
+  const int rows = min(bwd::kPostRows, len - t0);
   const int items = rows * H * 4;
   for (int w = threadIdx.x; w < items; w += blockDim.x) {
     const int part = w & 3;
@@ -479,8 +509,8 @@ __global__ void __launch_bounds__(256)
 }
 
 cudaError_t launch_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                       const CUtensorMap& tmDO, const BwdParams& p, int n_tiles,
-                       cudaStream_t stream) {
+                       const CUtensorMap& tmDO, const CUtensorMap& tmDQ, const BwdParams& p,
+                       int n_tiles, cudaStream_t stream, cudaEvent_t ev_pre, cudaEvent_t ev_main) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(ne_attn_bwd_kernel,
@@ -496,11 +526,14 @@ cudaError_t launch_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
                                                             n_pairs, p.pb.H, p.pb.n_tot);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (ev_pre && (e = cudaEventRecord(ev_pre, stream)) != cudaSuccess) return e;
   dim3 grid(p.pb.nseq * p.pb.H, n_tiles);
-  ne_attn_bwd_kernel<<<grid, bwd::kThreads, bwd::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, tmDO, p);
+  ne_attn_bwd_kernel<<<grid, bwd::kThreads, bwd::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, tmDO, tmDQ,
+                                                                       p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dim3 pgrid(n_tiles, p.pb.nseq);
+  if (ev_main && (e = cudaEventRecord(ev_main, stream)) != cudaSuccess) return e;
+  dim3 pgrid((n_tiles * kBM + bwd::kPostRows - 1) / bwd::kPostRows, p.pb.nseq);
   ne_attn_dq_postprocess_kernel<<<pgrid, 256, 0, stream>>>(p.dq_acc, p.dq, p.pb, p.rope, p.scale);
   return cudaGetLastError();
 }

@@ -29,7 +29,11 @@ __global__ void __launch_bounds__(128, 1)
   }
   if (!mbar_wait(bar, 0, abort_flag, status, 20)) return;
   const int r = threadIdx.x;
-  if (rotate) rope_rotate_row(smem, r, pos0 + r, rope);
+  if (rotate) {
+    RopeRow tab;
+    rope_load_row(rope, pos0 + r, tab);
+    rope_rotate_row(smem, r, tab);
+  }
   __syncthreads();
   if (dst_raw) {
     const uint4* s = reinterpret_cast<const uint4*>(smem);

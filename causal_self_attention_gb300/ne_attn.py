@@ -25,7 +25,8 @@ STATUS_NAMES = {0: "NE_OK", 1: "NE_ERR_INVALID_ARG", 2: "NE_ERR_UNSUPPORTED",
 
 EXPORTED = ("ne_attn_fwd", "ne_attn_fwd_f32out", "ne_attn_bwd", "ne_attn_bwd_workspace_bytes",
             "ne_attn_varlen_fwd", "ne_attn_varlen_fwd_f32out", "ne_attn_varlen_bwd",
-            "ne_attn_get_device_status", "ne_attn_last_device_code", "ne_status_string",
+            "ne_attn_set_bwd_phase_events", "ne_attn_get_device_status",
+            "ne_attn_last_device_code", "ne_status_string",
             "ne_attn_release", "ne_debug_tma_tile", "ne_debug_rope_tile", "ne_debug_umma")
 
 
@@ -57,6 +58,7 @@ def lib():
         "ne_attn_varlen_fwd": [P, P, P, P, I, I, I, I, I, F, F, P, P, P],
         "ne_attn_varlen_fwd_f32out": [P, P, P, P, I, I, I, I, I, F, F, P, P, P],
         "ne_attn_varlen_bwd": [P, P, P, P, P, P, P, I, I, I, I, I, F, F, P, P, P, P, Z, P],
+        "ne_attn_set_bwd_phase_events": [P, P],
         "ne_attn_get_device_status": [P],
         "ne_attn_last_device_code": [],
         "ne_attn_release": [],
@@ -184,6 +186,14 @@ def ne_attn_varlen_bwd(q, k, v, out, dout, lse, cu_seqlens, max_seqlen, rope_bas
         cu_seqlens.numel() - 1, N, int(max_seqlen), H, D, float(rope_base), float(scale),
         _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), ws_bytes, _stream(stream)))
     return dq, dk, dv
+
+
+def ne_attn_set_bwd_phase_events(ev_after_preprocess=None, ev_after_main=None) -> None:
+    """Record the given torch.cuda.Event objects after the backward's
+    preprocess and main kernels of every following backward call (None: off)."""
+    a = ctypes.c_void_p(ev_after_preprocess.cuda_event) if ev_after_preprocess else None
+    b = ctypes.c_void_p(ev_after_main.cuda_event) if ev_after_main else None
+    _check("ne_attn_set_bwd_phase_events", lib().ne_attn_set_bwd_phase_events(a, b))
 
 
 def ne_attn_get_device_status(stream=None) -> int:

@@ -121,6 +121,14 @@ ne_status ne_attn_varlen_bwd(const ne_bf16* q, const ne_bf16* k, const ne_bf16* 
                              int D, float rope_base, float scale, ne_bf16* dq, ne_bf16* dk,
                              ne_bf16* dv, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Timing hook for profilers and benchmarks.  When set (non-NULL cudaEvent_t
+ * handles created by the caller on the current device), every following
+ * ne_attn_bwd / ne_attn_varlen_bwd call records ev_after_preprocess right
+ * after its preprocess kernel and ev_after_main right after its main kernel,
+ * on the call's stream, so the three backward kernels can be timed apart.
+ * Pass NULL, NULL to turn it off.  Process-wide; not for concurrent callers. */
+ne_status ne_attn_set_bwd_phase_events(void* ev_after_preprocess, void* ev_after_main);
+
 /* Synchronize `stream`, then return and clear the device status word of the
  * current device: NE_OK, NE_ERR_TIMEOUT or NE_ERR_BAD_SEQLEN (or NE_ERR_CUDA
  * if the synchronization itself failed). */
