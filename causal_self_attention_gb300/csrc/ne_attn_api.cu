@@ -11,8 +11,8 @@
 
 #include <cudaTypedefs.h>
 
-#include "../../include/ne_attn.h"
-#include "../../include/ne_attn_debug.h"
+#include "ne_attn.h"
+#include "ne_attn_debug.h"
 #include "ne_common.cuh"
 
 namespace ne {

@@ -28,25 +28,28 @@ namespace ne {
 namespace fwd {
 
 constexpr int kThreads = 448;
-constexpr int kStages = 3;
+constexpr int kStages = 2;                            // K ring and V ring
 constexpr int OFF_Q = 0;                              // Q_A, Q_B
 constexpr int OFF_K = OFF_Q + 2 * kTileBytes;         // kStages
 constexpr int OFF_V = OFF_K + kStages * kTileBytes;   // kStages
-constexpr int OFF_P = OFF_V + kStages * kTileBytes;   // P_A, P_B: 2 x (2 x 16 KiB)
-constexpr int OFF_BAR = OFF_P + 4 * kTileBytes;
+constexpr int OFF_P = OFF_V + kStages * kTileBytes;   // P_X[2]: 4 buffers x (2 x 16 KiB)
+constexpr int OFF_BAR = OFF_P + 8 * kTileBytes;
 constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;      // + slack for 1024-byte alignment
 
 enum Bar {
   B_Q_FULL = 0,
   B_Q_ROT,
-  B_KV_FULL,                          // kStages
-  B_K_ROT = B_KV_FULL + kStages,      // kStages
-  B_KV_EMPTY = B_K_ROT + kStages,     // kStages
-  B_S_FULL = B_KV_EMPTY + kStages,    // per tile X
+  B_K_FULL,                           // kStages
+  B_K_ROT = B_K_FULL + kStages,       // kStages
+  B_K_EMPTY = B_K_ROT + kStages,      // kStages
+  B_V_FULL = B_K_EMPTY + kStages,     // kStages
+  B_V_EMPTY = B_V_FULL + kStages,     // kStages
+  B_S_FULL = B_V_EMPTY + kStages,     // per tile X
   B_S_FREE = B_S_FULL + 2,
-  B_P_FULL = B_S_FREE + 2,
-  B_PV_DONE = B_P_FULL + 2,
-  B_MMA_DONE = B_PV_DONE + 2,
+  B_P_FULL = B_S_FREE + 2,            // per tile X and P buffer: 2 * X + (j & 1)
+  B_PV_DONE = B_P_FULL + 4,
+  B_O_FINAL = B_PV_DONE + 2,         // once per tile: its last P V completed
+  B_MMA_DONE = B_O_FINAL + 2,
   B_COUNT
 };
 
@@ -57,9 +60,70 @@ constexpr uint32_t kColO = 256;  // O_X at 256 + 64 * X
 constexpr uint32_t kIdescS = make_idesc_bf16(128, 128, false, false);  // Q K^T
 constexpr uint32_t kIdescO = make_idesc_bf16(128, 64, false, true);    // P V (V MN-major)
 
+// Row max (log2 units) of one S row held in TMEM, masked on the diagonal.
+// The row is read in 16-column chunks, the next chunk's load in flight while
+// the current one is processed.
+__device__ __forceinline__ float row_max(uint32_t tS, float sl2, bool is_diag, int r) {
+  uint32_t a[16], b[16];
+  float mx = -INFINITY;
+  tmem_ld_x16(tS, a);
+  tmem_ld_wait16(a);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint32_t* cur = (c & 1) ? b : a;
+    uint32_t* nxt = (c & 1) ? a : b;
+    if (c < 7) tmem_ld_x16(tS + 16 * (c + 1), nxt);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const float v = (is_diag && 16 * c + e > r) ? -INFINITY : __uint_as_float(cur[e]) * sl2;
+      mx = fmaxf(mx, v);
+    }
+    if (c < 7) tmem_ld_wait16(nxt);
+  }
+  return mx;
+}
+
+// P = 2^(scale*log2e*S - m) for one row: bf16 to the swizzled K-major P
+// buffer, returns the fp32 row sum; `mx` receives the masked row max seen.
+__device__ __forceinline__ float row_exp(uint32_t tS, float sl2, float m, bool is_diag, int r,
+                                         uint8_t* pbuf, float& mx) {
+  uint32_t a[16], b[16];
+  float rs = 0.f;
+  mx = -INFINITY;
+  tmem_ld_x16(tS, a);
+  tmem_ld_wait16(a);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint32_t* cur = (c & 1) ? b : a;
+    uint32_t* nxt = (c & 1) ? a : b;
+    if (c < 7) tmem_ld_x16(tS + 16 * (c + 1), nxt);
+    uint32_t pw[8];
+#pragma unroll
+    for (int e = 0; e < 16; e += 2) {
+      float v0 = __uint_as_float(cur[e]) * sl2;
+      float v1 = __uint_as_float(cur[e + 1]) * sl2;
+      if (is_diag && 16 * c + e > r) v0 = -INFINITY;
+      if (is_diag && 16 * c + e + 1 > r) v1 = -INFINITY;
+      mx = fmaxf(mx, fmaxf(v0, v1));
+      const float p0 = ex2_approx(v0 - m);
+      const float p1 = ex2_approx(v1 - m);
+      rs += p0 + p1;
+      pw[e / 2] = pack_bf16x2(p0, p1);
+    }
+    // Columns 16c .. 16c+15: block c/4, 16-byte chunks 2(c%4), 2(c%4)+1.
+    uint8_t* blk = pbuf + (c >> 2) * kTileBytes;
+    *reinterpret_cast<uint4*>(blk + sw128_offset(r, 2 * (c & 3))) =
+        make_uint4(pw[0], pw[1], pw[2], pw[3]);
+    *reinterpret_cast<uint4*>(blk + sw128_offset(r, 2 * (c & 3) + 1)) =
+        make_uint4(pw[4], pw[5], pw[6], pw[7]);
+    if (c < 7) tmem_ld_wait16(nxt);
+  }
+  return rs;
+}
+
 }  // namespace fwd
 
-__global__ void __launch_bounds__(448, 1)
+__global__ void __launch_bounds__(fwd::kThreads, 1)
     ne_attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -93,15 +157,19 @@ __global__ void __launch_bounds__(448, 1)
     mbar_init(&bars[B_Q_FULL], 1);
     mbar_init(&bars[B_Q_ROT], 128);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars[B_KV_FULL + s], 1);
+      mbar_init(&bars[B_K_FULL + s], 1);
       mbar_init(&bars[B_K_ROT + s], 128);
-      mbar_init(&bars[B_KV_EMPTY + s], 1);
+      mbar_init(&bars[B_K_EMPTY + s], 1);
+      mbar_init(&bars[B_V_FULL + s], 1);
+      mbar_init(&bars[B_V_EMPTY + s], 1);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars[B_S_FULL + x], 1);
       mbar_init(&bars[B_S_FREE + x], 128);
-      mbar_init(&bars[B_P_FULL + x], 128);
+      mbar_init(&bars[B_P_FULL + 2 * x], 128);
+      mbar_init(&bars[B_P_FULL + 2 * x + 1], 128);
       mbar_init(&bars[B_PV_DONE + x], 1);
+      mbar_init(&bars[B_O_FINAL + x], 1);
     }
     mbar_init(&bars[B_MMA_DONE], 1);
     *abort_flag = 0;
@@ -122,33 +190,37 @@ __global__ void __launch_bounds__(448, 1)
   uint8_t* sP = smem + OFF_P;
 
   if (warp == 13) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(&bars[B_Q_FULL], 2 * kTileBytes);
-      tma_load_3d(sQ, &tmQ, &bars[B_Q_FULL], 0, h, start + rowA);
-      tma_load_3d(sQ + kTileBytes, &tmQ, &bars[B_Q_FULL], 0, h, start + rowA + kBM);
-      int last_issued[kStages];
-      for (int s = 0; s < kStages; ++s) last_issued[s] = -1;
+    // ---------------------------------------- TMA producers: lane 0 K, lane 1 V
+    if (lane < 2) {
+      const bool isK = (lane == 0);
+      const CUtensorMap* tm = isK ? &tmK : &tmV;
+      uint8_t* ring = isK ? sK : sV;
+      uint64_t* full = &bars[isK ? B_K_FULL : B_V_FULL];
+      uint64_t* empty = &bars[isK ? B_K_EMPTY : B_V_EMPTY];
+      tma_prefetch_desc(tm);
+      if (isK) {
+        tma_prefetch_desc(&tmQ);
+        mbar_arrive_expect_tx(&bars[B_Q_FULL], 2 * kTileBytes);
+        tma_load_3d(sQ, &tmQ, &bars[B_Q_FULL], 0, h, start + rowA);
+        tma_load_3d(sQ + kTileBytes, &tmQ, &bars[B_Q_FULL], 0, h, start + rowA + kBM);
+      }
+      int last_issued[kStages] = {-1, -1};
       for (int j = 0; j < nkv; ++j) {
         const int s = j % kStages;
         if (j >= kStages &&
-            !mbar_wait(&bars[B_KV_EMPTY + s], ((j - kStages) / kStages) & 1, abort_flag, p.status, 1))
+            !mbar_wait(&empty[s], ((j - kStages) / kStages) & 1, abort_flag, p.status, isK ? 1 : 12))
           break;
-        mbar_arrive_expect_tx(&bars[B_KV_FULL + s], 2 * kTileBytes);
-        tma_load_3d(sK + s * kTileBytes, &tmK, &bars[B_KV_FULL + s], 0, h, start + j * kBN);
-        tma_load_3d(sV + s * kTileBytes, &tmV, &bars[B_KV_FULL + s], 0, h, start + j * kBN);
+        mbar_arrive_expect_tx(&full[s], kTileBytes);
+        tma_load_3d(ring + s * kTileBytes, tm, &full[s], 0, h, start + j * kBN);
         last_issued[s] = j;
       }
       if (*abort_flag) {
         // Let the copies still in flight land before the CTA exits.
-        mbar_wait(&bars[B_Q_FULL], 0, abort_flag, nullptr, 0);
+        if (isK) mbar_wait(&bars[B_Q_FULL], 0, abort_flag, nullptr, 0);
         for (int s = 0; s < kStages; ++s)
           if (last_issued[s] >= 0) {
             const long long t0 = clock64();
-            while (!mbar_try_wait(&bars[B_KV_FULL + s], (last_issued[s] / kStages) & 1) &&
+            while (!mbar_try_wait(&full[s], (last_issued[s] / kStages) & 1) &&
                    clock64() - t0 < NE_WAIT_LIMIT_CYCLES) {
             }
           }
@@ -182,19 +254,26 @@ __global__ void __launch_bounds__(448, 1)
             umma_commit(&bars[B_S_FULL + x]);
           }
           if (!ok) break;
+          umma_commit(&bars[B_K_EMPTY + s]);
         }
         if (j >= 1) {
           const int jj = j - 1;
           const int s = jj % kStages;
+          if (!mbar_wait(&bars[B_V_FULL + s], (jj / kStages) & 1, abort_flag, p.status, 13)) {
+            ok = false;
+            break;
+          }
           const uint32_t aV = smem_u32(sV + s * kTileBytes);
           for (int x = 0; x < 2 && ok; ++x) {
             if (jj >= nkvX[x]) continue;
-            if (!mbar_wait(&bars[B_P_FULL + x], jj & 1, abort_flag, p.status, 5)) {
+            // One barrier per P buffer: the softmax may already have filled the
+            // other buffer, but it cannot refill this one before this P V is issued.
+            if (!mbar_wait(&bars[B_P_FULL + 2 * x + (jj & 1)], (jj >> 1) & 1, abort_flag, p.status, 5)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t aP = smem_u32(sP + x * 2 * kTileBytes);
+            const uint32_t aP = smem_u32(sP + (2 * x + (jj & 1)) * 2 * kTileBytes);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)  // K = 128 keys in steps of 16
               umma_bf16_ss(tmem + kColO + 64 * x,
@@ -202,9 +281,10 @@ __global__ void __launch_bounds__(448, 1)
                            make_sdesc_sw128(aV + kk * 2048, kTileBytes, 1024), kIdescO,
                            (jj > 0 || kk > 0) ? 1u : 0u);
             umma_commit(&bars[B_PV_DONE + x]);
+            if (jj == nkvX[x] - 1) umma_commit(&bars[B_O_FINAL + x]);
           }
           if (!ok) break;
-          umma_commit(&bars[B_KV_EMPTY + s]);
+          umma_commit(&bars[B_V_EMPTY + s]);
         }
       }
       // Drain: every MMA issued above completes before TMEM is released.
@@ -227,7 +307,7 @@ __global__ void __launch_bounds__(448, 1)
       rope_load_row(p.rope, r, tab);
       for (int j = 0; j < nkv; ++j) {
         const int s = j % kStages;
-        if (!mbar_wait(&bars[B_KV_FULL + s], (j / kStages) & 1, abort_flag, p.status, 7)) break;
+        if (!mbar_wait(&bars[B_K_FULL + s], (j / kStages) & 1, abort_flag, p.status, 7)) break;
         rope_rotate_row(sK + s * kTileBytes, r, tab);
         fence_proxy_async_smem();
         mbar_arrive(&bars[B_K_ROT + s]);
@@ -239,14 +319,12 @@ __global__ void __launch_bounds__(448, 1)
     const int x = warp >> 2;            // tile A (0) or B (1)
     const int wq = warp & 3;            // TMEM lane quarter
     const int r = wq * 32 + lane;       // row in tile
-    const int rowX = rowA + x * kBM;
-    const int qpos = rowX + r;          // position in sequence
+    const int qpos = rowA + x * kBM + r;  // position in sequence
     const int nkv_x = x ? nkvB : nkvA;
     const int diag = x ? 2 * blk + 1 : 2 * blk;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_base + kColS + 128 * x;
     const uint32_t tO = tmem + lane_base + kColO + 64 * x;
-    uint8_t* pbuf = sP + x * 2 * kTileBytes;
     const float sl2 = p.scale_log2;
     float m_ref = -INFINITY;  // reference max (log2 units) the P values are taken against
     float l_sum = 0.f;
@@ -258,80 +336,51 @@ __global__ void __launch_bounds__(448, 1)
       }
       tc_fence_after();
       const bool is_diag = (j == diag);
-      // Pass 1: row max of the scaled, masked scores.
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sr[32];
-        tmem_ld_x32(tS + 32 * c, sr);
-        tmem_ld_wait(sr);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float v = (is_diag && 32 * c + e > r) ? -INFINITY : __uint_as_float(sr[e]) * sl2;
-          mx = fmaxf(mx, v);
-        }
-      }
-      // Move the reference max only when the row max grows by more than 2^8.
-      const bool need = (mx > m_ref + 8.0f);
+      // The P buffer written here was last read by the P V of tile j-2, which
+      // completed before S_X(j) (tcgen05 operations complete in issue order).
+      uint8_t* pbuf = sP + (2 * x + (j & 1)) * 2 * kTileBytes;
+      float m_use = m_ref;
+      if (j == 0) m_use = row_max(tS, sl2, is_diag, r);  // first tile: no reference yet
+      float mx;
+      float rs = row_exp(tS, sl2, m_use, is_diag, r, pbuf, mx);
       float alpha = 1.f;
-      if (need) {
-        alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - mx);
-        m_ref = mx;
-      }
-      // P_X and O_X are in use by the previous tile's P V until it completes.
-      if (j >= 1) {
+      // Move the reference max only when the row max outgrows it by more than
+      // 2^8 (exact: O and l keep a common reference); then redo this tile's P.
+      const bool grow = (j > 0) && (mx > m_use + 8.0f);
+      if (__any_sync(0xffffffffu, grow)) {
+        const float m_new = grow ? mx : m_use;
+        float mx2;
+        rs = row_exp(tS, sl2, m_new, is_diag, r, pbuf, mx2);
+        alpha = ex2_approx(m_use - m_new);
+        m_use = m_new;
+        // O_X must be stable: wait for the P V of the previous tile.
         if (!mbar_wait_warp(&bars[B_PV_DONE + x], (j - 1) & 1, abort_flag, p.status, 9)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, need)) {
-          uint32_t o[32];
+        uint32_t o[32];
 #pragma unroll 1
-          for (int half = 0; half < 2; ++half) {
-            tmem_ld_x32(tO + half * 32, o);
-            tmem_ld_wait(o);
+        for (int half = 0; half < 2; ++half) {
+          tmem_ld_x32(tO + half * 32, o);
+          tmem_ld_wait(o);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-            tmem_st_x32(tO + half * 32, o);
-          }
-          tmem_st_wait();
+          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+          tmem_st_x32(tO + half * 32, o);
+          tmem_st_wait();  // the store has consumed `o` before it is reloaded
         }
       }
-      // Pass 2: P = 2^(x - m_ref) to smem (bf16, swizzled K-major), row sum.
-      float rs = 0.f;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sr[32];
-        tmem_ld_x32(tS + 32 * c, sr);
-        tmem_ld_wait(sr);
-        if (c == 3) {
-          tc_fence_before();
-          mbar_arrive(&bars[B_S_FREE + x]);  // S_X may be overwritten now
-        }
-        uint32_t pw[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float p0 = ex2_approx(__uint_as_float(sr[e]) * sl2 - m_ref);
-          float p1 = ex2_approx(__uint_as_float(sr[e + 1]) * sl2 - m_ref);
-          if (is_diag && 32 * c + e > r) p0 = 0.f;
-          if (is_diag && 32 * c + e + 1 > r) p1 = 0.f;
-          rs += p0 + p1;
-          pw[e / 2] = pack_bf16x2(p0, p1);
-        }
-#pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4)
-          *reinterpret_cast<uint4*>(pbuf + (c >> 1) * kTileBytes + sw128_offset(r, (c & 1) * 4 + k4)) =
-              make_uint4(pw[4 * k4], pw[4 * k4 + 1], pw[4 * k4 + 2], pw[4 * k4 + 3]);
-      }
+      tc_fence_before();
+      mbar_arrive(&bars[B_S_FREE + x]);  // S_X may be overwritten now
+      m_ref = m_use;
       l_sum = l_sum * alpha + rs;
       fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&bars[B_P_FULL + x]);
+      mbar_arrive(&bars[B_P_FULL + 2 * x + (j & 1)]);
     }
     // ---- epilogue: O / l and LSE for rows inside the sequence -------------
-    if (ok && nkv_x > 0 &&
-        mbar_wait_warp(&bars[B_PV_DONE + x], (nkv_x - 1) & 1, abort_flag, p.status, 11)) {
+    // (O_FINAL completes exactly once; PV_DONE may by now be more than one
+    // phase behind this thread, so its parity cannot be used here.)
+    if (ok && nkv_x > 0 && mbar_wait_warp(&bars[B_O_FINAL + x], 0, abort_flag, p.status, 11)) {
       tc_fence_after();
       uint32_t o[64];
       tmem_ld_x32(tO, o);

@@ -34,16 +34,13 @@ __device__ __forceinline__ void rope_load_row(const RopeTable& rt, int pos, Rope
 // Rotate one row (64 elements = 8 swizzled 16-byte chunks) of `tile` with the
 // table row `cs` of its position.
 __device__ __forceinline__ void rope_rotate_row(uint8_t* tile, int row, const RopeRow& cs) {
-  uint4 lo[4], hi[4];
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    lo[c] = *reinterpret_cast<const uint4*>(tile + sw128_offset(row, c));
-    hi[c] = *reinterpret_cast<const uint4*>(tile + sw128_offset(row, c + 4));
-  }
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    uint32_t wl[4] = {lo[c].x, lo[c].y, lo[c].z, lo[c].w};
-    uint32_t wh[4] = {hi[c].x, hi[c].y, hi[c].z, hi[c].w};
+    uint4* plo = reinterpret_cast<uint4*>(tile + sw128_offset(row, c));
+    uint4* phi = reinterpret_cast<uint4*>(tile + sw128_offset(row, c + 4));
+    const uint4 lo = *plo, hi = *phi;
+    uint32_t wl[4] = {lo.x, lo.y, lo.z, lo.w};
+    uint32_t wh[4] = {hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
       // Elements i = 8c + 2w and i + 1 (low and high half of the word).
@@ -57,13 +54,8 @@ __device__ __forceinline__ void rope_rotate_row(uint8_t* tile, int row, const Ro
       wl[w] = pack_bf16x2(lo0, lo1);
       wh[w] = pack_bf16x2(hi0, hi1);
     }
-    lo[c] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-    hi[c] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-  }
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    *reinterpret_cast<uint4*>(tile + sw128_offset(row, c)) = lo[c];
-    *reinterpret_cast<uint4*>(tile + sw128_offset(row, c + 4)) = hi[c];
+    *plo = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+    *phi = make_uint4(wh[0], wh[1], wh[2], wh[3]);
   }
 }
 
