@@ -201,7 +201,7 @@ ne_status run_fwd(const Shape& s, const void* q, const void* k, const void* v, f
   if (!q || !k || !v || !out || !lse) return NE_ERR_INVALID_ARG;
   ne_status rc = check_shape(s);
   if (rc != NE_OK) return rc;
-  if (!std::isfinite(scale) || !std::isfinite(rope_base) || rope_base <= 0.f)
+  if (!std::isfinite(scale) || scale <= 0.f || !std::isfinite(rope_base) || rope_base <= 0.f)
     return NE_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned4(lse))
     return NE_ERR_MISALIGNED;
@@ -233,7 +233,7 @@ ne_status run_bwd(const Shape& s, const void* q, const void* k, const void* v, c
   if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return NE_ERR_INVALID_ARG;
   ne_status rc = check_shape(s);
   if (rc != NE_OK) return rc;
-  if (!std::isfinite(scale) || !std::isfinite(rope_base) || rope_base <= 0.f)
+  if (!std::isfinite(scale) || scale <= 0.f || !std::isfinite(rope_base) || rope_base <= 0.f)
     return NE_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
       !aligned4(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
@@ -484,7 +484,7 @@ ne_status ne_debug_rope_tile(const ne_bf16* src, int n_rows, int H, int h, int r
 }
 
 ne_status ne_debug_umma(int form, const ne_bf16* a, const ne_bf16* b, float* d, void* stream) {
-  if (form < 0 || form > 2 || !a || !b || !d) return NE_ERR_INVALID_ARG;
+  if (form < 0 || form > 3 || !a || !b || !d) return NE_ERR_INVALID_ARG;
   if (!aligned16(a) || !aligned16(b) || !aligned16(d)) return NE_ERR_MISALIGNED;
   std::lock_guard<std::mutex> lock(g_mutex);
   DeviceState* st = nullptr;

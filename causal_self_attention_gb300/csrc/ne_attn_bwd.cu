@@ -8,21 +8,27 @@
 //      tiles i >= j, recomputing P from the saved LSE:
 //        S^T  = K' Q'^T,  P^T = exp(scale S^T - LSE),  dP^T = V dO^T,
 //        dS^T = P^T o (dP^T - D),
-//        dV  += P^T dO,   dK' += dS^T Q',   dQ'_i = dS K'  (-> TMA reduce-add),
+//        dV  += P^T dO (P^T from TMEM),  dK' += dS^T Q',  dQ'_i = dS K'
+//        (-> bulk tensor reduce-add),
 //      and at the end writes dV and dK = scale * R(n)^T dK' (bf16);
 //   3. postprocess: dQ = scale * R(m)^T dQ' (bf16).
 // q' = R(m) q and k' = R(n) k are rotated in shared memory right after their
 // TMA loads, as in the forward.
 //
-// Main-kernel warp roles (448 threads):
-//   warps 0-3   rotate + dQ': K_j once, every Q_i, LSE_i/D_i staging (table
-//               rows and LSE/D prefetched one tile ahead); then TMEM dQ'_i ->
-//               swizzled fp32 smem -> two bulk tensor reduce-adds into dQ'
+// Main-kernel warp roles (512 threads, registers re-split per warpgroup):
+//   warps 0-3   rotate + dQ': K_j once, every Q_i one tile ahead, LSE_i/D_i
+//               staging (table rows and LSE/D prefetched); TMEM dQ'_i ->
+//               swizzled fp32 smem (2 x 16 KiB) -> bulk tensor reduce-adds
 //   warps 4-7   softmax, query columns 0-63 of the tile (thread t: key row t)
-//   warps 8-11  softmax, query columns 64-127
+//   warps 8-11  softmax, query columns 64-127; a softmax thread reads its S^T
+//               and dP^T half-rows in one TMEM round trip and frees them at
+//               once, so the next tile's S^T/dP^T MMAs overlap its math; it
+//               writes P^T to TMEM (A operand of dV) and dS^T to smem
 //   warp 12     MMA: allocates TMEM; lane 0 issues the five MMAs per tile
 //   warp 13     TMA: lane 0 loads K_j, V_j once and Q_i, dO_i (2 stages)
-// TMEM columns: S^T 0-127, dP^T 128-255, dV 256-319, dK' 320-383, dQ' 384-447.
+//   warps 14-15 no role (complete the warpgroup for setmaxnreg)
+// TMEM columns: S^T 0-127, dP^T 128-255, dV 256-319, dK' 320-383, dQ' 384-447,
+// P^T 448-511 (bf16 pairs).
 #include "ne_rope.cuh"
 #include "ne_sm100.cuh"
 
@@ -30,26 +36,29 @@ namespace ne {
 
 namespace bwd {
 
-constexpr int kThreads = 448;
+constexpr int kThreads = 512;
+// Registers per thread of each warpgroup after setmaxnreg (launch: 128).
+constexpr uint32_t kRegsSoftmax = 160, kRegsRotate = 128, kRegsMma = 56;
+static_assert(valid_reg_split(kRegsSoftmax, kRegsRotate, kRegsMma), "register split");
+constexpr int kQStages = 3;                          // Q_i / dO_i ring depth
 constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + kTileBytes;
-constexpr int OFF_Q = OFF_V + kTileBytes;          // 2 stages
-constexpr int OFF_DO = OFF_Q + 2 * kTileBytes;     // 2 stages
-constexpr int OFF_PT = OFF_DO + 2 * kTileBytes;    // P^T: 2 blocks of 64 queries
-constexpr int OFF_DST = OFF_PT + 2 * kTileBytes;   // dS^T: same layout
-constexpr int OFF_DQ = OFF_DST + 2 * kTileBytes;   // dQ' staging: 2 x [128][32] fp32, SW128
-constexpr int OFF_LSE = OFF_DQ + 2 * kTileBytes;   // 2 stages x 128 fp32 (log2 units)
-constexpr int OFF_DEL = OFF_LSE + 2 * 128 * 4;     // 2 stages x 128 fp32
-constexpr int OFF_BAR = OFF_DEL + 2 * 128 * 4;
+constexpr int OFF_Q = OFF_V + kTileBytes;              // kQStages
+constexpr int OFF_DO = OFF_Q + kQStages * kTileBytes;  // kQStages
+constexpr int OFF_DST = OFF_DO + kQStages * kTileBytes;  // dS^T: 2 blocks of 64 queries
+constexpr int OFF_DQ = OFF_DST + 2 * kTileBytes;         // dQ' staging: 2 x [128][32] fp32, SW128
+constexpr int OFF_LSE = OFF_DQ + 2 * kTileBytes;         // kQStages x 128 fp32: -LSE (log2 units)
+constexpr int OFF_DEL = OFF_LSE + kQStages * 128 * 4;  // kQStages x 128 fp32: -D
+constexpr int OFF_BAR = OFF_DEL + kQStages * 128 * 4;
 constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
 
 enum Bar {
   B_KV_FULL = 0,
   B_K_ROT,
-  B_QDO_FULL,                     // 2
-  B_Q_ROT = B_QDO_FULL + 2,       // 2
-  B_QDO_EMPTY = B_Q_ROT + 2,      // 2
-  B_S_FULL = B_QDO_EMPTY + 2,
+  B_QDO_FULL,                            // kQStages
+  B_Q_ROT = B_QDO_FULL + kQStages,       // kQStages
+  B_QDO_EMPTY = B_Q_ROT + kQStages,      // kQStages
+  B_S_FULL = B_QDO_EMPTY + kQStages,
   B_S_FREE,
   B_DS_FULL,
   B_PDS_FREE,
@@ -60,7 +69,8 @@ enum Bar {
 };
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384;
+constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384,
+                   kColPT = 448;
 
 constexpr uint32_t kIdescNN = make_idesc_bf16(128, 128, false, false);  // S^T, dP^T
 constexpr uint32_t kIdescKM = make_idesc_bf16(128, 64, false, true);    // dV, dK
@@ -110,7 +120,7 @@ __global__ void __launch_bounds__(256)
 // ---------------------------------------------------------------------------
 // 2. main kernel
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(448, 1)
+__global__ void __launch_bounds__(512, 1)
     ne_attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
@@ -140,7 +150,7 @@ __global__ void __launch_bounds__(448, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bars[B_KV_FULL], 1);
     mbar_init(&bars[B_K_ROT], 128);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kQStages; ++s) {
       mbar_init(&bars[B_QDO_FULL + s], 1);
       mbar_init(&bars[B_Q_ROT + s], 128);
       mbar_init(&bars[B_QDO_EMPTY + s], 1);
@@ -168,7 +178,6 @@ __global__ void __launch_bounds__(448, 1)
   uint8_t* sV = smem + OFF_V;
   uint8_t* sQ = smem + OFF_Q;
   uint8_t* sDO = smem + OFF_DO;
-  uint8_t* sPT = smem + OFF_PT;
   uint8_t* sDST = smem + OFF_DST;
   uint8_t* sDQ = smem + OFF_DQ;
   float* sLSE = reinterpret_cast<float*>(smem + OFF_LSE);
@@ -176,6 +185,7 @@ __global__ void __launch_bounds__(448, 1)
 
   if (warp == 13) {
     // ------------------------------------------------------------ TMA producer
+    regs_decrease<kRegsMma>();
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
@@ -184,11 +194,12 @@ __global__ void __launch_bounds__(448, 1)
       mbar_arrive_expect_tx(&bars[B_KV_FULL], 2 * kTileBytes);
       tma_load_3d(sK, &tmK, &bars[B_KV_FULL], 0, h, start + kt * kBN);
       tma_load_3d(sV, &tmV, &bars[B_KV_FULL], 0, h, start + kt * kBN);
-      int last_issued[2] = {-1, -1};
+      int last_issued[kQStages] = {-1, -1, -1};
       for (int it = 0; it < n_it; ++it) {
-        const int s = it & 1;
-        if (it >= 2 &&
-            !mbar_wait(&bars[B_QDO_EMPTY + s], ((it - 2) >> 1) & 1, abort_flag, p.status, 31))
+        const int s = it % kQStages;
+        if (it >= kQStages &&
+            !mbar_wait(&bars[B_QDO_EMPTY + s], ((it - kQStages) / kQStages) & 1, abort_flag,
+                       p.status, 31))
           break;
         const int qrow = start + (kt + it) * kBM;
         mbar_arrive_expect_tx(&bars[B_QDO_FULL + s], 2 * kTileBytes);
@@ -198,10 +209,10 @@ __global__ void __launch_bounds__(448, 1)
       }
       if (*abort_flag) {
         mbar_wait(&bars[B_KV_FULL], 0, abort_flag, nullptr, 0);
-        for (int s = 0; s < 2; ++s)
+        for (int s = 0; s < kQStages; ++s)
           if (last_issued[s] >= 0) {
             const long long t0 = clock64();
-            while (!mbar_try_wait(&bars[B_QDO_FULL + s], (last_issued[s] >> 1) & 1) &&
+            while (!mbar_try_wait(&bars[B_QDO_FULL + s], (last_issued[s] / kQStages) & 1) &&
                    clock64() - t0 < NE_WAIT_LIMIT_CYCLES) {
             }
           }
@@ -209,14 +220,16 @@ __global__ void __launch_bounds__(448, 1)
     }
   } else if (warp == 12) {
     // ------------------------------------------------------------- MMA issuer
+    regs_decrease<kRegsMma>();
     if (lane == 0) {
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
-      const uint32_t aPT = smem_u32(sPT), aDST = smem_u32(sDST);
+      const uint32_t aDST = smem_u32(sDST);
       bool ok = mbar_wait(&bars[B_K_ROT], 0, abort_flag, p.status, 32);
       // S^T = K' Q'^T and dP^T = V dO^T for query tile `it`.
       auto issue_s_dp = [&](int it) -> bool {
-        const int s = it & 1;
-        if (!mbar_wait(&bars[B_Q_ROT + s], (it >> 1) & 1, abort_flag, p.status, 33)) return false;
+        const int s = it % kQStages;
+        if (!mbar_wait(&bars[B_Q_ROT + s], (it / kQStages) & 1, abort_flag, p.status, 33))
+          return false;
         if (it >= 1 && !mbar_wait(&bars[B_S_FREE], (it - 1) & 1, abort_flag, p.status, 34))
           return false;
         tc_fence_after();
@@ -234,16 +247,16 @@ __global__ void __launch_bounds__(448, 1)
       };
       if (ok) ok = issue_s_dp(0);
       for (int it = 0; ok && it < n_it; ++it) {
-        const int s = it & 1;
+        const int s = it % kQStages;
         if (it + 1 < n_it && !issue_s_dp(it + 1)) { ok = false; break; }
         if (!mbar_wait(&bars[B_DS_FULL], it & 1, abort_flag, p.status, 35)) { ok = false; break; }
         tc_fence_after();
         const uint32_t aQ = smem_u32(sQ + s * kTileBytes), aDO = smem_u32(sDO + s * kTileBytes);
-        // dV += P^T dO  (A: P^T K-major over queries; B: dO MN-major)
+        // dV += P^T dO  (A: P^T in TMEM, 16 queries = 8 packed columns per step;
+        // B: dO MN-major)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_bf16_ss(tmem + kColDV,
-                       make_sdesc_sw128(aPT + (kk >> 2) * kTileBytes + (kk & 3) * 32, 16, 1024),
+          umma_bf16_ts(tmem + kColDV, tmem + kColPT + kk * 8,
                        make_sdesc_sw128(aDO + kk * 2048, kTileBytes, 1024), kIdescKM,
                        (it > 0 || kk > 0) ? 1u : 0u);
         // dK' += dS^T Q'
@@ -253,6 +266,7 @@ __global__ void __launch_bounds__(448, 1)
                        make_sdesc_sw128(aDST + (kk >> 2) * kTileBytes + (kk & 3) * 32, 16, 1024),
                        make_sdesc_sw128(aQ + kk * 2048, kTileBytes, 1024), kIdescKM,
                        (it > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&bars[B_QDO_EMPTY + s]);  // dV and dK were the last readers of Q_i, dO_i
         // dQ'_i = dS K'  (A: dS^T read MN-major, i.e. as dS; B: K' MN-major)
         if (it >= 1 && !mbar_wait(&bars[B_DQ_FREE], (it - 1) & 1, abort_flag, p.status, 36)) {
           ok = false;
@@ -266,15 +280,17 @@ __global__ void __launch_bounds__(448, 1)
                        kk > 0 ? 1u : 0u);
         umma_commit(&bars[B_DQ_FULL]);
         umma_commit(&bars[B_PDS_FREE]);
-        umma_commit(&bars[B_QDO_EMPTY + s]);
       }
       umma_commit(&bars[B_MMA_DONE]);
       const long long t0 = clock64();
       while (!mbar_try_wait(&bars[B_MMA_DONE], 0) && clock64() - t0 < NE_WAIT_LIMIT_CYCLES) {
       }
     }
+  } else if (warp >= 12) {
+    regs_decrease<kRegsMma>();
   } else if (warp < 4) {
     // ------------------------------------- RoPE, LSE/D staging, dQ' reduction
+    if constexpr (kRegsRotate < 128) regs_decrease<kRegsRotate>();
     const int r = threadIdx.x;  // 0..127: tile row (key row for K, query row otherwise)
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     RopeRow tab;
@@ -290,34 +306,49 @@ __global__ void __launch_bounds__(448, 1)
         dl = __ldg(p.delta + static_cast<long long>(h) * p.pb.n_tot + start + qpos);
       }
     };
-    // dQ'_it: TMEM -> swizzled fp32 staging -> two bulk reduce-adds (32 columns each).
+    // dQ'_it: TMEM -> swizzled fp32 staging -> bulk reduce-add, one 32-column
+    // half (16 KiB) per staging buffer; a buffer is rewritten once the
+    // reduction issued from it one tile earlier has read it.
     auto reduce_dq = [&](int it) -> bool {
       if (!mbar_wait_warp(&bars[B_DQ_FULL], it & 1, abort_flag, p.status, 43)) return false;
       tc_fence_after();
-      uint32_t a[64];
-      tmem_ld_x32(tmem + lane_base + kColDQ, a);
-      tmem_ld_x32(tmem + lane_base + kColDQ + 32, a + 32);
-      tmem_ld_wait(a);
-      tmem_ld_wait(a + 32);
-      tc_fence_before();
-      mbar_arrive(&bars[B_DQ_FREE]);
-      if (r == 0) bulk_wait_group_read0();  // previous reduction has read the staging
-      named_bar_sync(1, 128);
+      const int qrow = start + (kt + it) * kBM;
+#pragma unroll 1
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t v[32];
+        tmem_ld_x32(tmem + lane_base + kColDQ + 32 * hf, v);
+        tmem_ld_wait(v);
+        if (hf == 1) {
+          tc_fence_before();
+          mbar_arrive(&bars[B_DQ_FREE]);
+        }
+        uint8_t* buf = sDQ + hf * kTileBytes;
+        if (r == 0) bulk_wait_group_read1();  // the group before the newest has read `buf`
+        named_bar_sync(1, 128);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        *reinterpret_cast<uint4*>(sDQ + sw128_offset(r, c)) =
-            make_uint4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
-        *reinterpret_cast<uint4*>(sDQ + kTileBytes + sw128_offset(r, c)) =
-            make_uint4(a[32 + 4 * c], a[33 + 4 * c], a[34 + 4 * c], a[35 + 4 * c]);
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(buf + sw128_offset(r, c)) =
+              make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (r == 0) {
+          tma_reduce_add_3d(&tmDQ, buf, 32 * hf, h, qrow);
+          bulk_commit_group();
+        }
       }
+      return true;
+    };
+    // Rotate Q_it (and stage its LSE/D rows); table and row terms of Q_it
+    // were prefetched.
+    auto rotate_q = [&](int it, float l2, float dl) -> bool {
+      const int s = it % kQStages;
+      if (!mbar_wait(&bars[B_QDO_FULL + s], (it / kQStages) & 1, abort_flag, p.status, 38))
+        return false;
+      rope_rotate_row(sQ + s * kTileBytes, r, tab);
+      sLSE[s * 128 + r] = -l2;  // stored negated: P = 2^(fma(s, scale log2e, -LSE))
+      sDEL[s * 128 + r] = -dl;
       fence_proxy_async_smem();
-      named_bar_sync(1, 128);
-      if (r == 0) {
-        const int qrow = start + (kt + it) * kBM;
-        tma_reduce_add_3d(&tmDQ, sDQ, 0, h, qrow);
-        tma_reduce_add_3d(&tmDQ, sDQ + kTileBytes, 32, h, qrow);
-        bulk_commit_group();
-      }
+      mbar_arrive(&bars[B_Q_ROT + s]);
       return true;
     };
     bool ok = mbar_wait(&bars[B_KV_FULL], 0, abort_flag, p.status, 37);
@@ -328,91 +359,99 @@ __global__ void __launch_bounds__(448, 1)
       float l2, dl;
       rope_load_row(p.rope, kt * kBM + r, tab);
       load_rowstats(0, l2, dl);
-      for (int it = 0; it < n_it; ++it) {
-        const int s = it & 1;
-        if (!mbar_wait(&bars[B_QDO_FULL + s], (it >> 1) & 1, abort_flag, p.status, 38)) {
-          ok = false;
-          break;
-        }
-        rope_rotate_row(sQ + s * kTileBytes, r, tab);
-        sLSE[s * 128 + r] = l2;
-        sDEL[s * 128 + r] = dl;
-        fence_proxy_async_smem();
-        mbar_arrive(&bars[B_Q_ROT + s]);
-        if (it >= 1 && !reduce_dq(it - 1)) {
-          ok = false;
-          break;
-        }
-        if (it + 1 < n_it) {  // prefetch the next tile's table rows and row terms
-          rope_load_row(p.rope, (kt + it + 1) * kBM + r, tab);
-          load_rowstats(it + 1, l2, dl);
-        }
+      ok = rotate_q(0, l2, dl);
+      if (ok && n_it > 1) {
+        rope_load_row(p.rope, (kt + 1) * kBM + r, tab);
+        load_rowstats(1, l2, dl);
       }
-      if (ok) reduce_dq(n_it - 1);
+      // Q_{it+1} is rotated before dQ'_it is reduced, so that the MMAs of
+      // tile it+1 never wait for the reduction of tile it; the table rows and
+      // row terms of Q_{it+2} are fetched while dQ'_it is reduced.
+      for (int it = 0; ok && it < n_it; ++it) {
+        if (it + 1 < n_it) {
+          if (!(ok = rotate_q(it + 1, l2, dl))) break;
+          if (it + 2 < n_it) {
+            rope_load_row(p.rope, (kt + it + 2) * kBM + r, tab);
+            load_rowstats(it + 2, l2, dl);
+          }
+        }
+        if (!(ok = reduce_dq(it))) break;
+      }
     }
     if (r == 0) bulk_wait_group0();
-  } else if (warp < 12) {
+  } else {
     // --------------------------------------------------------- softmax warps
+    regs_increase<kRegsSoftmax>();
     const int half = (warp - 4) >> 2;  // query columns 64*half .. 64*half+63
     const int wq = warp & 3;
     const int r = wq * 32 + lane;  // key row in tile
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const float sl2 = p.scale_log2;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
-      const int s = it & 1;
+      const int s = it % kQStages;
       if (!mbar_wait_warp(&bars[B_S_FULL], it & 1, abort_flag, p.status, 39)) { ok = false; break; }
       // LSE/D of this query tile were staged before Q_ROT[s] completed.
-      if (!mbar_wait_warp(&bars[B_Q_ROT + s], (it >> 1) & 1, abort_flag, p.status, 40)) {
-        ok = false;
-        break;
-      }
-      // P^T / dS^T buffers: free once the MMAs of the previous tile are done.
-      if (it >= 1 && !mbar_wait_warp(&bars[B_PDS_FREE], (it - 1) & 1, abort_flag, p.status, 41)) {
+      if (!mbar_wait_warp(&bars[B_Q_ROT + s], (it / kQStages) & 1, abort_flag, p.status, 40)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const bool diag = (it == 0);  // query tile == key tile: mask query < key
-      const float* lse2 = sLSE + s * 128;
-      const float* del = sDEL + s * 128;
-#pragma unroll 1
-      for (int cc = 0; cc < 2; ++cc) {  // 32 query columns at a time
-        const int c = 2 * half + cc;
-        uint32_t sr[32], dpr[32];
-        tmem_ld_x32(tmem + lane_base + kColS + c * 32, sr);
-        tmem_ld_x32(tmem + lane_base + kColDP + c * 32, dpr);
-        tmem_ld_wait(sr);
-        tmem_ld_wait(dpr);
-        if (cc == 1) {
-          tc_fence_before();
-          mbar_arrive(&bars[B_S_FREE]);
-        }
-        uint32_t pw[16], dw[16];
+      uint32_t sv[64], dv[64];
+      const uint32_t cs = kColS + 64 * half, cd = kColDP + 64 * half;
+      tmem_ld_x32(tmem + lane_base + cs, sv);
+      tmem_ld_x32(tmem + lane_base + cs + 32, sv + 32);
+      tmem_ld_x32(tmem + lane_base + cd, dv);
+      tmem_ld_x32(tmem + lane_base + cd + 32, dv + 32);
+      tmem_ld_wait(sv);
+      tmem_ld_wait(sv + 32);
+      tmem_ld_wait(dv);
+      tmem_ld_wait(dv + 32);
+      tc_fence_before();
+      mbar_arrive(&bars[B_S_FREE]);  // S^T/dP^T may be overwritten now
+      if (it == 0) {  // query tile == key tile: queries before the key get no weight
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float pv[2], dsv[2];
+        for (int col = 0; col < 64; ++col)
+          if (64 * half + col < r) sv[col] = 0xff800000u;  // -inf: P = 0, dS = 0
+      }
+      const float4* nl4 = reinterpret_cast<const float4*>(sLSE + s * 128 + 64 * half);
+      const float4* nd4 = reinterpret_cast<const float4*>(sDEL + s * 128 + 64 * half);
+      const uint64_t sl2x2 = f2_pack(sl2, sl2);
+      uint32_t pw[32], dw[32];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int col = c * 32 + e + u;
-            float pe = ex2_approx(__uint_as_float(sr[e + u]) * p.scale_log2 - lse2[col]);
-            if (diag && col < r) pe = 0.f;
-            pv[u] = pe;
-            dsv[u] = pe * (__uint_as_float(dpr[e + u]) - del[col]);
-          }
-          pw[e / 2] = pack_bf16x2(pv[0], pv[1]);
-          dw[e / 2] = pack_bf16x2(dsv[0], dsv[1]);
-        }
-        // Row r, columns c*32 .. c*32+31: block c/2, 16-byte chunks (c%2)*4 .. +3.
+      for (int q = 0; q < 16; ++q) {
+        const float4 nl = nl4[q], nd = nd4[q];
 #pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-          const uint32_t off = half * kTileBytes + sw128_offset(r, (c & 1) * 4 + k4);
-          *reinterpret_cast<uint4*>(sPT + off) =
-              make_uint4(pw[4 * k4], pw[4 * k4 + 1], pw[4 * k4 + 2], pw[4 * k4 + 3]);
-          *reinterpret_cast<uint4*>(sDST + off) =
-              make_uint4(dw[4 * k4], dw[4 * k4 + 1], dw[4 * k4 + 2], dw[4 * k4 + 3]);
+        for (int u = 0; u < 2; ++u) {
+          const int col = 4 * q + 2 * u;
+          const uint64_t t = f2_fma(f2_pack(__uint_as_float(sv[col]), __uint_as_float(sv[col + 1])),
+                                    sl2x2, u ? f2_pack(nl.z, nl.w) : f2_pack(nl.x, nl.y));
+          float t0, t1;
+          f2_unpack(t, t0, t1);
+          const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+          const uint64_t dd = f2_add(f2_pack(__uint_as_float(dv[col]), __uint_as_float(dv[col + 1])),
+                                     u ? f2_pack(nd.z, nd.w) : f2_pack(nd.x, nd.y));
+          float d0, d1;
+          f2_unpack(f2_mul(f2_pack(p0, p1), dd), d0, d1);
+          pw[col / 2] = pack_bf16x2(p0, p1);
+          dw[col / 2] = pack_bf16x2(d0, d1);
         }
       }
+      // P^T (TMEM) / dS^T (smem): free once the MMAs of the previous tile are done.
+      if (it >= 1 && !mbar_wait_warp(&bars[B_PDS_FREE], (it - 1) & 1, abort_flag, p.status, 41)) {
+        ok = false;
+        break;
+      }
+      // P^T row r, queries 64*half .. +63 -> TMEM (32 packed columns); dS^T row
+      // r -> smem block `half`, all eight 16-byte chunks.
+      tmem_st_x32(tmem + lane_base + kColPT + 32 * half, pw);
+#pragma unroll
+      for (int k8 = 0; k8 < 8; ++k8)
+        *reinterpret_cast<uint4*>(sDST + half * kTileBytes + sw128_offset(r, k8)) =
+            make_uint4(dw[4 * k8], dw[4 * k8 + 1], dw[4 * k8 + 2], dw[4 * k8 + 3]);
+      tmem_st_wait();
       fence_proxy_async_smem();
+      tc_fence_before();
       mbar_arrive(&bars[B_DS_FULL]);
     }
     // ---- epilogue: dV (first half) and dK = scale * R^T dK' (second half) --

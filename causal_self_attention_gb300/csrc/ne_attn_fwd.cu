@@ -9,16 +9,19 @@
 // section 3).  Both tiles share every rotated K/V tile, and while one tile's
 // softmax runs the tensor core works on the other tile's MMAs.
 //
-// Warp roles (448 threads):
-//   warps 0-3   softmax A: thread t owns row t of tile A (TMEM lane t)
+// Warp roles (512 threads, registers re-split per warpgroup with setmaxnreg):
+//   warps 0-3   softmax A: thread t owns row t of tile A (TMEM lane t), 176 regs
 //   warps 4-7   softmax B: same for tile B
-//   warps 8-11  rotate: RoPE on Q_A, Q_B once and on every K tile in smem
+//   warps 8-11  rotate: RoPE on Q_A, Q_B once and on every K tile in smem, 112
 //   warp 12     MMA: allocates TMEM; lane 0 issues S_X = Q_X K^T, O_X += P_X V
-//   warp 13     TMA: lane 0 loads Q_A, Q_B once and K/V tiles (3-stage ring)
+//   warp 13     TMA: lane 0 loads Q_A, Q_B once and the K ring (2 stages)
+//   warp 14     TMA: lane 0 loads the V ring (2 stages); warps 12-15 run at
+//               48 regs
 // TMEM columns: S_A 0-127, S_B 128-255, O_A 256-319, O_B 320-383.
-// The softmax reads S twice from TMEM (row max, then exponentials), so a row
-// never has to sit in registers whole; the reference max moves only when the
-// row max grows by more than 2^8 (exact: O and l keep a common reference).
+// A softmax thread loads its whole S row with one TMEM round trip and frees
+// S_X at once, so the next S_X = Q_X K^T overlaps the exponentials; the
+// reference max moves only when the row max grows by more than 2^8 (exact: O
+// and l keep a common reference).
 // Key tiles entirely above the diagonal are never loaded or computed.
 #include "ne_rope.cuh"
 #include "ne_sm100.cuh"
@@ -27,7 +30,10 @@ namespace ne {
 
 namespace fwd {
 
-constexpr int kThreads = 448;
+constexpr int kThreads = 512;
+// Registers per thread of each warpgroup after setmaxnreg (launch: 128).
+constexpr uint32_t kRegsSoftmax = 176, kRegsRotate = 112, kRegsMma = 48;
+static_assert(valid_reg_split(kRegsSoftmax, kRegsRotate, kRegsMma), "register split");
 constexpr int kStages = 2;                            // K ring and V ring
 constexpr int OFF_Q = 0;                              // Q_A, Q_B
 constexpr int OFF_K = OFF_Q + 2 * kTileBytes;         // kStages
@@ -59,67 +65,6 @@ constexpr uint32_t kColO = 256;  // O_X at 256 + 64 * X
 
 constexpr uint32_t kIdescS = make_idesc_bf16(128, 128, false, false);  // Q K^T
 constexpr uint32_t kIdescO = make_idesc_bf16(128, 64, false, true);    // P V (V MN-major)
-
-// Row max (log2 units) of one S row held in TMEM, masked on the diagonal.
-// The row is read in 16-column chunks, the next chunk's load in flight while
-// the current one is processed.
-__device__ __forceinline__ float row_max(uint32_t tS, float sl2, bool is_diag, int r) {
-  uint32_t a[16], b[16];
-  float mx = -INFINITY;
-  tmem_ld_x16(tS, a);
-  tmem_ld_wait16(a);
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    uint32_t* cur = (c & 1) ? b : a;
-    uint32_t* nxt = (c & 1) ? a : b;
-    if (c < 7) tmem_ld_x16(tS + 16 * (c + 1), nxt);
-#pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      const float v = (is_diag && 16 * c + e > r) ? -INFINITY : __uint_as_float(cur[e]) * sl2;
-      mx = fmaxf(mx, v);
-    }
-    if (c < 7) tmem_ld_wait16(nxt);
-  }
-  return mx;
-}
-
-// P = 2^(scale*log2e*S - m) for one row: bf16 to the swizzled K-major P
-// buffer, returns the fp32 row sum; `mx` receives the masked row max seen.
-__device__ __forceinline__ float row_exp(uint32_t tS, float sl2, float m, bool is_diag, int r,
-                                         uint8_t* pbuf, float& mx) {
-  uint32_t a[16], b[16];
-  float rs = 0.f;
-  mx = -INFINITY;
-  tmem_ld_x16(tS, a);
-  tmem_ld_wait16(a);
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    uint32_t* cur = (c & 1) ? b : a;
-    uint32_t* nxt = (c & 1) ? a : b;
-    if (c < 7) tmem_ld_x16(tS + 16 * (c + 1), nxt);
-    uint32_t pw[8];
-#pragma unroll
-    for (int e = 0; e < 16; e += 2) {
-      float v0 = __uint_as_float(cur[e]) * sl2;
-      float v1 = __uint_as_float(cur[e + 1]) * sl2;
-      if (is_diag && 16 * c + e > r) v0 = -INFINITY;
-      if (is_diag && 16 * c + e + 1 > r) v1 = -INFINITY;
-      mx = fmaxf(mx, fmaxf(v0, v1));
-      const float p0 = ex2_approx(v0 - m);
-      const float p1 = ex2_approx(v1 - m);
-      rs += p0 + p1;
-      pw[e / 2] = pack_bf16x2(p0, p1);
-    }
-    // Columns 16c .. 16c+15: block c/4, 16-byte chunks 2(c%4), 2(c%4)+1.
-    uint8_t* blk = pbuf + (c >> 2) * kTileBytes;
-    *reinterpret_cast<uint4*>(blk + sw128_offset(r, 2 * (c & 3))) =
-        make_uint4(pw[0], pw[1], pw[2], pw[3]);
-    *reinterpret_cast<uint4*>(blk + sw128_offset(r, 2 * (c & 3) + 1)) =
-        make_uint4(pw[4], pw[5], pw[6], pw[7]);
-    if (c < 7) tmem_ld_wait16(nxt);
-  }
-  return rs;
-}
 
 }  // namespace fwd
 
@@ -189,10 +134,11 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
   uint8_t* sV = smem + OFF_V;
   uint8_t* sP = smem + OFF_P;
 
-  if (warp == 13) {
-    // ---------------------------------------- TMA producers: lane 0 K, lane 1 V
-    if (lane < 2) {
-      const bool isK = (lane == 0);
+  if (warp == 13 || warp == 14) {
+    // ------------------------------------ TMA producers: warp 13 K, warp 14 V
+    regs_decrease<kRegsMma>();
+    if (lane == 0) {
+      const bool isK = (warp == 13);
       const CUtensorMap* tm = isK ? &tmK : &tmV;
       uint8_t* ring = isK ? sK : sV;
       uint64_t* full = &bars[isK ? B_K_FULL : B_V_FULL];
@@ -228,6 +174,7 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
     }
   } else if (warp == 12) {
     // ------------------------------------------------------------- MMA issuer
+    regs_decrease<kRegsMma>();
     if (lane == 0) {
       const int nkvX[2] = {nkvA, nkvB};
       bool ok = mbar_wait(&bars[B_Q_ROT], 0, abort_flag, p.status, 2);
@@ -293,8 +240,12 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
       while (!mbar_try_wait(&bars[B_MMA_DONE], 0) && clock64() - t0 < NE_WAIT_LIMIT_CYCLES) {
       }
     }
+  } else if (warp >= 12) {
+    // warp 15: no role (it completes the warpgroup for setmaxnreg)
+    regs_decrease<kRegsMma>();
   } else if (warp >= 8) {
     // ------------------------------------------------------------ RoPE warps
+    regs_decrease<kRegsRotate>();
     const int r = threadIdx.x - 256;  // 0..127: tile row
     RopeRow tab;
     rope_load_row(p.rope, rowA + r, tab);
@@ -316,6 +267,7 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
     }
   } else {
     // --------------------------------------------------------- softmax warps
+    regs_increase<kRegsSoftmax>();
     const int x = warp >> 2;            // tile A (0) or B (1)
     const int wq = warp & 3;            // TMEM lane quarter
     const int r = wq * 32 + lane;       // row in tile
@@ -326,7 +278,7 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
     const uint32_t tS = tmem + lane_base + kColS + 128 * x;
     const uint32_t tO = tmem + lane_base + kColO + 64 * x;
     const float sl2 = p.scale_log2;
-    float m_ref = -INFINITY;  // reference max (log2 units) the P values are taken against
+    float m_ref = 0.f;  // reference max (log2 units) the P values are taken against
     float l_sum = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv_x; ++j) {
@@ -335,24 +287,40 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
         break;
       }
       tc_fence_after();
-      const bool is_diag = (j == diag);
-      // The P buffer written here was last read by the P V of tile j-2, which
-      // completed before S_X(j) (tcgen05 operations complete in issue order).
-      uint8_t* pbuf = sP + (2 * x + (j & 1)) * 2 * kTileBytes;
-      float m_use = m_ref;
-      if (j == 0) m_use = row_max(tS, sl2, is_diag, r);  // first tile: no reference yet
-      float mx;
-      float rs = row_exp(tS, sl2, m_use, is_diag, r, pbuf, mx);
-      float alpha = 1.f;
+      // The whole S row in one TMEM round trip; S_X is then free for Q_X K_{j+1}^T.
+      uint32_t sr[128];
+      tmem_ld_x32(tS + 0, sr + 0);
+      tmem_ld_x32(tS + 32, sr + 32);
+      tmem_ld_x32(tS + 64, sr + 64);
+      tmem_ld_x32(tS + 96, sr + 96);
+      tmem_ld_wait(sr + 0);
+      tmem_ld_wait(sr + 32);
+      tmem_ld_wait(sr + 64);
+      tmem_ld_wait(sr + 96);
+      tc_fence_before();
+      mbar_arrive(&bars[B_S_FREE + x]);
+      if (j == diag) {  // diagonal tile: keys after the query get no weight
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c > r) sr[c] = 0xff800000u;  // -inf
+      }
+      // Row max of the raw scores (the scale is positive), four chains.
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < 128; c += 8)
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          m4[u] = fmax3(m4[u], __uint_as_float(sr[c + 2 * u]), __uint_as_float(sr[c + 2 * u + 1]));
+      const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
       // Move the reference max only when the row max outgrows it by more than
-      // 2^8 (exact: O and l keep a common reference); then redo this tile's P.
-      const bool grow = (j > 0) && (mx > m_use + 8.0f);
-      if (__any_sync(0xffffffffu, grow)) {
-        const float m_new = grow ? mx : m_use;
-        float mx2;
-        rs = row_exp(tS, sl2, m_new, is_diag, r, pbuf, mx2);
-        alpha = ex2_approx(m_use - m_new);
-        m_use = m_new;
+      // 2^8 (exact: O and l keep a common reference).
+      const bool grow = (j == 0) || (mx > m_ref + 8.0f);
+      float alpha = 1.f;
+      if (grow) {
+        alpha = (j == 0) ? 0.f : ex2_approx(m_ref - mx);
+        m_ref = mx;
+      }
+      if (j > 0 && __any_sync(0xffffffffu, grow)) {
         // O_X must be stable: wait for the P V of the previous tile.
         if (!mbar_wait_warp(&bars[B_PV_DONE + x], (j - 1) & 1, abort_flag, p.status, 9)) {
           ok = false;
@@ -369,10 +337,35 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
           tmem_st_x32(tO + half * 32, o);
           tmem_st_wait();  // the store has consumed `o` before it is reloaded
         }
+        tc_fence_before();
       }
-      tc_fence_before();
-      mbar_arrive(&bars[B_S_FREE + x]);  // S_X may be overwritten now
-      m_ref = m_use;
+      // P = 2^(x - m_ref) in bf16 to the swizzled K-major P buffer.  That
+      // buffer was last read by the P V of tile j-2, which completed before
+      // S_X(j) did (tcgen05 operations complete in issue order).
+      uint8_t* pbuf = sP + (2 * x + (j & 1)) * 2 * kTileBytes;
+      const uint64_t sl2x2 = f2_pack(sl2, sl2);
+      const uint64_t negm2 = f2_pack(-m_ref, -m_ref);
+      uint64_t acc[4] = {0, 0, 0, 0};  // packed partial row sums (0 = +0.f, +0.f)
+#pragma unroll
+      for (int c16 = 0; c16 < 16; ++c16) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = 8 * c16 + 2 * e;
+          const uint64_t t = f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])),
+                                    sl2x2, negm2);
+          float t0, t1;
+          f2_unpack(t, t0, t1);
+          const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+          acc[e] = f2_add(acc[e], f2_pack(p0, p1));
+          w[e] = pack_bf16x2(p0, p1);
+        }
+        *reinterpret_cast<uint4*>(pbuf + (c16 >> 3) * kTileBytes + sw128_offset(r, c16 & 7)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      float rs0, rs1;
+      f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), rs0, rs1);
+      const float rs = rs0 + rs1;
       l_sum = l_sum * alpha + rs;
       fence_proxy_async_smem();
       mbar_arrive(&bars[B_P_FULL + 2 * x + (j & 1)]);

@@ -78,11 +78,13 @@ __global__ void __launch_bounds__(128, 1)
     debug_store_rows(sA, a, 128, 128);
     debug_store_rows(sA + kTileBytes, a + 64, 128, 128);
     debug_store_rows(sB, b, 128, 64);  // b [K=128 rows, N=64]
-  } else {
+  } else if (form == 2) {
     // a [K=128 rows, M=128]: two M blocks of 64 columns.
     debug_store_rows(sA, a, 128, 128);
     debug_store_rows(sA + kTileBytes, a + 64, 128, 128);
     debug_store_rows(sB, b, 128, 64);
+  } else {
+    debug_store_rows(sB, b, 128, 64);  // a goes to TMEM below
   }
   fence_proxy_async_smem();
   if (threadIdx.x == 0) {
@@ -99,6 +101,20 @@ __global__ void __launch_bounds__(128, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int ncols = (form == 0) ? 128 : 64;
+  if (form == 3) {
+    // Row r of a -> TMEM lane r, columns 128..191 (bf16 pairs packed per column).
+    const int row = warp * 32 + lane;
+    const uint32_t* arow = reinterpret_cast<const uint32_t*>(a + row * 128);
+    for (int c0 = 0; c0 < 64; c0 += 32) {
+      uint32_t r[32];
+      for (int c = 0; c < 32; ++c) r[c] = arow[c0 + c];
+      tmem_st_x32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + 128 + c0, r);
+      tmem_st_wait();
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
   if (threadIdx.x == 0) {
     const uint32_t aA = smem_u32(sA), aB = smem_u32(sB);
     if (form == 0) {
@@ -111,11 +127,16 @@ __global__ void __launch_bounds__(128, 1)
       for (int kk = 0; kk < 8; ++kk)
         umma_bf16_ss(tmem, make_sdesc_sw128(aA + (kk >> 2) * kTileBytes + (kk & 3) * 32, 16, 1024),
                      make_sdesc_sw128(aB + kk * 2048, kTileBytes, 1024), idesc, kk > 0);
-    } else {
+    } else if (form == 2) {
       const uint32_t idesc = make_idesc_bf16(128, 64, true, true);
       for (int kk = 0; kk < 8; ++kk)
         umma_bf16_ss(tmem, make_sdesc_sw128(aA + kk * 2048, kTileBytes, 1024),
                      make_sdesc_sw128(aB + kk * 2048, kTileBytes, 1024), idesc, kk > 0);
+    } else {
+      const uint32_t idesc = make_idesc_bf16(128, 64, false, true);
+      for (int kk = 0; kk < 8; ++kk)  // 16 K elements = 8 packed TMEM columns per step
+        umma_bf16_ts(tmem, tmem + 128 + kk * 8, make_sdesc_sw128(aB + kk * 2048, kTileBytes, 1024),
+                     idesc, kk > 0);
     }
     umma_commit(bar);
   }

@@ -65,8 +65,9 @@ typedef uint16_t ne_bf16; /* raw bfloat16 bits */
 
 /* Forward, fixed length.  q, k, v: [B, T, H, 64] bf16.  out: [B, T, H, 64]
  * bf16 (written).  lse: [B, H, T] fp32 (written), natural log.  scale is the
- * softmax scale (1/sqrt(64) = 0.125 for the usual choice); rope_base is the
- * RoPE theta base (10000 for the usual choice).  B, H, T >= 1. */
+ * softmax scale, finite and > 0 (1/sqrt(64) = 0.125 for the usual choice);
+ * rope_base is the RoPE theta base, finite and > 0 (10000 for the usual
+ * choice).  B, H, T >= 1. */
 ne_status ne_attn_fwd(const ne_bf16* q, const ne_bf16* k, const ne_bf16* v, int B, int H, int T,
                       int D, float rope_base, float scale, ne_bf16* out, float* lse,
                       void* stream);

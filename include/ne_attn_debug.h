@@ -36,6 +36,10 @@ ne_status ne_debug_rope_tile(const ne_bf16* src, int n_rows, int H, int h, int r
  *                                                     [K=128, N=64], MN-major)
  *   form 2: d[128,64]  = a[128,128]^T . b[128,64]      (a is [K=128, M=128],
  *                                                     MN-major; b as form 1)
+ *   form 3: d[128,64]  = a[128,128] . b[128,64]        (a held in TMEM, row m
+ *                                                     in lane m, bf16 pairs
+ *                                                     packed per column; b as
+ *                                                     form 1)
  * a, b: row-major bf16 as written above; d: row-major fp32. */
 ne_status ne_debug_umma(int form, const ne_bf16* a, const ne_bf16* b, float* d, void* stream);
 

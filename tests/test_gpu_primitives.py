@@ -52,7 +52,7 @@ def test_rope_tile_bitwise(na, pos0):
     np.testing.assert_array_equal(got, ref)
 
 
-@pytest.mark.parametrize("form", [0, 1, 2])
+@pytest.mark.parametrize("form", [0, 1, 2, 3])
 def test_umma_forms(na, form):
     if form == 0:
         a, b = _bf16((128, 64), 3), _bf16((128, 64), 4)
@@ -60,9 +60,12 @@ def test_umma_forms(na, form):
     elif form == 1:
         a, b = _bf16((128, 128), 5), _bf16((128, 64), 6)
         ref = a.double() @ b.double()
-    else:
+    elif form == 2:
         a, b = _bf16((128, 128), 7), _bf16((128, 64), 8)
         ref = a.double().T @ b.double()
+    else:
+        a, b = _bf16((128, 128), 9), _bf16((128, 64), 10)
+        ref = a.double() @ b.double()
     d = na.ne_debug_umma(form, a.cuda(), b.cuda()).cpu().double()
     assert na.ne_attn_get_device_status() == 0
     err = (d - ref).abs().max().item()
