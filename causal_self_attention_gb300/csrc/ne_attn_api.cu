@@ -288,6 +288,26 @@ ne_status run_bwd(const Shape& s, const void* q, const void* k, const void* v, c
 
 }  // namespace
 
+namespace ne {
+// Helpers for the allocation-free backward entry point (ne_attn_noalloc.cu):
+// per-device set-up, the device status word, and the tensor-map encoders.
+ne_status internal_prepare(int** status_word) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState* st = nullptr;
+  ne_status rc = device_state(&st);
+  if (rc != NE_OK) return rc;
+  if ((rc = get_encoder()) != NE_OK) return rc;
+  *status_word = st->status;
+  return NE_OK;
+}
+ne_status internal_encode_rows(CUtensorMap* map, const void* base, int n_rows, int H) {
+  return encode_rows(map, base, n_rows, H);
+}
+ne_status internal_encode_rows_f32(CUtensorMap* map, void* base, int n_rows, int H) {
+  return encode_rows_f32(map, base, n_rows, H);
+}
+}  // namespace ne
+
 extern "C" {
 
 const char* ne_status_string(ne_status s) {
@@ -300,6 +320,7 @@ const char* ne_status_string(ne_status s) {
     case NE_ERR_TIMEOUT: return "NE_ERR_TIMEOUT";
     case NE_ERR_OOM: return "NE_ERR_OOM";
     case NE_ERR_BAD_SEQLEN: return "NE_ERR_BAD_SEQLEN";
+    case NE_ERR_TOO_LARGE: return "NE_ERR_TOO_LARGE";
     default: return "NE_ERR_UNKNOWN";
   }
 }

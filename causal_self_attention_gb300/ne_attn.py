@@ -21,9 +21,10 @@ _lib = None
 NE_OK = 0
 STATUS_NAMES = {0: "NE_OK", 1: "NE_ERR_INVALID_ARG", 2: "NE_ERR_UNSUPPORTED",
                 3: "NE_ERR_MISALIGNED", 4: "NE_ERR_CUDA", 5: "NE_ERR_TIMEOUT", 6: "NE_ERR_OOM",
-                7: "NE_ERR_BAD_SEQLEN"}
+                7: "NE_ERR_BAD_SEQLEN", 8: "NE_ERR_TOO_LARGE"}
 
 EXPORTED = ("ne_attn_fwd", "ne_attn_fwd_f32out", "ne_attn_bwd", "ne_attn_bwd_workspace_bytes",
+            "ne_attn_bwd_noalloc",
             "ne_attn_varlen_fwd", "ne_attn_varlen_fwd_f32out", "ne_attn_varlen_bwd",
             "ne_attn_set_bwd_phase_events", "ne_attn_get_device_status",
             "ne_attn_last_device_code", "ne_status_string",
@@ -55,6 +56,7 @@ def lib():
         "ne_attn_fwd": [P, P, P, I, I, I, I, F, F, P, P, P],
         "ne_attn_fwd_f32out": [P, P, P, I, I, I, I, F, F, P, P, P],
         "ne_attn_bwd": [P, P, P, P, P, P, I, I, I, I, F, F, P, P, P, P, Z, P],
+        "ne_attn_bwd_noalloc": [P, P, P, P, P, P, I, I, I, I, F, F, P, P, P, P],
         "ne_attn_varlen_fwd": [P, P, P, P, I, I, I, I, I, F, F, P, P, P],
         "ne_attn_varlen_fwd_f32out": [P, P, P, P, I, I, I, I, I, F, F, P, P, P],
         "ne_attn_varlen_bwd": [P, P, P, P, P, P, P, I, I, I, I, I, F, F, P, P, P, P, Z, P],
@@ -143,6 +145,27 @@ def ne_attn_bwd(q, k, v, out, dout, lse, rope_base=10000.0, scale=None, dq=None,
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), B, H, T, D,
         float(rope_base), float(scale), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
         ws_bytes, _stream(stream)))
+    return dq, dk, dv
+
+
+def ne_attn_bwd_noalloc(q, k, v, out, dout, lse, rope_base=10000.0, scale=None, dq=None,
+                        dk=None, dv=None, stream=None):
+    """Backward on ``[B, T, H, 64]`` tensors that allocates no device memory:
+    for callers that cannot allocate (the library's fixed scratch array is used
+    instead of a workspace; see include/ne_attn.h for its limits and for why
+    overlapping calls race).  ``dq``, ``dk``, ``dv`` must be passed in by such
+    callers; they are only created here when omitted.  Returns ``(dq, dk, dv)``."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        _need(t, torch.bfloat16, n)
+    _need(lse, torch.float32, "lse")
+    B, T, H, D = q.shape
+    scale = D ** -0.5 if scale is None else scale
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check("ne_attn_bwd_noalloc", lib().ne_attn_bwd_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), B, H, T, D,
+        float(rope_base), float(scale), _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)))
     return dq, dk, dv
 
 

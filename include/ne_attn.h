@@ -60,6 +60,7 @@ typedef int ne_status;
 #define NE_ERR_TIMEOUT 5     /* a device pipeline wait expired (reported by get_device_status) */
 #define NE_ERR_OOM 6         /* allocation of a table or temporary failed */
 #define NE_ERR_BAD_SEQLEN 7  /* a varlen sequence was longer than max_seqlen (device-detected) */
+#define NE_ERR_TOO_LARGE 8   /* problem exceeds the fixed scratch of ne_attn_bwd_noalloc */
 
 typedef uint16_t ne_bf16; /* raw bfloat16 bits */
 
@@ -129,6 +130,37 @@ ne_status ne_attn_varlen_bwd(const ne_bf16* q, const ne_bf16* k, const ne_bf16* 
  * on the call's stream, so the three backward kernels can be timed apart.
  * Pass NULL, NULL to turn it off.  Process-wide; not for concurrent callers. */
 ne_status ne_attn_set_bwd_phase_events(void* ev_after_preprocess, void* ev_after_main);
+
+/* Backward that allocates no device memory at all, for callers that cannot
+ * call cudaMalloc (or let a library do it for them): for example code running
+ * under an allocator that must own every byte of device memory, a serving
+ * process whose memory budget is fixed after start-up, or a plug-in that is
+ * handed tensors but no allocator.  The paper pages have no counterpart; this
+ * is a property of the library's interface, not of the method.
+ *
+ * Arguments are those of ne_attn_bwd without the workspace.  Instead of a
+ * workspace and the library's RoPE-table cache, it uses one fixed scratch
+ * array of NE_NOALLOC_SCRATCH_BYTES in the library's own device memory (a
+ * static array that every GPU which loads the library holds until the process
+ * exits).  Limits: B*T*H <= NE_NOALLOC_MAX_ROWS (token-head rows of the fp32
+ * dQ accumulator) and T <= NE_NOALLOC_MAX_POSITIONS; beyond them the call
+ * returns NE_ERR_TOO_LARGE before touching the device.
+ *
+ * The first call on a device (and the first call with a new rope_base) looks
+ * up the array's device address and writes the RoPE table into it with a
+ * synchronous copy; make that first call before any stream capture.  Every
+ * call shares the one array and leaves the last call's contents in it (the
+ * parts that must start from zero are cleared on every call), so calls whose
+ * work overlaps on the GPU -- on different streams, or on different host
+ * threads -- race and must be serialized by the caller.  Results equal those
+ * of ne_attn_bwd (dq up to the order of its fp32 atomic adds). */
+#define NE_NOALLOC_SCRATCH_BYTES (32u << 20)
+#define NE_NOALLOC_MAX_POSITIONS 16384
+#define NE_NOALLOC_MAX_ROWS 108000
+ne_status ne_attn_bwd_noalloc(const ne_bf16* q, const ne_bf16* k, const ne_bf16* v,
+                              const ne_bf16* out, const ne_bf16* dout, const float* lse, int B,
+                              int H, int T, int D, float rope_base, float scale, ne_bf16* dq,
+                              ne_bf16* dk, ne_bf16* dv, void* stream);
 
 /* Synchronize `stream`, then return and clear the device status word of the
  * current device: NE_OK, NE_ERR_TIMEOUT or NE_ERR_BAD_SEQLEN (or NE_ERR_CUDA
