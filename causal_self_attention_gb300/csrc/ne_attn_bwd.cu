@@ -16,14 +16,16 @@
 // TMA loads, as in the forward.
 //
 // Main-kernel warp roles (512 threads, registers re-split per warpgroup):
-//   warps 0-3   rotate + dQ': K_j once, every Q_i one tile ahead, LSE_i/D_i
-//               staging (table rows and LSE/D prefetched); TMEM dQ'_i ->
-//               swizzled fp32 smem (2 x 16 KiB) -> bulk tensor reduce-adds
+//   warps 0-3   rotate: K_j once, then every Q_i as soon as it lands (up to
+//               three tiles ahead), staging -LSE_i and -D_i; table rows and
+//               row terms prefetched one tile ahead
 //   warps 4-7   softmax, query columns 0-63 of the tile (thread t: key row t)
 //   warps 8-11  softmax, query columns 64-127; a softmax thread reads its S^T
 //               and dP^T half-rows in one TMEM round trip and frees them at
 //               once, so the next tile's S^T/dP^T MMAs overlap its math; it
-//               writes P^T to TMEM (A operand of dV) and dS^T to smem
+//               writes P^T to TMEM (A operand of dV) and dS^T to smem; after
+//               tile i it moves half h of dQ'_{i-1} (32 columns) from TMEM to
+//               a swizzled fp32 staging buffer and issues its bulk reduce-add
 //   warp 12     MMA: allocates TMEM; lane 0 issues the five MMAs per tile
 //   warp 13     TMA: lane 0 loads K_j, V_j once and Q_i, dO_i (2 stages)
 //   warps 14-15 no role (complete the warpgroup for setmaxnreg)
@@ -38,7 +40,7 @@ namespace bwd {
 
 constexpr int kThreads = 512;
 // Registers per thread of each warpgroup after setmaxnreg (launch: 128).
-constexpr uint32_t kRegsSoftmax = 160, kRegsRotate = 128, kRegsMma = 56;
+constexpr uint32_t kRegsSoftmax = 168, kRegsRotate = 112, kRegsMma = 56;
 static_assert(valid_reg_split(kRegsSoftmax, kRegsRotate, kRegsMma), "register split");
 constexpr int kQStages = 3;                          // Q_i / dO_i ring depth
 constexpr int OFF_K = 0;
@@ -50,7 +52,8 @@ constexpr int OFF_DQ = OFF_DST + 2 * kTileBytes;         // dQ' staging: 2 x [12
 constexpr int OFF_LSE = OFF_DQ + 2 * kTileBytes;         // kQStages x 128 fp32: -LSE (log2 units)
 constexpr int OFF_DEL = OFF_LSE + kQStages * 128 * 4;  // kQStages x 128 fp32: -D
 constexpr int OFF_BAR = OFF_DEL + kQStages * 128 * 4;
-constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
+constexpr int kBarBytes = 512;  // mbarriers, TMEM address, abort flag
+constexpr int SMEM_BYTES = OFF_BAR + kBarBytes + 1024;  // + slack for 1024-byte alignment
 
 enum Bar {
   B_KV_FULL = 0,
@@ -67,6 +70,7 @@ enum Bar {
   B_MMA_DONE,
   B_COUNT
 };
+static_assert(8 * B_COUNT + 8 <= kBarBytes, "barrier region overflow");
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384,
@@ -160,7 +164,7 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(&bars[B_DS_FULL], 256);
     mbar_init(&bars[B_PDS_FREE], 1);
     mbar_init(&bars[B_DQ_FULL], 1);
-    mbar_init(&bars[B_DQ_FREE], 128);
+    mbar_init(&bars[B_DQ_FREE], 256);
     mbar_init(&bars[B_MMA_DONE], 1);
     *abort_flag = 0;
     mbar_fence_init();
@@ -289,10 +293,9 @@ __global__ void __launch_bounds__(512, 1)
   } else if (warp >= 12) {
     regs_decrease<kRegsMma>();
   } else if (warp < 4) {
-    // ------------------------------------- RoPE, LSE/D staging, dQ' reduction
+    // ----------------------------------------------- RoPE and LSE/D staging
     if constexpr (kRegsRotate < 128) regs_decrease<kRegsRotate>();
     const int r = threadIdx.x;  // 0..127: tile row (key row for K, query row otherwise)
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     RopeRow tab;
     rope_load_row(p.rope, kt * kBN + r, tab);
     // LSE (log2 units) and D of query row r of tile `it`; rows past the
@@ -305,38 +308,6 @@ __global__ void __launch_bounds__(512, 1)
         l2 = __ldg(p.lse + lse_index(p.pb, h, seq, start, qpos)) * 1.4426950408889634f;
         dl = __ldg(p.delta + static_cast<long long>(h) * p.pb.n_tot + start + qpos);
       }
-    };
-    // dQ'_it: TMEM -> swizzled fp32 staging -> bulk reduce-add, one 32-column
-    // half (16 KiB) per staging buffer; a buffer is rewritten once the
-    // reduction issued from it one tile earlier has read it.
-    auto reduce_dq = [&](int it) -> bool {
-      if (!mbar_wait_warp(&bars[B_DQ_FULL], it & 1, abort_flag, p.status, 43)) return false;
-      tc_fence_after();
-      const int qrow = start + (kt + it) * kBM;
-#pragma unroll 1
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t v[32];
-        tmem_ld_x32(tmem + lane_base + kColDQ + 32 * hf, v);
-        tmem_ld_wait(v);
-        if (hf == 1) {
-          tc_fence_before();
-          mbar_arrive(&bars[B_DQ_FREE]);
-        }
-        uint8_t* buf = sDQ + hf * kTileBytes;
-        if (r == 0) bulk_wait_group_read1();  // the group before the newest has read `buf`
-        named_bar_sync(1, 128);
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(buf + sw128_offset(r, c)) =
-              make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-        fence_proxy_async_smem();
-        named_bar_sync(1, 128);
-        if (r == 0) {
-          tma_reduce_add_3d(&tmDQ, buf, 32 * hf, h, qrow);
-          bulk_commit_group();
-        }
-      }
-      return true;
     };
     // Rotate Q_it (and stage its LSE/D rows); table and row terms of Q_it
     // were prefetched.
@@ -359,26 +330,15 @@ __global__ void __launch_bounds__(512, 1)
       float l2, dl;
       rope_load_row(p.rope, kt * kBM + r, tab);
       load_rowstats(0, l2, dl);
-      ok = rotate_q(0, l2, dl);
-      if (ok && n_it > 1) {
-        rope_load_row(p.rope, (kt + 1) * kBM + r, tab);
-        load_rowstats(1, l2, dl);
-      }
-      // Q_{it+1} is rotated before dQ'_it is reduced, so that the MMAs of
-      // tile it+1 never wait for the reduction of tile it; the table rows and
-      // row terms of Q_{it+2} are fetched while dQ'_it is reduced.
       for (int it = 0; ok && it < n_it; ++it) {
-        if (it + 1 < n_it) {
-          if (!(ok = rotate_q(it + 1, l2, dl))) break;
-          if (it + 2 < n_it) {
-            rope_load_row(p.rope, (kt + it + 2) * kBM + r, tab);
-            load_rowstats(it + 2, l2, dl);
-          }
+        ok = rotate_q(it, l2, dl);
+        if (ok && it + 1 < n_it) {  // next tile's table rows and row terms
+          rope_load_row(p.rope, (kt + it + 1) * kBM + r, tab);
+          load_rowstats(it + 1, l2, dl);
         }
-        if (!(ok = reduce_dq(it))) break;
       }
     }
-    if (r == 0) bulk_wait_group0();
+
   } else {
     // --------------------------------------------------------- softmax warps
     regs_increase<kRegsSoftmax>();
@@ -387,6 +347,31 @@ __global__ void __launch_bounds__(512, 1)
     const int r = wq * 32 + lane;  // key row in tile
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const float sl2 = p.scale_log2;
+    // Columns 32*half .. +31 of dQ'_it: TMEM -> swizzled fp32 staging buffer
+    // `half` -> one bulk tensor reduce-add, issued by the warpgroup's thread 0.
+    auto reduce_dq_half = [&](int it) -> bool {
+      if (!mbar_wait_warp(&bars[B_DQ_FULL], it & 1, abort_flag, p.status, 43)) return false;
+      tc_fence_after();
+      uint32_t v[32];
+      tmem_ld_x32(tmem + lane_base + kColDQ + 32 * half, v);
+      tmem_ld_wait(v);
+      tc_fence_before();
+      mbar_arrive(&bars[B_DQ_FREE]);
+      uint8_t* buf = sDQ + half * kTileBytes;
+      if (r == 0) bulk_wait_group_read0();  // this buffer's previous reduction has read it
+      named_bar_sync(1 + half, 128);
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(buf + sw128_offset(r, c)) =
+            make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+      fence_proxy_async_smem();
+      named_bar_sync(1 + half, 128);
+      if (r == 0) {
+        tma_reduce_add_3d(&tmDQ, buf, 32 * half, h, start + (kt + it) * kBM);
+        bulk_commit_group();
+      }
+      return true;
+    };
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int s = it % kQStages;
@@ -453,7 +438,10 @@ __global__ void __launch_bounds__(512, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bars[B_DS_FULL]);
+      if (it >= 1 && !(ok = reduce_dq_half(it - 1))) break;
     }
+    if (ok) ok = reduce_dq_half(n_it - 1);
+    if (r == 0) bulk_wait_group0();
     // ---- epilogue: dV (first half) and dK = scale * R^T dK' (second half) --
     if (ok && mbar_wait_warp(&bars[B_MMA_DONE], 0, abort_flag, p.status, 42)) {
       tc_fence_after();

@@ -14,10 +14,11 @@
 //   warps 4-7   softmax B: same for tile B
 //   warps 8-11  rotate: RoPE on Q_A, Q_B once and on every K tile in smem, 112
 //   warp 12     MMA: allocates TMEM; lane 0 issues S_X = Q_X K^T, O_X += P_X V
-//   warp 13     TMA: lane 0 loads Q_A, Q_B once and the K ring (2 stages)
-//   warp 14     TMA: lane 0 loads the V ring (2 stages); warps 12-15 run at
+//   warp 13     TMA: lane 0 loads Q_A, Q_B once and the K ring (5 stages)
+//   warp 14     TMA: lane 0 loads the V ring (5 stages); warps 12-15 run at
 //               48 regs
-// TMEM columns: S_A 0-127, S_B 128-255, O_A 256-319, O_B 320-383.
+// TMEM columns: S_A 0-127, S_B 128-255, O_A 256-319, O_B 320-383,
+// P_A 384-447, P_B 448-511 (bf16 pairs: P is the TMEM A operand of P V).
 // A softmax thread loads its whole S row with one TMEM round trip and frees
 // S_X at once, so the next S_X = Q_X K^T overlaps the exponentials; the
 // reference max moves only when the row max grows by more than 2^8 (exact: O
@@ -34,13 +35,13 @@ constexpr int kThreads = 512;
 // Registers per thread of each warpgroup after setmaxnreg (launch: 128).
 constexpr uint32_t kRegsSoftmax = 176, kRegsRotate = 112, kRegsMma = 48;
 static_assert(valid_reg_split(kRegsSoftmax, kRegsRotate, kRegsMma), "register split");
-constexpr int kStages = 2;                            // K ring and V ring
+constexpr int kStages = 5;                            // K ring and V ring
 constexpr int OFF_Q = 0;                              // Q_A, Q_B
 constexpr int OFF_K = OFF_Q + 2 * kTileBytes;         // kStages
 constexpr int OFF_V = OFF_K + kStages * kTileBytes;   // kStages
-constexpr int OFF_P = OFF_V + kStages * kTileBytes;   // P_X[2]: 4 buffers x (2 x 16 KiB)
-constexpr int OFF_BAR = OFF_P + 8 * kTileBytes;
-constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;      // + slack for 1024-byte alignment
+constexpr int OFF_BAR = OFF_V + kStages * kTileBytes;
+constexpr int kBarBytes = 512;  // mbarriers, TMEM address, abort flag
+constexpr int SMEM_BYTES = OFF_BAR + kBarBytes + 1024;  // + slack for 1024-byte alignment
 
 enum Bar {
   B_Q_FULL = 0,
@@ -52,16 +53,18 @@ enum Bar {
   B_V_EMPTY = B_V_FULL + kStages,     // kStages
   B_S_FULL = B_V_EMPTY + kStages,     // per tile X
   B_S_FREE = B_S_FULL + 2,
-  B_P_FULL = B_S_FREE + 2,            // per tile X and P buffer: 2 * X + (j & 1)
-  B_PV_DONE = B_P_FULL + 4,
+  B_P_FULL = B_S_FREE + 2,
+  B_PV_DONE = B_P_FULL + 2,
   B_O_FINAL = B_PV_DONE + 2,         // once per tile: its last P V completed
   B_MMA_DONE = B_O_FINAL + 2,
   B_COUNT
 };
+static_assert(8 * B_COUNT + 8 <= kBarBytes, "barrier region overflow");
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;    // S_X at 128 * X
 constexpr uint32_t kColO = 256;  // O_X at 256 + 64 * X
+constexpr uint32_t kColP = 384;  // P_X at 384 + 64 * X
 
 constexpr uint32_t kIdescS = make_idesc_bf16(128, 128, false, false);  // Q K^T
 constexpr uint32_t kIdescO = make_idesc_bf16(128, 64, false, true);    // P V (V MN-major)
@@ -111,8 +114,7 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars[B_S_FULL + x], 1);
       mbar_init(&bars[B_S_FREE + x], 128);
-      mbar_init(&bars[B_P_FULL + 2 * x], 128);
-      mbar_init(&bars[B_P_FULL + 2 * x + 1], 128);
+      mbar_init(&bars[B_P_FULL + x], 128);
       mbar_init(&bars[B_PV_DONE + x], 1);
       mbar_init(&bars[B_O_FINAL + x], 1);
     }
@@ -132,7 +134,6 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
   uint8_t* sQ = smem + OFF_Q;
   uint8_t* sK = smem + OFF_K;
   uint8_t* sV = smem + OFF_V;
-  uint8_t* sP = smem + OFF_P;
 
   if (warp == 13 || warp == 14) {
     // ------------------------------------ TMA producers: warp 13 K, warp 14 V
@@ -150,7 +151,8 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
         tma_load_3d(sQ, &tmQ, &bars[B_Q_FULL], 0, h, start + rowA);
         tma_load_3d(sQ + kTileBytes, &tmQ, &bars[B_Q_FULL], 0, h, start + rowA + kBM);
       }
-      int last_issued[kStages] = {-1, -1};
+      int last_issued[kStages];
+      for (int s = 0; s < kStages; ++s) last_issued[s] = -1;
       for (int j = 0; j < nkv; ++j) {
         const int s = j % kStages;
         if (j >= kStages &&
@@ -213,18 +215,14 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
           const uint32_t aV = smem_u32(sV + s * kTileBytes);
           for (int x = 0; x < 2 && ok; ++x) {
             if (jj >= nkvX[x]) continue;
-            // One barrier per P buffer: the softmax may already have filled the
-            // other buffer, but it cannot refill this one before this P V is issued.
-            if (!mbar_wait(&bars[B_P_FULL + 2 * x + (jj & 1)], (jj >> 1) & 1, abort_flag, p.status, 5)) {
+            if (!mbar_wait(&bars[B_P_FULL + x], jj & 1, abort_flag, p.status, 5)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t aP = smem_u32(sP + (2 * x + (jj & 1)) * 2 * kTileBytes);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)  // K = 128 keys in steps of 16
-              umma_bf16_ss(tmem + kColO + 64 * x,
-                           make_sdesc_sw128(aP + (kk >> 2) * kTileBytes + (kk & 3) * 32, 16, 1024),
+            for (int kk = 0; kk < 8; ++kk)  // K = 128 keys in steps of 16 (8 packed P columns)
+              umma_bf16_ts(tmem + kColO + 64 * x, tmem + kColP + 64 * x + kk * 8,
                            make_sdesc_sw128(aV + kk * 2048, kTileBytes, 1024), kIdescO,
                            (jj > 0 || kk > 0) ? 1u : 0u);
             umma_commit(&bars[B_PV_DONE + x]);
@@ -277,6 +275,7 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_base + kColS + 128 * x;
     const uint32_t tO = tmem + lane_base + kColO + 64 * x;
+    const uint32_t tP = tmem + lane_base + kColP + 64 * x;
     const float sl2 = p.scale_log2;
     float m_ref = 0.f;  // reference max (log2 units) the P values are taken against
     float l_sum = 0.f;
@@ -320,55 +319,51 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
         alpha = (j == 0) ? 0.f : ex2_approx(m_ref - mx);
         m_ref = mx;
       }
-      if (j > 0 && __any_sync(0xffffffffu, grow)) {
-        // O_X must be stable: wait for the P V of the previous tile.
+      // P = 2^(x - m_ref) in bf16 pairs, computed before P_X / O_X are touched.
+      const uint64_t sl2x2 = f2_pack(sl2, sl2);
+      const uint64_t negm2 = f2_pack(-m_ref, -m_ref);
+      uint64_t acc[4] = {0, 0, 0, 0};  // packed partial row sums (0 = +0.f, +0.f)
+      uint32_t pw[64];
+#pragma unroll
+      for (int c = 0; c < 128; c += 2) {
+        const uint64_t t = f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])),
+                                  sl2x2, negm2);
+        float t0, t1;
+        f2_unpack(t, t0, t1);
+        const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+        acc[(c >> 1) & 3] = f2_add(acc[(c >> 1) & 3], f2_pack(p0, p1));
+        pw[c >> 1] = pack_bf16x2(p0, p1);
+      }
+      float rs0, rs1;
+      f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), rs0, rs1);
+      const float rs = rs0 + rs1;
+      // P_X and O_X are in use by the P V of the previous tile until it
+      // completes (waited every tile, so PV_DONE is never two phases behind).
+      if (j > 0) {
         if (!mbar_wait_warp(&bars[B_PV_DONE + x], (j - 1) & 1, abort_flag, p.status, 9)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        uint32_t o[32];
+        if (__any_sync(0xffffffffu, grow)) {
+          uint32_t o[32];
 #pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          tmem_ld_x32(tO + half * 32, o);
-          tmem_ld_wait(o);
+          for (int half = 0; half < 2; ++half) {
+            tmem_ld_x32(tO + half * 32, o);
+            tmem_ld_wait(o);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-          tmem_st_x32(tO + half * 32, o);
-          tmem_st_wait();  // the store has consumed `o` before it is reloaded
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            tmem_st_x32(tO + half * 32, o);
+            tmem_st_wait();  // the store has consumed `o` before it is reloaded
+          }
         }
-        tc_fence_before();
       }
-      // P = 2^(x - m_ref) in bf16 to the swizzled K-major P buffer.  That
-      // buffer was last read by the P V of tile j-2, which completed before
-      // S_X(j) did (tcgen05 operations complete in issue order).
-      uint8_t* pbuf = sP + (2 * x + (j & 1)) * 2 * kTileBytes;
-      const uint64_t sl2x2 = f2_pack(sl2, sl2);
-      const uint64_t negm2 = f2_pack(-m_ref, -m_ref);
-      uint64_t acc[4] = {0, 0, 0, 0};  // packed partial row sums (0 = +0.f, +0.f)
-#pragma unroll
-      for (int c16 = 0; c16 < 16; ++c16) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c = 8 * c16 + 2 * e;
-          const uint64_t t = f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])),
-                                    sl2x2, negm2);
-          float t0, t1;
-          f2_unpack(t, t0, t1);
-          const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
-          acc[e] = f2_add(acc[e], f2_pack(p0, p1));
-          w[e] = pack_bf16x2(p0, p1);
-        }
-        *reinterpret_cast<uint4*>(pbuf + (c16 >> 3) * kTileBytes + sw128_offset(r, c16 & 7)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
-      }
-      float rs0, rs1;
-      f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), rs0, rs1);
-      const float rs = rs0 + rs1;
+      tmem_st_x32(tP, pw);
+      tmem_st_x32(tP + 32, pw + 32);
+      tmem_st_wait();
       l_sum = l_sum * alpha + rs;
-      fence_proxy_async_smem();
-      mbar_arrive(&bars[B_P_FULL + 2 * x + (j & 1)]);
+      tc_fence_before();
+      mbar_arrive(&bars[B_P_FULL + x]);
     }
     // ---- epilogue: O / l and LSE for rows inside the sequence -------------
     // (O_FINAL completes exactly once; PV_DONE may by now be more than one
