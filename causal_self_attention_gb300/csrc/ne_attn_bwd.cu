@@ -26,7 +26,7 @@
 //               writes P^T to TMEM (A operand of dV) and dS^T to smem; after
 //               tile i it moves half h of dQ'_{i-1} (32 columns) from TMEM to
 //               a swizzled fp32 staging buffer and issues its bulk reduce-add
-//   warp 12     MMA: allocates TMEM; lane 0 issues the five MMAs per tile
+//   warp 12     MMA: allocates TMEM; one elected lane issues the five MMAs per tile
 //   warp 13     TMA: lane 0 loads K_j, V_j once and Q_i, dO_i (2 stages)
 //   warps 14-15 no role (complete the warpgroup for setmaxnreg)
 // TMEM columns: S^T 0-127, dP^T 128-255, dV 256-319, dK' 320-383, dQ' 384-447,
@@ -40,7 +40,7 @@ namespace bwd {
 
 constexpr int kThreads = 512;
 // Registers per thread of each warpgroup after setmaxnreg (launch: 128).
-constexpr uint32_t kRegsSoftmax = 168, kRegsRotate = 112, kRegsMma = 56;
+constexpr uint32_t kRegsSoftmax = 160, kRegsRotate = 120, kRegsMma = 72;
 static_assert(valid_reg_split(kRegsSoftmax, kRegsRotate, kRegsMma), "register split");
 constexpr int kQStages = 3;                          // Q_i / dO_i ring depth
 constexpr int OFF_K = 0;
@@ -224,72 +224,94 @@ __global__ void __launch_bounds__(512, 1)
     }
   } else if (warp == 12) {
     // ------------------------------------------------------------- MMA issuer
+    // The whole warp runs the loop and waits; the elected lane issues each
+    // group of MMAs together with the commits that track it.  Shared-memory
+    // descriptors are built once: a K step or a ring stage only adds a
+    // constant to the start-address field (16-byte units).
     regs_decrease<kRegsMma>();
-    if (lane == 0) {
-      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
-      const uint32_t aDST = smem_u32(sDST);
-      bool ok = mbar_wait(&bars[B_K_ROT], 0, abort_flag, p.status, 32);
-      // S^T = K' Q'^T and dP^T = V dO^T for query tile `it`.
-      auto issue_s_dp = [&](int it) -> bool {
-        const int s = it % kQStages;
-        if (!mbar_wait(&bars[B_Q_ROT + s], (it / kQStages) & 1, abort_flag, p.status, 33))
-          return false;
-        if (it >= 1 && !mbar_wait(&bars[B_S_FREE], (it - 1) & 1, abort_flag, p.status, 34))
-          return false;
-        tc_fence_after();
-        const uint32_t aQ = smem_u32(sQ + s * kTileBytes), aDO = smem_u32(sDO + s * kTileBytes);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_bf16_ss(tmem + kColS, make_sdesc_sw128(aK + kk * 32, 16, 1024),
-                       make_sdesc_sw128(aQ + kk * 32, 16, 1024), kIdescNN, kk > 0 ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_bf16_ss(tmem + kColDP, make_sdesc_sw128(aV + kk * 32, 16, 1024),
-                       make_sdesc_sw128(aDO + kk * 32, 16, 1024), kIdescNN, kk > 0 ? 1u : 0u);
-        umma_commit(&bars[B_S_FULL]);
-        return true;
-      };
-      if (ok) ok = issue_s_dp(0);
-      for (int it = 0; ok && it < n_it; ++it) {
-        const int s = it % kQStages;
-        if (it + 1 < n_it && !issue_s_dp(it + 1)) { ok = false; break; }
-        if (!mbar_wait(&bars[B_DS_FULL], it & 1, abort_flag, p.status, 35)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t aQ = smem_u32(sQ + s * kTileBytes), aDO = smem_u32(sDO + s * kTileBytes);
-        // dV += P^T dO  (A: P^T in TMEM, 16 queries = 8 packed columns per step;
-        // B: dO MN-major)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_bf16_ts(tmem + kColDV, tmem + kColPT + kk * 8,
-                       make_sdesc_sw128(aDO + kk * 2048, kTileBytes, 1024), kIdescKM,
-                       (it > 0 || kk > 0) ? 1u : 0u);
-        // dK' += dS^T Q'
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_bf16_ss(tmem + kColDK,
-                       make_sdesc_sw128(aDST + (kk >> 2) * kTileBytes + (kk & 3) * 32, 16, 1024),
-                       make_sdesc_sw128(aQ + kk * 2048, kTileBytes, 1024), kIdescKM,
-                       (it > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&bars[B_QDO_EMPTY + s]);  // dV and dK were the last readers of Q_i, dO_i
-        // dQ'_i = dS K'  (A: dS^T read MN-major, i.e. as dS; B: K' MN-major)
-        if (it >= 1 && !mbar_wait(&bars[B_DQ_FREE], (it - 1) & 1, abort_flag, p.status, 36)) {
+    constexpr uint64_t kTileD = kTileBytes >> 4;
+    const uint64_t dKk = make_sdesc_sw128(smem_u32(sK), 16, 1024);            // K' K-major
+    const uint64_t dKm = make_sdesc_sw128(smem_u32(sK), kTileBytes, 1024);    // K' MN-major
+    const uint64_t dVk = make_sdesc_sw128(smem_u32(sV), 16, 1024);            // V K-major
+    const uint64_t dQk0 = make_sdesc_sw128(smem_u32(sQ), 16, 1024);           // Q' K-major
+    const uint64_t dQm0 = make_sdesc_sw128(smem_u32(sQ), kTileBytes, 1024);   // Q' MN-major
+    const uint64_t dOk0 = make_sdesc_sw128(smem_u32(sDO), 16, 1024);          // dO K-major
+    const uint64_t dOm0 = make_sdesc_sw128(smem_u32(sDO), kTileBytes, 1024);  // dO MN-major
+    const uint64_t dSk = make_sdesc_sw128(smem_u32(sDST), 16, 1024);          // dS^T K-major
+    const uint64_t dSm = make_sdesc_sw128(smem_u32(sDST), kTileBytes, 1024);  // as dS, MN-major
+    bool ok = mbar_wait_warp(&bars[B_K_ROT], 0, abort_flag, p.status, 32);
+    // Iteration it issues S^T = K' Q'^T and dP^T = V dO^T of query tile it+1,
+    // then dV, dK' and dQ' of tile it (it = -1 only starts tile 0).
+    for (int it = -1; ok && it < n_it; ++it) {
+      if (it + 1 < n_it) {
+        const int n = it + 1, sn = n % kQStages;
+        if (!mbar_wait_warp(&bars[B_Q_ROT + sn], (n / kQStages) & 1, abort_flag, p.status, 33)) {
+          ok = false;
+          break;
+        }
+        if (n >= 1 && !mbar_wait_warp(&bars[B_S_FREE], (n - 1) & 1, abort_flag, p.status, 34)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        if (elect_one()) {
+          const uint64_t dQ = dQk0 + kTileD * sn, dO = dOk0 + kTileD * sn;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)  // K = 64 head dims: 32 bytes per step
+            umma_bf16_ss(tmem + kColS, dKk + 2 * kk, dQ + 2 * kk, kIdescNN, kk > 0 ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16_ss(tmem + kColDP, dVk + 2 * kk, dO + 2 * kk, kIdescNN, kk > 0 ? 1u : 0u);
+          umma_commit(&bars[B_S_FULL]);
+        }
+        __syncwarp();
+      }
+      if (it < 0) continue;
+      const int s = it % kQStages;
+      if (!mbar_wait_warp(&bars[B_DS_FULL], it & 1, abort_flag, p.status, 35)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (elect_one()) {
+        const uint64_t dQm = dQm0 + kTileD * s, dOm = dOm0 + kTileD * s;
+        const uint32_t acc0 = it > 0 ? 1u : 0u;
+        // dV += P^T dO  (A: P^T in TMEM, 16 queries = 8 packed columns per step;
+        // B: dO MN-major, 16 rows = 2048 bytes per step)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_bf16_ss(tmem + kColDQ, make_sdesc_sw128(aDST + kk * 2048, kTileBytes, 1024),
-                       make_sdesc_sw128(aK + kk * 2048, kTileBytes, 1024), kIdescMM,
-                       kk > 0 ? 1u : 0u);
+          umma_bf16_ts(tmem + kColDV, tmem + kColPT + 8 * kk, dOm + 128 * kk, kIdescKM,
+                       kk > 0 ? 1u : acc0);
+        // dK' += dS^T Q'  (A: dS^T K-major, 64-query blocks 16 KiB apart)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16_ss(tmem + kColDK, dSk + kTileD * (kk >> 2) + 2 * (kk & 3), dQm + 128 * kk,
+                       kIdescKM, kk > 0 ? 1u : acc0);
+        umma_commit(&bars[B_QDO_EMPTY + s]);  // dV and dK were the last readers of Q_i, dO_i
+      }
+      __syncwarp();
+      // dQ'_i = dS K'  (A: dS^T read MN-major, i.e. as dS; B: K' MN-major)
+      if (it >= 1 && !mbar_wait_warp(&bars[B_DQ_FREE], (it - 1) & 1, abort_flag, p.status, 36)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // K = 128 keys: 16 rows = 2048 bytes per step
+          umma_bf16_ss(tmem + kColDQ, dSm + 128 * kk, dKm + 128 * kk, kIdescMM, kk > 0 ? 1u : 0u);
         umma_commit(&bars[B_DQ_FULL]);
         umma_commit(&bars[B_PDS_FREE]);
       }
-      umma_commit(&bars[B_MMA_DONE]);
-      const long long t0 = clock64();
-      while (!mbar_try_wait(&bars[B_MMA_DONE], 0) && clock64() - t0 < NE_WAIT_LIMIT_CYCLES) {
-      }
+      __syncwarp();
     }
+    // Drain: every MMA issued above completes before TMEM is released.
+    if (elect_one()) umma_commit(&bars[B_MMA_DONE]);
+    __syncwarp();
+    const long long t0 = clock64();
+    while (!mbar_try_wait(&bars[B_MMA_DONE], 0) && clock64() - t0 < NE_WAIT_LIMIT_CYCLES) {
+    }
+    __syncwarp();
   } else if (warp >= 12) {
     regs_decrease<kRegsMma>();
   } else if (warp < 4) {

@@ -10,13 +10,13 @@
 // softmax runs the tensor core works on the other tile's MMAs.
 //
 // Warp roles (512 threads, registers re-split per warpgroup with setmaxnreg):
-//   warps 0-3   softmax A: thread t owns row t of tile A (TMEM lane t), 176 regs
+//   warps 0-3   softmax A: thread t owns row t of tile A (TMEM lane t), 168 regs
 //   warps 4-7   softmax B: same for tile B
 //   warps 8-11  rotate: RoPE on Q_A, Q_B once and on every K tile in smem, 112
-//   warp 12     MMA: allocates TMEM; lane 0 issues S_X = Q_X K^T, O_X += P_X V
+//   warp 12     MMA: allocates TMEM; one elected lane issues S_X = Q_X K^T, O_X += P_X V
 //   warp 13     TMA: lane 0 loads Q_A, Q_B once and the K ring (5 stages)
 //   warp 14     TMA: lane 0 loads the V ring (5 stages); warps 12-15 run at
-//               48 regs
+//               64 regs
 // TMEM columns: S_A 0-127, S_B 128-255, O_A 256-319, O_B 320-383,
 // P_A 384-447, P_B 448-511 (bf16 pairs: P is the TMEM A operand of P V).
 // A softmax thread loads its whole S row with one TMEM round trip and frees
@@ -33,7 +33,7 @@ namespace fwd {
 
 constexpr int kThreads = 512;
 // Registers per thread of each warpgroup after setmaxnreg (launch: 128).
-constexpr uint32_t kRegsSoftmax = 176, kRegsRotate = 112, kRegsMma = 48;
+constexpr uint32_t kRegsSoftmax = 168, kRegsRotate = 112, kRegsMma = 64;
 static_assert(valid_reg_split(kRegsSoftmax, kRegsRotate, kRegsMma), "register split");
 constexpr int kStages = 5;                            // K ring and V ring
 constexpr int OFF_Q = 0;                              // Q_A, Q_B
@@ -176,68 +176,83 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
     }
   } else if (warp == 12) {
     // ------------------------------------------------------------- MMA issuer
+    // The whole warp runs the loop and waits; the elected lane issues each
+    // group of MMAs together with the commit that tracks it.  Shared-memory
+    // descriptors are built once: a K step, a tile or a ring stage only adds a
+    // constant to the start-address field (16-byte units).
     regs_decrease<kRegsMma>();
-    if (lane == 0) {
-      const int nkvX[2] = {nkvA, nkvB};
-      bool ok = mbar_wait(&bars[B_Q_ROT], 0, abort_flag, p.status, 2);
-      for (int j = 0; ok && j <= nkv; ++j) {
-        if (j < nkv) {
-          const int s = j % kStages;
-          if (!mbar_wait(&bars[B_K_ROT + s], (j / kStages) & 1, abort_flag, p.status, 3)) {
-            ok = false;
-            break;
-          }
-          const uint32_t aK = smem_u32(sK + s * kTileBytes);
-          for (int x = 0; x < 2 && ok; ++x) {
-            if (j >= nkvX[x]) continue;
-            if (j >= 1 && !mbar_wait(&bars[B_S_FREE + x], (j - 1) & 1, abort_flag, p.status, 4)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t aQ = smem_u32(sQ + x * kTileBytes);
+    constexpr uint64_t kTileD = kTileBytes >> 4;
+    const uint64_t dQ0 = make_sdesc_sw128(smem_u32(sQ), 16, 1024);          // Q K-major
+    const uint64_t dK0 = make_sdesc_sw128(smem_u32(sK), 16, 1024);          // K K-major
+    const uint64_t dV0 = make_sdesc_sw128(smem_u32(sV), kTileBytes, 1024);  // V MN-major
+    bool ok = mbar_wait_warp(&bars[B_Q_ROT], 0, abort_flag, p.status, 2);
+    for (int j = 0; ok && j <= nkv; ++j) {
+      if (j < nkv) {
+        const int s = j % kStages;
+        if (!mbar_wait_warp(&bars[B_K_ROT + s], (j / kStages) & 1, abort_flag, p.status, 3)) {
+          ok = false;
+          break;
+        }
+        const uint64_t dK = dK0 + kTileD * s;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)  // K = 64 head dims in steps of 16
-              umma_bf16_ss(tmem + kColS + 128 * x, make_sdesc_sw128(aQ + kk * 32, 16, 1024),
-                           make_sdesc_sw128(aK + kk * 32, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+        for (int x = 0; x < 2; ++x) {
+          if (!ok || j >= (x ? nkvB : nkvA)) continue;
+          if (j >= 1 && !mbar_wait_warp(&bars[B_S_FREE + x], (j - 1) & 1, abort_flag, p.status, 4)) {
+            ok = false;
+            continue;
+          }
+          tc_fence_after();
+          if (elect_one()) {
+            const uint64_t dQ = dQ0 + kTileD * x;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)  // K = 64 head dims: 32 bytes per step
+              umma_bf16_ss(tmem + kColS + 128 * x, dQ + 2 * kk, dK + 2 * kk, kIdescS,
+                           kk > 0 ? 1u : 0u);
             umma_commit(&bars[B_S_FULL + x]);
+            if (x == 1 || j >= nkvB) umma_commit(&bars[B_K_EMPTY + s]);
           }
-          if (!ok) break;
-          umma_commit(&bars[B_K_EMPTY + s]);
+          __syncwarp();
         }
-        if (j >= 1) {
-          const int jj = j - 1;
-          const int s = jj % kStages;
-          if (!mbar_wait(&bars[B_V_FULL + s], (jj / kStages) & 1, abort_flag, p.status, 13)) {
-            ok = false;
-            break;
-          }
-          const uint32_t aV = smem_u32(sV + s * kTileBytes);
-          for (int x = 0; x < 2 && ok; ++x) {
-            if (jj >= nkvX[x]) continue;
-            if (!mbar_wait(&bars[B_P_FULL + x], jj & 1, abort_flag, p.status, 5)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)  // K = 128 keys in steps of 16 (8 packed P columns)
-              umma_bf16_ts(tmem + kColO + 64 * x, tmem + kColP + 64 * x + kk * 8,
-                           make_sdesc_sw128(aV + kk * 2048, kTileBytes, 1024), kIdescO,
-                           (jj > 0 || kk > 0) ? 1u : 0u);
-            umma_commit(&bars[B_PV_DONE + x]);
-            if (jj == nkvX[x] - 1) umma_commit(&bars[B_O_FINAL + x]);
-          }
-          if (!ok) break;
-          umma_commit(&bars[B_V_EMPTY + s]);
-        }
+        if (!ok) break;
       }
-      // Drain: every MMA issued above completes before TMEM is released.
-      umma_commit(&bars[B_MMA_DONE]);
-      const long long t0 = clock64();
-      while (!mbar_try_wait(&bars[B_MMA_DONE], 0) && clock64() - t0 < NE_WAIT_LIMIT_CYCLES) {
+      if (j >= 1) {
+        const int jj = j - 1;
+        const int s = jj % kStages;
+        if (!mbar_wait_warp(&bars[B_V_FULL + s], (jj / kStages) & 1, abort_flag, p.status, 13)) {
+          ok = false;
+          break;
+        }
+        const uint64_t dV = dV0 + kTileD * s;
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          if (!ok || jj >= (x ? nkvB : nkvA)) continue;
+          if (!mbar_wait_warp(&bars[B_P_FULL + x], jj & 1, abort_flag, p.status, 5)) {
+            ok = false;
+            continue;
+          }
+          tc_fence_after();
+          if (elect_one()) {
+            const uint32_t acc0 = jj > 0 ? 1u : 0u;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)  // K = 128 keys: 8 packed P columns, 16 V rows
+              umma_bf16_ts(tmem + kColO + 64 * x, tmem + kColP + 64 * x + 8 * kk,
+                           dV + 128 * kk, kIdescO, kk > 0 ? 1u : acc0);
+            umma_commit(&bars[B_PV_DONE + x]);
+            if (jj == (x ? nkvB : nkvA) - 1) umma_commit(&bars[B_O_FINAL + x]);
+            if (x == 1 || jj >= nkvB) umma_commit(&bars[B_V_EMPTY + s]);
+          }
+          __syncwarp();
+        }
+        if (!ok) break;
       }
     }
+    // Drain: every MMA issued above completes before TMEM is released.
+    if (elect_one()) umma_commit(&bars[B_MMA_DONE]);
+    __syncwarp();
+    const long long t0 = clock64();
+    while (!mbar_try_wait(&bars[B_MMA_DONE], 0) && clock64() - t0 < NE_WAIT_LIMIT_CYCLES) {
+    }
+    __syncwarp();
   } else if (warp >= 12) {
     // warp 15: no role (it completes the warpgroup for setmaxnreg)
     regs_decrease<kRegsMma>();

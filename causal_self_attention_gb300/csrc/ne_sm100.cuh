@@ -79,6 +79,21 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
   return __all_sync(0xffffffffu, ok);
 }
 
+// One lane of a fully converged warp gets true (elect.sync).  The MMA issuers
+// run their loops with the whole warp and issue each group of tcgen05.mma from
+// the elected lane: a loop that runs in a single-lane divergent branch pays
+// several times more issue slots per MMA once the neighbouring warps of the
+// SM sub-partition keep it busy.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .b32 rx;\n\t.reg .pred px;\n\t"
+      "elect.sync rx|px, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, px;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // Per-warpgroup register reallocation (all four warps of a warpgroup execute
 // the same one).  The attention kernels launch 512 threads at 128 registers
 // and re-split them per warpgroup; a decrease cannot go above 128, and the
