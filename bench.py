@@ -336,7 +336,8 @@ def run_ours(args):
                 "traffic": recorded_traffic(dom)}
     # HBM-bound helpers: algorithmic bytes / time.
     n_el = B * T * H * D
-    pre_bytes = 2 * n_el * 2 + B * H * T * 4 + n_el * 4  # read O, dO; write D, zero dQ'
+    # read O, dO, q, k; write D, zero dQ', write q', k'
+    pre_bytes = 4 * n_el * 2 + B * H * T * 4 + n_el * 4 + 2 * n_el * 2
     post_bytes = n_el * 4 + n_el * 2                      # read dQ', write dQ
     kernels = {
         "ne_attn_fwd_kernel": {"ms": per_kernel["ne_attn_fwd_kernel"],

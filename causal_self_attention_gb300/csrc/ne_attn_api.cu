@@ -260,8 +260,6 @@ ne_status run_bwd(const Shape& s, const void* q, const void* k, const void* v, c
   p.status = st->status;
   if ((rc = rope_table(*st, rope_base, n_tiles * 128, &p.rope)) != NE_OK) return rc;
   CUtensorMap tq, tk, tv, tdo;
-  if ((rc = encode_rows(&tq, q, s.n_tot, s.H)) != NE_OK) return rc;
-  if ((rc = encode_rows(&tk, k, s.n_tot, s.H)) != NE_OK) return rc;
   if ((rc = encode_rows(&tv, v, s.n_tot, s.H)) != NE_OK) return rc;
   if ((rc = encode_rows(&tdo, dout, s.n_tot, s.H)) != NE_OK) return rc;
   void* ws = workspace;
@@ -271,11 +269,21 @@ ne_status run_bwd(const Shape& s, const void* q, const void* k, const void* v, c
     if (e != cudaSuccess) return cuda_status(e);
     owned = true;
   }
+  // Workspace: [dQ' fp32][D fp32][q' bf16][k' bf16], each part 256-byte aligned.
   const size_t acc_bytes = align256(static_cast<size_t>(s.n_tot) * s.H * 64 * sizeof(float));
-  p.dq_acc = static_cast<float*>(ws);
-  p.delta = reinterpret_cast<float*>(static_cast<char*>(ws) + acc_bytes);
+  const size_t del_bytes = align256(static_cast<size_t>(s.n_tot) * s.H * sizeof(float));
+  const size_t rot_bytes = align256(static_cast<size_t>(s.n_tot) * s.H * 64 * 2);
+  char* wsb = static_cast<char*>(ws);
+  p.dq_acc = reinterpret_cast<float*>(wsb);
+  p.delta = reinterpret_cast<float*>(wsb + acc_bytes);
+  p.qr = reinterpret_cast<__nv_bfloat16*>(wsb + acc_bytes + del_bytes);
+  p.kr = reinterpret_cast<__nv_bfloat16*>(wsb + acc_bytes + del_bytes + rot_bytes);
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k);
   CUtensorMap tdq;
-  rc = encode_rows_f32(&tdq, p.dq_acc, s.n_tot, s.H);
+  rc = encode_rows(&tq, p.qr, s.n_tot, s.H);
+  if (rc == NE_OK) rc = encode_rows(&tk, p.kr, s.n_tot, s.H);
+  if (rc == NE_OK) rc = encode_rows_f32(&tdq, p.dq_acc, s.n_tot, s.H);
   cudaError_t e = rc == NE_OK ? ne::launch_bwd(tq, tk, tv, tdo, tdq, p, n_tiles, cs, g_ev_pre,
                                                 g_ev_main)
                               : cudaErrorInvalidValue;
@@ -283,6 +291,7 @@ ne_status run_bwd(const Shape& s, const void* q, const void* k, const void* v, c
     cudaError_t e2 = cudaFreeAsync(ws, cs);
     if (e == cudaSuccess) e = e2;
   }
+  if (rc != NE_OK) return rc;
   return cuda_status(e);
 }
 
@@ -328,7 +337,8 @@ const char* ne_status_string(ne_status s) {
 size_t ne_attn_bwd_workspace_bytes(int n_tot, int H, int D) {
   if (n_tot <= 0 || H <= 0 || D != 64) return 0;
   return align256(static_cast<size_t>(n_tot) * H * 64 * sizeof(float)) +
-         align256(static_cast<size_t>(n_tot) * H * sizeof(float));
+         align256(static_cast<size_t>(n_tot) * H * sizeof(float)) +
+         2 * align256(static_cast<size_t>(n_tot) * H * 64 * 2);
 }
 
 ne_status ne_attn_fwd(const ne_bf16* q, const ne_bf16* k, const ne_bf16* v, int B, int H, int T,

@@ -1,9 +1,13 @@
-// ne_attn_bwd.cu -- backward of causal self-attention with fused RoPE, sm_103a.
+// ne_attn_bwd.cu -- backward of causal self-attention with RoPE, sm_103a.
 //
 // Three kernels on one stream (gradients hand-derived, no autograd, as the
 // NanoEuler Show HN page, paragraph 2, describes for its engine):
-//   1. preprocess: D_m = dO_m . O_m (fp32, [H, N_tot]) and zero the fp32 dQ'
-//      accumulator;
+//   1. preprocess, once per element: D_m = dO_m . O_m (fp32, [H, N_tot]); zero
+//      the fp32 dQ' accumulator; and q' = R(m) q, k' = R(n) k into bf16
+//      workspace buffers with the forward's fp32 rule, so the main kernel
+//      multiplies exactly the operands the forward did and rotates nothing
+//      (a query tile is used by every key tile at or before it: rotating it
+//      there would repeat the work once per key tile);
 //   2. main: one CTA per (128-key tile j, head, sequence) walks the query
 //      tiles i >= j, recomputing P from the saved LSE:
 //        S^T  = K' Q'^T,  P^T = exp(scale S^T - LSE),  dP^T = V dO^T,
@@ -12,22 +16,18 @@
 //        (-> bulk tensor reduce-add),
 //      and at the end writes dV and dK = scale * R(n)^T dK' (bf16);
 //   3. postprocess: dQ = scale * R(m)^T dQ' (bf16).
-// q' = R(m) q and k' = R(n) k are rotated in shared memory right after their
-// TMA loads, as in the forward.
 //
 // Main-kernel warp roles (512 threads, registers re-split per warpgroup):
-//   warps 0-3   rotate: K_j once, then every Q_i as soon as it lands (up to
-//               three tiles ahead), staging -LSE_i and -D_i; table rows and
-//               row terms prefetched one tile ahead
+//   warps 0-3   row terms and dQ': stage -LSE_i and -D_i two tiles ahead;
+//               after tile i, move dQ'_i (64 fp32 columns per query row) from TMEM to two swizzled staging buffers and
+//               issue their bulk reduce-adds
 //   warps 4-7   softmax, query columns 0-63 of the tile (thread t: key row t)
 //   warps 8-11  softmax, query columns 64-127; a softmax thread reads its S^T
 //               and dP^T half-rows in one TMEM round trip and frees them at
 //               once, so the next tile's S^T/dP^T MMAs overlap its math; it
-//               writes P^T to TMEM (A operand of dV) and dS^T to smem; after
-//               tile i it moves half h of dQ'_{i-1} (32 columns) from TMEM to
-//               a swizzled fp32 staging buffer and issues its bulk reduce-add
+//               writes P^T to TMEM (A operand of dV) and dS^T to smem
 //   warp 12     MMA: allocates TMEM; one elected lane issues the five MMAs per tile
-//   warp 13     TMA: lane 0 loads K_j, V_j once and Q_i, dO_i (2 stages)
+//   warp 13     TMA: lane 0 loads K'_j, V_j once and Q'_i, dO_i (3 stages)
 //   warps 14-15 no role (complete the warpgroup for setmaxnreg)
 // TMEM columns: S^T 0-127, dP^T 128-255, dV 256-319, dK' 320-383, dQ' 384-447,
 // P^T 448-511 (bf16 pairs).
@@ -40,8 +40,8 @@ namespace bwd {
 
 constexpr int kThreads = 512;
 // Registers per thread of each warpgroup after setmaxnreg (launch: 128).
-constexpr uint32_t kRegsSoftmax = 160, kRegsRotate = 120, kRegsMma = 72;
-static_assert(valid_reg_split(kRegsSoftmax, kRegsRotate, kRegsMma), "register split");
+constexpr uint32_t kRegsSoftmax = 168, kRegsDrain = 104, kRegsMma = 72;
+static_assert(valid_reg_split(kRegsSoftmax, kRegsDrain, kRegsMma), "register split");
 constexpr int kQStages = 3;                          // Q_i / dO_i ring depth
 constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + kTileBytes;
@@ -57,10 +57,9 @@ constexpr int SMEM_BYTES = OFF_BAR + kBarBytes + 1024;  // + slack for 1024-byte
 
 enum Bar {
   B_KV_FULL = 0,
-  B_K_ROT,
   B_QDO_FULL,                            // kQStages
-  B_Q_ROT = B_QDO_FULL + kQStages,       // kQStages
-  B_QDO_EMPTY = B_Q_ROT + kQStages,      // kQStages
+  B_ROW_FULL = B_QDO_FULL + kQStages,    // kQStages: -LSE_i, -D_i staged
+  B_QDO_EMPTY = B_ROW_FULL + kQStages,   // kQStages
   B_S_FULL = B_QDO_EMPTY + kQStages,
   B_S_FREE,
   B_DS_FULL,
@@ -80,44 +79,86 @@ constexpr uint32_t kIdescNN = make_idesc_bf16(128, 128, false, false);  // S^T, 
 constexpr uint32_t kIdescKM = make_idesc_bf16(128, 64, false, true);    // dV, dK
 constexpr uint32_t kIdescMM = make_idesc_bf16(128, 64, true, true);     // dQ
 
+constexpr int kPreRows = 16;   // rows per CTA of the preprocess
 constexpr int kPostRows = 16;  // rows per CTA of the dQ postprocess
 
 }  // namespace bwd
 
 // ---------------------------------------------------------------------------
-// 1. preprocess: delta[h, row] = sum_d dO . O ; zero dq_acc.  8 threads per
-//    (row, head) pair, each on 8 of the 64 elements.
+// 1. preprocess.  Grid (row blocks of kPreRows, sequences); 8 threads per
+//    (row, head) pair.  Thread `part` (0..7) of a pair:
+//      - multiplies its 8 of the 64 products dO . O (summed over the 8
+//        threads by shuffles) -> D_m;
+//      - zeroes its 8 floats of the dQ' accumulator row;
+//      - parts 0-3 rotate chunk `part` of q (dims 8c..8c+7) against chunk
+//        `part` + 4 into q', parts 4-7 the same chunks of k into k', with the
+//        fp32 rule of the forward's in-tile rotation (bitwise the same values).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256)
-    ne_attn_bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ out,
-                                  const __nv_bfloat16* __restrict__ dout, float* __restrict__ delta,
-                                  float* __restrict__ dq_acc, long long n_pairs, int H,
-                                  int n_tot) {
-  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long long pair = t >> 3;  // row * H + h
-  const int part = static_cast<int>(t & 7);
-  float acc = 0.f;
-  if (pair < n_pairs) {
-    const uint4 o = __ldg(reinterpret_cast<const uint4*>(out + pair * 64) + part);
-    const uint4 g = __ldg(reinterpret_cast<const uint4*>(dout + pair * 64) + part);
-    const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
-    const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+    ne_attn_bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ q,
+                                  const __nv_bfloat16* __restrict__ k,
+                                  const __nv_bfloat16* __restrict__ out,
+                                  const __nv_bfloat16* __restrict__ dout,
+                                  __nv_bfloat16* __restrict__ qr, __nv_bfloat16* __restrict__ kr,
+                                  float* __restrict__ delta, float* __restrict__ dq_acc,
+                                  const Problem pb, RopeTable rope) {
+  const int seq = blockIdx.y;
+  int start, len;
+  if (!seq_bounds(pb, seq, start, len, nullptr)) return;
+  const int t0 = blockIdx.x * bwd::kPreRows;
+  if (t0 >= len) return;
+  const int H = pb.H;
+  const int items = min(bwd::kPreRows, len - t0) * H * 8;
+  const int items_all = (items + 255) & ~255;  // every thread runs every round (shuffles)
+  for (int w = threadIdx.x; w < items_all; w += 256) {
+    const bool valid = w < items;
+    const int part = w & 7;
+    const int rh = w >> 3;
+    const int rr = rh / H, h = rh - rr * H;
+    const int pos = t0 + rr;
+    const long long pair = static_cast<long long>(start + pos) * H + h;
+    float acc = 0.f;
+    if (valid) {
+      const uint4 o = __ldg(reinterpret_cast<const uint4*>(out + pair * kHD) + part);
+      const uint4 g = __ldg(reinterpret_cast<const uint4*>(dout + pair * kHD) + part);
+      const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+      const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      acc = __fmaf_rn(bf16lo_to_f32(ow[w]), bf16lo_to_f32(gw[w]), acc);
-      acc = __fmaf_rn(bf16hi_to_f32(ow[w]), bf16hi_to_f32(gw[w]), acc);
+      for (int u = 0; u < 4; ++u) {
+        acc = __fmaf_rn(bf16lo_to_f32(ow[u]), bf16lo_to_f32(gw[u]), acc);
+        acc = __fmaf_rn(bf16hi_to_f32(ow[u]), bf16hi_to_f32(gw[u]), acc);
+      }
+      float4* z = reinterpret_cast<float4*>(dq_acc + pair * kHD) + part * 2;
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      // RoPE of one chunk pair of q (parts 0-3) or k (parts 4-7).
+      const int c = part & 3;
+      const __nv_bfloat16* src = (part < 4 ? q : k) + pair * kHD;
+      __nv_bfloat16* dst = (part < 4 ? qr : kr) + pair * kHD;
+      const uint4 lo = __ldg(reinterpret_cast<const uint4*>(src) + c);
+      const uint4 hi = __ldg(reinterpret_cast<const uint4*>(src) + c + 4);
+      const float4* cs = reinterpret_cast<const float4*>(rope.cs + static_cast<long long>(pos) * 32 + 8 * c);
+      uint32_t wl[4] = {lo.x, lo.y, lo.z, lo.w};
+      uint32_t wh[4] = {hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float4 t = __ldg(cs + u);  // (cos, sin) of dims 8c + 2u and 8c + 2u + 1
+        const float a0 = bf16lo_to_f32(wl[u]), a1 = bf16hi_to_f32(wl[u]);
+        const float b0 = bf16lo_to_f32(wh[u]), b1 = bf16hi_to_f32(wh[u]);
+        const float lo0 = __fmaf_rn(a0, t.x, -__fmul_rn(b0, t.y));
+        const float hi0 = __fmaf_rn(b0, t.x, __fmul_rn(a0, t.y));
+        const float lo1 = __fmaf_rn(a1, t.z, -__fmul_rn(b1, t.w));
+        const float hi1 = __fmaf_rn(b1, t.z, __fmul_rn(a1, t.w));
+        wl[u] = pack_bf16x2(lo0, lo1);
+        wh[u] = pack_bf16x2(hi0, hi1);
+      }
+      reinterpret_cast<uint4*>(dst)[c] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+      reinterpret_cast<uint4*>(dst)[c + 4] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
     }
-    float4* z = reinterpret_cast<float4*>(dq_acc + pair * 64) + part * 2;
-    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-  acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-  acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-  if (pair < n_pairs && part == 0) {
-    const long long row = pair / H;
-    const int h = static_cast<int>(pair - row * H);
-    delta[static_cast<long long>(h) * n_tot + row] = acc;
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    if (valid && part == 0) delta[static_cast<long long>(h) * pb.n_tot + start + pos] = acc;
   }
 }
 
@@ -153,10 +194,9 @@ __global__ void __launch_bounds__(512, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars[B_KV_FULL], 1);
-    mbar_init(&bars[B_K_ROT], 128);
     for (int s = 0; s < kQStages; ++s) {
       mbar_init(&bars[B_QDO_FULL + s], 1);
-      mbar_init(&bars[B_Q_ROT + s], 128);
+      mbar_init(&bars[B_ROW_FULL + s], 128);
       mbar_init(&bars[B_QDO_EMPTY + s], 1);
     }
     mbar_init(&bars[B_S_FULL], 1);
@@ -164,7 +204,7 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(&bars[B_DS_FULL], 256);
     mbar_init(&bars[B_PDS_FREE], 1);
     mbar_init(&bars[B_DQ_FULL], 1);
-    mbar_init(&bars[B_DQ_FREE], 256);
+    mbar_init(&bars[B_DQ_FREE], 128);
     mbar_init(&bars[B_MMA_DONE], 1);
     *abort_flag = 0;
     mbar_fence_init();
@@ -239,13 +279,13 @@ __global__ void __launch_bounds__(512, 1)
     const uint64_t dOm0 = make_sdesc_sw128(smem_u32(sDO), kTileBytes, 1024);  // dO MN-major
     const uint64_t dSk = make_sdesc_sw128(smem_u32(sDST), 16, 1024);          // dS^T K-major
     const uint64_t dSm = make_sdesc_sw128(smem_u32(sDST), kTileBytes, 1024);  // as dS, MN-major
-    bool ok = mbar_wait_warp(&bars[B_K_ROT], 0, abort_flag, p.status, 32);
+    bool ok = mbar_wait_warp(&bars[B_KV_FULL], 0, abort_flag, p.status, 32);
     // Iteration it issues S^T = K' Q'^T and dP^T = V dO^T of query tile it+1,
     // then dV, dK' and dQ' of tile it (it = -1 only starts tile 0).
     for (int it = -1; ok && it < n_it; ++it) {
       if (it + 1 < n_it) {
         const int n = it + 1, sn = n % kQStages;
-        if (!mbar_wait_warp(&bars[B_Q_ROT + sn], (n / kQStages) & 1, abort_flag, p.status, 33)) {
+        if (!mbar_wait_warp(&bars[B_QDO_FULL + sn], (n / kQStages) & 1, abort_flag, p.status, 33)) {
           ok = false;
           break;
         }
@@ -315,11 +355,10 @@ __global__ void __launch_bounds__(512, 1)
   } else if (warp >= 12) {
     regs_decrease<kRegsMma>();
   } else if (warp < 4) {
-    // ----------------------------------------------- RoPE and LSE/D staging
-    if constexpr (kRegsRotate < 128) regs_decrease<kRegsRotate>();
-    const int r = threadIdx.x;  // 0..127: tile row (key row for K, query row otherwise)
-    RopeRow tab;
-    rope_load_row(p.rope, kt * kBN + r, tab);
+    // ------------------------------------------------ row terms and dQ' drain
+    regs_decrease<kRegsDrain>();
+    const int r = threadIdx.x;  // 0..127: query row of the tile (TMEM lane r)
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     // LSE (log2 units) and D of query row r of tile `it`; rows past the
     // sequence get LSE = +inf, hence P = 0.
     auto load_rowstats = [&](int it, float& l2, float& dl) {
@@ -331,36 +370,59 @@ __global__ void __launch_bounds__(512, 1)
         dl = __ldg(p.delta + static_cast<long long>(h) * p.pb.n_tot + start + qpos);
       }
     };
-    // Rotate Q_it (and stage its LSE/D rows); table and row terms of Q_it
-    // were prefetched.
-    auto rotate_q = [&](int it, float l2, float dl) -> bool {
+    // Stored negated: P = 2^(fma(s, scale log2 e, -LSE)), dS = P (dP - D).
+    auto stage_rowstats = [&](int it, float l2, float dl) {
       const int s = it % kQStages;
-      if (!mbar_wait(&bars[B_QDO_FULL + s], (it / kQStages) & 1, abort_flag, p.status, 38))
-        return false;
-      rope_rotate_row(sQ + s * kTileBytes, r, tab);
-      sLSE[s * 128 + r] = -l2;  // stored negated: P = 2^(fma(s, scale log2e, -LSE))
+      sLSE[s * 128 + r] = -l2;
       sDEL[s * 128 + r] = -dl;
-      fence_proxy_async_smem();
-      mbar_arrive(&bars[B_Q_ROT + s]);
-      return true;
+      mbar_arrive(&bars[B_ROW_FULL + s]);
     };
-    bool ok = mbar_wait(&bars[B_KV_FULL], 0, abort_flag, p.status, 37);
-    if (ok) {
-      rope_rotate_row(sK, r, tab);
+    float l2, dl;
+    for (int it = 0; it < kQStages - 1 && it < n_it; ++it) {
+      load_rowstats(it, l2, dl);
+      stage_rowstats(it, l2, dl);
+    }
+    for (int it = 0; it < n_it; ++it) {
+      const int ahead = it + kQStages - 1;  // tile whose row terms are staged now
+      if (ahead < n_it) load_rowstats(ahead, l2, dl);  // loads in flight during the drain
+      // dQ'_it: TMEM -> swizzled fp32 staging (columns 0-31 and 32-63) ->
+      // two bulk tensor reduce-adds, issued by thread 0.
+      if (!mbar_wait_warp(&bars[B_DQ_FULL], it & 1, abort_flag, p.status, 43)) break;
+      tc_fence_after();
+      uint32_t v0[32], v1[32];
+      tmem_ld_x32(tmem + lane_base + kColDQ, v0);
+      tmem_ld_x32(tmem + lane_base + kColDQ + 32, v1);
+      tmem_ld_wait(v0);
+      tmem_ld_wait(v1);
+      tc_fence_before();
+      mbar_arrive(&bars[B_DQ_FREE]);
+      if (r == 0) bulk_wait_group_read0();  // the previous reductions have read the buffers
+      named_bar_sync(1, 128);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        *reinterpret_cast<uint4*>(sDQ + sw128_offset(r, c)) =
+            make_uint4(v0[4 * c], v0[4 * c + 1], v0[4 * c + 2], v0[4 * c + 3]);
+        *reinterpret_cast<uint4*>(sDQ + kTileBytes + sw128_offset(r, c)) =
+            make_uint4(v1[4 * c], v1[4 * c + 1], v1[4 * c + 2], v1[4 * c + 3]);
+      }
       fence_proxy_async_smem();
-      mbar_arrive(&bars[B_K_ROT]);
-      float l2, dl;
-      rope_load_row(p.rope, kt * kBM + r, tab);
-      load_rowstats(0, l2, dl);
-      for (int it = 0; ok && it < n_it; ++it) {
-        ok = rotate_q(it, l2, dl);
-        if (ok && it + 1 < n_it) {  // next tile's table rows and row terms
-          rope_load_row(p.rope, (kt + it + 1) * kBM + r, tab);
-          load_rowstats(it + 1, l2, dl);
-        }
+      named_bar_sync(1, 128);
+      if (r == 0) {
+        const int qrow = start + (kt + it) * kBM;
+        tma_reduce_add_3d(&tmDQ, sDQ, 0, h, qrow);
+        tma_reduce_add_3d(&tmDQ, sDQ + kTileBytes, 32, h, qrow);
+        bulk_commit_group();
+      }
+      if (ahead < n_it) {
+        // The stage of tile ahead last held tile it - 1, whose softmax has
+        // read it before the dV/dK MMAs that completed QDO_EMPTY.
+        if (it >= 1 && !mbar_wait(&bars[B_QDO_EMPTY + (it - 1) % kQStages],
+                                  ((it - 1) / kQStages) & 1, abort_flag, p.status, 44))
+          break;
+        stage_rowstats(ahead, l2, dl);
       }
     }
-
+    if (r == 0) bulk_wait_group0();
   } else {
     // --------------------------------------------------------- softmax warps
     regs_increase<kRegsSoftmax>();
@@ -369,37 +431,12 @@ __global__ void __launch_bounds__(512, 1)
     const int r = wq * 32 + lane;  // key row in tile
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const float sl2 = p.scale_log2;
-    // Columns 32*half .. +31 of dQ'_it: TMEM -> swizzled fp32 staging buffer
-    // `half` -> one bulk tensor reduce-add, issued by the warpgroup's thread 0.
-    auto reduce_dq_half = [&](int it) -> bool {
-      if (!mbar_wait_warp(&bars[B_DQ_FULL], it & 1, abort_flag, p.status, 43)) return false;
-      tc_fence_after();
-      uint32_t v[32];
-      tmem_ld_x32(tmem + lane_base + kColDQ + 32 * half, v);
-      tmem_ld_wait(v);
-      tc_fence_before();
-      mbar_arrive(&bars[B_DQ_FREE]);
-      uint8_t* buf = sDQ + half * kTileBytes;
-      if (r == 0) bulk_wait_group_read0();  // this buffer's previous reduction has read it
-      named_bar_sync(1 + half, 128);
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(buf + sw128_offset(r, c)) =
-            make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-      fence_proxy_async_smem();
-      named_bar_sync(1 + half, 128);
-      if (r == 0) {
-        tma_reduce_add_3d(&tmDQ, buf, 32 * half, h, start + (kt + it) * kBM);
-        bulk_commit_group();
-      }
-      return true;
-    };
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int s = it % kQStages;
       if (!mbar_wait_warp(&bars[B_S_FULL], it & 1, abort_flag, p.status, 39)) { ok = false; break; }
-      // LSE/D of this query tile were staged before Q_ROT[s] completed.
-      if (!mbar_wait_warp(&bars[B_Q_ROT + s], (it / kQStages) & 1, abort_flag, p.status, 40)) {
+      // LSE/D of this query tile are staged in stage s.
+      if (!mbar_wait_warp(&bars[B_ROW_FULL + s], (it / kQStages) & 1, abort_flag, p.status, 40)) {
         ok = false;
         break;
       }
@@ -460,10 +497,7 @@ __global__ void __launch_bounds__(512, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bars[B_DS_FULL]);
-      if (it >= 1 && !(ok = reduce_dq_half(it - 1))) break;
     }
-    if (ok) ok = reduce_dq_half(n_it - 1);
-    if (r == 0) bulk_wait_group0();
     // ---- epilogue: dV (first half) and dK = scale * R^T dK' (second half) --
     if (ok && mbar_wait_warp(&bars[B_MMA_DONE], 0, abort_flag, p.status, 42)) {
       tc_fence_after();
@@ -568,11 +602,9 @@ cudaError_t launch_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const long long n_pairs = static_cast<long long>(p.pb.n_tot) * p.pb.H;
-  const long long threads = n_pairs * 8;
-  const int blocks = static_cast<int>((threads + 255) / 256);
-  ne_attn_bwd_preprocess_kernel<<<blocks, 256, 0, stream>>>(p.out, p.dout, p.delta, p.dq_acc,
-                                                            n_pairs, p.pb.H, p.pb.n_tot);
+  dim3 pre_grid((n_tiles * kBM + bwd::kPreRows - 1) / bwd::kPreRows, p.pb.nseq);
+  ne_attn_bwd_preprocess_kernel<<<pre_grid, 256, 0, stream>>>(
+      p.q, p.k, p.out, p.dout, p.qr, p.kr, p.delta, p.dq_acc, p.pb, p.rope);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (ev_pre && (e = cudaEventRecord(ev_pre, stream)) != cudaSuccess) return e;

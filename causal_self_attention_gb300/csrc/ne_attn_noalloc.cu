@@ -1,8 +1,8 @@
 // ne_attn_noalloc.cu -- ne_attn_bwd_noalloc: the backward for callers that can
 // allocate no device memory (see include/ne_attn.h).  Everything the backward
 // needs beyond its inputs and outputs -- the RoPE cos/sin table, the fp32 dQ'
-// accumulator and the D_m row terms -- lives in one file-scope device array
-// owned by the library.  It launches the same kernels as ne_attn_bwd.
+// accumulator, the D_m row terms and the rotated copies q', k' -- lives in one
+// file-scope device array owned by the library.  It launches the same kernels as ne_attn_bwd.
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -22,14 +22,15 @@ ne_status internal_encode_rows_f32(CUtensorMap* map, void* base, int n_rows, int
 namespace {
 
 // Layout of the scratch: [RoPE table: positions x 32 (cos, sin)] [dQ' fp32
-// accumulator: rows x 64] [D_m: rows], each part 256-byte aligned.
+// accumulator: rows x 64] [D_m: rows] [q' bf16: rows x 64] [k' bf16: rows x
+// 64], each part 256-byte aligned.
 constexpr size_t kScratchBytes = NE_NOALLOC_SCRATCH_BYTES;
 constexpr int kMaxPositions = NE_NOALLOC_MAX_POSITIONS;
 constexpr long long kMaxRows = NE_NOALLOC_MAX_ROWS;
 constexpr size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 constexpr size_t kTableBytes = align256(static_cast<size_t>(kMaxPositions) * 32 * sizeof(float2));
 static_assert(kTableBytes + align256(kMaxRows * 64 * sizeof(float)) +
-                      align256(kMaxRows * sizeof(float)) <=
+                      align256(kMaxRows * sizeof(float)) + 2 * align256(kMaxRows * 64 * 2) <=
                   kScratchBytes,
               "scratch too small for the stated limits");
 
@@ -128,15 +129,22 @@ extern "C" ne_status ne_attn_bwd_noalloc(const ne_bf16* q, const ne_bf16* k, con
   p.status = status;
   p.rope.cs = reinterpret_cast<const float2*>(nd.scratch);
   p.rope.capacity = kMaxPositions;
-  // The dQ' accumulator is zeroed by the preprocess kernel of every call and
-  // D_m is overwritten, so nothing left by an earlier call is read.
-  p.dq_acc = reinterpret_cast<float*>(nd.scratch + kTableBytes);
-  p.delta = reinterpret_cast<float*>(nd.scratch + kTableBytes +
-                                     align256(static_cast<size_t>(rows) * 64 * sizeof(float)));
+  // The preprocess kernel of every call zeroes the dQ' accumulator and
+  // overwrites D_m, q' and k', so nothing left by an earlier call is read.
+  const size_t acc_bytes = align256(static_cast<size_t>(rows) * 64 * sizeof(float));
+  const size_t del_bytes = align256(static_cast<size_t>(rows) * sizeof(float));
+  const size_t rot_bytes = align256(static_cast<size_t>(rows) * 64 * 2);
+  unsigned char* w = nd.scratch + kTableBytes;
+  p.dq_acc = reinterpret_cast<float*>(w);
+  p.delta = reinterpret_cast<float*>(w + acc_bytes);
+  p.qr = reinterpret_cast<__nv_bfloat16*>(w + acc_bytes + del_bytes);
+  p.kr = reinterpret_cast<__nv_bfloat16*>(w + acc_bytes + del_bytes + rot_bytes);
+  p.q = reinterpret_cast<const __nv_bfloat16*>(q);
+  p.k = reinterpret_cast<const __nv_bfloat16*>(k);
 
   CUtensorMap tq, tk, tv, tdo, tdq;
-  if ((rc = ne::internal_encode_rows(&tq, q, n_tot, H)) != NE_OK) return rc;
-  if ((rc = ne::internal_encode_rows(&tk, k, n_tot, H)) != NE_OK) return rc;
+  if ((rc = ne::internal_encode_rows(&tq, p.qr, n_tot, H)) != NE_OK) return rc;
+  if ((rc = ne::internal_encode_rows(&tk, p.kr, n_tot, H)) != NE_OK) return rc;
   if ((rc = ne::internal_encode_rows(&tv, v, n_tot, H)) != NE_OK) return rc;
   if ((rc = ne::internal_encode_rows(&tdo, dout, n_tot, H)) != NE_OK) return rc;
   if ((rc = ne::internal_encode_rows_f32(&tdq, p.dq_acc, n_tot, H)) != NE_OK) return rc;

@@ -53,6 +53,10 @@ struct FwdParams {
 
 struct BwdParams {
   Problem pb;
+  const __nv_bfloat16* q;   // un-rotated inputs, read by the preprocess
+  const __nv_bfloat16* k;
+  __nv_bfloat16* qr;        // [N_tot, H, 64] bf16 workspace: q' = R(m) q
+  __nv_bfloat16* kr;        // [N_tot, H, 64] bf16 workspace: k' = R(n) k
   const __nv_bfloat16* out;
   const __nv_bfloat16* dout;
   const float* lse;

@@ -79,8 +79,10 @@ ne_status ne_attn_fwd_f32out(const ne_bf16* q, const ne_bf16* k, const ne_bf16* 
                              void* stream);
 
 /* Bytes of workspace ne_attn_bwd / ne_attn_varlen_bwd need for n_tot tokens
- * (B*T for fixed length) and H heads: an fp32 dQ accumulator [n_tot, H, D]
- * and the fp32 row terms D_m = dO_m . O_m [H, n_tot], each 256-byte aligned. */
+ * (B*T for fixed length) and H heads: an fp32 dQ accumulator [n_tot, H, D],
+ * the fp32 row terms D_m = dO_m . O_m [H, n_tot] and the rotated copies
+ * q' = R(m) q and k' = R(n) k (bf16 [n_tot, H, D] each), every part 256-byte
+ * aligned: 516 bytes per token and head at D = 64, plus alignment. */
 size_t ne_attn_bwd_workspace_bytes(int n_tot, int H, int D);
 
 /* Backward, fixed length.  q, k, v, out (the forward's O), dout: [B, T, H, 64]
@@ -154,7 +156,7 @@ ne_status ne_attn_set_bwd_phase_events(void* ev_after_preprocess, void* ev_after
  * work overlaps on the GPU -- on different streams, or on different host
  * threads -- race and must be serialized by the caller.  Results equal those
  * of ne_attn_bwd (dq up to the order of its fp32 atomic adds). */
-#define NE_NOALLOC_SCRATCH_BYTES (32u << 20)
+#define NE_NOALLOC_SCRATCH_BYTES (64u << 20)
 #define NE_NOALLOC_MAX_POSITIONS 16384
 #define NE_NOALLOC_MAX_ROWS 108000
 ne_status ne_attn_bwd_noalloc(const ne_bf16* q, const ne_bf16* k, const ne_bf16* v,

@@ -52,7 +52,8 @@ def test_status_strings_and_workspace(lib):
     assert lib.ne_status_string(5) == b"NE_ERR_TIMEOUT"
     lib.ne_attn_bwd_workspace_bytes.restype = ctypes.c_size_t
     ws = lib.ne_attn_bwd_workspace_bytes(8192, 12, 64)
-    assert ws == 8192 * 12 * 64 * 4 + 8192 * 12 * 4
+    # fp32 dQ' accumulator, fp32 D, bf16 q' and k' (all multiples of 256 here)
+    assert ws == 8192 * 12 * 64 * 4 + 8192 * 12 * 4 + 2 * 8192 * 12 * 64 * 2
     assert lib.ne_attn_bwd_workspace_bytes(8192, 12, 128) == 0
 
 
