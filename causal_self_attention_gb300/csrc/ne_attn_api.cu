@@ -96,24 +96,34 @@ ne_status get_encoder() {
   return NE_OK;
 }
 
+RopeTable table_view(float2* dev, int cap) {
+  return RopeTable{dev, reinterpret_cast<const float4*>(dev + static_cast<size_t>(cap) * 32), cap};
+}
+
 // RoPE table for (base, D = 64) covering at least `positions` positions:
 // cs[p * 32 + i] = ((float)cos(p * theta_i), (float)sin(p * theta_i)),
-// theta_i = base^(-(2i)/64), all in double before the final fp32 rounding.
+// theta_i = base^(-(2i)/64), all in double before the final fp32 rounding;
+// followed by the same values in the warp-interleaved layout of RopeTable::csw.
 ne_status rope_table(DeviceState& st, float base, int positions, RopeTable* out) {
   for (auto& e : st.tables)
     if (e.base == base && e.capacity >= positions) {
-      *out = RopeTable{e.dev, e.capacity};
+      *out = table_view(e.dev, e.capacity);
       return NE_OK;
     }
   int cap = 4096;
   while (cap < positions) cap *= 2;
-  std::vector<float2> host(static_cast<size_t>(cap) * 32);
+  std::vector<float2> host(static_cast<size_t>(cap) * 64);
+  float2* inter = host.data() + static_cast<size_t>(cap) * 32;
   for (int i = 0; i < 32; ++i) {
     const double theta = std::pow(static_cast<double>(base), -(2.0 * i) / 64.0);
     for (int pos = 0; pos < cap; ++pos) {
       const double a = static_cast<double>(pos) * theta;
-      host[static_cast<size_t>(pos) * 32 + i] =
+      const float2 v =
           make_float2(static_cast<float>(std::cos(a)), static_cast<float>(std::sin(a)));
+      host[static_cast<size_t>(pos) * 32 + i] = v;
+      // float4 (i / 2) of position pos = 32 g + l sits at ((16 g + i / 2) * 32 + l).
+      const size_t q4 = (static_cast<size_t>(pos >> 5) * 16 + (i >> 1)) * 32 + (pos & 31);
+      inter[q4 * 2 + (i & 1)] = v;
     }
   }
   float2* dev = nullptr;
@@ -130,11 +140,11 @@ ne_status rope_table(DeviceState& st, float base, int positions, RopeTable* out)
       st.retired.push_back(t.dev);
       t.dev = dev;
       t.capacity = cap;
-      *out = RopeTable{dev, cap};
+      *out = table_view(dev, cap);
       return NE_OK;
     }
   st.tables.push_back(RopeEntry{base, cap, dev});
-  *out = RopeTable{dev, cap};
+  *out = table_view(dev, cap);
   return NE_OK;
 }
 
@@ -489,7 +499,7 @@ ne_status ne_debug_tma_tile(const ne_bf16* src, int n_rows, int H, int h, int ro
   if ((rc = get_encoder()) != NE_OK) return rc;
   CUtensorMap tm;
   if ((rc = encode_rows(&tm, src, n_rows, H)) != NE_OK) return rc;
-  return cuda_status(ne::launch_debug_tile(tm, h, row0, 0, 0, RopeTable{nullptr, 0}, dst_raw,
+  return cuda_status(ne::launch_debug_tile(tm, h, row0, 0, 0, RopeTable{nullptr, nullptr, 0}, dst_raw,
                                            nullptr, st->status,
                                            static_cast<cudaStream_t>(stream)));
 }

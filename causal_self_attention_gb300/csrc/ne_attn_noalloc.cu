@@ -128,6 +128,7 @@ extern "C" ne_status ne_attn_bwd_noalloc(const ne_bf16* q, const ne_bf16* k, con
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = status;
   p.rope.cs = reinterpret_cast<const float2*>(nd.scratch);
+  p.rope.csw = nullptr;  // the backward reads the row layout only
   p.rope.capacity = kMaxPositions;
   // The preprocess kernel of every call zeroes the dQ' accumulator and
   // overwrites D_m, q' and k', so nothing left by an earlier call is read.

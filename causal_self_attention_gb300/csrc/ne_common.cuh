@@ -25,8 +25,12 @@ constexpr int NE_DEV_TIMEOUT_BASE = 0x100;  // + wait site id
 // RoPE table: for position p and frequency i < 32, rope[p * 32 + i] = (cos, sin)
 // of p * theta_i in fp32, each the fp32 rounding of the double value.
 struct RopeTable {
-  const float2* cs;
-  int capacity;  // number of positions
+  const float2* cs;   // row layout: cs[p * 32 + i] = (cos, sin) of p * theta_i
+  const float4* csw;  // the same values warp-interleaved: for the 32 positions
+                      // p = 32 g + l, csw[(16 g + c) * 32 + l] = (cos, sin, cos,
+                      // sin) of dims 2c, 2c + 1 of position p, so that a warp
+                      // reading 32 consecutive positions reads whole lines
+  int capacity;       // number of positions (a multiple of 32)
 };
 
 // One attention problem in the packed form: tokens are rows of [N_tot, H, 64];

@@ -11,9 +11,10 @@
 // projections.)
 //
 // The table row of a position (32 (cos, sin) pairs = 256 bytes) is loaded into
-// registers by rope_load_row ahead of time, so that the L2 latency of the
-// table is off the critical path; rope_rotate_row then only touches shared
-// memory.
+// registers by rope_load_row ahead of time, from the warp-interleaved copy of
+// the table (a warp's 32 consecutive positions come in 16 fully used
+// 512-byte pieces instead of 512 scattered 16-byte pieces), so that the table
+// is off the critical path; rope_rotate_row then only touches shared memory.
 #pragma once
 
 #include "ne_sm100.cuh"
@@ -26,9 +27,9 @@ struct RopeRow {
 
 __device__ __forceinline__ void rope_load_row(const RopeTable& rt, int pos, RopeRow& r) {
   if (pos >= rt.capacity) pos = rt.capacity - 1;  // only rows past the sequence end
-  const float4* cs = reinterpret_cast<const float4*>(rt.cs + static_cast<long long>(pos) * 32);
+  const float4* cs = rt.csw + static_cast<long long>(pos >> 5) * (16 * 32) + (pos & 31);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) r.t[i] = __ldg(cs + i);
+  for (int i = 0; i < 16; ++i) r.t[i] = __ldg(cs + 32 * i);
 }
 
 // Rotate one row (64 elements = 8 swizzled 16-byte chunks) of `tile` with the
