@@ -66,6 +66,24 @@ def rank_env():
             int(os.environ.get("WORLD_SIZE", "1")))
 
 
+def slowest_rank_ms(ms, world, device=None):
+    """The largest of the ranks' times (every rank gets it).  Replicas share
+    nothing, so the job is as fast as its slowest rank."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_step_per_rank, steps, ms, world):
+    """Whole-job throughput: the FLOPs of all ranks' steps over the slowest
+    rank's time for them (ms)."""
+    return world * flops_per_step_per_rank * steps / (ms * 1e-3) / 1e12
+
+
 # --------------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi clock/throttle samples of one GPU while it runs."""
@@ -274,12 +292,8 @@ def run_ours(args):
     t_main = [e[2].elapsed_time(e[3]) for e in ev]
     t_post = [e[3].elapsed_time(e[4]) for e in ev]
     t_step = [e[0].elapsed_time(e[4]) for e in ev]
-    total_ms = sum(t_step)
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
-    value = world * f_step * K / (total_ms * 1e-3) / 1e12
+    total_ms = slowest_rank_ms(sum(t_step), world, dev)
+    value = job_tflops(f_step, K, total_ms, world)
 
     # ---- end to end through the public API with host buffers ------------------
     # Every step uploads its q, k, v, dO from pinned host memory and downloads
@@ -344,12 +358,8 @@ def run_ours(args):
         return t0.elapsed_time(t1) / n_steps
 
     e2e_run(3)  # warm-up
-    e2e_ms = e2e_run(KE)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e_value = world * f_step / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = slowest_rank_ms(e2e_run(KE), world, dev)
+    e2e_value = job_tflops(f_step, 1, e2e_ms, world)
 
     if rank != 0:
         if world > 1:
