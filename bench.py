@@ -45,6 +45,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", choices=("train", "decode"), default="train",
+                    help="train: the fwd+bwd step (the headline); decode: one generation "
+                         "step against a KV cache (decode16k)")
     return ap.parse_args()
 
 
@@ -437,8 +440,138 @@ def run_ours(args):
     return 0
 
 
+# ------------------------------------------------------------------- decode
+DECODE_WORKLOAD = "decode16k"
+DECODE_METRIC = "decode attention KV-cache read GB/s at B8 H12 Tmax16384 D64"
+
+
+def decode_kv_bytes(inp):
+    """Algorithmic bytes of one decode step: every attended K and V row once."""
+    return sum(int(p) + 1 for p in inp["pos"]) * inp["H"] * inp["D"] * 2 * 2
+
+
+def run_decode(args):
+    import torch
+
+    from causal_self_attention_gb300 import build as nb
+    rank, local_rank, world = rank_env()
+    if world > 1 and rank != 0:
+        return 0  # one GPU is enough: the decode line is measured on rank 0 only
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    nb.build()
+    from causal_self_attention_gb300 import ne_attn as na
+    from causal_self_attention_gb300.inputs import make_decode
+
+    inp = make_decode(DECODE_WORKLOAD)
+    B, H, Tmax, D = inp["B"], inp["H"], inp["Tmax"], inp["D"]
+    base, scale = inp["rope_base"], inp["scale"]
+    q, kc, vc, pos = (inp[n].to(dev) for n in ("q", "k_cache", "v_cache", "pos"))
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    ws = torch.empty(na.ne_attn_decode_workspace_bytes(B, H, Tmax), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    kv_bytes = decode_kv_bytes(inp)
+
+    def step(s=stream):
+        na.ne_attn_decode(q, kc, vc, pos, base, scale, out=out, lse=lse, workspace=ws, stream=s)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    assert na.ne_attn_get_device_status() == 0
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    clocks = ClockSampler(local_rank)
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    for i in range(K):  # the cache (2 x 403 MB) is larger than L2: no flush needed
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    status = na.ne_attn_get_device_status()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    gbs = kv_bytes / (ms * 1e-3) / 1e9
+
+    # End to end: the new token's q, k, v rows uploaded into the cache, O and
+    # LSE read back, every step (the cache itself stays resident, as a KV
+    # cache does).
+    h_q = inp["q"].pin_memory()
+    h_k = inp["k_cache"][:, -1].contiguous().pin_memory()
+    h_v = inp["v_cache"][:, -1].contiguous().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    d_k = torch.empty_like(h_k, device=dev)
+    d_v = torch.empty_like(h_v, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v))
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+    KE = max(args.e2e_steps, 2)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    last = int(inp["pos"][0])
+    for _ in range(KE):
+        q.copy_(h_q, non_blocking=True)
+        d_k.copy_(h_k, non_blocking=True)
+        d_v.copy_(h_v, non_blocking=True)
+        kc[:, last].copy_(d_k)
+        vc[:, last].copy_(d_v)
+        step()
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = t0.elapsed_time(t1) / KE
+
+    peaks, peak_kind = load_peaks()
+    line = {
+        "metric": DECODE_METRIC, "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": K,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{DECODE_WORKLOAD}: B={B} H={H} Tmax={Tmax} D={D}, one new "
+                               "token per sequence at the last cache row, RoPE base 10000",
+                   "B": B, "H": H, "Tmax": Tmax, "D": D,
+                   "l2": "cache larger than L2 (2 x 403 MB)"},
+        "roofline": {"bound": "hbm", "kernel": "ne_attn_decode_split_kernel", "achieved": gbs,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                     "peak_source": f"{peak_kind} HBM copy (MEASURED_PEAKS.json)",
+                     "traffic": recorded_traffic("ne_attn_decode_split_kernel")},
+        "e2e": {"value": kv_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 2 * K,
+        "clocks": clk,
+        "device_status": status,
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        t_start = time.perf_counter()
+        done = 0
+        Lc = int(inp["pos"][0]) + 1
+        for b in range(B):
+            qs = torch.zeros((Lc, H, D), dtype=torch.bfloat16)
+            qs[Lc - 1] = inp["q"][b]
+            oracle.attention_sampled(qs, inp["k_cache"][b, :Lc], inp["v_cache"][b, :Lc], None,
+                                     [0, Lc], [(0, h, [Lc - 1], []) for h in range(H)],
+                                     base=base, scale=scale, mode=1)
+            done += Lc * H * D * 2 * 2
+            if time.perf_counter() - t_start > args.cpu_seconds:
+                break
+        sec = time.perf_counter() - t_start
+        line["cpu_baseline"] = {"value": done / sec / 1e9, "unit": "GB/s",
+                                "cores": oracle.num_threads(), "kind": "oracle",
+                                "sample": f"{done // (Lc * H * D * 4)} of {B} sequences' decode "
+                                          f"rows (all heads), {sec:.1f} s"}
+    print(json.dumps(line))
+    return 0
+
+
 def main():
     args = parse()
+    if args.path == "decode":
+        return run_decode(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -26,6 +26,11 @@ cudaError_t launch_debug_tile(const CUtensorMap& tm, int h, int row0, int rotate
                               int* status, cudaStream_t stream);
 cudaError_t launch_debug_umma(int form, const __nv_bfloat16* a, const __nv_bfloat16* b, float* d,
                               int* status, cudaStream_t stream);
+size_t decode_part_bytes(int B, int H, int Tmax);
+cudaError_t launch_decode(const __nv_bfloat16* q, const __nv_bfloat16* kc,
+                          const __nv_bfloat16* vc, const int* pos, int B, int H, int Tmax,
+                          const RopeTable& rope, float scale_log2, float* part,
+                          __nv_bfloat16* out, float* lse, int* status, cudaStream_t stream);
 }  // namespace ne
 
 namespace {
@@ -437,6 +442,52 @@ ne_status ne_attn_varlen_bwd(const ne_bf16* q, const ne_bf16* k, const ne_bf16* 
   s.D = D;
   return run_bwd(s, q, k, v, out, dout, lse, rope_base, scale, dq, dk, dv, workspace,
                  workspace_bytes, stream);
+}
+
+size_t ne_attn_decode_workspace_bytes(int B, int H, int Tmax) {
+  if (B <= 0 || H <= 0 || Tmax <= 0) return 0;
+  return ne::decode_part_bytes(B, H, Tmax);
+}
+
+ne_status ne_attn_decode(const ne_bf16* q, const ne_bf16* k_cache, const ne_bf16* v_cache,
+                         const int* pos, int B, int H, int Tmax, int D, float rope_base,
+                         float scale, ne_bf16* out, float* lse, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  if (!q || !k_cache || !v_cache || !pos || !out || !lse) return NE_ERR_INVALID_ARG;
+  if (D != 64) return NE_ERR_UNSUPPORTED;
+  if (B <= 0 || H <= 0 || Tmax <= 0) return NE_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale <= 0.f || !std::isfinite(rope_base) || rope_base <= 0.f)
+    return NE_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned4(pos) ||
+      !aligned4(out) || !aligned4(lse))
+    return NE_ERR_MISALIGNED;
+  const size_t need = ne::decode_part_bytes(B, H, Tmax);
+  if (workspace && workspace_bytes < need) return NE_ERR_INVALID_ARG;
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 15u)) return NE_ERR_MISALIGNED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState* st = nullptr;
+  ne_status rc = device_state(&st);
+  if (rc != NE_OK) return rc;
+  RopeTable rope;
+  if ((rc = rope_table(*st, rope_base, Tmax, &rope)) != NE_OK) return rc;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  void* ws = workspace;
+  bool owned = false;
+  if (!ws) {
+    cudaError_t e = cudaMallocAsync(&ws, need, cs);
+    if (e != cudaSuccess) return cuda_status(e);
+    owned = true;
+  }
+  cudaError_t e = ne::launch_decode(
+      reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k_cache),
+      reinterpret_cast<const __nv_bfloat16*>(v_cache), pos, B, H, Tmax, rope,
+      scale * 1.4426950408889634f, static_cast<float*>(ws), reinterpret_cast<__nv_bfloat16*>(out),
+      lse, st->status, cs);
+  if (owned) {
+    cudaError_t e2 = cudaFreeAsync(ws, cs);
+    if (e == cudaSuccess) e = e2;
+  }
+  return cuda_status(e);
 }
 
 ne_status ne_attn_set_bwd_phase_events(void* ev_after_preprocess, void* ev_after_main) {

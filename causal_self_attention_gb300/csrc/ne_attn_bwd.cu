@@ -113,7 +113,10 @@ __global__ void __launch_bounds__(256)
   for (int w = threadIdx.x; w < items_all; w += 256) {
     const bool valid = w < items;
     const int part = w & 7;
-    const int rh = w >> 3;
+    // A lane past the last item works on item 0 of the block (always inside
+    // the sequence) and discards the result, so that every address it forms
+    // is valid.
+    const int rh = valid ? (w >> 3) : 0;
     const int rr = rh / H, h = rh - rr * H;
     const int pos = t0 + rr;
     const long long pair = static_cast<long long>(start + pos) * H + h;
@@ -363,12 +366,14 @@ __global__ void __launch_bounds__(512, 1)
     // sequence get LSE = +inf, hence P = 0.
     auto load_rowstats = [&](int it, float& l2, float& dl) {
       const int qpos = (kt + it) * kBM + r;
-      l2 = INFINITY;
-      dl = 0.f;
-      if (qpos < len) {
-        l2 = __ldg(p.lse + lse_index(p.pb, h, seq, start, qpos)) * 1.4426950408889634f;
-        dl = __ldg(p.delta + static_cast<long long>(h) * p.pb.n_tot + start + qpos);
-      }
+      // The loads always address a row of the sequence (read-only loads may
+      // run ahead of the condition that guards them); rows past the end then
+      // take LSE = +inf.
+      const int qc = qpos < len ? qpos : len - 1;
+      const float l = __ldg(p.lse + lse_index(p.pb, h, seq, start, qc));
+      const float d = __ldg(p.delta + static_cast<long long>(h) * p.pb.n_tot + start + qc);
+      l2 = qpos < len ? l * 1.4426950408889634f : INFINITY;
+      dl = qpos < len ? d : 0.f;
     };
     // Stored negated: P = 2^(fma(s, scale log2 e, -LSE)), dS = P (dP - D).
     auto stage_rowstats = [&](int it, float l2, float dl) {

@@ -20,6 +20,18 @@ long16k    B=1, H=12, T=16384, D=64                long-sequence stress
 varlen     32 sequences, L ~ U[64, 2048], H=12     packed with cu_seqlens
 =========  =====================================  ====================================
 
+Decode workloads (one new token per sequence against a KV cache, the
+generation path of the NanoEuler Show HN page and "Tiny Hackable CUDA",
+section 7): ``make_decode`` draws q ``[B, H, D]`` and the un-rotated caches
+``[B, Tmax, H, D]`` (N(0,1), bf16) from ``manual_seed(2000 + index)`` in the
+order q, k, v; ``pos`` holds each sequence's position (the last cache row
+unless given).
+
+==========  ==============================  ============================
+decode1k    B=8, H=12, Tmax=1024, D=64      end of a GPT-2-small context
+decode16k   B=8, H=12, Tmax=16384, D=64     end of a long byte-level context
+==========  ==============================  ============================
+
 Recipe: ``torch.Generator('cpu').manual_seed(1000 + index)``; draw order:
 sequence lengths (varlen only, ``randint(64, 2049, (32,))``), then q, k, v, dO as
 float32 ``randn``, each rounded to bf16 (round to nearest even).  byte4k
@@ -39,6 +51,12 @@ CONFIGS = {
     "byte4k": dict(B=2, H=12, T=4096, D=64, qk_mult=2.0),
     "long16k": dict(B=1, H=12, T=16384, D=64, qk_mult=1.0),
     "varlen": dict(nseq=32, H=12, D=64, lmin=64, lmax=2048, qk_mult=1.0),
+}
+
+DECODE_NAMES = ("decode1k", "decode16k")
+DECODE_CONFIGS = {
+    "decode1k": dict(B=8, H=12, Tmax=1024, D=64),
+    "decode16k": dict(B=8, H=12, Tmax=16384, D=64),
 }
 
 ROPE_BASE = 10000.0
@@ -98,4 +116,26 @@ def make_custom(B: int, T: int, H: int, D: int = 64, seed: int = 0, qk_mult: flo
         if key in ("q", "k") and qk_mult != 1.0:
             x = x * qk_mult
         out[key] = x.to(torch.bfloat16)
+    return out
+
+
+def make_decode(name: str | None = None, B: int = 0, H: int = 0, Tmax: int = 0, D: int = 64,
+                positions=None, seed: int | None = None) -> dict:
+    """Inputs of a decode step: ``q`` ``[B, H, D]``, ``k_cache``/``v_cache``
+    ``[B, Tmax, H, D]`` (bf16, CPU) and ``pos`` (int32 ``[B]``, CPU).  Either a
+    named workload or explicit sizes; ``positions`` defaults to Tmax - 1."""
+    if name is not None:
+        cfg = DECODE_CONFIGS[name]
+        B, H, Tmax, D = cfg["B"], cfg["H"], cfg["Tmax"], cfg["D"]
+        seed = 2000 + DECODE_NAMES.index(name) if seed is None else seed
+    g = torch.Generator("cpu").manual_seed(0 if seed is None else seed)
+    out = dict(name=name or "custom", B=B, H=H, Tmax=Tmax, D=D, scale=1.0 / D ** 0.5,
+               rope_base=ROPE_BASE)
+    out["q"] = torch.randn((B, H, D), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    for key in ("k_cache", "v_cache"):
+        out[key] = torch.randn((B, Tmax, H, D), generator=g,
+                               dtype=torch.float32).to(torch.bfloat16)
+    if positions is None:
+        positions = [Tmax - 1] * B
+    out["pos"] = torch.tensor([int(x) for x in positions], dtype=torch.int32)
     return out

@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "NE_OK", 1: "NE_ERR_INVALID_ARG", 2: "NE_ERR_UNSUPPORTED",
                 7: "NE_ERR_BAD_SEQLEN", 8: "NE_ERR_TOO_LARGE"}
 
 EXPORTED = ("ne_attn_fwd", "ne_attn_fwd_f32out", "ne_attn_bwd", "ne_attn_bwd_workspace_bytes",
-            "ne_attn_bwd_noalloc",
+            "ne_attn_bwd_noalloc", "ne_attn_decode", "ne_attn_decode_workspace_bytes",
             "ne_attn_varlen_fwd", "ne_attn_varlen_fwd_f32out", "ne_attn_varlen_bwd",
             "ne_attn_set_bwd_phase_events", "ne_attn_get_device_status",
             "ne_attn_last_device_code", "ne_status_string",
@@ -60,6 +60,7 @@ def lib():
         "ne_attn_varlen_fwd": [P, P, P, P, I, I, I, I, I, F, F, P, P, P],
         "ne_attn_varlen_fwd_f32out": [P, P, P, P, I, I, I, I, I, F, F, P, P, P],
         "ne_attn_varlen_bwd": [P, P, P, P, P, P, P, I, I, I, I, I, F, F, P, P, P, P, Z, P],
+        "ne_attn_decode": [P, P, P, P, I, I, I, I, F, F, P, P, P, Z, P],
         "ne_attn_set_bwd_phase_events": [P, P],
         "ne_attn_get_device_status": [P],
         "ne_attn_last_device_code": [],
@@ -74,6 +75,8 @@ def lib():
         fn.restype = None if name == "ne_attn_release" else I
     L.ne_attn_bwd_workspace_bytes.argtypes = [I, I, I]
     L.ne_attn_bwd_workspace_bytes.restype = Z
+    L.ne_attn_decode_workspace_bytes.argtypes = [I, I, I]
+    L.ne_attn_decode_workspace_bytes.restype = Z
     L.ne_status_string.argtypes = [I]
     L.ne_status_string.restype = ctypes.c_char_p
     _lib = L
@@ -209,6 +212,35 @@ def ne_attn_varlen_bwd(q, k, v, out, dout, lse, cu_seqlens, max_seqlen, rope_bas
         cu_seqlens.numel() - 1, N, int(max_seqlen), H, D, float(rope_base), float(scale),
         _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), ws_bytes, _stream(stream)))
     return dq, dk, dv
+
+
+def ne_attn_decode_workspace_bytes(B: int, H: int, Tmax: int) -> int:
+    return int(lib().ne_attn_decode_workspace_bytes(int(B), int(H), int(Tmax)))
+
+
+def ne_attn_decode(q, k_cache, v_cache, pos, rope_base=10000.0, scale=None, out=None, lse=None,
+                   workspace=None, stream=None):
+    """Decode attention: ``q`` ``[B, H, 64]`` bf16 (the new tokens), ``k_cache``
+    / ``v_cache`` ``[B, Tmax, H, 64]`` bf16 (un-rotated), ``pos`` int32 ``[B]``
+    on the device (each new token's position; rows 0..pos[b] are attended).
+    Returns ``(out [B, H, 64] bf16, lse [B, H] fp32)``."""
+    _need(q, torch.bfloat16, "q")
+    _need(k_cache, torch.bfloat16, "k_cache")
+    _need(v_cache, torch.bfloat16, "v_cache")
+    _need(pos, torch.int32, "pos")
+    B, H, D = q.shape
+    Tmax = k_cache.shape[1]
+    if tuple(k_cache.shape) != (B, Tmax, H, D) or tuple(v_cache.shape) != (B, Tmax, H, D):
+        raise ValueError("k_cache / v_cache must be [B, Tmax, H, D] matching q")
+    scale = D ** -0.5 if scale is None else scale
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H), dtype=torch.float32, device=q.device) if lse is None else lse
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("ne_attn_decode",
+           lib().ne_attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(pos), B, H, Tmax, D,
+                                float(rope_base), float(scale), _ptr(out), _ptr(lse),
+                                _ptr(workspace), ws_bytes, _stream(stream)))
+    return out, lse
 
 
 def ne_attn_set_bwd_phase_events(ev_after_preprocess=None, ev_after_main=None) -> None:

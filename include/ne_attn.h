@@ -164,6 +164,31 @@ ne_status ne_attn_bwd_noalloc(const ne_bf16* q, const ne_bf16* k, const ne_bf16*
                               int H, int T, int D, float rope_base, float scale, ne_bf16* dq,
                               ne_bf16* dk, ne_bf16* dv, void* stream);
 
+/* Decode attention over a KV cache: one new token per sequence attends to
+ * every cached position up to and including its own (the generation path:
+ * the interactive text generation of the NanoEuler Show HN page and of "Tiny
+ * Hackable CUDA", section 7).
+ *   q:        [B, H, 64] bf16, the new tokens' un-rotated queries;
+ *   k_cache,
+ *   v_cache:  [B, Tmax, H, 64] bf16, un-rotated keys and values; rows
+ *             0..pos[b] of sequence b are attended (the new token's own key
+ *             and value already written at row pos[b]);
+ *   pos:      DEVICE int32 [B], the new token's position, 0 <= pos[b] < Tmax
+ *             (an entry outside that range is reported as NE_ERR_BAD_SEQLEN
+ *             by ne_attn_get_device_status and its outputs are zero / -inf);
+ *   out:      [B, H, 64] bf16 (written);  lse: [B, H] fp32, natural log
+ *             (written).
+ * RoPE and the softmax are those of ne_attn_fwd: the query is rotated at
+ * pos[b], each key at its own position (same fp32 rule and table), so a
+ * decode at pos = T-1 reproduces row T-1 of the training forward.
+ * workspace: ne_attn_decode_workspace_bytes(B, H, Tmax) bytes (split-K
+ * partials), 16-byte aligned, or NULL for a stream-ordered temporary. */
+size_t ne_attn_decode_workspace_bytes(int B, int H, int Tmax);
+ne_status ne_attn_decode(const ne_bf16* q, const ne_bf16* k_cache, const ne_bf16* v_cache,
+                         const int* pos, int B, int H, int Tmax, int D, float rope_base,
+                         float scale, ne_bf16* out, float* lse, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
 /* Synchronize `stream`, then return and clear the device status word of the
  * current device: NE_OK, NE_ERR_TIMEOUT or NE_ERR_BAD_SEQLEN (or NE_ERR_CUDA
  * if the synchronization itself failed). */

@@ -72,3 +72,27 @@ def test_argument_errors_return_before_any_launch(lib):
                            None) == 3
     # bad rope base
     assert lib.ne_attn_fwd(fake, fake, fake, 1, 1, 64, 64, -1.0, 0.125, fake, fake, None) == 1
+
+
+def test_decode_argument_errors_return_before_any_launch(lib):
+    P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.ne_attn_decode.argtypes = [P, P, P, P, I, I, I, I, F, F, P, P, P, Z, P]
+    lib.ne_attn_decode_workspace_bytes.restype = Z
+    lib.ne_attn_decode_workspace_bytes.argtypes = [I, I, I]
+    fake = P(0x10000)  # never dereferenced: every case below fails its host check first
+
+    def call(q=fake, pos=fake, B=2, H=3, Tmax=100, D=64, base=10000.0, scale=0.125, ws=None,
+             ws_bytes=0):
+        return lib.ne_attn_decode(q, fake, fake, pos, B, H, Tmax, D, base, scale, fake, fake, ws,
+                                  ws_bytes, None)
+
+    assert call(q=None) == 1
+    assert call(pos=None) == 1
+    assert call(D=128) == 2
+    assert call(Tmax=0) == 1
+    assert call(scale=0.0) == 1
+    assert call(q=P(0x10008)) == 3
+    assert call(ws=fake, ws_bytes=16) == 1  # too small
+    # workspace: one (m, l, o[64]) partial of 68 floats per 256-key chunk per (b, h)
+    assert lib.ne_attn_decode_workspace_bytes(2, 3, 1000) == 2 * 3 * 4 * 68 * 4
+    assert lib.ne_attn_decode_workspace_bytes(0, 3, 1000) == 0
