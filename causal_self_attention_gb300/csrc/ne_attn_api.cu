@@ -27,10 +27,11 @@ cudaError_t launch_debug_tile(const CUtensorMap& tm, int h, int row0, int rotate
 cudaError_t launch_debug_umma(int form, const __nv_bfloat16* a, const __nv_bfloat16* b, float* d,
                               int* status, cudaStream_t stream);
 size_t decode_part_bytes(int B, int H, int Tmax);
-cudaError_t launch_decode(const __nv_bfloat16* q, const __nv_bfloat16* kc,
-                          const __nv_bfloat16* vc, const int* pos, int B, int H, int Tmax,
+cudaError_t launch_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmT,
+                          const __nv_bfloat16* q, const int* pos, int B, int H, int Tmax,
                           const RopeTable& rope, float scale_log2, float* part,
                           __nv_bfloat16* out, float* lse, int* status, cudaStream_t stream);
+constexpr unsigned kDecodeBoxRows = 32;  // keys per pipeline stage of the decode kernel
 }  // namespace ne
 
 namespace {
@@ -154,10 +155,11 @@ ne_status rope_table(DeviceState& st, float base, int positions, RopeTable* out)
 }
 
 // 3-d tensor map over [n_rows, H, 64] bf16, box 64 x 1 x 128, 128-byte swizzle.
-ne_status encode_rows(CUtensorMap* map, const void* base, int n_rows, int H) {
+ne_status encode_rows(CUtensorMap* map, const void* base, int n_rows, int H,
+                      unsigned box_rows = 128) {
   cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(n_rows)};
   cuuint64_t strides[2] = {64 * 2, static_cast<cuuint64_t>(H) * 64 * 2};
-  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t box[3] = {64, 1, box_rows};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -174,6 +176,21 @@ ne_status encode_rows_f32(CUtensorMap* map, void* base, int n_rows, int H) {
   cuuint32_t box[3] = {32, 1, 128};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NE_OK : NE_ERR_CUDA;
+}
+
+// 2-d tensor map over the RoPE table's row layout: `positions` rows of 64
+// fp32 (32 (cos, sin) pairs), box 32 x `box_rows` (one 128-byte half row per
+// box row), 128-byte swizzle.
+ne_status encode_table(CUtensorMap* map, const float2* cs, int positions, unsigned box_rows) {
+  cuuint64_t dims[2] = {64, static_cast<cuuint64_t>(positions)};
+  cuuint64_t strides[1] = {64 * 4};
+  cuuint32_t box[2] = {32, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                        const_cast<void*>(static_cast<const void*>(cs)), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? NE_OK : NE_ERR_CUDA;
@@ -456,6 +473,7 @@ ne_status ne_attn_decode(const ne_bf16* q, const ne_bf16* k_cache, const ne_bf16
   if (!q || !k_cache || !v_cache || !pos || !out || !lse) return NE_ERR_INVALID_ARG;
   if (D != 64) return NE_ERR_UNSUPPORTED;
   if (B <= 0 || H <= 0 || Tmax <= 0) return NE_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * Tmax > 0x7fffffffLL) return NE_ERR_UNSUPPORTED;
   if (!std::isfinite(scale) || scale <= 0.f || !std::isfinite(rope_base) || rope_base <= 0.f)
     return NE_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned4(pos) ||
@@ -468,8 +486,14 @@ ne_status ne_attn_decode(const ne_bf16* q, const ne_bf16* k_cache, const ne_bf16
   DeviceState* st = nullptr;
   ne_status rc = device_state(&st);
   if (rc != NE_OK) return rc;
+  if ((rc = get_encoder()) != NE_OK) return rc;
   RopeTable rope;
   if ((rc = rope_table(*st, rope_base, Tmax, &rope)) != NE_OK) return rc;
+  CUtensorMap tk, tv;  // the caches as [B * Tmax, H, 64], 32-row boxes
+  if ((rc = encode_rows(&tk, k_cache, B * Tmax, H, ne::kDecodeBoxRows)) != NE_OK) return rc;
+  if ((rc = encode_rows(&tv, v_cache, B * Tmax, H, ne::kDecodeBoxRows)) != NE_OK) return rc;
+  CUtensorMap tt;  // the RoPE table, 32-row boxes of half rows
+  if ((rc = encode_table(&tt, rope.cs, rope.capacity, ne::kDecodeBoxRows)) != NE_OK) return rc;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   void* ws = workspace;
   bool owned = false;
@@ -479,8 +503,7 @@ ne_status ne_attn_decode(const ne_bf16* q, const ne_bf16* k_cache, const ne_bf16
     owned = true;
   }
   cudaError_t e = ne::launch_decode(
-      reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k_cache),
-      reinterpret_cast<const __nv_bfloat16*>(v_cache), pos, B, H, Tmax, rope,
+      tk, tv, tt, reinterpret_cast<const __nv_bfloat16*>(q), pos, B, H, Tmax, rope,
       scale * 1.4426950408889634f, static_cast<float*>(ws), reinterpret_cast<__nv_bfloat16*>(out),
       lse, st->status, cs);
   if (owned) {

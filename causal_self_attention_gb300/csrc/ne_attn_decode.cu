@@ -10,13 +10,22 @@
 // product, nothing for the tensor cores to share).
 //
 // Two kernels on one stream:
-//   1. split: one CTA per (256-key chunk, head, sequence).  Each round the
-//      CTA's 4 warps take 16 consecutive keys, 4 per warp; eight lanes share
-//      one 128-byte key row (lane l: chunk l % 8, 16 bytes), its RoPE partner
-//      chunk comes from lane l ^ 4 by a shuffle.  A
-//      group of eight lanes keeps its own online softmax (max, sum, the 8
-//      output dims of its chunk); groups, then warps, are merged and the CTA
-//      writes one partial (m, l, o[64]) of its chunk.
+//   1. split: one CTA per (chunk of keys, head, sequence) -- 1024 keys when
+//      that still gives a few waves of CTAs, else 256.  Warp 8 streams the
+//      chunk through a 3-stage shared-memory ring with TMA: per stage the K
+//      and V boxes of 32 consecutive positions (4 KiB each) and the 32 rows
+//      of the RoPE table as two boxes of half rows (4 KiB each), all with the
+//      128-byte swizzle, so that the warps' reads spread over the banks (the
+//      table rows read contiguously made 8-way bank conflicts).  Warps 0-7
+//      take 4 keys of each stage; eight lanes share one 128-byte key row
+//      (lane l: chunk l % 8, 16 bytes), its RoPE partner chunk comes from
+//      lane l ^ 4 by a shuffle.  A group of eight lanes keeps its own online
+//      softmax (max, sum, the 8 output dims of its chunk); groups, then
+//      warps, are merged and the CTA writes one partial (m, l, o[64]).
+//      Three CTAs per SM (24 consumer warps) measured best: 3.86 TB/s at
+//      B8 H12 Tmax16384 against 2.69 with 4 warps and 8 stages -- the
+//      consumers' per-key chain (swizzled loads, RoPE, dot, shuffles, exp)
+//      needs the warps more than the ring needs depth.
 //   2. merge: one warp per (sequence, head) combines the chunk partials with
 //      their log-sum-exp weights into o (bf16) and LSE (fp32, natural log).
 // Keys are rotated with the fp32 rule of the training kernels and rounded to
@@ -28,7 +37,16 @@ namespace ne {
 
 namespace dec {
 constexpr int kChunkUnit = 256;      // keys per CTA are a multiple of this
-constexpr int kWarps = 4;            // a round covers 16 consecutive keys: 4 per warp
+constexpr int kWarps = 8;            // consumer warps: a stage's 32 keys, 4 per warp
+constexpr int kThreads = (kWarps + 1) * 32;  // + the TMA producer warp
+constexpr int kKeys = 32;            // keys per stage (the TMA box height)
+constexpr int kStages = 3;
+constexpr int kKvBytes = kKeys * 128;                  // one K or V box
+constexpr int kTabBytes = kKeys * 256;                 // 16 table rows
+constexpr int kStageBytes = 2 * kKvBytes + kTabBytes;  // 8 KiB
+constexpr int OFF_BAR = kStages * kStageBytes;
+constexpr int OFF_RED = OFF_BAR + 2 * kStages * 8 + 16;
+constexpr int SMEM_BYTES = OFF_RED + kWarps * 66 * 4 + 1024;  // + slack for 1024-byte alignment
 constexpr int kPartFloats = 68;      // m, l, 2 pad, o[64] (16-byte multiple)
 }  // namespace dec
 
@@ -86,26 +104,83 @@ __device__ __forceinline__ void merge_state(float& m, float& l, float (&o)[8], f
   m = mn;
 }
 
-__global__ void __launch_bounds__(dec::kWarps * 32)
-    ne_attn_decode_split_kernel(const __nv_bfloat16* __restrict__ q,
-                                const __nv_bfloat16* __restrict__ kc,
-                                const __nv_bfloat16* __restrict__ vc, const int* __restrict__ pos,
+__global__ void __launch_bounds__(dec::kThreads)
+    ne_attn_decode_split_kernel(const __grid_constant__ CUtensorMap tmK,
+                                const __grid_constant__ CUtensorMap tmV,
+                                const __grid_constant__ CUtensorMap tmT,
+                                const __nv_bfloat16* __restrict__ q, const int* __restrict__ pos,
                                 int H, int Tmax, RopeTable rope, float scale_log2,
                                 float* __restrict__ part, int chunk, int n_chunks, int* status) {
   using namespace dec;
-  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint64_t* empty = full + kStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_BAR + 2 * kStages * 8);
+  float (*red)[66] = reinterpret_cast<float (*)[66]>(smem + OFF_RED);
+
+  // Heads vary fastest over the grid: the CTAs running together read the
+  // 12 neighbouring 128-byte pieces of the same cache rows.
+  const int h = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int cl = lane & 7;   // 16-byte chunk of the row this lane holds
-  const int grp = lane >> 3; // which of the warp's 4 keys per round
-  __shared__ float red[kWarps][2 + 64];
+  const int grp = lane >> 3; // which of the warp's 4 keys per stage
 
-  int m_pos = __ldg(pos + b);
+  const int m_pos = __ldg(pos + b);
   const bool bad = (m_pos < 0 || m_pos >= Tmax);
   if (bad && c == 0 && h == 0 && threadIdx.x == 0 && status) atomicCAS(status, 0, NE_DEV_BAD_SEQLEN);
   const int n_keys = bad ? 0 : m_pos + 1;
-  const int k0 = c * chunk + 4 * warp;                        // this warp's first key
-  const int k_end = min(c * chunk + chunk, n_keys);
+  const int kbeg = c * chunk;
+  const int k_end = min(kbeg + chunk, n_keys);
+  const int n_st = k_end > kbeg ? (k_end - kbeg + kKeys - 1) / kKeys : 0;  // stages of this CTA
 
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kWarps);
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  if (warp == kWarps) {
+    // ------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmT);
+      int i = 0;
+      for (; i < n_st; ++i) {
+        const int s = i % kStages;
+        if (i >= kStages &&
+            !mbar_wait(&empty[s], ((i - kStages) / kStages) & 1, abort_flag, status, 50))
+          break;
+        uint8_t* st = smem + s * kStageBytes;
+        const int key0 = kbeg + kKeys * i;
+        mbar_arrive_expect_tx(&full[s], kStageBytes);
+        // Rows past the cache of the last sequence (and table rows past the
+        // table) are filled with zeros by the TMA unit.
+        tma_load_3d(st, &tmK, &full[s], 0, h, b * Tmax + key0);
+        tma_load_3d(st + kKvBytes, &tmV, &full[s], 0, h, b * Tmax + key0);
+        tma_load_2d(st + 2 * kKvBytes, &tmT, &full[s], 0, key0);
+        tma_load_2d(st + 3 * kKvBytes, &tmT, &full[s], 32, key0);
+      }
+      // Every copy issued has landed before this warp exits (on the normal
+      // path the consumers have already waited for them; after an abort they
+      // may not have).
+      for (int j = (i > kStages ? i - kStages : 0); j < i; ++j) {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(&full[j % kStages], (j / kStages) & 1) &&
+               clock64() - t0 < NE_WAIT_LIMIT_CYCLES) {
+        }
+      }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ consumers
   // q' = R(m) q, the 8 dims of chunk cl (every lane group holds a copy).
   float qr[8];
   {
@@ -120,54 +195,48 @@ __global__ void __launch_bounds__(dec::kWarps * 32)
   }
 
   float m = -INFINITY, l = 0.f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  const long long row_stride = static_cast<long long>(H) * 64;  // elements between positions
-  const __nv_bfloat16* kb = kc + (static_cast<long long>(b) * Tmax * H + h) * 64;
-  const __nv_bfloat16* vb = vc + (static_cast<long long>(b) * Tmax * H + h) * 64;
-  // Rounds of 16 keys (4 per warp), in batches of 4 rounds whose loads (K, V
-  // and the keys' table rows) are all issued before any of them is used.
-  constexpr int kBatch = 4;
-  const int rounds = chunk / 16;
-  for (int r0 = 0; r0 < rounds; r0 += kBatch) {
-    if (k0 + 16 * r0 >= k_end) break;  // warp-uniform: no key of this batch is attended
-    uint4 wk[kBatch], wv[kBatch];
-    float4 tb[kBatch][4];
-    bool live[kBatch];
+  const int row = 4 * warp + grp;  // this lane group's row of every stage
+  bool ok = true;
+  for (int i = 0; ok && i < n_st; ++i) {
+    const int s = i % kStages;
+    if (!(ok = mbar_wait_warp(&full[s], (i / kStages) & 1, abort_flag, status, 51))) break;
+    const uint8_t* st = smem + s * kStageBytes;
+    const uint4 wk = *reinterpret_cast<const uint4*>(st + sw128_offset(row, cl));
+    const uint4 wv = *reinterpret_cast<const uint4*>(st + kKvBytes + sw128_offset(row, cl));
+    float4 tb[4];
+    {
+      // Pairs 8q .. 8q + 7 (q = cl & 3): half q >> 1 of the row, 16-byte
+      // units 4 (q & 1) .. + 3 of that half, swizzled like K and V.
+      const uint8_t* half = st + (2 + ((cl & 3) >> 1)) * kKvBytes;
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int key = k0 + 16 * (r0 + u) + grp;
-      live[u] = key < k_end;
-      // A key past the end reads row 0 instead, whose value is then ignored:
-      // every address formed is inside the cache (read-only loads may run
-      // ahead of the condition that guards them).
-      const int key_ld = live[u] ? key : 0;
-      wk[u] = __ldg(reinterpret_cast<const uint4*>(kb + key_ld * row_stride) + cl);
-      wv[u] = __ldg(reinterpret_cast<const uint4*>(vb + key_ld * row_stride) + cl);
-      load_pairs(rope.cs + static_cast<long long>(key_ld) * 32, cl, tb[u]);
+      for (int u = 0; u < 4; ++u)
+        tb[u] = *reinterpret_cast<const float4*>(half + sw128_offset(row, 4 * (cl & 1) + u));
     }
+    const bool live = kbeg + kKeys * i + row < k_end;
+    float x[8], y[8], kr[8];
+    unpack8(wk, x);
+    unpack8(shfl_xor_u4(wk, 4), y);
+    rope_chunk(x, y, cl, tb, kr);
+    float dot = 0.f;
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      float x[8], y[8], kr[8];
-      unpack8(wk[u], x);
-      unpack8(shfl_xor_u4(wk[u], 4), y);
-      rope_chunk(x, y, cl, tb[u], kr);
-      float dot = 0.f;
+    for (int e = 0; e < 8; ++e) dot = __fmaf_rn(qr[e], kr[e], dot);
+    dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+    dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+    dot += __shfl_xor_sync(0xffffffffu, dot, 4);
+    float vv[8];
+    unpack8(wv, vv);
+    // Every value read from the stage is in registers now: release it.
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    if (live) {
+      const float sc = dot * scale_log2;
+      const float mn = fmaxf(m, sc);
+      const float a = (m == -INFINITY) ? 0.f : ex2_approx(m - mn);
+      const float p = ex2_approx(sc - mn);
+      l = l * a + p;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) dot = __fmaf_rn(qr[e], kr[e], dot);
-      dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-      dot += __shfl_xor_sync(0xffffffffu, dot, 2);
-      dot += __shfl_xor_sync(0xffffffffu, dot, 4);
-      if (live[u]) {
-        const float sc = dot * scale_log2;
-        const float mn = fmaxf(m, sc);
-        const float a = (m == -INFINITY) ? 0.f : ex2_approx(m - mn);
-        const float p = ex2_approx(sc - mn);
-        float vv[8];
-        unpack8(wv[u], vv);
-        l = l * a + p;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = __fmaf_rn(p, vv[e], o[e] * a);
-        m = mn;
-      }
+      for (int e = 0; e < 8; ++e) o[e] = __fmaf_rn(p, vv[e], o[e] * a);
+      m = mn;
     }
   }
   // Merge the 4 lane groups (lanes cl, cl + 8, cl + 16, cl + 24).
@@ -188,7 +257,7 @@ __global__ void __launch_bounds__(dec::kWarps * 32)
       red[warp][1] = l;
     }
   }
-  __syncthreads();
+  named_bar_sync(1, kWarps * 32);  // the consumer warps only
   // Merge the warps: thread t < 64 owns output dim t.
   float* dst = part + ((static_cast<long long>(b) * H + h) * n_chunks + c) * kPartFloats;
   if (threadIdx.x < 64) {
@@ -245,17 +314,26 @@ size_t decode_part_bytes(int B, int H, int Tmax) {
   return static_cast<size_t>(B) * H * decode_chunks(Tmax) * dec::kPartFloats * sizeof(float);
 }
 
-cudaError_t launch_decode(const __nv_bfloat16* q, const __nv_bfloat16* kc,
-                          const __nv_bfloat16* vc, const int* pos, int B, int H, int Tmax,
+cudaError_t launch_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmT,
+                          const __nv_bfloat16* q, const int* pos, int B, int H, int Tmax,
                           const RopeTable& rope, float scale_log2, float* part,
                           __nv_bfloat16* out, float* lse, int* status, cudaStream_t stream) {
-  // 256 keys per CTA measured faster than larger chunks sized to fill the
-  // GPU in a few waves (2.5 against 2.0 TB/s at B8 H12 Tmax16384).
-  const int chunk = dec::kChunkUnit;
-  const int n_chunks = decode_chunks(Tmax);
-  dim3 grid(n_chunks, H, B);
-  ne_attn_decode_split_kernel<<<grid, dec::kWarps * 32, 0, stream>>>(
-      q, kc, vc, pos, H, Tmax, rope, scale_log2, part, chunk, n_chunks, status);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(ne_attn_decode_split_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         dec::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  // 1024 keys per CTA when that still leaves a few waves of CTAs (each CTA's
+  // set-up, pipeline fill and merge are then spread over more keys).
+  const long long big = static_cast<long long>(B) * H * ((Tmax + 1023) / 1024);
+  const int chunk = big >= 1024 ? 1024 : dec::kChunkUnit;
+  const int n_chunks = (Tmax + chunk - 1) / chunk;
+  dim3 grid(H, n_chunks, B);
+  ne_attn_decode_split_kernel<<<grid, dec::kThreads, dec::SMEM_BYTES, stream>>>(
+      tmK, tmV, tmT, q, pos, H, Tmax, rope, scale_log2, part, chunk, n_chunks, status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ne_attn_decode_merge_kernel<<<B * H, 32, 0, stream>>>(part, n_chunks, out, lse);
