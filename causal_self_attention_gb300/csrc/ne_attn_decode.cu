@@ -288,21 +288,32 @@ __global__ void __launch_bounds__(32)
   const long long bh = blockIdx.x;
   const int lane = threadIdx.x;
   const float* src = part + bh * n_chunks * kPartFloats;
+  // Lane c holds chunk c's (m, l) (chunks past 32 fold in by lane stride);
+  // an empty chunk has m = -inf, l = 0 and a zero partial output.
   float M = -INFINITY;
   for (int c = lane; c < n_chunks; c += 32) M = fmaxf(M, src[c * kPartFloats]);
 #pragma unroll
   for (int sh = 16; sh >= 1; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, sh));
   float L = 0.f, o0 = 0.f, o1 = 0.f;  // lane owns dims 2*lane, 2*lane + 1
-  for (int c = 0; c < n_chunks; ++c) {
-    const float* pc = src + c * kPartFloats;
-    const float mc = pc[0];
-    if (mc == -INFINITY) continue;
-    const float a = ex2_approx(mc - M);
-    L += pc[1] * a;
-    const float2 oc = reinterpret_cast<const float2*>(pc + 4)[lane];
-    o0 = __fmaf_rn(oc.x, a, o0);
-    o1 = __fmaf_rn(oc.y, a, o1);
+  for (int c0 = 0; c0 < n_chunks; c0 += 32) {
+    const int c = c0 + lane;
+    float w = 0.f, lw = 0.f;
+    if (c < n_chunks) {
+      const float mc = src[c * kPartFloats];
+      w = (mc == -INFINITY) ? 0.f : ex2_approx(mc - M);
+      lw = src[c * kPartFloats + 1] * w;
+    }
+    L += lw;
+    const int nc = min(32, n_chunks - c0);
+    for (int j = 0; j < nc; ++j) {  // weights from lane j; loads independent of each other
+      const float wj = __shfl_sync(0xffffffffu, w, j);
+      const float2 oc = reinterpret_cast<const float2*>(src + (c0 + j) * kPartFloats + 4)[lane];
+      o0 = __fmaf_rn(oc.x, wj, o0);
+      o1 = __fmaf_rn(oc.y, wj, o1);
+    }
   }
+#pragma unroll
+  for (int sh = 16; sh >= 1; sh >>= 1) L += __shfl_xor_sync(0xffffffffu, L, sh);
   const float inv = (L > 0.f) ? 1.f / L : 0.f;
   reinterpret_cast<uint32_t*>(out + bh * 64)[lane] = pack_bf16x2(o0 * inv, o1 * inv);
   if (lane == 0) lse[bh] = (L > 0.f) ? (M + __log2f(L)) * 0.69314718055994531f : -INFINITY;
