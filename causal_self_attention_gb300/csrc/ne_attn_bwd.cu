@@ -26,9 +26,14 @@
 //               and dP^T half-rows in one TMEM round trip and frees them at
 //               once, so the next tile's S^T/dP^T MMAs overlap its math; it
 //               writes P^T to TMEM (A operand of dV) and dS^T to smem
-//   warp 12     MMA: allocates TMEM; one elected lane issues the five MMAs per tile
+//   warp 12     MMA: allocates TMEM; its elected lane issues dV, dK' and dQ'
+//               of every tile (24 MMAs)
 //   warp 13     TMA: lane 0 loads K'_j, V_j once and Q'_i, dO_i (3 stages)
-//   warps 14-15 no role (complete the warpgroup for setmaxnreg)
+//   warp 14     MMA: its elected lane issues S^T and dP^T of every tile (8
+//               MMAs).  Two issuing warps: one warp issuing all 32 MMAs of a
+//               tile was measured to pace the whole loop (its instructions
+//               compete with the softmax warps for issue slots).
+//   warp 15     no role (completes the warpgroup for setmaxnreg)
 // TMEM columns: S^T 0-127, dP^T 128-255, dV 256-319, dK' 320-383, dQ' 384-447,
 // P^T 448-511 (bf16 pairs).
 #include "ne_rope.cuh"
@@ -66,7 +71,8 @@ enum Bar {
   B_PDS_FREE,
   B_DQ_FULL,
   B_DQ_FREE,
-  B_MMA_DONE,
+  B_MMA_DONE,                            // warp 12's MMAs all completed
+  B_SDP_DONE,                            // warp 14's MMAs all completed
   B_COUNT
 };
 static_assert(8 * B_COUNT + 8 <= kBarBytes, "barrier region overflow");
@@ -208,6 +214,7 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(&bars[B_DQ_FULL], 1);
     mbar_init(&bars[B_DQ_FREE], 128);
     mbar_init(&bars[B_MMA_DONE], 1);
+    mbar_init(&bars[B_SDP_DONE], 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -264,12 +271,12 @@ __global__ void __launch_bounds__(512, 1)
           }
       }
     }
-  } else if (warp == 12) {
-    // ------------------------------------------------------------- MMA issuer
-    // The whole warp runs the loop and waits; the elected lane issues each
-    // group of MMAs together with the commits that track it.  Shared-memory
-    // descriptors are built once: a K step or a ring stage only adds a
-    // constant to the start-address field (16-byte units).
+  } else if (warp == 12 || warp == 14) {
+    // ------------------------------------------------------------ MMA issuers
+    // Each issuing warp runs its loop and waits with the whole warp; the
+    // elected lane issues each group of MMAs together with the commits that
+    // track it.  Shared-memory descriptors are built once: a K step or a ring
+    // stage only adds a constant to the start-address field (16-byte units).
     regs_decrease<kRegsMma>();
     constexpr uint64_t kTileD = kTileBytes >> 4;
     const uint64_t dKk = make_sdesc_sw128(smem_u32(sK), 16, 1024);            // K' K-major
@@ -282,16 +289,14 @@ __global__ void __launch_bounds__(512, 1)
     const uint64_t dSk = make_sdesc_sw128(smem_u32(sDST), 16, 1024);          // dS^T K-major
     const uint64_t dSm = make_sdesc_sw128(smem_u32(sDST), kTileBytes, 1024);  // as dS, MN-major
     bool ok = mbar_wait_warp(&bars[B_KV_FULL], 0, abort_flag, p.status, 32);
-    // Iteration it issues S^T = K' Q'^T and dP^T = V dO^T of query tile it+1,
-    // then dV, dK' and dQ' of tile it (it = -1 only starts tile 0).
-    for (int it = -1; ok && it < n_it; ++it) {
-      if (it + 1 < n_it) {
-        const int n = it + 1, sn = n % kQStages;
-        if (!mbar_wait_warp(&bars[B_QDO_FULL + sn], (n / kQStages) & 1, abort_flag, p.status, 33)) {
-          ok = false;
-          break;
-        }
-        if (n >= 1 && !mbar_wait_warp(&bars[B_S_FREE], (n - 1) & 1, abort_flag, p.status, 34)) {
+    uint64_t* done = &bars[warp == 12 ? B_MMA_DONE : B_SDP_DONE];
+    if (warp == 14) {
+      // S^T = K' Q'^T and dP^T = V dO^T of every query tile n, as soon as Q_n
+      // and dO_n have landed and the softmax has read the previous S^T, dP^T.
+      for (int n = 0; ok && n < n_it; ++n) {
+        const int sn = n % kQStages;
+        if (!mbar_wait_warp(&bars[B_QDO_FULL + sn], (n / kQStages) & 1, abort_flag, p.status, 33) ||
+            (n >= 1 && !mbar_wait_warp(&bars[B_S_FREE], (n - 1) & 1, abort_flag, p.status, 34))) {
           ok = false;
           break;
         }
@@ -308,50 +313,55 @@ __global__ void __launch_bounds__(512, 1)
         }
         __syncwarp();
       }
-      if (it < 0) continue;
-      const int s = it % kQStages;
-      if (!mbar_wait_warp(&bars[B_DS_FULL], it & 1, abort_flag, p.status, 35)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      if (elect_one()) {
-        const uint64_t dQm = dQm0 + kTileD * s, dOm = dOm0 + kTileD * s;
-        const uint32_t acc0 = it > 0 ? 1u : 0u;
-        // dV += P^T dO  (A: P^T in TMEM, 16 queries = 8 packed columns per step;
-        // B: dO MN-major, 16 rows = 2048 bytes per step)
+    } else {
+      // dV, dK' and dQ' of every query tile it, once its softmax is done.
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int s = it % kQStages;
+        if (!mbar_wait_warp(&bars[B_DS_FULL], it & 1, abort_flag, p.status, 35)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (elect_one()) {
+          const uint64_t dQm = dQm0 + kTileD * s, dOm = dOm0 + kTileD * s;
+          const uint32_t acc0 = it > 0 ? 1u : 0u;
+          // dV += P^T dO  (A: P^T in TMEM, 16 queries = 8 packed columns per
+          // step; B: dO MN-major, 16 rows = 2048 bytes per step)
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_bf16_ts(tmem + kColDV, tmem + kColPT + 8 * kk, dOm + 128 * kk, kIdescKM,
-                       kk > 0 ? 1u : acc0);
-        // dK' += dS^T Q'  (A: dS^T K-major, 64-query blocks 16 KiB apart)
+          for (int kk = 0; kk < 8; ++kk)
+            umma_bf16_ts(tmem + kColDV, tmem + kColPT + 8 * kk, dOm + 128 * kk, kIdescKM,
+                         kk > 0 ? 1u : acc0);
+          // dK' += dS^T Q'  (A: dS^T K-major, 64-query blocks 16 KiB apart)
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_bf16_ss(tmem + kColDK, dSk + kTileD * (kk >> 2) + 2 * (kk & 3), dQm + 128 * kk,
-                       kIdescKM, kk > 0 ? 1u : acc0);
-        umma_commit(&bars[B_QDO_EMPTY + s]);  // dV and dK were the last readers of Q_i, dO_i
-      }
-      __syncwarp();
-      // dQ'_i = dS K'  (A: dS^T read MN-major, i.e. as dS; B: K' MN-major)
-      if (it >= 1 && !mbar_wait_warp(&bars[B_DQ_FREE], (it - 1) & 1, abort_flag, p.status, 36)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      if (elect_one()) {
+          for (int kk = 0; kk < 8; ++kk)
+            umma_bf16_ss(tmem + kColDK, dSk + kTileD * (kk >> 2) + 2 * (kk & 3), dQm + 128 * kk,
+                         kIdescKM, kk > 0 ? 1u : acc0);
+          // Q_it, dO_it are free: their S^T, dP^T completed before the softmax
+          // of tile it began, and dV, dK' are their last readers.
+          umma_commit(&bars[B_QDO_EMPTY + s]);
+        }
+        __syncwarp();
+        // dQ'_i = dS K'  (A: dS^T read MN-major, i.e. as dS; B: K' MN-major)
+        if (it >= 1 && !mbar_wait_warp(&bars[B_DQ_FREE], (it - 1) & 1, abort_flag, p.status, 36)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // K = 128 keys: 16 rows = 2048 bytes per step
-          umma_bf16_ss(tmem + kColDQ, dSm + 128 * kk, dKm + 128 * kk, kIdescMM, kk > 0 ? 1u : 0u);
-        umma_commit(&bars[B_DQ_FULL]);
-        umma_commit(&bars[B_PDS_FREE]);
+          for (int kk = 0; kk < 8; ++kk)  // K = 128 keys: 16 rows = 2048 bytes per step
+            umma_bf16_ss(tmem + kColDQ, dSm + 128 * kk, dKm + 128 * kk, kIdescMM, kk > 0 ? 1u : 0u);
+          umma_commit(&bars[B_DQ_FULL]);
+          umma_commit(&bars[B_PDS_FREE]);
+        }
+        __syncwarp();
       }
-      __syncwarp();
     }
-    // Drain: every MMA issued above completes before TMEM is released.
-    if (elect_one()) umma_commit(&bars[B_MMA_DONE]);
+    // Drain: every MMA this warp issued completes before TMEM is released.
+    if (elect_one()) umma_commit(done);
     __syncwarp();
     const long long t0 = clock64();
-    while (!mbar_try_wait(&bars[B_MMA_DONE], 0) && clock64() - t0 < NE_WAIT_LIMIT_CYCLES) {
+    while (!mbar_try_wait(done, 0) && clock64() - t0 < NE_WAIT_LIMIT_CYCLES) {
     }
     __syncwarp();
   } else if (warp >= 12) {
