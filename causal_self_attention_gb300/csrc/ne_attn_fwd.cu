@@ -15,14 +15,15 @@
 // current item's last tiles and its epilogue.  Q is double-buffered.
 //
 // Warp roles (512 threads, registers re-split per warpgroup with setmaxnreg):
-//   warps 0-3   softmax A: thread t owns row t of tile A (TMEM lane t), 168 regs
+//   warps 0-3   softmax A: thread t owns row t of tile A (TMEM lane t), 176 regs
 //   warps 4-7   softmax B: same for tile B
 //   warps 8-11  rotate: RoPE on each item's Q_A, Q_B and on every K tile in
 //               smem, 104 regs
-//   warp 12     MMA: allocates TMEM; one elected lane issues S_X = Q_X K^T, O_X += P_X V
+//   warp 12     MMA: allocates TMEM; one elected lane issues S_X = Q_X K^T
 //   warp 13     TMA: lane 0 loads each item's Q_A, Q_B and the K ring (5 stages)
-//   warp 14     TMA: lane 0 loads the V ring (5 stages); warps 12-15 run at
-//               72 regs
+//   warp 14     TMA: lane 0 loads the V ring (5 stages)
+//   warp 15     MMA: one elected lane issues O_X += P_X V; warps 12-15 run at
+//               56 regs
 // TMEM columns: S_A 0-127, S_B 128-255, O_A 256-319, O_B 320-383,
 // P_A 384-447, P_B 448-511 (bf16 pairs: P is the TMEM A operand of P V).
 // A softmax thread loads its whole S row with one TMEM round trip and frees
@@ -43,7 +44,7 @@ namespace fwd {
 
 constexpr int kThreads = 512;
 // Registers per thread of each warpgroup after setmaxnreg (launch: 128).
-constexpr uint32_t kRegsSoftmax = 168, kRegsRotate = 104, kRegsMma = 72;
+constexpr uint32_t kRegsSoftmax = 176, kRegsRotate = 104, kRegsMma = 56;
 static_assert(valid_reg_split(kRegsSoftmax, kRegsRotate, kRegsMma), "register split");
 constexpr int kStages = 5;                            // K ring and V ring
 constexpr int OFF_Q = 0;                              // 2 buffers x (Q_A, Q_B)
@@ -69,8 +70,8 @@ enum Bar {
   B_PV_DONE = B_P_FULL + 2,
   B_O_FINAL = B_PV_DONE + 2,          // per tile: the item's last P V completed
   B_O_FREE = B_O_FINAL + 2,           // per tile: the epilogue has read O_X
-  B_MMA_DONE = B_O_FREE + 2,
-  B_COUNT = B_MMA_DONE + 1
+  B_MMA_DONE = B_O_FREE + 2,         // per issuing warp (S, P V)
+  B_COUNT = B_MMA_DONE + 2
 };
 static_assert(8 * B_COUNT + 8 <= kBarBytes, "barrier region overflow");
 
@@ -111,6 +112,13 @@ __device__ __forceinline__ bool get_item(const FwdParams& p, int nblk, int r, It
   it.nkvB = it.hasB ? 2 * it.blk + 2 : 0;
   it.nkv = it.hasB ? it.nkvB : it.nkvA;
   return true;
+}
+
+// The value v, hidden from the optimiser (it cannot reuse earlier results
+// computed from the same value).
+__device__ __forceinline__ int opaque_int(int v) {
+  asm volatile("" : "+r"(v));
+  return v;
 }
 
 // The k-th item of CTA c among G: rounds of G items, dealt c = 0..G-1 in even
@@ -162,6 +170,7 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
       mbar_init(&bars[B_O_FREE + x], 128);
     }
     mbar_init(&bars[B_MMA_DONE], 1);
+    mbar_init(&bars[B_MMA_DONE + 1], 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -245,13 +254,17 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
           }
       }
     }
-  } else if (warp == 12) {
-    // ------------------------------------------------------------- MMA issuer
-    // The whole warp runs the loop and waits; the elected lane issues each
-    // group of MMAs together with the commits that track it.  Shared-memory
-    // descriptors are built once: a K step, a tile or a ring stage only adds a
-    // constant to the start-address field (16-byte units).
+  } else if (warp == 12 || warp == 15) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 12 issues S_X = Q_X K^T and warp 15 issues O_X += P_X V, both
+    // walking the same items; each commit sits on the warp whose MMAs it
+    // tracks (a commit covers only the MMAs its own thread issued).  The whole
+    // warp runs the loop and waits; the elected lane issues each group of MMAs
+    // together with its commits.  Shared-memory descriptors are built once: a
+    // K step, a tile or a ring stage only adds a constant to the start-address
+    // field (16-byte units).
     regs_decrease<kRegsMma>();
+    const bool isS = (warp == 12);
     constexpr uint64_t kTileD = kTileBytes >> 4;
     const uint64_t dQ0 = make_sdesc_sw128(smem_u32(sQ), 16, 1024);          // Q K-major
     const uint64_t dK0 = make_sdesc_sw128(smem_u32(sK), 16, 1024);          // K K-major
@@ -264,10 +277,10 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
     NE_FOR_EACH_ITEM(it) {
       if (!ok) break;
       const int b = nq & 1;
-      ok = mbar_wait_warp(&bars[B_Q_ROT + b], (nq >> 1) & 1, abort_flag, p.status, 2);
       const int g0 = g;
-      for (int j = 0; ok && j <= it.nkv; ++j) {
-        if (j < it.nkv) {
+      if (isS) {
+        ok = mbar_wait_warp(&bars[B_Q_ROT + b], (nq >> 1) & 1, abort_flag, p.status, 2);
+        for (int j = 0; ok && j < it.nkv; ++j) {
           const int gj = g0 + j, s = gj % kStages;
           if (!mbar_wait_warp(&bars[B_K_ROT + s], (gj / kStages) & 1, abort_flag, p.status, 3)) {
             ok = false;
@@ -295,10 +308,9 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
             }
             __syncwarp();
           }
-          if (!ok) break;
         }
-        if (j >= 1) {
-          const int jj = j - 1;
+      } else {
+        for (int jj = 0; ok && jj < it.nkv; ++jj) {
           const int gj = g0 + jj, s = gj % kStages;
           if (!mbar_wait_warp(&bars[B_V_FULL + s], (gj / kStages) & 1, abort_flag, p.status, 13)) {
             ok = false;
@@ -333,7 +345,6 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
             }
             __syncwarp();
           }
-          if (!ok) break;
         }
       }
       g = g0 + it.nkv;
@@ -343,16 +354,14 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
       nit[1] += it.hasB ? 1 : 0;
       ++nq;
     }
-    // Drain: every MMA issued above completes before TMEM is released.
-    if (elect_one()) umma_commit(&bars[B_MMA_DONE]);
+    // Drain: every MMA this warp issued completes before TMEM is released.
+    uint64_t* done = &bars[B_MMA_DONE + (isS ? 0 : 1)];
+    if (elect_one()) umma_commit(done);
     __syncwarp();
     const long long t0 = clock64();
-    while (!mbar_try_wait(&bars[B_MMA_DONE], 0) && clock64() - t0 < NE_WAIT_LIMIT_CYCLES) {
+    while (!mbar_try_wait(done, 0) && clock64() - t0 < NE_WAIT_LIMIT_CYCLES) {
     }
     __syncwarp();
-  } else if (warp >= 12) {
-    // warp 15: no role (it completes the warpgroup for setmaxnreg)
-    regs_decrease<kRegsMma>();
   } else if (warp >= 8) {
     // ------------------------------------------------------------ RoPE warps
     regs_decrease<kRegsRotate>();
@@ -400,7 +409,6 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
       if (!ok) break;
       const int nkv_x = x ? it.nkvB : it.nkvA;
       if (nkv_x == 0) continue;  // tile B outside the sequence
-      const int qpos = it.rowA + x * kBM + r;  // position in sequence
       const int diag = x ? 2 * it.blk + 1 : 2 * it.blk;
       float m_ref = 0.f;  // reference max (log2 units) the P values are taken against
       float l_sum = 0.f;
@@ -493,6 +501,12 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
       // ---- epilogue: O / l and LSE for rows inside the sequence -----------
       if (!(ok = mbar_wait_warp(&bars[B_O_FINAL + x], nit & 1, abort_flag, p.status, 11))) break;
       ++nit;
+      // The item's placement is derived again here from an opaque copy of its
+      // index, so that none of it stays live (in registers or spilled) through
+      // the loop above.
+      Item e;
+      get_item(p, nblk, opaque_int(r_), e, false);
+      const int erow = e.rowA + x * kBM + r;
       tc_fence_after();
       uint32_t o[64];
       tmem_ld_x32(tO, o);
@@ -501,9 +515,9 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
       tmem_ld_wait(o + 32);
       tc_fence_before();
       mbar_arrive(&bars[B_O_FREE + x]);  // the next item's first P V may overwrite O_X
-      if (qpos < it.len) {
+      if (erow < e.len) {
         const float inv_l = 1.f / l_sum;
-        const long long orow = (static_cast<long long>(it.start + qpos) * p.pb.H + it.h) * kHD;
+        const long long orow = (static_cast<long long>(e.start + erow) * p.pb.H + e.h) * kHD;
         if (p.out_f32) {
           float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow);
 #pragma unroll
@@ -525,7 +539,7 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
           }
         }
         // LSE in natural-log units: (m_ref + log2 l) * ln 2.
-        p.lse[lse_index(p.pb, it.h, it.seq, it.start, qpos)] =
+        p.lse[lse_index(p.pb, e.h, e.seq, e.start, erow)] =
             (m_ref + __log2f(l_sum)) * 0.69314718055994531f;
       }
     }
