@@ -279,18 +279,15 @@ __global__ void __launch_bounds__(512, 1)
     // stage only adds a constant to the start-address field (16-byte units).
     regs_decrease<kRegsMma>();
     constexpr uint64_t kTileD = kTileBytes >> 4;
-    const uint64_t dKk = make_sdesc_sw128(smem_u32(sK), 16, 1024);            // K' K-major
-    const uint64_t dKm = make_sdesc_sw128(smem_u32(sK), kTileBytes, 1024);    // K' MN-major
-    const uint64_t dVk = make_sdesc_sw128(smem_u32(sV), 16, 1024);            // V K-major
-    const uint64_t dQk0 = make_sdesc_sw128(smem_u32(sQ), 16, 1024);           // Q' K-major
-    const uint64_t dQm0 = make_sdesc_sw128(smem_u32(sQ), kTileBytes, 1024);   // Q' MN-major
-    const uint64_t dOk0 = make_sdesc_sw128(smem_u32(sDO), 16, 1024);          // dO K-major
-    const uint64_t dOm0 = make_sdesc_sw128(smem_u32(sDO), kTileBytes, 1024);  // dO MN-major
-    const uint64_t dSk = make_sdesc_sw128(smem_u32(sDST), 16, 1024);          // dS^T K-major
-    const uint64_t dSm = make_sdesc_sw128(smem_u32(sDST), kTileBytes, 1024);  // as dS, MN-major
     bool ok = mbar_wait_warp(&bars[B_KV_FULL], 0, abort_flag, p.status, 32);
     uint64_t* done = &bars[warp == 12 ? B_MMA_DONE : B_SDP_DONE];
+    // Each warp builds only the descriptors it uses (registers are scarce at
+    // this warpgroup's share).
     if (warp == 14) {
+      const uint64_t dKk = make_sdesc_sw128(smem_u32(sK), 16, 1024);    // K' K-major
+      const uint64_t dVk = make_sdesc_sw128(smem_u32(sV), 16, 1024);    // V K-major
+      const uint64_t dQk0 = make_sdesc_sw128(smem_u32(sQ), 16, 1024);   // Q' K-major
+      const uint64_t dOk0 = make_sdesc_sw128(smem_u32(sDO), 16, 1024);  // dO K-major
       // S^T = K' Q'^T and dP^T = V dO^T of every query tile n, as soon as Q_n
       // and dO_n have landed and the softmax has read the previous S^T, dP^T.
       for (int n = 0; ok && n < n_it; ++n) {
@@ -315,6 +312,11 @@ __global__ void __launch_bounds__(512, 1)
       }
     } else {
       // dV, dK' and dQ' of every query tile it, once its softmax is done.
+      const uint64_t dKm = make_sdesc_sw128(smem_u32(sK), kTileBytes, 1024);    // K' MN-major
+      const uint64_t dQm0 = make_sdesc_sw128(smem_u32(sQ), kTileBytes, 1024);   // Q' MN-major
+      const uint64_t dOm0 = make_sdesc_sw128(smem_u32(sDO), kTileBytes, 1024);  // dO MN-major
+      const uint64_t dSk = make_sdesc_sw128(smem_u32(sDST), 16, 1024);          // dS^T K-major
+      const uint64_t dSm = make_sdesc_sw128(smem_u32(sDST), kTileBytes, 1024);  // as dS, MN-major
       for (int it = 0; ok && it < n_it; ++it) {
         const int s = it % kQStages;
         if (!mbar_wait_warp(&bars[B_DS_FULL], it & 1, abort_flag, p.status, 35)) {
@@ -324,6 +326,7 @@ __global__ void __launch_bounds__(512, 1)
         tc_fence_after();
         if (elect_one()) {
           const uint64_t dQm = dQm0 + kTileD * s, dOm = dOm0 + kTileD * s;
+          const uint64_t dS = opaque_u64(dSk);  // descriptors formed at issue, not hoisted
           const uint32_t acc0 = it > 0 ? 1u : 0u;
           // dV += P^T dO  (A: P^T in TMEM, 16 queries = 8 packed columns per
           // step; B: dO MN-major, 16 rows = 2048 bytes per step)
@@ -334,7 +337,7 @@ __global__ void __launch_bounds__(512, 1)
           // dK' += dS^T Q'  (A: dS^T K-major, 64-query blocks 16 KiB apart)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            umma_bf16_ss(tmem + kColDK, dSk + kTileD * (kk >> 2) + 2 * (kk & 3), dQm + 128 * kk,
+            umma_bf16_ss(tmem + kColDK, dS + kTileD * (kk >> 2) + 2 * (kk & 3), dQm + 128 * kk,
                          kIdescKM, kk > 0 ? 1u : acc0);
           // Q_it, dO_it are free: their S^T, dP^T completed before the softmax
           // of tile it began, and dV, dK' are their last readers.
@@ -348,9 +351,10 @@ __global__ void __launch_bounds__(512, 1)
         }
         tc_fence_after();
         if (elect_one()) {
+          const uint64_t dSq = opaque_u64(dSm), dKq = opaque_u64(dKm);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // K = 128 keys: 16 rows = 2048 bytes per step
-            umma_bf16_ss(tmem + kColDQ, dSm + 128 * kk, dKm + 128 * kk, kIdescMM, kk > 0 ? 1u : 0u);
+            umma_bf16_ss(tmem + kColDQ, dSq + 128 * kk, dKq + 128 * kk, kIdescMM, kk > 0 ? 1u : 0u);
           umma_commit(&bars[B_DQ_FULL]);
           umma_commit(&bars[B_PDS_FREE]);
         }

@@ -114,13 +114,6 @@ __device__ __forceinline__ bool get_item(const FwdParams& p, int nblk, int r, It
   return true;
 }
 
-// The value v, hidden from the optimiser (it cannot reuse earlier results
-// computed from the same value).
-__device__ __forceinline__ int opaque_int(int v) {
-  asm volatile("" : "+r"(v));
-  return v;
-}
-
 // The k-th item of CTA c among G: rounds of G items, dealt c = 0..G-1 in even
 // rounds and G-1..0 in odd rounds, so that long and short items mix.
 __device__ __forceinline__ int item_index(int k, int c, int G) {
@@ -297,10 +290,12 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
             }
             tc_fence_after();
             if (elect_one()) {
-              const uint64_t dQ = dQ0 + kTileD * (2 * b + x);
+              // Descriptors formed at issue, not hoisted out of the loop.
+              const uint64_t dQ = opaque_u64(dQ0) + kTileD * (2 * b + x);
+              const uint64_t dKs = opaque_u64(dK);
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)  // K = 64 head dims: 32 bytes per step
-                umma_bf16_ss(tmem + kColS + 128 * x, dQ + 2 * kk, dK + 2 * kk, kIdescS,
+                umma_bf16_ss(tmem + kColS + 128 * x, dQ + 2 * kk, dKs + 2 * kk, kIdescS,
                              kk > 0 ? 1u : 0u);
               umma_commit(&bars[B_S_FULL + x]);
               if (x == 1 || j >= it.nkvB) umma_commit(&bars[B_K_EMPTY + s]);
@@ -335,10 +330,11 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
             tc_fence_after();
             if (elect_one()) {
               const uint32_t acc0 = jj > 0 ? 1u : 0u;
+              const uint64_t dVs = opaque_u64(dV);  // formed at issue, not hoisted
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk)  // K = 128 keys: 8 packed P columns, 16 V rows
                 umma_bf16_ts(tmem + kColO + 64 * x, tmem + kColP + 64 * x + 8 * kk,
-                             dV + 128 * kk, kIdescO, kk > 0 ? 1u : acc0);
+                             dVs + 128 * kk, kIdescO, kk > 0 ? 1u : acc0);
               umma_commit(&bars[B_PV_DONE + x]);
               if (jj == (x ? it.nkvB : it.nkvA) - 1) umma_commit(&bars[B_O_FINAL + x]);
               if (x == 1 || jj >= it.nkvB) umma_commit(&bars[B_V_EMPTY + s]);

@@ -389,6 +389,17 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
+// The value v, hidden from the optimiser: it can neither reuse earlier
+// results computed from v nor hoist work on v out of the enclosing loop (used
+// to keep such results out of scarce registers).
+__device__ __forceinline__ int opaque_int(int v) {
+  asm volatile("" : "+r"(v));
+  return v;
+}
+__device__ __forceinline__ uint64_t opaque_u64(uint64_t v) {
+  asm volatile("" : "+l"(v));
+  return v;
+}
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
