@@ -564,46 +564,47 @@ __global__ void __launch_bounds__(512, 1)
 }
 
 // ---------------------------------------------------------------------------
-// 3. postprocess: dq = bf16(scale * R(m)^T dq_acc).  Grid (blocks of 256
-//    items, sequences); one thread per item = (row, head, part): part c
-//    rotates chunk c (dims 8c..8c+7) against chunk c + 4.
+// 3. postprocess: dq = bf16(scale * R(m)^T dq_acc).  Grid (blocks of
+//    kPostThreads items, sequences); an item is (row, head, part): part c
+//    rotates dims 4c..4c+3 against dims 32+4c..32+4c+3.  Items this small
+//    keep a thread under 32 registers, so that a full SM's worth of threads
+//    is resident and the grid spans several waves (a small last wave costs
+//    little); each warp still reads and writes whole 32-byte sectors.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256)
+constexpr int kPostThreads = 256, kPostParts = 8;
+
+__global__ void __launch_bounds__(kPostThreads)
     ne_attn_dq_postprocess_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq,
                                   const Problem pb, RopeTable rope, float scale) {
   const int seq = blockIdx.y;
   int start, len;
   if (!seq_bounds(pb, seq, start, len, nullptr)) return;
   const int H = pb.H;
-  const long long w = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (w >= static_cast<long long>(len) * H * 4) return;
-  const int part = static_cast<int>(w & 3);
-  const long long rh = w >> 2;
+  const long long w = static_cast<long long>(blockIdx.x) * kPostThreads + threadIdx.x;
+  if (w >= static_cast<long long>(len) * H * kPostParts) return;
+  const int part = static_cast<int>(w % kPostParts);
+  const long long rh = w / kPostParts;
   const int pos = static_cast<int>(rh / H), h = static_cast<int>(rh - static_cast<long long>(pos) * H);
-  const float* src = dq_acc + (static_cast<long long>(start + pos) * H + h) * kHD;
-  const float4* lo4 = reinterpret_cast<const float4*>(src + part * 8);
-  const float4* hi4 = reinterpret_cast<const float4*>(src + 32 + part * 8);
-  const float4* cs4 = reinterpret_cast<const float4*>(rope.cs + static_cast<long long>(pos) * 32 + part * 8);
-  const float4 l0 = lo4[0], l1 = lo4[1], h0 = hi4[0], h1 = hi4[1];
-  const float4 t0 = __ldg(cs4), t1 = __ldg(cs4 + 1), t2 = __ldg(cs4 + 2), t3 = __ldg(cs4 + 3);
-  const float lo[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
-  const float hi[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-  const float cz[8] = {t0.x, t0.z, t1.x, t1.z, t2.x, t2.z, t3.x, t3.z};  // cos of dims 8c + i
-  const float sz[8] = {t0.y, t0.w, t1.y, t1.w, t2.y, t2.w, t3.y, t3.w};  // sin
-  float go[8], gh[8];
+  const long long row_off = (static_cast<long long>(start + pos) * H + h) * kHD;
+  const float4 lo = *reinterpret_cast<const float4*>(dq_acc + row_off + part * 4);
+  const float4 hi = *reinterpret_cast<const float4*>(dq_acc + row_off + 32 + part * 4);
+  const float4* cs4 =
+      reinterpret_cast<const float4*>(rope.cs + static_cast<long long>(pos) * 32 + part * 4);
+  const float4 t0 = __ldg(cs4), t1 = __ldg(cs4 + 1);  // (cos, sin) of dims 4c .. 4c + 3
+  const float a[4] = {lo.x * scale, lo.y * scale, lo.z * scale, lo.w * scale};
+  const float b[4] = {hi.x * scale, hi.y * scale, hi.z * scale, hi.w * scale};
+  const float cz[4] = {t0.x, t0.z, t1.x, t1.z};
+  const float sz[4] = {t0.y, t0.w, t1.y, t1.w};
+  float go[4], gh[4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float a = lo[i] * scale, b = hi[i] * scale;
-    go[i] = a * cz[i] + b * sz[i];
-    gh[i] = b * cz[i] - a * sz[i];
+  for (int i = 0; i < 4; ++i) {
+    go[i] = a[i] * cz[i] + b[i] * sz[i];
+    gh[i] = b[i] * cz[i] - a[i] * sz[i];
   }
-  __nv_bfloat16* d = dq + (static_cast<long long>(start + pos) * H + h) * kHD;
-  *reinterpret_cast<uint4*>(d + part * 8) =
-      make_uint4(pack_bf16x2(go[0], go[1]), pack_bf16x2(go[2], go[3]),
-                 pack_bf16x2(go[4], go[5]), pack_bf16x2(go[6], go[7]));
-  *reinterpret_cast<uint4*>(d + 32 + part * 8) =
-      make_uint4(pack_bf16x2(gh[0], gh[1]), pack_bf16x2(gh[2], gh[3]),
-                 pack_bf16x2(gh[4], gh[5]), pack_bf16x2(gh[6], gh[7]));
+  __nv_bfloat16* d = dq + row_off;
+  *reinterpret_cast<uint2*>(d + part * 4) = make_uint2(pack_bf16x2(go[0], go[1]), pack_bf16x2(go[2], go[3]));
+  *reinterpret_cast<uint2*>(d + 32 + part * 4) =
+      make_uint2(pack_bf16x2(gh[0], gh[1]), pack_bf16x2(gh[2], gh[3]));
 }
 
 cudaError_t launch_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
@@ -629,9 +630,10 @@ cudaError_t launch_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (ev_main && (e = cudaEventRecord(ev_main, stream)) != cudaSuccess) return e;
-  const long long post_items = static_cast<long long>(n_tiles) * kBM * p.pb.H * 4;
-  dim3 pgrid(static_cast<unsigned>((post_items + 255) / 256), p.pb.nseq);
-  ne_attn_dq_postprocess_kernel<<<pgrid, 256, 0, stream>>>(p.dq_acc, p.dq, p.pb, p.rope, p.scale);
+  const long long post_items = static_cast<long long>(n_tiles) * kBM * p.pb.H * kPostParts;
+  dim3 pgrid(static_cast<unsigned>((post_items + kPostThreads - 1) / kPostThreads), p.pb.nseq);
+  ne_attn_dq_postprocess_kernel<<<pgrid, kPostThreads, 0, stream>>>(p.dq_acc, p.dq, p.pb, p.rope,
+                                                                    p.scale);
   return cudaGetLastError();
 }
 
