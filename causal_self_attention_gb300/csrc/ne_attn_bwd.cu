@@ -217,6 +217,11 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(&bars[B_SDP_DONE], 1);
     *abort_flag = 0;
     mbar_fence_init();
+    // K', V of this key tile: issued before the block-wide set-up (TMEM
+    // allocation, the barrier below), which their latency then covers.
+    mbar_arrive_expect_tx(&bars[B_KV_FULL], 2 * kTileBytes);
+    tma_load_3d(smem + OFF_K, &tmK, &bars[B_KV_FULL], 0, h, start + kt * kBN);
+    tma_load_3d(smem + OFF_V, &tmV, &bars[B_KV_FULL], 0, h, start + kt * kBN);
   }
   if (warp == 12) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -241,12 +246,7 @@ __global__ void __launch_bounds__(512, 1)
     regs_decrease<kRegsMma>();
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmDO);
-      mbar_arrive_expect_tx(&bars[B_KV_FULL], 2 * kTileBytes);
-      tma_load_3d(sK, &tmK, &bars[B_KV_FULL], 0, h, start + kt * kBN);
-      tma_load_3d(sV, &tmV, &bars[B_KV_FULL], 0, h, start + kt * kBN);
       int last_issued[kQStages] = {-1, -1, -1};
       for (int it = 0; it < n_it; ++it) {
         const int s = it % kQStages;
@@ -440,7 +440,9 @@ __global__ void __launch_bounds__(512, 1)
         stage_rowstats(ahead, l2, dl);
       }
     }
-    if (r == 0) bulk_wait_group0();
+    // Before exit the staging buffers must have been read; the reduce-adds
+    // themselves complete with the kernel.
+    if (r == 0) bulk_wait_group_read0();
   } else {
     // --------------------------------------------------------- softmax warps
     regs_increase<kRegsSoftmax>();
@@ -517,6 +519,16 @@ __global__ void __launch_bounds__(512, 1)
       mbar_arrive(&bars[B_DS_FULL]);
     }
     // ---- epilogue: dV (first half) and dK = scale * R^T dK' (second half) --
+    // The key's table row (for dK) is loaded before the last MMAs are waited
+    // for; a key past the sequence end reads the last row and writes nothing.
+    const int kpos = kt * kBN + r;
+    float4 tab[16];  // (cos, sin) of dims 2i, 2i + 1 in tab[i]
+    if (half) {
+      const float4* cs4 = reinterpret_cast<const float4*>(
+          p.rope.cs + static_cast<long long>(kpos < len ? kpos : len - 1) * 32);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) tab[i] = __ldg(cs4 + i);
+    }
     if (ok && mbar_wait_warp(&bars[B_MMA_DONE], 0, abort_flag, p.status, 42)) {
       tc_fence_after();
       uint32_t g[64];
@@ -525,31 +537,37 @@ __global__ void __launch_bounds__(512, 1)
       tmem_ld_x32(tmem + lane_base + col + 32, g + 32);
       tmem_ld_wait(g);
       tmem_ld_wait(g + 32);
-      const int kpos = kt * kBN + r;
       if (kpos < len) {
         const long long orow = (static_cast<long long>(start + kpos) * H + h) * kHD;
-        float v[64];
+        uint4* dst = reinterpret_cast<uint4*>((half ? p.dk : p.dv) + orow);
         if (half == 0) {
 #pragma unroll
-          for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(g[i]);
+          for (int c = 0; c < 8; ++c)
+            dst[c] = make_uint4(pack_bf16x2(__uint_as_float(g[8 * c + 0]), __uint_as_float(g[8 * c + 1])),
+                                pack_bf16x2(__uint_as_float(g[8 * c + 2]), __uint_as_float(g[8 * c + 3])),
+                                pack_bf16x2(__uint_as_float(g[8 * c + 4]), __uint_as_float(g[8 * c + 5])),
+                                pack_bf16x2(__uint_as_float(g[8 * c + 6]), __uint_as_float(g[8 * c + 7])));
         } else {
-          const float2* cs = p.rope.cs + static_cast<long long>(kpos) * 32;
+          // Chunk c (dims 8c..8c+7) and its partner c + 4 together.
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float2 t = __ldg(cs + i);
-            const float a = __uint_as_float(g[i]) * p.scale;
-            const float b = __uint_as_float(g[i + 32]) * p.scale;
-            v[i] = a * t.x + b * t.y;
-            v[i + 32] = b * t.x - a * t.y;
+          for (int c = 0; c < 4; ++c) {
+            float lo[8], hi[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int i = 8 * c + u;
+              const float4 t4 = tab[i >> 1];
+              const float cz = (i & 1) ? t4.z : t4.x, sz = (i & 1) ? t4.w : t4.y;
+              const float a = __uint_as_float(g[i]) * p.scale;
+              const float b = __uint_as_float(g[i + 32]) * p.scale;
+              lo[u] = a * cz + b * sz;
+              hi[u] = b * cz - a * sz;
+            }
+            dst[c] = make_uint4(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]),
+                                pack_bf16x2(lo[4], lo[5]), pack_bf16x2(lo[6], lo[7]));
+            dst[c + 4] = make_uint4(pack_bf16x2(hi[0], hi[1]), pack_bf16x2(hi[2], hi[3]),
+                                    pack_bf16x2(hi[4], hi[5]), pack_bf16x2(hi[6], hi[7]));
           }
         }
-        uint4* dst = reinterpret_cast<uint4*>((half ? p.dk : p.dv) + orow);
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          dst[c] = make_uint4(pack_bf16x2(v[8 * c + 0], v[8 * c + 1]),
-                              pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
-                              pack_bf16x2(v[8 * c + 4], v[8 * c + 5]),
-                              pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
       }
     }
   }
