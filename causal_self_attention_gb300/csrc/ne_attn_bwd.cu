@@ -217,11 +217,18 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(&bars[B_SDP_DONE], 1);
     *abort_flag = 0;
     mbar_fence_init();
-    // K', V of this key tile: issued before the block-wide set-up (TMEM
-    // allocation, the barrier below), which their latency then covers.
+    // K', V of this key tile and the ring's first Q', dO stages (which wait
+    // for no release): issued before the block-wide set-up (TMEM allocation,
+    // the barrier below), which their latency then covers.
     mbar_arrive_expect_tx(&bars[B_KV_FULL], 2 * kTileBytes);
     tma_load_3d(smem + OFF_K, &tmK, &bars[B_KV_FULL], 0, h, start + kt * kBN);
     tma_load_3d(smem + OFF_V, &tmV, &bars[B_KV_FULL], 0, h, start + kt * kBN);
+    for (int it = 0; it < kQStages && it < n_it; ++it) {
+      const int qrow = start + (kt + it) * kBM;
+      mbar_arrive_expect_tx(&bars[B_QDO_FULL + it], 2 * kTileBytes);
+      tma_load_3d(smem + OFF_Q + it * kTileBytes, &tmQ, &bars[B_QDO_FULL + it], 0, h, qrow);
+      tma_load_3d(smem + OFF_DO + it * kTileBytes, &tmDO, &bars[B_QDO_FULL + it], 0, h, qrow);
+    }
   }
   if (warp == 12) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -247,8 +254,10 @@ __global__ void __launch_bounds__(512, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmDO);
+      // Stages 0 .. kQStages-1 were issued by thread 0 before the set-up.
       int last_issued[kQStages] = {-1, -1, -1};
-      for (int it = 0; it < n_it; ++it) {
+      for (int it = 0; it < kQStages && it < n_it; ++it) last_issued[it] = it;
+      for (int it = kQStages; it < n_it; ++it) {
         const int s = it % kQStages;
         if (it >= kQStages &&
             !mbar_wait(&bars[B_QDO_EMPTY + s], ((it - kQStages) / kQStages) & 1, abort_flag,
@@ -529,7 +538,12 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
       for (int i = 0; i < 16; ++i) tab[i] = __ldg(cs4 + i);
     }
-    if (ok && mbar_wait_warp(&bars[B_MMA_DONE], 0, abort_flag, p.status, 42)) {
+    // dV, dK' are final once the last tile's dV/dK' MMAs have completed: the
+    // release of its Q', dO stage is committed right after them (and tracks
+    // every earlier MMA of that warp), before the last dQ' MMAs.
+    const int last = n_it - 1;
+    if (ok && mbar_wait_warp(&bars[B_QDO_EMPTY + last % kQStages], (last / kQStages) & 1,
+                             abort_flag, p.status, 42)) {
       tc_fence_after();
       uint32_t g[64];
       const uint32_t col = half ? kColDK : kColDV;
