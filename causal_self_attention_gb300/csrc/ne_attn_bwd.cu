@@ -8,8 +8,9 @@
 //      multiplies exactly the operands the forward did and rotates nothing
 //      (a query tile is used by every key tile at or before it: rotating it
 //      there would repeat the work once per key tile);
-//   2. main: one CTA per (128-key tile j, head, sequence) walks the query
-//      tiles i >= j, recomputing P from the saved LSE:
+//   2. main: persistent, one CTA per SM; each walks its units (128-key tile
+//      j of one (sequence, head)) and, per unit, the query tiles i >= j,
+//      recomputing P from the saved LSE:
 //        S^T  = K' Q'^T,  P^T = exp(scale S^T - LSE),  dP^T = V dO^T,
 //        dS^T = P^T o (dP^T - D),
 //        dV  += P^T dO (P^T from TMEM),  dK' += dS^T Q',  dQ'_i = dS K'
@@ -28,12 +29,13 @@
 //               writes P^T to TMEM (A operand of dV) and dS^T to smem
 //   warp 12     MMA: allocates TMEM; its elected lane issues dV, dK' and dQ'
 //               of every tile (24 MMAs)
-//   warp 13     TMA: lane 0 loads K'_j, V_j once and Q'_i, dO_i (3 stages)
+//   warp 13     TMA: lane 0 loads Q'_i, dO_i (3 stages, continuing across units)
 //   warp 14     MMA: its elected lane issues S^T and dP^T of every tile (8
 //               MMAs).  Two issuing warps: one warp issuing all 32 MMAs of a
 //               tile was measured to pace the whole loop (its instructions
 //               compete with the softmax warps for issue slots).
-//   warp 15     no role (completes the warpgroup for setmaxnreg)
+//   warp 15     TMA: lane 0 loads each unit's K'_j, V_j once both issuing
+//               warps are done with the previous unit's
 // TMEM columns: S^T 0-127, dP^T 128-255, dV 256-319, dK' 320-383, dQ' 384-447,
 // P^T 448-511 (bf16 pairs).
 #include "ne_rope.cuh"
@@ -61,7 +63,8 @@ constexpr int kBarBytes = 512;  // mbarriers, TMEM address, abort flag
 constexpr int SMEM_BYTES = OFF_BAR + kBarBytes + 1024;  // + slack for 1024-byte alignment
 
 enum Bar {
-  B_KV_FULL = 0,
+  B_KV_FULL = 0,                         // per unit: K', V landed
+  B_KV_EMPTY,                            // per unit: both issuing warps done with K', V
   B_QDO_FULL,                            // kQStages
   B_ROW_FULL = B_QDO_FULL + kQStages,    // kQStages: -LSE_i, -D_i staged
   B_QDO_EMPTY = B_ROW_FULL + kQStages,   // kQStages
@@ -171,14 +174,52 @@ __global__ void __launch_bounds__(256)
 }
 
 // ---------------------------------------------------------------------------
-// 2. main kernel
+// 2. main kernel: persistent.  A unit is one 128-key tile kt of one (sequence,
+//    head); the CTAs (one per SM) walk the units longest first (key tile 0,
+//    whose query tiles are the most, for every (sequence, head), then tile 1,
+//    ...), dealt in a snake order.  TMEM, barriers and the Q'/dO ring persist
+//    across units, so a unit's start (its K', V loads, first S^T/dP^T) overlaps
+//    the previous unit's tail (last dQ' drain, dV/dK epilogue) instead of
+//    waiting for a new CTA.  Barrier phases count query tiles over all of the
+//    CTA's units (ring stages and per-tile hand-offs) or units (K', V).
 // ---------------------------------------------------------------------------
+namespace bwd {
+
+// One unit: key tile kt of (sequence seq, head h).
+struct Unit {
+  int seq, h, kt;
+  int start, len;  // the sequence's first row in the packed tensors, its length
+  int n_it;        // query tiles kt .. n_qt - 1
+};
+
+// Unit r of the longest-first order; false for an empty unit (the sequence
+// has no such key tile, or a bad cu_seqlens entry).
+__device__ __forceinline__ bool get_unit(const BwdParams& p, int r, Unit& u) {
+  const int n_sh = p.pb.nseq * p.pb.H;
+  const int sh = r % n_sh;
+  u.kt = r / n_sh;
+  u.seq = sh / p.pb.H;
+  u.h = sh % p.pb.H;
+  if (!seq_bounds(p.pb, u.seq, u.start, u.len, nullptr)) return false;
+  if (u.kt * kBN >= u.len) return false;
+  u.n_it = (u.len + kBM - 1) / kBM - u.kt;
+  return true;
+}
+
+// The k-th unit of CTA c among G: rounds of G units, dealt c = 0..G-1 in even
+// rounds and G-1..0 in odd rounds.
+__device__ __forceinline__ int unit_index(int k, int c, int G) {
+  return k * G + ((k & 1) ? (G - 1 - c) : c);
+}
+
+}  // namespace bwd
+
 __global__ void __launch_bounds__(512, 1)
     ne_attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
                        const __grid_constant__ CUtensorMap tmDO,
-                       const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
+                       const __grid_constant__ CUtensorMap tmDQ, const BwdParams p, int n_tiles) {
   using namespace bwd;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -187,21 +228,15 @@ __global__ void __launch_bounds__(512, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + 8 * B_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_BAR + 8 * B_COUNT + 4);
 
-  const int H = p.pb.H;
-  const int seq = blockIdx.x / H;
-  const int h = blockIdx.x % H;
-  const int kt = blockIdx.y;  // key tile; tile 0 has the most query tiles: launched first
-  int start, len;
-  if (!seq_bounds(p.pb, seq, start, len, nullptr)) return;
-  if (kt * kBN >= len) return;
-  const int n_qt = (len + kBM - 1) / kBM;
-  const int n_it = n_qt - kt;  // query tiles kt .. n_qt-1
-
+  const int G = gridDim.x;
+  const int cta = blockIdx.x;
+  const int n_units = n_tiles * p.pb.nseq * p.pb.H;
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars[B_KV_FULL], 1);
+    mbar_init(&bars[B_KV_EMPTY], 2);  // one commit from each issuing warp
     for (int s = 0; s < kQStages; ++s) {
       mbar_init(&bars[B_QDO_FULL + s], 1);
       mbar_init(&bars[B_ROW_FULL + s], 128);
@@ -217,18 +252,6 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(&bars[B_SDP_DONE], 1);
     *abort_flag = 0;
     mbar_fence_init();
-    // K', V of this key tile and the ring's first Q', dO stages (which wait
-    // for no release): issued before the block-wide set-up (TMEM allocation,
-    // the barrier below), which their latency then covers.
-    mbar_arrive_expect_tx(&bars[B_KV_FULL], 2 * kTileBytes);
-    tma_load_3d(smem + OFF_K, &tmK, &bars[B_KV_FULL], 0, h, start + kt * kBN);
-    tma_load_3d(smem + OFF_V, &tmV, &bars[B_KV_FULL], 0, h, start + kt * kBN);
-    for (int it = 0; it < kQStages && it < n_it; ++it) {
-      const int qrow = start + (kt + it) * kBM;
-      mbar_arrive_expect_tx(&bars[B_QDO_FULL + it], 2 * kTileBytes);
-      tma_load_3d(smem + OFF_Q + it * kTileBytes, &tmQ, &bars[B_QDO_FULL + it], 0, h, qrow);
-      tma_load_3d(smem + OFF_DO + it * kTileBytes, &tmDO, &bars[B_QDO_FULL + it], 0, h, qrow);
-    }
   }
   if (warp == 12) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -247,30 +270,38 @@ __global__ void __launch_bounds__(512, 1)
   uint8_t* sDQ = smem + OFF_DQ;
   float* sLSE = reinterpret_cast<float*>(smem + OFF_LSE);
   float* sDEL = reinterpret_cast<float*>(smem + OFF_DEL);
+  // The units of this CTA, in order (the same sequence in every role).
+#define NE_FOR_EACH_UNIT(u)                                                                   \
+  for (int k_ = 0, r_ = unit_index(0, cta, G); r_ < n_units; ++k_, r_ = unit_index(k_, cta, G)) \
+    if (Unit u; get_unit(p, r_, u))
 
-  if (warp == 13) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp == 13 || warp == 15) {
+    // ------------------------------- TMA producers: warp 13 Q'/dO, warp 15 K'/V
     regs_decrease<kRegsMma>();
-    if (lane == 0) {
+    if (lane == 0 && warp == 13) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmDO);
-      // Stages 0 .. kQStages-1 were issued by thread 0 before the set-up.
+      bool ok = true;
+      int g = 0;  // query tiles loaded over all units
       int last_issued[kQStages] = {-1, -1, -1};
-      for (int it = 0; it < kQStages && it < n_it; ++it) last_issued[it] = it;
-      for (int it = kQStages; it < n_it; ++it) {
-        const int s = it % kQStages;
-        if (it >= kQStages &&
-            !mbar_wait(&bars[B_QDO_EMPTY + s], ((it - kQStages) / kQStages) & 1, abort_flag,
-                       p.status, 31))
-          break;
-        const int qrow = start + (kt + it) * kBM;
-        mbar_arrive_expect_tx(&bars[B_QDO_FULL + s], 2 * kTileBytes);
-        tma_load_3d(sQ + s * kTileBytes, &tmQ, &bars[B_QDO_FULL + s], 0, h, qrow);
-        tma_load_3d(sDO + s * kTileBytes, &tmDO, &bars[B_QDO_FULL + s], 0, h, qrow);
-        last_issued[s] = it;
+      NE_FOR_EACH_UNIT(u) {
+        if (!ok) break;
+        for (int it = 0; it < u.n_it; ++it, ++g) {
+          const int s = g % kQStages;
+          if (g >= kQStages &&
+              !mbar_wait(&bars[B_QDO_EMPTY + s], ((g - kQStages) / kQStages) & 1, abort_flag,
+                         p.status, 31)) {
+            ok = false;
+            break;
+          }
+          const int qrow = u.start + (u.kt + it) * kBM;
+          mbar_arrive_expect_tx(&bars[B_QDO_FULL + s], 2 * kTileBytes);
+          tma_load_3d(sQ + s * kTileBytes, &tmQ, &bars[B_QDO_FULL + s], 0, u.h, qrow);
+          tma_load_3d(sDO + s * kTileBytes, &tmDO, &bars[B_QDO_FULL + s], 0, u.h, qrow);
+          last_issued[s] = g;
+        }
       }
-      if (*abort_flag) {
-        mbar_wait(&bars[B_KV_FULL], 0, abort_flag, nullptr, 0);
+      if (*abort_flag) {  // copies in flight land before the CTA exits
         for (int s = 0; s < kQStages; ++s)
           if (last_issued[s] >= 0) {
             const long long t0 = clock64();
@@ -279,95 +310,138 @@ __global__ void __launch_bounds__(512, 1)
             }
           }
       }
+    } else if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      int nu = 0;  // units loaded
+      NE_FOR_EACH_UNIT(u) {
+        // The buffer is free once both issuing warps' last MMAs of the
+        // previous unit (the last S^T/dP^T; the last dQ') have completed.
+        if (nu >= 1 && !mbar_wait(&bars[B_KV_EMPTY], (nu - 1) & 1, abort_flag, p.status, 30)) break;
+        mbar_arrive_expect_tx(&bars[B_KV_FULL], 2 * kTileBytes);
+        tma_load_3d(sK, &tmK, &bars[B_KV_FULL], 0, u.h, u.start + u.kt * kBN);
+        tma_load_3d(sV, &tmV, &bars[B_KV_FULL], 0, u.h, u.start + u.kt * kBN);
+        ++nu;
+      }
+      if (*abort_flag && nu >= 1) {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(&bars[B_KV_FULL], (nu - 1) & 1) &&
+               clock64() - t0 < NE_WAIT_LIMIT_CYCLES) {
+        }
+      }
     }
   } else if (warp == 12 || warp == 14) {
     // ------------------------------------------------------------ MMA issuers
     // Each issuing warp runs its loop and waits with the whole warp; the
     // elected lane issues each group of MMAs together with the commits that
-    // track it.  Shared-memory descriptors are built once: a K step or a ring
-    // stage only adds a constant to the start-address field (16-byte units).
+    // track it.  Descriptors: a K step or a ring stage only adds a constant
+    // to the start-address field (16-byte units).
     regs_decrease<kRegsMma>();
     constexpr uint64_t kTileD = kTileBytes >> 4;
-    bool ok = mbar_wait_warp(&bars[B_KV_FULL], 0, abort_flag, p.status, 32);
     uint64_t* done = &bars[warp == 12 ? B_MMA_DONE : B_SDP_DONE];
-    // Each warp builds only the descriptors it uses (registers are scarce at
-    // this warpgroup's share).
+    bool ok = true;
+    int g = 0;   // query tiles over all units
+    int nu = 0;  // units
     if (warp == 14) {
       const uint64_t dKk = make_sdesc_sw128(smem_u32(sK), 16, 1024);    // K' K-major
       const uint64_t dVk = make_sdesc_sw128(smem_u32(sV), 16, 1024);    // V K-major
       const uint64_t dQk0 = make_sdesc_sw128(smem_u32(sQ), 16, 1024);   // Q' K-major
       const uint64_t dOk0 = make_sdesc_sw128(smem_u32(sDO), 16, 1024);  // dO K-major
-      // S^T = K' Q'^T and dP^T = V dO^T of every query tile n, as soon as Q_n
+      // S^T = K' Q'^T and dP^T = V dO^T of every query tile, as soon as Q_n
       // and dO_n have landed and the softmax has read the previous S^T, dP^T.
-      for (int n = 0; ok && n < n_it; ++n) {
-        const int sn = n % kQStages;
-        if (!mbar_wait_warp(&bars[B_QDO_FULL + sn], (n / kQStages) & 1, abort_flag, p.status, 33) ||
-            (n >= 1 && !mbar_wait_warp(&bars[B_S_FREE], (n - 1) & 1, abort_flag, p.status, 34))) {
+      NE_FOR_EACH_UNIT(u) {
+        if (!ok) break;
+        if (!mbar_wait_warp(&bars[B_KV_FULL], nu & 1, abort_flag, p.status, 32)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        if (elect_one()) {
-          const uint64_t dQ = dQk0 + kTileD * sn, dO = dOk0 + kTileD * sn;
+        for (int it = 0; it < u.n_it; ++it, ++g) {
+          const int sn = g % kQStages;
+          if (!mbar_wait_warp(&bars[B_QDO_FULL + sn], (g / kQStages) & 1, abort_flag, p.status, 33) ||
+              (g >= 1 && !mbar_wait_warp(&bars[B_S_FREE], (g - 1) & 1, abort_flag, p.status, 34))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (elect_one()) {
+            const uint64_t dQ = opaque_u64(dQk0) + kTileD * sn, dO = opaque_u64(dOk0) + kTileD * sn;
+            const uint64_t dK = opaque_u64(dKk), dV = opaque_u64(dVk);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)  // K = 64 head dims: 32 bytes per step
-            umma_bf16_ss(tmem + kColS, dKk + 2 * kk, dQ + 2 * kk, kIdescNN, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk)  // K = 64 head dims: 32 bytes per step
+              umma_bf16_ss(tmem + kColS, dK + 2 * kk, dQ + 2 * kk, kIdescNN, kk > 0 ? 1u : 0u);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16_ss(tmem + kColDP, dVk + 2 * kk, dO + 2 * kk, kIdescNN, kk > 0 ? 1u : 0u);
-          umma_commit(&bars[B_S_FULL]);
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16_ss(tmem + kColDP, dV + 2 * kk, dO + 2 * kk, kIdescNN, kk > 0 ? 1u : 0u);
+            umma_commit(&bars[B_S_FULL]);
+            if (it == u.n_it - 1) umma_commit(&bars[B_KV_EMPTY]);  // last reader of V (and K' here)
+          }
+          __syncwarp();
         }
-        __syncwarp();
+        ++nu;
       }
     } else {
-      // dV, dK' and dQ' of every query tile it, once its softmax is done.
+      // dV, dK' and dQ' of every query tile, once its softmax is done.
       const uint64_t dKm = make_sdesc_sw128(smem_u32(sK), kTileBytes, 1024);    // K' MN-major
       const uint64_t dQm0 = make_sdesc_sw128(smem_u32(sQ), kTileBytes, 1024);   // Q' MN-major
       const uint64_t dOm0 = make_sdesc_sw128(smem_u32(sDO), kTileBytes, 1024);  // dO MN-major
       const uint64_t dSk = make_sdesc_sw128(smem_u32(sDST), 16, 1024);          // dS^T K-major
       const uint64_t dSm = make_sdesc_sw128(smem_u32(sDST), kTileBytes, 1024);  // as dS, MN-major
-      for (int it = 0; ok && it < n_it; ++it) {
-        const int s = it % kQStages;
-        if (!mbar_wait_warp(&bars[B_DS_FULL], it & 1, abort_flag, p.status, 35)) {
+      NE_FOR_EACH_UNIT(u) {
+        if (!ok) break;
+        // K' of this unit (B operand of dQ') has landed.
+        if (!mbar_wait_warp(&bars[B_KV_FULL], nu & 1, abort_flag, p.status, 37)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        if (elect_one()) {
-          const uint64_t dQm = dQm0 + kTileD * s, dOm = dOm0 + kTileD * s;
-          const uint64_t dS = opaque_u64(dSk);  // descriptors formed at issue, not hoisted
-          const uint32_t acc0 = it > 0 ? 1u : 0u;
-          // dV += P^T dO  (A: P^T in TMEM, 16 queries = 8 packed columns per
-          // step; B: dO MN-major, 16 rows = 2048 bytes per step)
+        for (int it = 0; it < u.n_it; ++it, ++g) {
+          const int s = g % kQStages;
+          if (!mbar_wait_warp(&bars[B_DS_FULL], g & 1, abort_flag, p.status, 35)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (elect_one()) {
+            const uint64_t dQm = opaque_u64(dQm0) + kTileD * s, dOm = opaque_u64(dOm0) + kTileD * s;
+            const uint64_t dS = opaque_u64(dSk);
+            // The unit's first tile overwrites dV, dK': the softmax threads
+            // read the previous unit's values (their epilogue) before they
+            // arrived on DS_FULL for this tile.
+            const uint32_t acc0 = it > 0 ? 1u : 0u;
+            // dV += P^T dO  (A: P^T in TMEM, 16 queries = 8 packed columns per
+            // step; B: dO MN-major, 16 rows = 2048 bytes per step)
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_bf16_ts(tmem + kColDV, tmem + kColPT + 8 * kk, dOm + 128 * kk, kIdescKM,
-                         kk > 0 ? 1u : acc0);
-          // dK' += dS^T Q'  (A: dS^T K-major, 64-query blocks 16 KiB apart)
+            for (int kk = 0; kk < 8; ++kk)
+              umma_bf16_ts(tmem + kColDV, tmem + kColPT + 8 * kk, dOm + 128 * kk, kIdescKM,
+                           kk > 0 ? 1u : acc0);
+            // dK' += dS^T Q'  (A: dS^T K-major, 64-query blocks 16 KiB apart)
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_bf16_ss(tmem + kColDK, dS + kTileD * (kk >> 2) + 2 * (kk & 3), dQm + 128 * kk,
-                         kIdescKM, kk > 0 ? 1u : acc0);
-          // Q_it, dO_it are free: their S^T, dP^T completed before the softmax
-          // of tile it began, and dV, dK' are their last readers.
-          umma_commit(&bars[B_QDO_EMPTY + s]);
-        }
-        __syncwarp();
-        // dQ'_i = dS K'  (A: dS^T read MN-major, i.e. as dS; B: K' MN-major)
-        if (it >= 1 && !mbar_wait_warp(&bars[B_DQ_FREE], (it - 1) & 1, abort_flag, p.status, 36)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (elect_one()) {
-          const uint64_t dSq = opaque_u64(dSm), dKq = opaque_u64(dKm);
+            for (int kk = 0; kk < 8; ++kk)
+              umma_bf16_ss(tmem + kColDK, dS + kTileD * (kk >> 2) + 2 * (kk & 3), dQm + 128 * kk,
+                           kIdescKM, kk > 0 ? 1u : acc0);
+            // Q_it, dO_it are free: their S^T, dP^T completed before the
+            // softmax of the tile began, and dV, dK' are their last readers.
+            umma_commit(&bars[B_QDO_EMPTY + s]);
+          }
+          __syncwarp();
+          // dQ'_i = dS K'  (A: dS^T read MN-major, i.e. as dS; B: K' MN-major)
+          if (g >= 1 && !mbar_wait_warp(&bars[B_DQ_FREE], (g - 1) & 1, abort_flag, p.status, 36)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (elect_one()) {
+            const uint64_t dSq = opaque_u64(dSm), dKq = opaque_u64(dKm);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // K = 128 keys: 16 rows = 2048 bytes per step
-            umma_bf16_ss(tmem + kColDQ, dSq + 128 * kk, dKq + 128 * kk, kIdescMM, kk > 0 ? 1u : 0u);
-          umma_commit(&bars[B_DQ_FULL]);
-          umma_commit(&bars[B_PDS_FREE]);
+            for (int kk = 0; kk < 8; ++kk)  // K = 128 keys: 16 rows = 2048 bytes per step
+              umma_bf16_ss(tmem + kColDQ, dSq + 128 * kk, dKq + 128 * kk, kIdescMM,
+                           kk > 0 ? 1u : 0u);
+            umma_commit(&bars[B_DQ_FULL]);
+            umma_commit(&bars[B_PDS_FREE]);
+            if (it == u.n_it - 1) umma_commit(&bars[B_KV_EMPTY]);  // last reader of K'
+          }
+          __syncwarp();
         }
-        __syncwarp();
+        ++nu;
       }
     }
     // Drain: every MMA this warp issued completes before TMEM is released.
@@ -377,77 +451,95 @@ __global__ void __launch_bounds__(512, 1)
     while (!mbar_try_wait(done, 0) && clock64() - t0 < NE_WAIT_LIMIT_CYCLES) {
     }
     __syncwarp();
-  } else if (warp >= 12) {
-    regs_decrease<kRegsMma>();
   } else if (warp < 4) {
     // ------------------------------------------------ row terms and dQ' drain
     regs_decrease<kRegsDrain>();
     const int r = threadIdx.x;  // 0..127: query row of the tile (TMEM lane r)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    // LSE (log2 units) and D of query row r of tile `it`; rows past the
-    // sequence get LSE = +inf, hence P = 0.
-    auto load_rowstats = [&](int it, float& l2, float& dl) {
-      const int qpos = (kt + it) * kBM + r;
-      // The loads always address a row of the sequence (read-only loads may
-      // run ahead of the condition that guards them); rows past the end then
-      // take LSE = +inf.
-      const int qc = qpos < len ? qpos : len - 1;
-      const float l = __ldg(p.lse + lse_index(p.pb, h, seq, start, qc));
-      const float d = __ldg(p.delta + static_cast<long long>(h) * p.pb.n_tot + start + qc);
-      l2 = qpos < len ? l * 1.4426950408889634f : INFINITY;
-      dl = qpos < len ? d : 0.f;
-    };
-    // Stored negated: P = 2^(fma(s, scale log2 e, -LSE)), dS = P (dP - D).
-    auto stage_rowstats = [&](int it, float l2, float dl) {
-      const int s = it % kQStages;
-      sLSE[s * 128 + r] = -l2;
-      sDEL[s * 128 + r] = -dl;
-      mbar_arrive(&bars[B_ROW_FULL + s]);
-    };
-    float l2, dl;
-    for (int it = 0; it < kQStages - 1 && it < n_it; ++it) {
-      load_rowstats(it, l2, dl);
-      stage_rowstats(it, l2, dl);
-    }
-    for (int it = 0; it < n_it; ++it) {
-      const int ahead = it + kQStages - 1;  // tile whose row terms are staged now
-      if (ahead < n_it) load_rowstats(ahead, l2, dl);  // loads in flight during the drain
-      // dQ'_it: TMEM -> swizzled fp32 staging (columns 0-31 and 32-63) ->
-      // two bulk tensor reduce-adds, issued by thread 0.
-      if (!mbar_wait_warp(&bars[B_DQ_FULL], it & 1, abort_flag, p.status, 43)) break;
-      tc_fence_after();
-      uint32_t v0[32], v1[32];
-      tmem_ld_x32(tmem + lane_base + kColDQ, v0);
-      tmem_ld_x32(tmem + lane_base + kColDQ + 32, v1);
-      tmem_ld_wait(v0);
-      tmem_ld_wait(v1);
-      tc_fence_before();
-      mbar_arrive(&bars[B_DQ_FREE]);
-      if (r == 0) bulk_wait_group_read0();  // the previous reductions have read the buffers
-      named_bar_sync(1, 128);
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        *reinterpret_cast<uint4*>(sDQ + sw128_offset(r, c)) =
-            make_uint4(v0[4 * c], v0[4 * c + 1], v0[4 * c + 2], v0[4 * c + 3]);
-        *reinterpret_cast<uint4*>(sDQ + kTileBytes + sw128_offset(r, c)) =
-            make_uint4(v1[4 * c], v1[4 * c + 1], v1[4 * c + 2], v1[4 * c + 3]);
-      }
-      fence_proxy_async_smem();
-      named_bar_sync(1, 128);
-      if (r == 0) {
-        const int qrow = start + (kt + it) * kBM;
-        tma_reduce_add_3d(&tmDQ, sDQ, 0, h, qrow);
-        tma_reduce_add_3d(&tmDQ, sDQ + kTileBytes, 32, h, qrow);
-        bulk_commit_group();
-      }
-      if (ahead < n_it) {
-        // The stage of tile ahead last held tile it - 1, whose softmax has
-        // read it before the dV/dK MMAs that completed QDO_EMPTY.
-        if (it >= 1 && !mbar_wait(&bars[B_QDO_EMPTY + (it - 1) % kQStages],
-                                  ((it - 1) / kQStages) & 1, abort_flag, p.status, 44))
+    bool ok = true;
+    int g = 0;  // query tiles over all units
+    NE_FOR_EACH_UNIT(u) {
+      if (!ok) break;
+      // LSE (log2 units) and D of query row r of the unit's tile `it`; rows
+      // past the sequence get LSE = +inf, hence P = 0.  The loads always
+      // address a row of the sequence (read-only loads may run ahead of the
+      // condition that guards them).
+      auto load_rowstats = [&](int it, float& l2, float& dl) {
+        const int qpos = (u.kt + it) * kBM + r;
+        const int qc = qpos < u.len ? qpos : u.len - 1;
+        const float l = __ldg(p.lse + lse_index(p.pb, u.h, u.seq, u.start, qc));
+        const float d = __ldg(p.delta + static_cast<long long>(u.h) * p.pb.n_tot + u.start + qc);
+        l2 = qpos < u.len ? l * 1.4426950408889634f : INFINITY;
+        dl = qpos < u.len ? d : 0.f;
+      };
+      // Stored negated: P = 2^(fma(s, scale log2 e, -LSE)), dS = P (dP - D).
+      auto stage_rowstats = [&](int gq, float l2, float dl) {
+        const int s = gq % kQStages;
+        sLSE[s * 128 + r] = -l2;
+        sDEL[s * 128 + r] = -dl;
+        mbar_arrive(&bars[B_ROW_FULL + s]);
+      };
+      float l2, dl;
+      // The unit's first two tiles; their stages last held tiles g - 3 and
+      // g - 2 (of earlier units), free once those tiles' dV/dK' completed.
+      for (int it = 0; it < kQStages - 1 && it < u.n_it; ++it) {
+        const int gq = g + it;
+        load_rowstats(it, l2, dl);
+        if (gq >= kQStages &&
+            !mbar_wait(&bars[B_QDO_EMPTY + gq % kQStages], ((gq - kQStages) / kQStages) & 1,
+                       abort_flag, p.status, 45)) {
+          ok = false;
           break;
-        stage_rowstats(ahead, l2, dl);
+        }
+        stage_rowstats(gq, l2, dl);
       }
+      for (int it = 0; ok && it < u.n_it; ++it) {
+        const int gq = g + it;
+        const int ahead = it + kQStages - 1;  // the unit's tile whose row terms are staged now
+        if (ahead < u.n_it) load_rowstats(ahead, l2, dl);  // loads in flight during the drain
+        // dQ'_it: TMEM -> swizzled fp32 staging (columns 0-31 and 32-63) ->
+        // two bulk tensor reduce-adds, issued by thread 0.
+        if (!mbar_wait_warp(&bars[B_DQ_FULL], gq & 1, abort_flag, p.status, 43)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t v0[32], v1[32];
+        tmem_ld_x32(tmem + lane_base + kColDQ, v0);
+        tmem_ld_x32(tmem + lane_base + kColDQ + 32, v1);
+        tmem_ld_wait(v0);
+        tmem_ld_wait(v1);
+        tc_fence_before();
+        mbar_arrive(&bars[B_DQ_FREE]);
+        if (r == 0) bulk_wait_group_read0();  // the previous reductions have read the buffers
+        named_bar_sync(1, 128);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          *reinterpret_cast<uint4*>(sDQ + sw128_offset(r, c)) =
+              make_uint4(v0[4 * c], v0[4 * c + 1], v0[4 * c + 2], v0[4 * c + 3]);
+          *reinterpret_cast<uint4*>(sDQ + kTileBytes + sw128_offset(r, c)) =
+              make_uint4(v1[4 * c], v1[4 * c + 1], v1[4 * c + 2], v1[4 * c + 3]);
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (r == 0) {
+          const int qrow = u.start + (u.kt + it) * kBM;
+          tma_reduce_add_3d(&tmDQ, sDQ, 0, u.h, qrow);
+          tma_reduce_add_3d(&tmDQ, sDQ + kTileBytes, 32, u.h, qrow);
+          bulk_commit_group();
+        }
+        if (ahead < u.n_it) {
+          // The stage of tile gq + 2 last held tile gq - 1, whose softmax has
+          // read it before the dV/dK MMAs that completed QDO_EMPTY.
+          if (gq >= 1 && !mbar_wait(&bars[B_QDO_EMPTY + (gq - 1) % kQStages],
+                                    ((gq - 1) / kQStages) & 1, abort_flag, p.status, 44)) {
+            ok = false;
+            break;
+          }
+          stage_rowstats(gq + kQStages - 1, l2, dl);
+        }
+      }
+      g += u.n_it;
     }
     // Before exit the staging buffers must have been read; the reduce-adds
     // themselves complete with the kernel.
@@ -461,120 +553,129 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const float sl2 = p.scale_log2;
     bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
-      const int s = it % kQStages;
-      if (!mbar_wait_warp(&bars[B_S_FULL], it & 1, abort_flag, p.status, 39)) { ok = false; break; }
-      // LSE/D of this query tile are staged in stage s.
-      if (!mbar_wait_warp(&bars[B_ROW_FULL + s], (it / kQStages) & 1, abort_flag, p.status, 40)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sv[64], dv[64];
-      const uint32_t cs = kColS + 64 * half, cd = kColDP + 64 * half;
-      tmem_ld_x32(tmem + lane_base + cs, sv);
-      tmem_ld_x32(tmem + lane_base + cs + 32, sv + 32);
-      tmem_ld_x32(tmem + lane_base + cd, dv);
-      tmem_ld_x32(tmem + lane_base + cd + 32, dv + 32);
-      tmem_ld_wait(sv);
-      tmem_ld_wait(sv + 32);
-      tmem_ld_wait(dv);
-      tmem_ld_wait(dv + 32);
-      tc_fence_before();
-      mbar_arrive(&bars[B_S_FREE]);  // S^T/dP^T may be overwritten now
-      if (it == 0) {  // query tile == key tile: queries before the key get no weight
-#pragma unroll
-        for (int col = 0; col < 64; ++col)
-          if (64 * half + col < r) sv[col] = 0xff800000u;  // -inf: P = 0, dS = 0
-      }
-      const float4* nl4 = reinterpret_cast<const float4*>(sLSE + s * 128 + 64 * half);
-      const float4* nd4 = reinterpret_cast<const float4*>(sDEL + s * 128 + 64 * half);
-      const uint64_t sl2x2 = f2_pack(sl2, sl2);
-      uint32_t pw[32], dw[32];
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const float4 nl = nl4[q], nd = nd4[q];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int col = 4 * q + 2 * u;
-          const uint64_t t = f2_fma(f2_pack(__uint_as_float(sv[col]), __uint_as_float(sv[col + 1])),
-                                    sl2x2, u ? f2_pack(nl.z, nl.w) : f2_pack(nl.x, nl.y));
-          float t0, t1;
-          f2_unpack(t, t0, t1);
-          const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
-          const uint64_t dd = f2_add(f2_pack(__uint_as_float(dv[col]), __uint_as_float(dv[col + 1])),
-                                     u ? f2_pack(nd.z, nd.w) : f2_pack(nd.x, nd.y));
-          float d0, d1;
-          f2_unpack(f2_mul(f2_pack(p0, p1), dd), d0, d1);
-          pw[col / 2] = pack_bf16x2(p0, p1);
-          dw[col / 2] = pack_bf16x2(d0, d1);
+    int g = 0;  // query tiles over all units
+    NE_FOR_EACH_UNIT(u) {
+      if (!ok) break;
+      for (int it = 0; it < u.n_it; ++it) {
+        const int gq = g + it;
+        const int s = gq % kQStages;
+        if (!mbar_wait_warp(&bars[B_S_FULL], gq & 1, abort_flag, p.status, 39)) {
+          ok = false;
+          break;
         }
+        // LSE/D of this query tile are staged in stage s.
+        if (!mbar_wait_warp(&bars[B_ROW_FULL + s], (gq / kQStages) & 1, abort_flag, p.status, 40)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sv[64], dv[64];
+        const uint32_t cs = kColS + 64 * half, cd = kColDP + 64 * half;
+        tmem_ld_x32(tmem + lane_base + cs, sv);
+        tmem_ld_x32(tmem + lane_base + cs + 32, sv + 32);
+        tmem_ld_x32(tmem + lane_base + cd, dv);
+        tmem_ld_x32(tmem + lane_base + cd + 32, dv + 32);
+        tmem_ld_wait(sv);
+        tmem_ld_wait(sv + 32);
+        tmem_ld_wait(dv);
+        tmem_ld_wait(dv + 32);
+        tc_fence_before();
+        mbar_arrive(&bars[B_S_FREE]);  // S^T/dP^T may be overwritten now
+        if (it == 0) {  // query tile == key tile: queries before the key get no weight
+#pragma unroll
+          for (int col = 0; col < 64; ++col)
+            if (64 * half + col < r) sv[col] = 0xff800000u;  // -inf: P = 0, dS = 0
+        }
+        const float4* nl4 = reinterpret_cast<const float4*>(sLSE + s * 128 + 64 * half);
+        const float4* nd4 = reinterpret_cast<const float4*>(sDEL + s * 128 + 64 * half);
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
+        uint32_t pw[32], dw[32];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const float4 nl = nl4[q], nd = nd4[q];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int col = 4 * q + 2 * e;
+            const uint64_t t = f2_fma(f2_pack(__uint_as_float(sv[col]), __uint_as_float(sv[col + 1])),
+                                      sl2x2, e ? f2_pack(nl.z, nl.w) : f2_pack(nl.x, nl.y));
+            float t0, t1;
+            f2_unpack(t, t0, t1);
+            const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+            const uint64_t dd = f2_add(f2_pack(__uint_as_float(dv[col]), __uint_as_float(dv[col + 1])),
+                                       e ? f2_pack(nd.z, nd.w) : f2_pack(nd.x, nd.y));
+            float d0, d1;
+            f2_unpack(f2_mul(f2_pack(p0, p1), dd), d0, d1);
+            pw[col / 2] = pack_bf16x2(p0, p1);
+            dw[col / 2] = pack_bf16x2(d0, d1);
+          }
+        }
+        // P^T (TMEM) / dS^T (smem): free once the MMAs of the previous tile are done.
+        if (gq >= 1 && !mbar_wait_warp(&bars[B_PDS_FREE], (gq - 1) & 1, abort_flag, p.status, 41)) {
+          ok = false;
+          break;
+        }
+        // P^T row r, queries 64*half .. +63 -> TMEM (32 packed columns); dS^T row
+        // r -> smem block `half`, all eight 16-byte chunks.
+        tmem_st_x32(tmem + lane_base + kColPT + 32 * half, pw);
+#pragma unroll
+        for (int k8 = 0; k8 < 8; ++k8)
+          *reinterpret_cast<uint4*>(sDST + half * kTileBytes + sw128_offset(r, k8)) =
+              make_uint4(dw[4 * k8], dw[4 * k8 + 1], dw[4 * k8 + 2], dw[4 * k8 + 3]);
+        tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&bars[B_DS_FULL]);
       }
-      // P^T (TMEM) / dS^T (smem): free once the MMAs of the previous tile are done.
-      if (it >= 1 && !mbar_wait_warp(&bars[B_PDS_FREE], (it - 1) & 1, abort_flag, p.status, 41)) {
-        ok = false;
+      if (!ok) break;
+      // ---- epilogue of the unit: dV (first half), dK = scale R^T dK' (second)
+      // (overlapped by the next unit's first MMAs, which need no TMEM column
+      // this reads until this thread's next DS_FULL arrival)
+      const int kpos = u.kt * kBN + r;
+      // dV, dK' are final once the last tile's dV/dK' MMAs have completed:
+      // the release of its Q', dO stage is committed right after them (and
+      // tracks every earlier MMA of that warp), before the last dQ' MMAs.
+      const int last = g + u.n_it - 1;
+      if (!(ok = mbar_wait_warp(&bars[B_QDO_EMPTY + last % kQStages], (last / kQStages) & 1,
+                                abort_flag, p.status, 42)))
         break;
-      }
-      // P^T row r, queries 64*half .. +63 -> TMEM (32 packed columns); dS^T row
-      // r -> smem block `half`, all eight 16-byte chunks.
-      tmem_st_x32(tmem + lane_base + kColPT + 32 * half, pw);
-#pragma unroll
-      for (int k8 = 0; k8 < 8; ++k8)
-        *reinterpret_cast<uint4*>(sDST + half * kTileBytes + sw128_offset(r, k8)) =
-            make_uint4(dw[4 * k8], dw[4 * k8 + 1], dw[4 * k8 + 2], dw[4 * k8 + 3]);
-      tmem_st_wait();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&bars[B_DS_FULL]);
-    }
-    // ---- epilogue: dV (first half) and dK = scale * R^T dK' (second half) --
-    // The key's table row (for dK) is loaded before the last MMAs are waited
-    // for; a key past the sequence end reads the last row and writes nothing.
-    const int kpos = kt * kBN + r;
-    float4 tab[16];  // (cos, sin) of dims 2i, 2i + 1 in tab[i]
-    if (half) {
-      const float4* cs4 = reinterpret_cast<const float4*>(
-          p.rope.cs + static_cast<long long>(kpos < len ? kpos : len - 1) * 32);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) tab[i] = __ldg(cs4 + i);
-    }
-    // dV, dK' are final once the last tile's dV/dK' MMAs have completed: the
-    // release of its Q', dO stage is committed right after them (and tracks
-    // every earlier MMA of that warp), before the last dQ' MMAs.
-    const int last = n_it - 1;
-    if (ok && mbar_wait_warp(&bars[B_QDO_EMPTY + last % kQStages], (last / kQStages) & 1,
-                             abort_flag, p.status, 42)) {
       tc_fence_after();
-      uint32_t g[64];
+      uint32_t gr[64];
       const uint32_t col = half ? kColDK : kColDV;
-      tmem_ld_x32(tmem + lane_base + col, g);
-      tmem_ld_x32(tmem + lane_base + col + 32, g + 32);
-      tmem_ld_wait(g);
-      tmem_ld_wait(g + 32);
-      if (kpos < len) {
-        const long long orow = (static_cast<long long>(start + kpos) * H + h) * kHD;
+      tmem_ld_x32(tmem + lane_base + col, gr);
+      tmem_ld_x32(tmem + lane_base + col + 32, gr + 32);
+      tmem_ld_wait(gr);
+      tmem_ld_wait(gr + 32);
+      // (The next unit's first dV/dK' MMAs overwrite these columns only after
+      // this thread's next DS_FULL arrival, which is fenced behind this load.)
+      if (kpos < u.len) {
+        const long long orow = (static_cast<long long>(u.start + kpos) * p.pb.H + u.h) * kHD;
         uint4* dst = reinterpret_cast<uint4*>((half ? p.dk : p.dv) + orow);
         if (half == 0) {
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            dst[c] = make_uint4(pack_bf16x2(__uint_as_float(g[8 * c + 0]), __uint_as_float(g[8 * c + 1])),
-                                pack_bf16x2(__uint_as_float(g[8 * c + 2]), __uint_as_float(g[8 * c + 3])),
-                                pack_bf16x2(__uint_as_float(g[8 * c + 4]), __uint_as_float(g[8 * c + 5])),
-                                pack_bf16x2(__uint_as_float(g[8 * c + 6]), __uint_as_float(g[8 * c + 7])));
+            dst[c] = make_uint4(pack_bf16x2(__uint_as_float(gr[8 * c + 0]), __uint_as_float(gr[8 * c + 1])),
+                                pack_bf16x2(__uint_as_float(gr[8 * c + 2]), __uint_as_float(gr[8 * c + 3])),
+                                pack_bf16x2(__uint_as_float(gr[8 * c + 4]), __uint_as_float(gr[8 * c + 5])),
+                                pack_bf16x2(__uint_as_float(gr[8 * c + 6]), __uint_as_float(gr[8 * c + 7])));
         } else {
+          const float4* cs4 =
+              reinterpret_cast<const float4*>(p.rope.cs + static_cast<long long>(kpos) * 32);
           // Chunk c (dims 8c..8c+7) and its partner c + 4 together.
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
+            float4 tab[4];  // (cos, sin) of dims 8c + 2j, 8c + 2j + 1 in tab[j]
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tab[j] = __ldg(cs4 + 4 * c + j);
             float lo[8], hi[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int i = 8 * c + u;
-              const float4 t4 = tab[i >> 1];
+            for (int e = 0; e < 8; ++e) {
+              const int i = 8 * c + e;
+              const float4 t4 = tab[e >> 1];
               const float cz = (i & 1) ? t4.z : t4.x, sz = (i & 1) ? t4.w : t4.y;
-              const float a = __uint_as_float(g[i]) * p.scale;
-              const float b = __uint_as_float(g[i + 32]) * p.scale;
-              lo[u] = a * cz + b * sz;
-              hi[u] = b * cz - a * sz;
+              const float a = __uint_as_float(gr[i]) * p.scale;
+              const float b = __uint_as_float(gr[i + 32]) * p.scale;
+              lo[e] = a * cz + b * sz;
+              hi[e] = b * cz - a * sz;
             }
             dst[c] = make_uint4(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]),
                                 pack_bf16x2(lo[4], lo[5]), pack_bf16x2(lo[6], lo[7]));
@@ -583,8 +684,10 @@ __global__ void __launch_bounds__(512, 1)
           }
         }
       }
+      g += u.n_it;
     }
   }
+#undef NE_FOR_EACH_UNIT
 
   tc_fence_before();
   __syncthreads();
@@ -656,9 +759,18 @@ cudaError_t launch_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (ev_pre && (e = cudaEventRecord(ev_pre, stream)) != cudaSuccess) return e;
-  dim3 grid(p.pb.nseq * p.pb.H, n_tiles);
-  ne_attn_bwd_kernel<<<grid, bwd::kThreads, bwd::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, tmDO, tmDQ,
-                                                                       p);
+  // One persistent CTA per SM (at most one per unit).
+  static int sm_count[64] = {0};
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!sm_count[dev] &&
+      (e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  const long long n_units = static_cast<long long>(n_tiles) * p.pb.nseq * p.pb.H;
+  const int G = static_cast<int>(n_units < sm_count[dev] ? n_units : sm_count[dev]);
+  ne_attn_bwd_kernel<<<G, bwd::kThreads, bwd::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, tmDO, tmDQ, p,
+                                                                    n_tiles);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (ev_main && (e = cudaEventRecord(ev_main, stream)) != cudaSuccess) return e;
