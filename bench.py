@@ -389,7 +389,7 @@ def run_ours(args):
     n_el = B * T * H * D
     # read O, dO, q, k; write D, zero dQ', write q', k'
     pre_bytes = 4 * n_el * 2 + B * H * T * 4 + n_el * 4 + 2 * n_el * 2
-    post_bytes = n_el * 4 + n_el * 2                      # read dQ', write dQ
+    post_bytes = n_el * 4 + n_el * 2 + 2 * n_el * 2       # read dQ', write dQ; dK in place
     kernels = {
         "ne_attn_fwd_kernel": {"ms": per_kernel["ne_attn_fwd_kernel"],
                                "tflops": f_fwd / (per_kernel["ne_attn_fwd_kernel"] * 1e-3) / 1e12},

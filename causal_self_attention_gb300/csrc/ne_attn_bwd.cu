@@ -15,8 +15,10 @@
 //        dS^T = P^T o (dP^T - D),
 //        dV  += P^T dO (P^T from TMEM),  dK' += dS^T Q',  dQ'_i = dS K'
 //        (-> bulk tensor reduce-add),
-//      and at the end writes dV and dK = scale * R(n)^T dK' (bf16);
-//   3. postprocess: dQ = scale * R(m)^T dQ' (bf16).
+//      and at the end of each unit writes dV and scale * dK' (bf16);
+//   3. postprocess: dQ = scale * R(m)^T dQ' (bf16), and dK = R(n)^T (scale dK')
+//      in place (rotating dK here rather than at the end of each unit keeps
+//      table loads off the unit boundary, where they held up the next unit).
 //
 // Main-kernel warp roles (512 threads, registers re-split per warpgroup):
 //   warps 0-3   row terms and dQ': stage -LSE_i and -D_i two tiles ahead;
@@ -648,41 +650,19 @@ __global__ void __launch_bounds__(512, 1)
       // (The next unit's first dV/dK' MMAs overwrite these columns only after
       // this thread's next DS_FULL arrival, which is fenced behind this load.)
       if (kpos < u.len) {
+        // dV as it is; dK as scale dK' (still rotated: the dK pass that
+        // follows applies R(n)^T, away from the end of the unit, where table
+        // loads would hold up the next unit's first tiles).
         const long long orow = (static_cast<long long>(u.start + kpos) * p.pb.H + u.h) * kHD;
         uint4* dst = reinterpret_cast<uint4*>((half ? p.dk : p.dv) + orow);
-        if (half == 0) {
+        const float sc = half ? p.scale : 1.f;
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            dst[c] = make_uint4(pack_bf16x2(__uint_as_float(gr[8 * c + 0]), __uint_as_float(gr[8 * c + 1])),
-                                pack_bf16x2(__uint_as_float(gr[8 * c + 2]), __uint_as_float(gr[8 * c + 3])),
-                                pack_bf16x2(__uint_as_float(gr[8 * c + 4]), __uint_as_float(gr[8 * c + 5])),
-                                pack_bf16x2(__uint_as_float(gr[8 * c + 6]), __uint_as_float(gr[8 * c + 7])));
-        } else {
-          const float4* cs4 =
-              reinterpret_cast<const float4*>(p.rope.cs + static_cast<long long>(kpos) * 32);
-          // Chunk c (dims 8c..8c+7) and its partner c + 4 together.
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            float4 tab[4];  // (cos, sin) of dims 8c + 2j, 8c + 2j + 1 in tab[j]
-#pragma unroll
-            for (int j = 0; j < 4; ++j) tab[j] = __ldg(cs4 + 4 * c + j);
-            float lo[8], hi[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int i = 8 * c + e;
-              const float4 t4 = tab[e >> 1];
-              const float cz = (i & 1) ? t4.z : t4.x, sz = (i & 1) ? t4.w : t4.y;
-              const float a = __uint_as_float(gr[i]) * p.scale;
-              const float b = __uint_as_float(gr[i + 32]) * p.scale;
-              lo[e] = a * cz + b * sz;
-              hi[e] = b * cz - a * sz;
-            }
-            dst[c] = make_uint4(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]),
-                                pack_bf16x2(lo[4], lo[5]), pack_bf16x2(lo[6], lo[7]));
-            dst[c + 4] = make_uint4(pack_bf16x2(hi[0], hi[1]), pack_bf16x2(hi[2], hi[3]),
-                                    pack_bf16x2(hi[4], hi[5]), pack_bf16x2(hi[6], hi[7]));
-          }
-        }
+        for (int c = 0; c < 8; ++c)
+          dst[c] = make_uint4(
+              pack_bf16x2(__uint_as_float(gr[8 * c + 0]) * sc, __uint_as_float(gr[8 * c + 1]) * sc),
+              pack_bf16x2(__uint_as_float(gr[8 * c + 2]) * sc, __uint_as_float(gr[8 * c + 3]) * sc),
+              pack_bf16x2(__uint_as_float(gr[8 * c + 4]) * sc, __uint_as_float(gr[8 * c + 5]) * sc),
+              pack_bf16x2(__uint_as_float(gr[8 * c + 6]) * sc, __uint_as_float(gr[8 * c + 7]) * sc));
       }
       g += u.n_it;
     }
@@ -699,8 +679,9 @@ __global__ void __launch_bounds__(512, 1)
 }
 
 // ---------------------------------------------------------------------------
-// 3. postprocess: dq = bf16(scale * R(m)^T dq_acc).  Grid (blocks of
-//    kPostThreads items, sequences); an item is (row, head, part): part c
+// 3. postprocess: dq = bf16(scale * R(m)^T dq_acc) (grid layer z = 0) and dk
+//    rotated in place (layer z = 1).  Grid (blocks of kPostThreads items,
+//    sequences, 2); an item is (row, head, part): part c
 //    rotates dims 4c..4c+3 against dims 32+4c..32+4c+3.  Items this small
 //    keep a thread under 32 registers, so that a full SM's worth of threads
 //    is resident and the grid spans several waves (a small last wave costs
@@ -708,12 +689,52 @@ __global__ void __launch_bounds__(512, 1)
 // ---------------------------------------------------------------------------
 constexpr int kPostThreads = 256, kPostParts = 8;
 
+// ---------------------------------------------------------------------------
+// dK item of the postprocess (grid layer z = 1): dk = R(n)^T dk in place (the
+// main kernel wrote scale dK', still rotated).  Items as for dQ: (row, head,
+// part), part c rotates dims 4c..4c+3 against 32+4c..32+4c+3, in fp32 from
+// bf16.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void dk_rotate_item(__nv_bfloat16* __restrict__ dk, const Problem& pb,
+                                               const RopeTable& rope, int start, int len) {
+  const int H = pb.H;
+  const long long w = static_cast<long long>(blockIdx.x) * kPostThreads + threadIdx.x;
+  if (w >= static_cast<long long>(len) * H * kPostParts) return;
+  const int part = static_cast<int>(w % kPostParts);
+  const long long rh = w / kPostParts;
+  const int pos = static_cast<int>(rh / H), h = static_cast<int>(rh - static_cast<long long>(pos) * H);
+  __nv_bfloat16* row = dk + (static_cast<long long>(start + pos) * H + h) * kHD;
+  const uint2 lo = *reinterpret_cast<const uint2*>(row + part * 4);
+  const uint2 hi = *reinterpret_cast<const uint2*>(row + 32 + part * 4);
+  const float4* cs4 =
+      reinterpret_cast<const float4*>(rope.cs + static_cast<long long>(pos) * 32 + part * 4);
+  const float4 t0 = __ldg(cs4), t1 = __ldg(cs4 + 1);  // (cos, sin) of dims 4c .. 4c + 3
+  const float a[4] = {bf16lo_to_f32(lo.x), bf16hi_to_f32(lo.x), bf16lo_to_f32(lo.y), bf16hi_to_f32(lo.y)};
+  const float b[4] = {bf16lo_to_f32(hi.x), bf16hi_to_f32(hi.x), bf16lo_to_f32(hi.y), bf16hi_to_f32(hi.y)};
+  const float cz[4] = {t0.x, t0.z, t1.x, t1.z};
+  const float sz[4] = {t0.y, t0.w, t1.y, t1.w};
+  float go[4], gh[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    go[i] = a[i] * cz[i] + b[i] * sz[i];
+    gh[i] = b[i] * cz[i] - a[i] * sz[i];
+  }
+  *reinterpret_cast<uint2*>(row + part * 4) = make_uint2(pack_bf16x2(go[0], go[1]), pack_bf16x2(go[2], go[3]));
+  *reinterpret_cast<uint2*>(row + 32 + part * 4) =
+      make_uint2(pack_bf16x2(gh[0], gh[1]), pack_bf16x2(gh[2], gh[3]));
+}
+
 __global__ void __launch_bounds__(kPostThreads)
     ne_attn_dq_postprocess_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq,
-                                  const Problem pb, RopeTable rope, float scale) {
+                                  __nv_bfloat16* __restrict__ dk, const Problem pb, RopeTable rope,
+                                  float scale) {
   const int seq = blockIdx.y;
   int start, len;
   if (!seq_bounds(pb, seq, start, len, nullptr)) return;
+  if (blockIdx.z == 1) {
+    dk_rotate_item(dk, pb, rope, start, len);
+    return;
+  }
   const int H = pb.H;
   const long long w = static_cast<long long>(blockIdx.x) * kPostThreads + threadIdx.x;
   if (w >= static_cast<long long>(len) * H * kPostParts) return;
@@ -775,9 +796,10 @@ cudaError_t launch_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
   if (e != cudaSuccess) return e;
   if (ev_main && (e = cudaEventRecord(ev_main, stream)) != cudaSuccess) return e;
   const long long post_items = static_cast<long long>(n_tiles) * kBM * p.pb.H * kPostParts;
-  dim3 pgrid(static_cast<unsigned>((post_items + kPostThreads - 1) / kPostThreads), p.pb.nseq);
-  ne_attn_dq_postprocess_kernel<<<pgrid, kPostThreads, 0, stream>>>(p.dq_acc, p.dq, p.pb, p.rope,
-                                                                    p.scale);
+  // Layer z = 0: dQ from the accumulator; z = 1: dK rotated in place.
+  dim3 pgrid(static_cast<unsigned>((post_items + kPostThreads - 1) / kPostThreads), p.pb.nseq, 2);
+  ne_attn_dq_postprocess_kernel<<<pgrid, kPostThreads, 0, stream>>>(p.dq_acc, p.dq, p.dk, p.pb,
+                                                                    p.rope, p.scale);
   return cudaGetLastError();
 }
 
