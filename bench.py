@@ -48,11 +48,25 @@ def parse():
     ap.add_argument("--path", choices=("train", "decode"), default="train",
                     help="train: the fwd+bwd step (the headline); decode: one generation "
                          "step against a KV cache (decode16k)")
+    ap.add_argument("--extra-steps", type=int, default=50,
+                    help="timed steps of each longer workload reported beside the headline")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the longer workloads and the decode step")
+    ap.add_argument("--cpu-sample", type=float, default=None, help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
 def flops_fwd_bwd(B, H, T, D):
     fwd = 2.0 * B * H * T * T * D
+    return fwd, 2.5 * fwd
+
+
+def workload_flops(inp):
+    """Causal fwd and bwd FLOPs of a workload: 2*H*D*sum(L^2) forward (2*B*H*T^2*D
+    for a fixed-length batch), 2.5x that backward."""
+    H, D = inp["H"], inp["D"]
+    lengths = inp["lengths"] if "lengths" in inp else [inp["T"]] * inp["B"]
+    fwd = 2.0 * H * D * sum(float(L) * L for L in lengths)
     return fwd, 2.5 * fwd
 
 
@@ -154,6 +168,35 @@ def oracle_sample(seconds_target, inp, fixed_T=None):
     return heads * (fwd + bwd), el, heads, T
 
 
+def run_cpu_sample(args):
+    """Print the oracle's throughput on a bounded sample of the headline workload
+    (used by the benchmark to time the oracle on one core in a child process)."""
+    import oracle
+    from causal_self_attention_gb300.inputs import make_inputs
+    oracle.build()
+    fl, sec, heads, Ts = oracle_sample(args.cpu_sample, make_inputs(WORKLOAD))
+    print(json.dumps({"flops": fl, "seconds": sec, "heads": heads, "T": Ts,
+                      "cores": oracle.num_threads()}))
+    return 0
+
+
+def oracle_one_core(seconds):
+    """The oracle's TFLOP/s on one host core, measured in a child process with
+    OMP_NUM_THREADS=1 (spawned with exec, so it shares nothing with this
+    process's CUDA context)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    for k in ("RANK", "LOCAL_RANK", "WORLD_SIZE"):
+        env.pop(k, None)
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-sample", str(seconds)],
+                       env=env, capture_output=True, text=True, timeout=600)
+    if r.returncode != 0:
+        return None
+    rec = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": rec["flops"] / rec["seconds"] / 1e12, "unit": UNIT, "cores": rec["cores"],
+            "sample": f"{rec['heads']} whole heads (b, h) of the {WORKLOAD} workload, "
+                      f"T={rec['T']}, fwd+bwd in fp64, {rec['seconds']:.1f} s"}
+
+
 def run_reference(args):
     rank, _, world = rank_env()
     if world > 1 and rank != 0:
@@ -218,6 +261,120 @@ def recorded_traffic(kernel):
     if rec.get("source_sha") != source_sha(rec["sources"]):
         return None
     return rec.get("dram_bytes_per_launch")
+
+
+def bench_workloads(args, dev, stream, flush, peak_tf):
+    """Fwd+bwd throughput of the longer workloads (byte-level contexts and the
+    packed varlen batch), each with the L2 flushed before every timed step.
+    The headline stays the GPT-2-small line; these are reported beside it."""
+    import torch
+
+    from causal_self_attention_gb300 import ne_attn as na
+    from causal_self_attention_gb300.inputs import make_inputs
+    res = {}
+    for name in ("byte4k", "long16k", "varlen"):
+        inp = make_inputs(name)
+        q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "dout"))
+        base, scale = inp["rope_base"], inp["scale"]
+        H, D = inp["H"], inp["D"]
+        N = q.shape[0] * (q.shape[1] if q.dim() == 4 else 1)
+        ws = torch.empty(na.ne_attn_bwd_workspace_bytes(N, H, D), dtype=torch.uint8, device=dev)
+        out = torch.empty_like(q)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        if "cu_seqlens" in inp:
+            cu, mx = inp["cu_seqlens"].to(dev), inp["max_seqlen"]
+            lse = torch.empty((H, N), dtype=torch.float32, device=dev)
+
+            def step():
+                na.ne_attn_varlen_fwd(q, k, v, cu, mx, base, scale, out=out, lse=lse,
+                                      stream=stream)
+                na.ne_attn_varlen_bwd(q, k, v, out, do, lse, cu, mx, base, scale, dq=dq, dk=dk,
+                                      dv=dv, workspace=ws, stream=stream)
+        else:
+            B, T = inp["B"], inp["T"]
+            lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+
+            def step():
+                na.ne_attn_fwd(q, k, v, base, scale, out=out, lse=lse, stream=stream)
+                na.ne_attn_bwd(q, k, v, out, do, lse, base, scale, dq=dq, dk=dk, dv=dv,
+                               workspace=ws, stream=stream)
+        for _ in range(3):
+            flush.zero_()
+            step()
+        n = max(args.extra_steps, 3)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+        for e in ev:
+            flush.zero_()
+            e[0].record(stream)
+            if "cu_seqlens" in inp:
+                na.ne_attn_varlen_fwd(q, k, v, cu, mx, base, scale, out=out, lse=lse,
+                                      stream=stream)
+                e[1].record(stream)
+                na.ne_attn_varlen_bwd(q, k, v, out, do, lse, cu, mx, base, scale, dq=dq, dk=dk,
+                                      dv=dv, workspace=ws, stream=stream)
+            else:
+                na.ne_attn_fwd(q, k, v, base, scale, out=out, lse=lse, stream=stream)
+                e[1].record(stream)
+                na.ne_attn_bwd(q, k, v, out, do, lse, base, scale, dq=dq, dk=dk, dv=dv,
+                               workspace=ws, stream=stream)
+            e[2].record(stream)
+        torch.cuda.synchronize()
+        assert na.ne_attn_get_device_status() == 0
+        f_fwd, f_bwd = workload_flops(inp)
+        t_all = [e[0].elapsed_time(e[2]) for e in ev]
+        t_f = [e[0].elapsed_time(e[1]) for e in ev]
+        t_b = [e[1].elapsed_time(e[2]) for e in ev]
+        mean, medi = statistics.mean(t_all), statistics.median(t_all)
+        shape = (f"B={inp['B']} H={H} T={inp['T']} D={D}" if "B" in inp else
+                 f"{len(inp['lengths'])} sequences, L~U[64,2048] (sum {N}), H={H} D={D}")
+        res[name] = {
+            "shape": shape, "steps": n, "gflop_per_step": (f_fwd + f_bwd) / 1e9,
+            "ms_per_step": mean, "ms_per_step_median": medi,
+            "tflops": (f_fwd + f_bwd) / (mean * 1e-3) / 1e12,
+            "tflops_at_median": (f_fwd + f_bwd) / (medi * 1e-3) / 1e12,
+            "pct_bf16_peak": 100.0 * (f_fwd + f_bwd) / (mean * 1e-3) / 1e12 / peak_tf,
+            "fwd_ms_median": statistics.median(t_f), "bwd_ms_median": statistics.median(t_b),
+            "fwd_tflops_at_median": f_fwd / (statistics.median(t_f) * 1e-3) / 1e12,
+            "bwd_tflops_at_median": f_bwd / (statistics.median(t_b) * 1e-3) / 1e12,
+        }
+        del q, k, v, do, ws, out, dq, dk, dv, lse
+    return res
+
+
+def decode_summary(args, dev, stream, peaks):
+    """One decode step over a KV cache (decode16k), timed with CUDA events:
+    GB/s of K and V read, against the measured HBM bandwidth."""
+    import torch
+
+    from causal_self_attention_gb300 import ne_attn as na
+    from causal_self_attention_gb300.inputs import make_decode
+    inp = make_decode(DECODE_WORKLOAD)
+    B, H, Tmax = inp["B"], inp["H"], inp["Tmax"]
+    q, kc, vc, pos = (inp[n].to(dev) for n in ("q", "k_cache", "v_cache", "pos"))
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    ws = torch.empty(na.ne_attn_decode_workspace_bytes(B, H, Tmax), dtype=torch.uint8, device=dev)
+    for _ in range(5):
+        na.ne_attn_decode(q, kc, vc, pos, inp["rope_base"], inp["scale"], out=out, lse=lse,
+                          workspace=ws, stream=stream)
+    n = max(4 * args.extra_steps, 3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    for a, b in ev:  # the cache (2 x 403 MB) is larger than L2: no flush needed
+        a.record(stream)
+        na.ne_attn_decode(q, kc, vc, pos, inp["rope_base"], inp["scale"], out=out, lse=lse,
+                          workspace=ws, stream=stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    assert na.ne_attn_get_device_status() == 0
+    t = [a.elapsed_time(b) for a, b in ev]
+    kv = decode_kv_bytes(inp)
+    medi = statistics.median(t)
+    return {"workload": f"{DECODE_WORKLOAD}: B={B} H={H} Tmax={Tmax} D=64, one new token per "
+                        "sequence at the last cache row", "steps": n,
+            "ms_per_step": statistics.mean(t), "ms_per_step_median": medi,
+            "gbs_at_median": kv / (medi * 1e-3) / 1e9, "kv_bytes_per_step": kv,
+            "frac_hbm": kv / (medi * 1e-3) / 1e9 / peaks["hbm_gbs"]}
 
 
 def run_ours(args):
@@ -297,6 +454,7 @@ def run_ours(args):
     t_step = [e[0].elapsed_time(e[4]) for e in ev]
     total_ms = slowest_rank_ms(sum(t_step), world, dev)
     value = job_tflops(f_step, K, total_ms, world)
+    median_ms = slowest_rank_ms(statistics.median(t_step), world, dev)
 
     # ---- end to end through the public API with host buffers ------------------
     # Every step uploads its q, k, v, dO from pinned host memory and downloads
@@ -390,6 +548,10 @@ def run_ours(args):
     # read O, dO, q, k; write D, zero dQ', write q', k'
     pre_bytes = 4 * n_el * 2 + B * H * T * 4 + n_el * 4 + 2 * n_el * 2
     post_bytes = n_el * 4 + n_el * 2 + 2 * n_el * 2       # read dQ', write dQ; dK in place
+    med = {"ne_attn_fwd_kernel": statistics.median(t_fwd),
+           "ne_attn_bwd_preprocess_kernel": statistics.median(t_pre),
+           "ne_attn_bwd_kernel": statistics.median(t_main),
+           "ne_attn_dq_postprocess_kernel": statistics.median(t_post)}
     kernels = {
         "ne_attn_fwd_kernel": {"ms": per_kernel["ne_attn_fwd_kernel"],
                                "tflops": f_fwd / (per_kernel["ne_attn_fwd_kernel"] * 1e-3) / 1e12},
@@ -402,9 +564,13 @@ def run_ours(args):
             "ms": per_kernel["ne_attn_dq_postprocess_kernel"],
             "gbs": post_bytes / (per_kernel["ne_attn_dq_postprocess_kernel"] * 1e-3) / 1e9},
     }
+    for name in kernels:
+        kernels[name]["ms_median"] = med[name]
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-        "warmup": max(args.warmup, 3), "ms_per_step": total_ms / K, "higher_is_better": True,
+        "warmup": max(args.warmup, 3), "ms_per_step": total_ms / K,
+        "ms_per_step_median": median_ms,
+        "value_at_median": job_tflops(f_step, 1, median_ms, world), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{WORKLOAD}: B={B} H={H} T={T} D={D}, causal, RoPE base 10000, "
                                "fwd+bwd", "B": B, "H": H, "T": T, "D": D,
@@ -426,6 +592,9 @@ def run_ours(args):
         "wall_s": wall,
         "device_status": status,
     }
+    if not args.no_extras:
+        line["workloads"] = bench_workloads(args, dev, stream, flush, peak_tf)
+        line["decode"] = decode_summary(args, dev, stream, peaks)
     if not args.no_cpu_baseline and (world == 1 or rank == 0):
         import oracle
         oracle.build()
@@ -434,6 +603,9 @@ def run_ours(args):
             "value": fl / s / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{heads} whole heads (b, h) of the {WORKLOAD} workload, T={Ts}, fwd+bwd "
                       f"in fp64, {s:.1f} s"}
+        one = oracle_one_core(args.cpu_seconds)
+        if one is not None:
+            line["cpu_baseline"]["one_core"] = one
     print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
@@ -570,6 +742,8 @@ def run_decode(args):
 
 def main():
     args = parse()
+    if args.cpu_sample is not None:
+        return run_cpu_sample(args)
     if args.path == "decode":
         return run_decode(args)
     if args.impl == "reference":

@@ -26,6 +26,8 @@ cudaError_t launch_debug_tile(const CUtensorMap& tm, int h, int row0, int rotate
                               int* status, cudaStream_t stream);
 cudaError_t launch_debug_umma(int form, const __nv_bfloat16* a, const __nv_bfloat16* b, float* d,
                               int* status, cudaStream_t stream);
+cudaError_t launch_debug_pipeline(const CUtensorMap& tm, int n_items, int drop_item,
+                                  long long limit, float* d, int* status, cudaStream_t stream);
 size_t decode_part_bytes(int B, int H, int Tmax);
 cudaError_t launch_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmT,
                           const __nv_bfloat16* q, const int* pos, int B, int H, int Tmax,
@@ -608,6 +610,24 @@ ne_status ne_debug_umma(int form, const ne_bf16* a, const ne_bf16* b, float* d, 
   return cuda_status(ne::launch_debug_umma(form, reinterpret_cast<const __nv_bfloat16*>(a),
                                            reinterpret_cast<const __nv_bfloat16*>(b), d,
                                            st->status, static_cast<cudaStream_t>(stream)));
+}
+
+ne_status ne_debug_pipeline(const ne_bf16* src, int n_rows, int H, int n_items, int drop_item,
+                            long long wait_limit_cycles, float* d, void* stream) {
+  if (!src || !d || n_rows <= 0 || H <= 0 || n_items < 1 || n_items > 64 ||
+      static_cast<long long>(n_items) * 128 > n_rows || drop_item < -1 || drop_item >= n_items ||
+      wait_limit_cycles < 1000 || wait_limit_cycles > 2000000000LL)
+    return NE_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(d)) return NE_ERR_MISALIGNED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState* st = nullptr;
+  ne_status rc = device_state(&st);
+  if (rc != NE_OK) return rc;
+  if ((rc = get_encoder()) != NE_OK) return rc;
+  CUtensorMap tm;
+  if ((rc = encode_rows(&tm, src, n_rows, H)) != NE_OK) return rc;
+  return cuda_status(ne::launch_debug_pipeline(tm, n_items, drop_item, wait_limit_cycles, d,
+                                               st->status, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -48,23 +48,25 @@ NoAllocDevice g_noalloc_dev[kMaxDevices];
 
 // The RoPE table for `base`, built on the host in double with the same rule as
 // the library's cached tables (cs[p * 32 + i] = fp32 cos / sin of p * theta_i,
-// theta_i = base^(-(2i)/64)), copied into the scratch in fixed-size pieces.
-ne_status upload_table(unsigned char* dst, float base) {
-  constexpr int kChunk = 256;  // positions per piece
-  static float2 piece[kChunk * 32];
+// theta_i = base^(-(2i)/64)), and copied into the scratch with one copy
+// enqueued on `stream`.  Being stream-ordered, the copy starts only after the
+// kernels of earlier calls on this stream, which read the old table, have
+// finished, and the kernels this call launches next see the new table.  The
+// host image is a pageable array: an asynchronous copy from pageable memory
+// has taken its bytes by the time it returns, so the image may be rebuilt by
+// the next call at once.
+ne_status upload_table(unsigned char* dst, float base, cudaStream_t stream) {
+  static float2 image[static_cast<size_t>(kMaxPositions) * 32];
   double theta[32];
   for (int i = 0; i < 32; ++i) theta[i] = std::pow(static_cast<double>(base), -(2.0 * i) / 64.0);
-  for (int p0 = 0; p0 < kMaxPositions; p0 += kChunk) {
-    for (int pp = 0; pp < kChunk; ++pp)
-      for (int i = 0; i < 32; ++i) {
-        const double a = static_cast<double>(p0 + pp) * theta[i];
-        piece[pp * 32 + i] =
-            make_float2(static_cast<float>(std::cos(a)), static_cast<float>(std::sin(a)));
-      }
-    if (cudaMemcpy(dst + static_cast<size_t>(p0) * 32 * sizeof(float2), piece, sizeof(piece),
-                   cudaMemcpyHostToDevice) != cudaSuccess)
-      return NE_ERR_CUDA;
-  }
+  for (int p = 0; p < kMaxPositions; ++p)
+    for (int i = 0; i < 32; ++i) {
+      const double a = static_cast<double>(p) * theta[i];
+      image[static_cast<size_t>(p) * 32 + i] =
+          make_float2(static_cast<float>(std::cos(a)), static_cast<float>(std::sin(a)));
+    }
+  if (cudaMemcpyAsync(dst, image, sizeof(image), cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return NE_ERR_CUDA;
   return NE_OK;
 }
 
@@ -105,7 +107,8 @@ extern "C" ne_status ne_attn_bwd_noalloc(const ne_bf16* q, const ne_bf16* k, con
   }
   if (nd.table_base != rope_base) {
     nd.table_base = 0.f;
-    if ((rc = upload_table(nd.scratch, rope_base)) != NE_OK) return rc;
+    if ((rc = upload_table(nd.scratch, rope_base, static_cast<cudaStream_t>(stream))) != NE_OK)
+      return rc;
     nd.table_base = rope_base;
   }
 

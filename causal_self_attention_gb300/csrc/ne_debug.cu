@@ -161,6 +161,121 @@ __global__ void __launch_bounds__(128, 1)
   }
 }
 
+// A two-stage TMA -> tcgen05 pipeline shaped like the attention kernels' own:
+// a producer lane streams 128 x 64 tiles A_i into a ring, an MMA warp
+// accumulates D += A_i A_i^T in TMEM and frees each stage with a commit, and
+// every wait is bounded -- here by the runtime limit `limit` (cycles).  With
+// drop_item >= 0 the producer leaves out the load of that item and its arrive,
+// so the MMA warp's wait for it expires.  The kernel must then take the
+// attention kernels' abort path: the timeout (site 51) is recorded in the
+// status word, every role stops, the copies and MMAs already in flight are
+// waited for (bounded), TMEM is released, and the kernel exits normally.  D
+// (row-major [128, 128] fp32) is written only when nothing aborted.
+__global__ void __launch_bounds__(128, 1)
+    ne_debug_pipeline_kernel(const __grid_constant__ CUtensorMap tm, int n_items, int drop_item,
+                             long long limit, float* d, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * kTileBytes);  // FULL 0-1, EMPTY 2-3, DONE 4
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 2 * kTileBytes + 64);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 2 * kTileBytes + 68);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < 5; ++b) mbar_init(&bars[b], 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 128);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (warp == 1 && lane == 0) {
+    int last_issued[2] = {-1, -1};
+    for (int i = 0; i < n_items; ++i) {
+      const int s = i & 1;
+      if (i >= 2 && !mbar_wait_limit(&bars[2 + s], ((i - 2) >> 1) & 1, abort_flag, status, 50,
+                                     limit))
+        break;
+      if (i == drop_item) continue;  // the left-out producer arrive
+      mbar_arrive_expect_tx(&bars[s], kTileBytes);
+      tma_load_3d(smem + s * kTileBytes, &tm, &bars[s], 0, 0, i * kBM);
+      last_issued[s] = i;
+    }
+    // Copies in flight land before the CTA exits (after an abort the consumer
+    // may not have waited for them).
+    {
+      for (int s = 0; s < 2; ++s)
+        if (last_issued[s] >= 0) {
+          const long long t0 = clock64();
+          while (!mbar_try_wait(&bars[s], (last_issued[s] >> 1) & 1) &&
+                 clock64() - t0 < NE_WAIT_LIMIT_CYCLES) {
+          }
+        }
+    }
+  } else if (warp == 2) {
+    const uint32_t idesc = make_idesc_bf16(128, 128, false, false);
+    for (int i = 0; i < n_items; ++i) {
+      const int s = i & 1;
+      const bool ok =
+          mbar_wait_limit(&bars[s], (i >> 1) & 1, abort_flag, status, 51, limit);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      if (elect_one()) {
+        const uint64_t dA = make_sdesc_sw128(smem_u32(smem + s * kTileBytes), 16, 1024);
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16_ss(tmem, dA + 2 * kk, dA + 2 * kk, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&bars[2 + s]);
+      }
+      __syncwarp();
+    }
+    // Drain: every MMA issued completes before TMEM is read or released.
+    if (elect_one()) umma_commit(&bars[4]);
+    __syncwarp();
+    const long long t0 = clock64();
+    while (!mbar_try_wait(&bars[4], 0) && clock64() - t0 < NE_WAIT_LIMIT_CYCLES) {
+    }
+    __syncwarp();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (!*abort_flag) {
+    const int row = warp * 32 + lane;
+    for (int c0 = 0; c0 < 128; c0 += 32) {
+      uint32_t r[32];
+      tmem_ld_x32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, r);
+      tmem_ld_wait(r);
+      for (int c = 0; c < 32; ++c) d[row * 128 + c0 + c] = __uint_as_float(r[c]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 128);
+  }
+}
+
+cudaError_t launch_debug_pipeline(const CUtensorMap& tm, int n_items, int drop_item,
+                                  long long limit, float* d, int* status, cudaStream_t stream) {
+  const int smem = 2 * kTileBytes + 128 + 1024;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(ne_debug_pipeline_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  ne_debug_pipeline_kernel<<<1, 128, smem, stream>>>(tm, n_items, drop_item, limit, d, status);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_debug_tile(const CUtensorMap& tm, int h, int row0, int rotate, int pos0,
                               RopeTable rope, void* dst_raw, __nv_bfloat16* dst_rows,
                               int* status, cudaStream_t stream) {

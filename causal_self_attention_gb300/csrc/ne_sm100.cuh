@@ -71,21 +71,26 @@ __device__ __forceinline__ void mbar_arrive_count(uint64_t* bar, uint32_t count)
 }
 
 // Wait for the phase with the given parity to complete.  Returns false (after
-// raising the CTA abort flag and the device status) if it does not complete in
-// time, or if another role of this CTA has already aborted.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status, int site) {
+// raising the CTA abort flag and the device status) if it does not complete
+// within `limit` cycles, or if another role of this CTA has already aborted.
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity,
+                                                volatile int* abort_flag, int* status, int site,
+                                                long long limit) {
   if (mbar_test_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > NE_WAIT_LIMIT_CYCLES) {
+    if (clock64() - t0 > limit) {
       *abort_flag = 1;
       if (status) atomicCAS(status, 0, NE_DEV_TIMEOUT_BASE + site);
       return false;
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status, int site) {
+  return mbar_wait_limit(bar, parity, abort_flag, status, site, NE_WAIT_LIMIT_CYCLES);
 }
 
 // Warp-uniform wait: every lane waits, then the lanes agree on the outcome

@@ -28,7 +28,8 @@ EXPORTED = ("ne_attn_fwd", "ne_attn_fwd_f32out", "ne_attn_bwd", "ne_attn_bwd_wor
             "ne_attn_varlen_fwd", "ne_attn_varlen_fwd_f32out", "ne_attn_varlen_bwd",
             "ne_attn_set_bwd_phase_events", "ne_attn_get_device_status",
             "ne_attn_last_device_code", "ne_status_string",
-            "ne_attn_release", "ne_debug_tma_tile", "ne_debug_rope_tile", "ne_debug_umma")
+            "ne_attn_release", "ne_debug_tma_tile", "ne_debug_rope_tile", "ne_debug_umma",
+            "ne_debug_pipeline")
 
 
 class NeAttnError(RuntimeError):
@@ -68,6 +69,7 @@ def lib():
         "ne_debug_tma_tile": [P, I, I, I, I, P, P],
         "ne_debug_rope_tile": [P, I, I, I, I, I, F, P, P],
         "ne_debug_umma": [I, P, P, P, P],
+        "ne_debug_pipeline": [P, I, I, I, I, ctypes.c_longlong, P, P],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -294,4 +296,17 @@ def ne_debug_umma(form, a, b, stream=None):
     d = torch.empty((128, 128 if form == 0 else 64), dtype=torch.float32, device=a.device)
     _check("ne_debug_umma", lib().ne_debug_umma(int(form), _ptr(a), _ptr(b), _ptr(d),
                                                 _stream(stream)))
+    return d
+
+
+def ne_debug_pipeline(src, n_items, drop_item=-1, wait_limit_cycles=2_000_000_000, stream=None):
+    """Run the bounded-wait pipeline of include/ne_attn_debug.h on ``src``
+    (``[n, H, 64]`` bf16).  Returns ``d`` ``[128, 128]`` fp32 (left unwritten
+    when the pipeline aborted; read the status with ne_attn_get_device_status)."""
+    _need(src, torch.bfloat16, "src")
+    n, H, _ = src.shape
+    d = torch.zeros((128, 128), dtype=torch.float32, device=src.device)
+    _check("ne_debug_pipeline", lib().ne_debug_pipeline(_ptr(src), n, H, int(n_items),
+                                                        int(drop_item), int(wait_limit_cycles),
+                                                        _ptr(d), _stream(stream)))
     return d

@@ -148,13 +148,16 @@ ne_status ne_attn_set_bwd_phase_events(void* ev_after_preprocess, void* ev_after
  * dQ accumulator) and T <= NE_NOALLOC_MAX_POSITIONS; beyond them the call
  * returns NE_ERR_TOO_LARGE before touching the device.
  *
- * The first call on a device (and the first call with a new rope_base) looks
- * up the array's device address and writes the RoPE table into it with a
- * synchronous copy; make that first call before any stream capture.  Every
- * call shares the one array and leaves the last call's contents in it (the
- * parts that must start from zero are cleared on every call), so calls whose
- * work overlaps on the GPU -- on different streams, or on different host
- * threads -- race and must be serialized by the caller.  Results equal those
+ * The first call on a device looks up the array's device address (with that
+ * device current).  The first call, and any call whose rope_base differs from
+ * the previous call's, writes the RoPE table for that base into the array with
+ * a copy from host memory enqueued on `stream`: it runs after the earlier work
+ * of that stream (whose kernels may still read the old table) and before this
+ * call's kernels.  Make the first call before any stream capture.  Every call
+ * shares the one array and leaves the last call's contents in it (the parts
+ * that must start from zero are cleared on every call), so calls whose work
+ * overlaps on the GPU -- on different streams, or on different host threads --
+ * race and must be serialized by the caller.  Results equal those
  * of ne_attn_bwd (dq up to the order of its fp32 atomic adds). */
 #define NE_NOALLOC_SCRATCH_BYTES (64u << 20)
 #define NE_NOALLOC_MAX_POSITIONS 16384

@@ -43,6 +43,23 @@ ne_status ne_debug_rope_tile(const ne_bf16* src, int n_rows, int H, int h, int r
  * a, b: row-major bf16 as written above; d: row-major fp32. */
 ne_status ne_debug_umma(int form, const ne_bf16* a, const ne_bf16* b, float* d, void* stream);
 
+/* A two-stage TMA -> tcgen05 pipeline shaped like the attention kernels' own
+ * (a producer lane streams the 128 x 64 tiles A_i = rows 128 i .. 128 i + 127
+ * of head 0 of src into a ring; an MMA warp accumulates d = sum_i A_i A_i^T in
+ * TMEM), whose bounded waits use the runtime limit wait_limit_cycles (1000 ..
+ * 2e9) instead of the kernels' fixed one.  drop_item = -1: every item is
+ * loaded and d ([128, 128] fp32, device) is written.  drop_item = i: the
+ * producer leaves out item i's load and its arrive, so the MMA warp's wait for
+ * it expires; the kernel then records NE_ERR_TIMEOUT (device code 0x100 + 51)
+ * for ne_attn_get_device_status, waits for its copies and MMAs in flight,
+ * releases its TMEM and returns without writing d.  This tests the failure
+ * path of the kernels without hanging or faulting the GPU (failure detection:
+ * the NanoEuler Show HN page, paragraph 5, on training that can be
+ * interrupted and resumed).  Requires 1 <= n_items <= 64 and
+ * 128 * n_items <= n_rows. */
+ne_status ne_debug_pipeline(const ne_bf16* src, int n_rows, int H, int n_items, int drop_item,
+                            long long wait_limit_cycles, float* d, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -96,11 +96,13 @@ def check_full(inp, gpu, bwd=True):
     return errs
 
 
-def check_sampled(inp, gpu, picks, bwd=True):
+def check_sampled(inp, gpu, picks, bwd=True, long_loop_tiles=None):
     """Compare sampled rows with the oracle, for workloads too large for the
     full oracle.  ``picks``: list of (seq, head, qrows, krows).  O and LSE are
     checked row by row against the bound; gradients by relative L2 over the
-    sampled rows."""
+    sampled rows.  With ``long_loop_tiles`` = n, the key rows whose gradients
+    sum over at least n query tiles of 128 rows are also judged on their own
+    (``dk_long_rel_l2``, ``dv_long_rel_l2``)."""
     (q, k, v, do), cu = packed_view(inp)
     base, scale = inp["rope_base"], inp["scale"]
     r1 = oracle.attention_sampled(q, k, v, None, cu, [(s, h, qr, []) for s, h, qr, _ in picks],
@@ -108,7 +110,7 @@ def check_sampled(inp, gpu, picks, bwd=True):
     r0 = (oracle.attention_sampled(q, k, v, do, cu, picks, base=base, scale=scale, mode=0)
           if bwd else None)
     o_err = lse_err = 0.0
-    acc = {n: ([], []) for n in ("dq", "dk", "dv")}
+    acc = {n: ([], []) for n in ("dq", "dk", "dv", "dk_long", "dv_long")}
     for idx, (s, h, qrows, krows) in enumerate(picks):
         t0 = cu[s]
         qi = np.asarray(qrows) + t0
@@ -124,6 +126,13 @@ def check_sampled(inp, gpu, picks, bwd=True):
                 acc["dk"][1].append(r0[idx]["dk"])
                 acc["dv"][0].append(gpu["dv"][ki, h].double().numpy())
                 acc["dv"][1].append(r0[idx]["dv"])
+                if long_loop_tiles:
+                    L = cu[s + 1] - cu[s]
+                    sel = (L - np.asarray(krows)) > 128 * (long_loop_tiles - 1)
+                    if sel.any():
+                        for n in ("dk", "dv"):
+                            acc[n + "_long"][0].append(gpu[n][ki[sel], h].double().numpy())
+                            acc[n + "_long"][1].append(r0[idx][n][sel])
     errs = {"o_max_abs": o_err, "lse_max_abs": lse_err}
     assert torch.equal(gpu["o16"], gpu["o32"].to(torch.bfloat16)), "bf16 O != rne(fp32 O)"
     assert o_err <= O_TOL and lse_err <= LSE_TOL, errs

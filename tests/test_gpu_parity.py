@@ -56,6 +56,16 @@ def test_gpt2s_config_full():
     _report("gpt2s", check_full(inp, run_gpu(inp)))
 
 
+def _long_loop_keys(L, rng):
+    """Key rows whose gradients sum over the most query tiles: the first key
+    tile (rows 0, 1, 127 and a few more), the first row of the second tile, and
+    a tile in the middle of the sequence."""
+    mid = (L // 2) // 128 * 128
+    rows = [0, 1, 127, 128, mid, mid + 1, mid + 127]
+    rows += list(rng.integers(0, min(L, 128), 6))
+    return [r for r in rows if r < L]
+
+
 def _picks_fixed(inp, n_q=48, n_k=48, seed=0):
     rng = np.random.default_rng(seed)
     B, T, H = inp["B"], inp["T"], inp["H"]
@@ -67,32 +77,48 @@ def _picks_fixed(inp, n_q=48, n_k=48, seed=0):
             qr = np.unique(np.concatenate([[0, 1, 127, 128, T - 1],
                                            rng.integers(0, T, n_q)])).astype(np.int32)
             kr = np.unique(np.concatenate([[T - 1, T - 128, T - 129],
-                                           rng.integers(T - 384, T, n_k)])).astype(np.int32)
+                                           rng.integers(T - 384, T, n_k),
+                                           _long_loop_keys(T, rng)])).astype(np.int32)
             picks.append((b, h, qr, kr))
     return picks
+
+
+def _report_long_loop(name, errs):
+    long = {k: v for k, v in errs.items() if "_long" in k}
+    print(f"\n[parity] {name} long-loop key rows: " +
+          ", ".join(f"{k}={v:.3e}" for k, v in long.items()))
 
 
 @pytest.mark.parametrize("name", ["byte4k", "long16k"])
 def test_long_configs_sampled(name):
     inp = make_inputs(name)
     gpu = run_gpu(inp)
-    _report(name, check_sampled(inp, gpu, _picks_fixed(inp)))
+    errs = check_sampled(inp, gpu, _picks_fixed(inp), long_loop_tiles=8)
+    _report(name, errs)
+    _report_long_loop(name, errs)
+    assert "dk_long_rel_l2" in errs
 
 
 def test_varlen_config_sampled():
     inp = make_inputs("varlen")
     gpu = run_gpu(inp)
     rng = np.random.default_rng(1)
+    lengths = [int(L) for L in inp["lengths"]]
+    longest = set(np.argsort(lengths)[-2:].tolist())
     picks = []
-    for s, L in enumerate(inp["lengths"]):
-        if s % 4:
+    for s, L in enumerate(lengths):
+        if s % 4 and s not in longest:
             continue
         h = int(rng.integers(inp["H"]))
         qr = np.unique(np.concatenate([[0, L - 1], rng.integers(0, L, 24)])).astype(np.int32)
-        kr = np.unique(np.concatenate([[L - 1, max(L - 130, 0)],
-                                       rng.integers(max(L - 300, 0), L, 24)])).astype(np.int32)
-        picks.append((s, h, qr, kr))
-    _report("varlen", check_sampled(inp, gpu, picks))
+        kr = [L - 1, max(L - 130, 0)] + list(rng.integers(max(L - 300, 0), L, 24))
+        if s in longest:
+            kr += _long_loop_keys(L, rng)
+        picks.append((s, h, qr, np.unique(np.asarray(kr)).astype(np.int32)))
+    errs = check_sampled(inp, gpu, picks, long_loop_tiles=8)
+    _report("varlen", errs)
+    _report_long_loop("varlen", errs)
+    assert "dk_long_rel_l2" in errs
 
 
 def test_varlen_equal_lengths_matches_fixed():

@@ -70,3 +70,29 @@ def test_umma_forms(na, form):
     assert na.ne_attn_get_device_status() == 0
     err = (d - ref).abs().max().item()
     assert err <= 1e-4 * max(1.0, ref.abs().max().item()), err
+
+
+def test_pipeline_completes_without_a_drop(na):
+    src = _bf16((4 * 128, 2, 64), 11)
+    d = na.ne_debug_pipeline(src.cuda(), 4).cpu().double()
+    assert na.ne_attn_get_device_status() == 0
+    a = src[:, 0].double().reshape(4, 128, 64)
+    ref = sum(a[i] @ a[i].T for i in range(4))
+    err = (d - ref).abs().max().item()
+    assert err <= 1e-4 * ref.abs().max().item(), err
+
+
+def test_expired_wait_reports_timeout_and_leaves_the_gpu_usable(na):
+    """A left-out producer arrive makes the consumer's bounded wait expire
+    (limit 1e5 cycles, about 50 us): the kernel reports NE_ERR_TIMEOUT with the
+    wait site, drains and exits; the next ordinary calls are correct."""
+    src = _bf16((4 * 128, 2, 64), 12)
+    na.ne_debug_pipeline(src.cuda(), 4, drop_item=2, wait_limit_cycles=100_000)
+    assert na.ne_attn_get_device_status() == 5  # NE_ERR_TIMEOUT
+    assert na.ne_attn_last_device_code() == 0x100 + 51
+    assert na.ne_attn_get_device_status() == 0  # reading the status cleared it
+    test_pipeline_completes_without_a_drop(na)
+    from causal_self_attention_gb300.inputs import make_inputs
+    from parity import check_full, run_gpu
+    inp = make_inputs("tiny")
+    check_full(inp, run_gpu(inp))
