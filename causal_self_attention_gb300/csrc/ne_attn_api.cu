@@ -19,8 +19,9 @@ namespace ne {
 cudaError_t launch_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                        const FwdParams& p, int n_qtiles, cudaStream_t stream);
 cudaError_t launch_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                       const CUtensorMap& tmDO, const CUtensorMap& tmDQ, const BwdParams& p,
-                       int n_tiles, cudaStream_t stream, cudaEvent_t ev_pre, cudaEvent_t ev_main);
+                       const CUtensorMap& tmDO, const CUtensorMap& tmDQ, const CUtensorMap& tmDV,
+                       const CUtensorMap& tmDK, const BwdParams& p, int n_tiles,
+                       cudaStream_t stream, cudaEvent_t ev_pre, cudaEvent_t ev_main);
 cudaError_t launch_debug_tile(const CUtensorMap& tm, int h, int row0, int rotate, int pos0,
                               RopeTable rope, void* dst_raw, __nv_bfloat16* dst_rows,
                               int* status, cudaStream_t stream);
@@ -314,12 +315,14 @@ ne_status run_bwd(const Shape& s, const void* q, const void* k, const void* v, c
   p.kr = reinterpret_cast<__nv_bfloat16*>(wsb + acc_bytes + del_bytes + rot_bytes);
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k = static_cast<const __nv_bfloat16*>(k);
-  CUtensorMap tdq;
+  CUtensorMap tdq, tdv, tdk;
   rc = encode_rows(&tq, p.qr, s.n_tot, s.H);
   if (rc == NE_OK) rc = encode_rows(&tk, p.kr, s.n_tot, s.H);
   if (rc == NE_OK) rc = encode_rows_f32(&tdq, p.dq_acc, s.n_tot, s.H);
-  cudaError_t e = rc == NE_OK ? ne::launch_bwd(tq, tk, tv, tdo, tdq, p, n_tiles, cs, g_ev_pre,
-                                                g_ev_main)
+  if (rc == NE_OK) rc = encode_rows(&tdv, dv, s.n_tot, s.H);
+  if (rc == NE_OK) rc = encode_rows(&tdk, dk, s.n_tot, s.H);
+  cudaError_t e = rc == NE_OK ? ne::launch_bwd(tq, tk, tv, tdo, tdq, tdv, tdk, p, n_tiles, cs,
+                                                g_ev_pre, g_ev_main)
                               : cudaErrorInvalidValue;
   if (owned) {
     cudaError_t e2 = cudaFreeAsync(ws, cs);

@@ -1,7 +1,9 @@
 // ne_attn_bwd.cu -- backward of causal self-attention with RoPE, sm_103a.
 //
-// Three kernels on one stream (gradients hand-derived, no autograd, as the
-// NanoEuler Show HN page, paragraph 2, describes for its engine):
+// Three kernels on one stream, each launched with programmatic dependent
+// launch so that its CTAs set up while the previous kernel drains (gradients
+// hand-derived, no autograd, as the NanoEuler Show HN page, paragraph 2,
+// describes for its engine):
 //   1. preprocess, once per element: D_m = dO_m . O_m (fp32, [H, N_tot]); zero
 //      the fp32 dQ' accumulator; and q' = R(m) q, k' = R(n) k into bf16
 //      workspace buffers with the forward's fp32 rule, so the main kernel
@@ -15,7 +17,10 @@
 //        dS^T = P^T o (dP^T - D),
 //        dV  += P^T dO (P^T from TMEM),  dK' += dS^T Q',  dQ'_i = dS K'
 //        (-> bulk tensor reduce-add),
-//      and at the end of each unit writes dV and scale * dK' (bf16);
+//      and at the end of each unit writes dV and scale * dK' (bf16).  K' is
+//      double-buffered across units, so the next unit's K' is loaded while
+//      the current unit runs; V is reloaded as soon as the unit's last dP^T
+//      has read it;
 //   3. postprocess: dQ = scale * R(m)^T dQ' (bf16), and dK = R(n)^T (scale dK')
 //      in place (rotating dK here rather than at the end of each unit keeps
 //      table loads off the unit boundary, where they held up the next unit).
@@ -36,8 +41,9 @@
 //               MMAs).  Two issuing warps: one warp issuing all 32 MMAs of a
 //               tile was measured to pace the whole loop (its instructions
 //               compete with the softmax warps for issue slots).
-//   warp 15     TMA: lane 0 loads each unit's K'_j, V_j once both issuing
-//               warps are done with the previous unit's
+//   warp 15     TMA: lane 0 loads each unit's K'_j into the K' buffer the
+//               unit before the previous one has released, and V_j once the
+//               previous unit's last dP^T has completed
 // TMEM columns: S^T 0-127, dP^T 128-255, dV 256-319, dK' 320-383, dQ' 384-447,
 // P^T 448-511 (bf16 pairs).
 #include "ne_rope.cuh"
@@ -52,24 +58,34 @@ constexpr int kThreads = 512;
 constexpr uint32_t kRegsSoftmax = 168, kRegsDrain = 104, kRegsMma = 72;
 static_assert(valid_reg_split(kRegsSoftmax, kRegsDrain, kRegsMma), "register split");
 constexpr int kQStages = 3;                          // Q_i / dO_i ring depth
-constexpr int OFF_K = 0;
-constexpr int OFF_V = OFF_K + kTileBytes;
+constexpr int OFF_K = 0;                               // 2 buffers (units alternate)
+constexpr int OFF_V = OFF_K + 2 * kTileBytes;
 constexpr int OFF_Q = OFF_V + kTileBytes;              // kQStages
 constexpr int OFF_DO = OFF_Q + kQStages * kTileBytes;  // kQStages
 constexpr int OFF_DST = OFF_DO + kQStages * kTileBytes;  // dS^T: 2 blocks of 64 queries
 constexpr int OFF_DQ = OFF_DST + 2 * kTileBytes;         // dQ' staging: 2 x [128][32] fp32, SW128
-constexpr int OFF_LSE = OFF_DQ + 2 * kTileBytes;         // kQStages x 128 fp32: -LSE (log2 units)
-constexpr int OFF_DEL = OFF_LSE + kQStages * 128 * 4;  // kQStages x 128 fp32: -D
-constexpr int OFF_BAR = OFF_DEL + kQStages * 128 * 4;
+// Row terms of the query tiles, staged kRowSlots - 1 tiles ahead of use.
+constexpr int kRowSlots = 4;
+constexpr int OFF_LSE = OFF_DQ + 2 * kTileBytes;          // kRowSlots x 128 fp32: -LSE (log2 units)
+constexpr int OFF_DEL = OFF_LSE + kRowSlots * 128 * 4;  // kRowSlots x 128 fp32: -D
+constexpr int OFF_BAR = OFF_DEL + kRowSlots * 128 * 4;
 constexpr int kBarBytes = 512;  // mbarriers, TMEM address, abort flag
 constexpr int SMEM_BYTES = OFF_BAR + kBarBytes + 1024;  // + slack for 1024-byte alignment
+static_assert(SMEM_BYTES <= 232448, "more shared memory than an sm_103 CTA may have");
 
 enum Bar {
-  B_KV_FULL = 0,                         // per unit: K', V landed
-  B_KV_EMPTY,                            // per unit: both issuing warps done with K', V
+  B_K_FULL = 0,                          // 2 (per K' buffer): K' landed
+  B_K_EMPTY = B_K_FULL + 2,              // 2: both issuing warps done with the buffer's K'
+  B_V_FULL = B_K_EMPTY + 2,              // per unit: V landed
+  B_V_EMPTY,                             // per unit: the unit's last dP^T completed
+  B_STG_FREE,                            // per tile: the dQ' staging may be written
+  B_STG_FULL,                            // per tile: all 128 rows of dQ' staged
+  B_EPI_FULL,                            // per unit: dV, scale dK' staged in the dS^T buffer
+  B_EPI_READ,                            // per unit: their tile stores have read the buffer
   B_QDO_FULL,                            // kQStages
-  B_ROW_FULL = B_QDO_FULL + kQStages,    // kQStages: -LSE_i, -D_i staged
-  B_QDO_EMPTY = B_ROW_FULL + kQStages,   // kQStages
+  B_ROW_FULL = B_QDO_FULL + kQStages,    // kRowSlots: -LSE_i, -D_i staged
+  B_ROW_EMPTY = B_ROW_FULL + kRowSlots,  // kRowSlots: every softmax warp has read them
+  B_QDO_EMPTY = B_ROW_EMPTY + kRowSlots, // kQStages
   B_S_FULL = B_QDO_EMPTY + kQStages,
   B_S_FREE,
   B_DS_FULL,
@@ -112,6 +128,7 @@ __global__ void __launch_bounds__(256)
                                   __nv_bfloat16* __restrict__ qr, __nv_bfloat16* __restrict__ kr,
                                   float* __restrict__ delta, float* __restrict__ dq_acc,
                                   const Problem pb, RopeTable rope) {
+  pdl_wait();  // the forward that wrote O (and anything before it) has completed
   const int seq = blockIdx.y;
   int start, len;
   if (!seq_bounds(pb, seq, start, len, nullptr)) return;
@@ -173,6 +190,7 @@ __global__ void __launch_bounds__(256)
     acc += __shfl_xor_sync(0xffffffffu, acc, 4);
     if (valid && part == 0) delta[static_cast<long long>(h) * pb.n_tot + start + pos] = acc;
   }
+  pdl_launch_dependents();
 }
 
 // ---------------------------------------------------------------------------
@@ -209,9 +227,19 @@ __device__ __forceinline__ bool get_unit(const BwdParams& p, int r, Unit& u) {
 }
 
 // The k-th unit of CTA c among G: rounds of G units, dealt c = 0..G-1 in even
-// rounds and G-1..0 in odd rounds.
+// rounds and G-1..0 in odd rounds (increasing in k).
 __device__ __forceinline__ int unit_index(int k, int c, int G) {
   return k * G + ((k & 1) ? (G - 1 - c) : c);
+}
+
+// The first k' >= k whose unit is not empty (its description in u), or -1.
+__device__ __forceinline__ int next_unit(const BwdParams& p, int n_units, int c, int G, int k,
+                                         Unit& u) {
+  for (;; ++k) {
+    const int r = unit_index(k, c, G);
+    if (r >= n_units) return -1;
+    if (get_unit(p, r, u)) return k;
+  }
 }
 
 }  // namespace bwd
@@ -221,7 +249,9 @@ __global__ void __launch_bounds__(512, 1)
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
                        const __grid_constant__ CUtensorMap tmDO,
-                       const __grid_constant__ CUtensorMap tmDQ, const BwdParams p, int n_tiles) {
+                       const __grid_constant__ CUtensorMap tmDQ,
+                       const __grid_constant__ CUtensorMap tmDV,
+                       const __grid_constant__ CUtensorMap tmDK, const BwdParams p, int n_tiles) {
   using namespace bwd;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -237,12 +267,23 @@ __global__ void __launch_bounds__(512, 1)
   const int lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars[B_KV_FULL], 1);
-    mbar_init(&bars[B_KV_EMPTY], 2);  // one commit from each issuing warp
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars[B_K_FULL + b], 1);
+      mbar_init(&bars[B_K_EMPTY + b], 2);  // one commit from each issuing warp
+    }
+    mbar_init(&bars[B_V_FULL], 1);
+    mbar_init(&bars[B_V_EMPTY], 1);
+    mbar_init(&bars[B_STG_FREE], 1);
+    mbar_init(&bars[B_STG_FULL], 128);
+    mbar_init(&bars[B_EPI_FULL], 256);
+    mbar_init(&bars[B_EPI_READ], 1);
     for (int s = 0; s < kQStages; ++s) {
       mbar_init(&bars[B_QDO_FULL + s], 1);
-      mbar_init(&bars[B_ROW_FULL + s], 128);
       mbar_init(&bars[B_QDO_EMPTY + s], 1);
+    }
+    for (int s = 0; s < kRowSlots; ++s) {
+      mbar_init(&bars[B_ROW_FULL + s], 128);
+      mbar_init(&bars[B_ROW_EMPTY + s], 8);  // one arrival per softmax warp
     }
     mbar_init(&bars[B_S_FULL], 1);
     mbar_init(&bars[B_S_FREE], 256);
@@ -263,6 +304,8 @@ __global__ void __launch_bounds__(512, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the preprocess (q', k', D, zeroed dQ') has completed
+  pdl_launch_dependents();
 
   uint8_t* sK = smem + OFF_K;
   uint8_t* sV = smem + OFF_V;
@@ -316,21 +359,67 @@ __global__ void __launch_bounds__(512, 1)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       int nu = 0;  // units loaded
+      int last_k[2] = {-1, -1};
+      bool ok = true;
       NE_FOR_EACH_UNIT(u) {
-        // The buffer is free once both issuing warps' last MMAs of the
-        // previous unit (the last S^T/dP^T; the last dQ') have completed.
-        if (nu >= 1 && !mbar_wait(&bars[B_KV_EMPTY], (nu - 1) & 1, abort_flag, p.status, 30)) break;
-        mbar_arrive_expect_tx(&bars[B_KV_FULL], 2 * kTileBytes);
-        tma_load_3d(sK, &tmK, &bars[B_KV_FULL], 0, u.h, u.start + u.kt * kBN);
-        tma_load_3d(sV, &tmV, &bars[B_KV_FULL], 0, u.h, u.start + u.kt * kBN);
+        const int b = nu & 1;
+        // K' buffer b last held unit nu - 2: free once both issuing warps'
+        // last MMAs reading it (that unit's last S^T; its last dQ') completed.
+        // It was released a unit ago, so this load runs a unit ahead.
+        if (nu >= 2 &&
+            !mbar_wait(&bars[B_K_EMPTY + b], ((nu - 2) >> 1) & 1, abort_flag, p.status, 30)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&bars[B_K_FULL + b], kTileBytes);
+        tma_load_3d(sK + b * kTileBytes, &tmK, &bars[B_K_FULL + b], 0, u.h, u.start + u.kt * kBN);
+        last_k[b] = nu;
+        // V: the one buffer is free once the previous unit's last dP^T completed.
+        if (nu >= 1 && !mbar_wait(&bars[B_V_EMPTY], (nu - 1) & 1, abort_flag, p.status, 29)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&bars[B_V_FULL], kTileBytes);
+        tma_load_3d(sV, &tmV, &bars[B_V_FULL], 0, u.h, u.start + u.kt * kBN);
         ++nu;
       }
-      if (*abort_flag && nu >= 1) {
-        const long long t0 = clock64();
-        while (!mbar_try_wait(&bars[B_KV_FULL], (nu - 1) & 1) &&
-               clock64() - t0 < NE_WAIT_LIMIT_CYCLES) {
+      if (!ok || *abort_flag) {  // copies in flight land before the CTA exits
+        for (int b = 0; b < 2; ++b)
+          if (last_k[b] >= 0) {
+            const long long t0 = clock64();
+            while (!mbar_try_wait(&bars[B_K_FULL + b], (last_k[b] >> 1) & 1) &&
+                   clock64() - t0 < NE_WAIT_LIMIT_CYCLES) {
+            }
+          }
+        if (nu >= 1) {
+          const long long t0 = clock64();
+          while (!mbar_try_wait(&bars[B_V_FULL], (nu - 1) & 1) &&
+                 clock64() - t0 < NE_WAIT_LIMIT_CYCLES) {
+          }
         }
       }
+    } else if (warp == 15 && lane == 1) {
+      // Tile stores of each unit's dV and scale dK', once the softmax threads
+      // have staged them in the dS^T buffer (a thread of its own, so that no
+      // softmax warp waits for the stores); the buffer is handed back when
+      // the stores have read it.  Partial tiles are written by the softmax
+      // threads themselves: only the hand-back is needed.
+      tma_prefetch_desc(&tmDV);
+      tma_prefetch_desc(&tmDK);
+      int nu = 0;
+      NE_FOR_EACH_UNIT(u) {
+        if (!mbar_wait(&bars[B_EPI_FULL], nu & 1, abort_flag, p.status, 50)) break;
+        if ((u.kt + 1) * kBN <= u.len) {
+          const int row0 = u.start + u.kt * kBN;
+          tma_store_3d(&tmDV, sDST, 0, u.h, row0);
+          tma_store_3d(&tmDK, sDST + kTileBytes, 0, u.h, row0);
+          bulk_commit_group();
+          bulk_wait_group_read0();
+        }
+        mbar_arrive(&bars[B_EPI_READ]);
+        ++nu;
+      }
+      bulk_wait_group0();  // the stores have completed before the kernel ends
     }
   } else if (warp == 12 || warp == 14) {
     // ------------------------------------------------------------ MMA issuers
@@ -353,7 +442,9 @@ __global__ void __launch_bounds__(512, 1)
       // and dO_n have landed and the softmax has read the previous S^T, dP^T.
       NE_FOR_EACH_UNIT(u) {
         if (!ok) break;
-        if (!mbar_wait_warp(&bars[B_KV_FULL], nu & 1, abort_flag, p.status, 32)) {
+        const int b = nu & 1;
+        if (!mbar_wait_warp(&bars[B_K_FULL + b], (nu >> 1) & 1, abort_flag, p.status, 32) ||
+            !mbar_wait_warp(&bars[B_V_FULL], nu & 1, abort_flag, p.status, 38)) {
           ok = false;
           break;
         }
@@ -367,7 +458,7 @@ __global__ void __launch_bounds__(512, 1)
           tc_fence_after();
           if (elect_one()) {
             const uint64_t dQ = opaque_u64(dQk0) + kTileD * sn, dO = opaque_u64(dOk0) + kTileD * sn;
-            const uint64_t dK = opaque_u64(dKk), dV = opaque_u64(dVk);
+            const uint64_t dK = opaque_u64(dKk) + kTileD * b, dV = opaque_u64(dVk);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)  // K = 64 head dims: 32 bytes per step
               umma_bf16_ss(tmem + kColS, dK + 2 * kk, dQ + 2 * kk, kIdescNN, kk > 0 ? 1u : 0u);
@@ -375,7 +466,10 @@ __global__ void __launch_bounds__(512, 1)
             for (int kk = 0; kk < 4; ++kk)
               umma_bf16_ss(tmem + kColDP, dV + 2 * kk, dO + 2 * kk, kIdescNN, kk > 0 ? 1u : 0u);
             umma_commit(&bars[B_S_FULL]);
-            if (it == u.n_it - 1) umma_commit(&bars[B_KV_EMPTY]);  // last reader of V (and K' here)
+            if (it == u.n_it - 1) {  // the unit's last readers of V and (here) of K'
+              umma_commit(&bars[B_V_EMPTY]);
+              umma_commit(&bars[B_K_EMPTY + b]);
+            }
           }
           __syncwarp();
         }
@@ -390,8 +484,9 @@ __global__ void __launch_bounds__(512, 1)
       const uint64_t dSm = make_sdesc_sw128(smem_u32(sDST), kTileBytes, 1024);  // as dS, MN-major
       NE_FOR_EACH_UNIT(u) {
         if (!ok) break;
+        const int b = nu & 1;
         // K' of this unit (B operand of dQ') has landed.
-        if (!mbar_wait_warp(&bars[B_KV_FULL], nu & 1, abort_flag, p.status, 37)) {
+        if (!mbar_wait_warp(&bars[B_K_FULL + b], (nu >> 1) & 1, abort_flag, p.status, 37)) {
           ok = false;
           break;
         }
@@ -432,14 +527,14 @@ __global__ void __launch_bounds__(512, 1)
           }
           tc_fence_after();
           if (elect_one()) {
-            const uint64_t dSq = opaque_u64(dSm), dKq = opaque_u64(dKm);
+            const uint64_t dSq = opaque_u64(dSm), dKq = opaque_u64(dKm) + kTileD * b;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)  // K = 128 keys: 16 rows = 2048 bytes per step
               umma_bf16_ss(tmem + kColDQ, dSq + 128 * kk, dKq + 128 * kk, kIdescMM,
                            kk > 0 ? 1u : 0u);
             umma_commit(&bars[B_DQ_FULL]);
             umma_commit(&bars[B_PDS_FREE]);
-            if (it == u.n_it - 1) umma_commit(&bars[B_KV_EMPTY]);  // last reader of K'
+            if (it == u.n_it - 1) umma_commit(&bars[B_K_EMPTY + b]);  // last reader of K'
           }
           __syncwarp();
         }
@@ -459,46 +554,57 @@ __global__ void __launch_bounds__(512, 1)
     const int r = threadIdx.x;  // 0..127: query row of the tile (TMEM lane r)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     bool ok = true;
+    // Row terms: a stream over all of the CTA's query tiles, across unit
+    // boundaries, kRowSlots - 1 tiles ahead of the drain (so a unit's first
+    // tiles are staged during the previous unit).  Cursor: unit ua (index
+    // ka, -1 past the end), its tile ita, the CTA's tile number ga.
+    Unit ua;
+    int ka = next_unit(p, n_units, cta, G, 0, ua);
+    int ita = 0, ga = 0;
+    // LSE (log2 units) and D of query row r of the cursor's tile; rows past
+    // the sequence get LSE = +inf, hence P = 0.  The loads always address a
+    // row of the sequence (read-only loads may run ahead of the condition
+    // that guards them).
+    auto load_rowstats = [&](float& l2, float& dl) {
+      const int qpos = (ua.kt + ita) * kBM + r;
+      const int qc = qpos < ua.len ? qpos : ua.len - 1;
+      const float l = __ldg(p.lse + lse_index(p.pb, ua.h, ua.seq, ua.start, qc));
+      const float d = __ldg(p.delta + static_cast<long long>(ua.h) * p.pb.n_tot + ua.start + qc);
+      l2 = qpos < ua.len ? l * 1.4426950408889634f : INFINITY;
+      dl = qpos < ua.len ? d : 0.f;
+    };
+    // Stored negated: P = 2^(fma(s, scale log2 e, -LSE)), dS = P (dP - D).
+    // The slot last held tile ga - kRowSlots, whose readers have all
+    // arrived on its ROW_EMPTY phase (the next phase of that barrier needs
+    // this staging first, so the parity cannot alias).
+    auto stage_rowstats = [&](float l2, float dl) -> bool {
+      const int sl = ga % kRowSlots;
+      if (ga >= kRowSlots &&
+          !mbar_wait_warp(&bars[B_ROW_EMPTY + sl], ((ga - kRowSlots) / kRowSlots) & 1, abort_flag,
+                          p.status, 44))
+        return false;
+      sLSE[sl * 128 + r] = -l2;
+      sDEL[sl * 128 + r] = -dl;
+      mbar_arrive(&bars[B_ROW_FULL + sl]);
+      ++ga;
+      if (++ita == ua.n_it) {
+        ita = 0;
+        ka = next_unit(p, n_units, cta, G, ka + 1, ua);
+      }
+      return true;
+    };
+    float l2, dl;
+    for (int j = 0; ok && j < kRowSlots - 1 && ka >= 0; ++j) {
+      load_rowstats(l2, dl);
+      ok = stage_rowstats(l2, dl);
+    }
     int g = 0;  // query tiles over all units
     NE_FOR_EACH_UNIT(u) {
       if (!ok) break;
-      // LSE (log2 units) and D of query row r of the unit's tile `it`; rows
-      // past the sequence get LSE = +inf, hence P = 0.  The loads always
-      // address a row of the sequence (read-only loads may run ahead of the
-      // condition that guards them).
-      auto load_rowstats = [&](int it, float& l2, float& dl) {
-        const int qpos = (u.kt + it) * kBM + r;
-        const int qc = qpos < u.len ? qpos : u.len - 1;
-        const float l = __ldg(p.lse + lse_index(p.pb, u.h, u.seq, u.start, qc));
-        const float d = __ldg(p.delta + static_cast<long long>(u.h) * p.pb.n_tot + u.start + qc);
-        l2 = qpos < u.len ? l * 1.4426950408889634f : INFINITY;
-        dl = qpos < u.len ? d : 0.f;
-      };
-      // Stored negated: P = 2^(fma(s, scale log2 e, -LSE)), dS = P (dP - D).
-      auto stage_rowstats = [&](int gq, float l2, float dl) {
-        const int s = gq % kQStages;
-        sLSE[s * 128 + r] = -l2;
-        sDEL[s * 128 + r] = -dl;
-        mbar_arrive(&bars[B_ROW_FULL + s]);
-      };
-      float l2, dl;
-      // The unit's first two tiles; their stages last held tiles g - 3 and
-      // g - 2 (of earlier units), free once those tiles' dV/dK' completed.
-      for (int it = 0; it < kQStages - 1 && it < u.n_it; ++it) {
-        const int gq = g + it;
-        load_rowstats(it, l2, dl);
-        if (gq >= kQStages &&
-            !mbar_wait(&bars[B_QDO_EMPTY + gq % kQStages], ((gq - kQStages) / kQStages) & 1,
-                       abort_flag, p.status, 45)) {
-          ok = false;
-          break;
-        }
-        stage_rowstats(gq, l2, dl);
-      }
       for (int it = 0; ok && it < u.n_it; ++it) {
         const int gq = g + it;
-        const int ahead = it + kQStages - 1;  // the unit's tile whose row terms are staged now
-        if (ahead < u.n_it) load_rowstats(ahead, l2, dl);  // loads in flight during the drain
+        const bool ahead = ka >= 0;  // tile gq + kRowSlots - 1 exists: its row terms are next
+        if (ahead) load_rowstats(l2, dl);  // loads in flight during the drain
         // dQ'_it: TMEM -> swizzled fp32 staging (columns 0-31 and 32-63) ->
         // two bulk tensor reduce-adds, issued by thread 0.
         if (!mbar_wait_warp(&bars[B_DQ_FULL], gq & 1, abort_flag, p.status, 43)) {
@@ -513,8 +619,17 @@ __global__ void __launch_bounds__(512, 1)
         tmem_ld_wait(v1);
         tc_fence_before();
         mbar_arrive(&bars[B_DQ_FREE]);
-        if (r == 0) bulk_wait_group_read0();  // the previous reductions have read the buffers
-        named_bar_sync(1, 128);
+        // The staging buffers are free once the previous tile's reductions
+        // have read them (thread 0 issued those and waits for it).  Bounded
+        // mbarrier waits rather than named barriers: every wait can give up.
+        if (r == 0) {
+          bulk_wait_group_read0();
+          mbar_arrive(&bars[B_STG_FREE]);
+        }
+        if (!mbar_wait_warp(&bars[B_STG_FREE], gq & 1, abort_flag, p.status, 47)) {
+          ok = false;
+          break;
+        }
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           *reinterpret_cast<uint4*>(sDQ + sw128_offset(r, c)) =
@@ -523,29 +638,25 @@ __global__ void __launch_bounds__(512, 1)
               make_uint4(v1[4 * c], v1[4 * c + 1], v1[4 * c + 2], v1[4 * c + 3]);
         }
         fence_proxy_async_smem();
-        named_bar_sync(1, 128);
+        mbar_arrive(&bars[B_STG_FULL]);
         if (r == 0) {
-          const int qrow = u.start + (u.kt + it) * kBM;
-          tma_reduce_add_3d(&tmDQ, sDQ, 0, u.h, qrow);
-          tma_reduce_add_3d(&tmDQ, sDQ + kTileBytes, 32, u.h, qrow);
-          bulk_commit_group();
-        }
-        if (ahead < u.n_it) {
-          // The stage of tile gq + 2 last held tile gq - 1, whose softmax has
-          // read it before the dV/dK MMAs that completed QDO_EMPTY.
-          if (gq >= 1 && !mbar_wait(&bars[B_QDO_EMPTY + (gq - 1) % kQStages],
-                                    ((gq - 1) / kQStages) & 1, abort_flag, p.status, 44)) {
+          if (mbar_wait(&bars[B_STG_FULL], gq & 1, abort_flag, p.status, 48)) {
+            const int qrow = u.start + (u.kt + it) * kBM;
+            tma_reduce_add_3d(&tmDQ, sDQ, 0, u.h, qrow);
+            tma_reduce_add_3d(&tmDQ, sDQ + kTileBytes, 32, u.h, qrow);
+            bulk_commit_group();
+          } else {
             ok = false;
-            break;
           }
-          stage_rowstats(gq + kQStages - 1, l2, dl);
         }
+        if (!__all_sync(0xffffffffu, ok)) break;
+        if (ahead && !(ok = stage_rowstats(l2, dl))) break;
       }
       g += u.n_it;
     }
-    // Before exit the staging buffers must have been read; the reduce-adds
-    // themselves complete with the kernel.
-    if (r == 0) bulk_wait_group_read0();
+    // Every reduce-add has completed (not only read its source) before the
+    // kernel ends.
+    if (r == 0) bulk_wait_group0();
   } else {
     // --------------------------------------------------------- softmax warps
     regs_increase<kRegsSoftmax>();
@@ -555,18 +666,19 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const float sl2 = p.scale_log2;
     bool ok = true;
-    int g = 0;  // query tiles over all units
+    int g = 0;   // query tiles over all units
+    int nu = 0;  // units
     NE_FOR_EACH_UNIT(u) {
       if (!ok) break;
       for (int it = 0; it < u.n_it; ++it) {
         const int gq = g + it;
-        const int s = gq % kQStages;
         if (!mbar_wait_warp(&bars[B_S_FULL], gq & 1, abort_flag, p.status, 39)) {
           ok = false;
           break;
         }
-        // LSE/D of this query tile are staged in stage s.
-        if (!mbar_wait_warp(&bars[B_ROW_FULL + s], (gq / kQStages) & 1, abort_flag, p.status, 40)) {
+        // LSE/D of this query tile are staged in slot gq % kRowSlots.
+        const int sl = gq % kRowSlots;
+        if (!mbar_wait_warp(&bars[B_ROW_FULL + sl], (gq / kRowSlots) & 1, abort_flag, p.status, 40)) {
           ok = false;
           break;
         }
@@ -588,8 +700,8 @@ __global__ void __launch_bounds__(512, 1)
           for (int col = 0; col < 64; ++col)
             if (64 * half + col < r) sv[col] = 0xff800000u;  // -inf: P = 0, dS = 0
         }
-        const float4* nl4 = reinterpret_cast<const float4*>(sLSE + s * 128 + 64 * half);
-        const float4* nd4 = reinterpret_cast<const float4*>(sDEL + s * 128 + 64 * half);
+        const float4* nl4 = reinterpret_cast<const float4*>(sLSE + sl * 128 + 64 * half);
+        const float4* nd4 = reinterpret_cast<const float4*>(sDEL + sl * 128 + 64 * half);
         const uint64_t sl2x2 = f2_pack(sl2, sl2);
         uint32_t pw[32], dw[32];
 #pragma unroll
@@ -611,8 +723,18 @@ __global__ void __launch_bounds__(512, 1)
             dw[col / 2] = pack_bf16x2(d0, d1);
           }
         }
-        // P^T (TMEM) / dS^T (smem): free once the MMAs of the previous tile are done.
+        // This warp is done with the slot's row terms.
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[B_ROW_EMPTY + sl]);
+        // P^T (TMEM) / dS^T (smem): free once the MMAs of the previous tile are
+        // done, and at a unit's first tile once the previous unit's dV/dK tile
+        // stores have read the dS^T buffer.
         if (gq >= 1 && !mbar_wait_warp(&bars[B_PDS_FREE], (gq - 1) & 1, abort_flag, p.status, 41)) {
+          ok = false;
+          break;
+        }
+        if (it == 0 && nu >= 1 &&
+            !mbar_wait_warp(&bars[B_EPI_READ], (nu - 1) & 1, abort_flag, p.status, 49)) {
           ok = false;
           break;
         }
@@ -629,16 +751,20 @@ __global__ void __launch_bounds__(512, 1)
         mbar_arrive(&bars[B_DS_FULL]);
       }
       if (!ok) break;
-      // ---- epilogue of the unit: dV (first half), dK = scale R^T dK' (second)
-      // (overlapped by the next unit's first MMAs, which need no TMEM column
-      // this reads until this thread's next DS_FULL arrival)
+      // ---- epilogue of the unit: dV (first half), scale dK' (second half),
+      // the latter still rotated (the postprocess applies R(n)^T, away from
+      // the end of the unit, where table loads would hold up the next unit).
+      // (Overlapped by the next unit's S^T/dP^T MMAs; its first dV/dK' MMAs
+      // need these TMEM columns only after this thread's next DS_FULL arrival.)
       const int kpos = u.kt * kBN + r;
-      // dV, dK' are final once the last tile's dV/dK' MMAs have completed:
-      // the release of its Q', dO stage is committed right after them (and
-      // tracks every earlier MMA of that warp), before the last dQ' MMAs.
+      const bool full_tile = (u.kt + 1) * kBN <= u.len;
+      // dV, dK' are final once the last tile's dV/dK' MMAs have completed; a
+      // full tile is staged in the dS^T buffer, free once the last dQ' MMA
+      // (its last reader) has completed too.
       const int last = g + u.n_it - 1;
-      if (!(ok = mbar_wait_warp(&bars[B_QDO_EMPTY + last % kQStages], (last / kQStages) & 1,
-                                abort_flag, p.status, 42)))
+      if (!(ok = full_tile ? mbar_wait_warp(&bars[B_PDS_FREE], last & 1, abort_flag, p.status, 42)
+                           : mbar_wait_warp(&bars[B_QDO_EMPTY + last % kQStages],
+                                            (last / kQStages) & 1, abort_flag, p.status, 42)))
         break;
       tc_fence_after();
       uint32_t gr[64];
@@ -647,24 +773,39 @@ __global__ void __launch_bounds__(512, 1)
       tmem_ld_x32(tmem + lane_base + col + 32, gr + 32);
       tmem_ld_wait(gr);
       tmem_ld_wait(gr + 32);
-      // (The next unit's first dV/dK' MMAs overwrite these columns only after
-      // this thread's next DS_FULL arrival, which is fenced behind this load.)
-      if (kpos < u.len) {
-        // dV as it is; dK as scale dK' (still rotated: the dK pass that
-        // follows applies R(n)^T, away from the end of the unit, where table
-        // loads would hold up the next unit's first tiles).
-        const long long orow = (static_cast<long long>(u.start + kpos) * p.pb.H + u.h) * kHD;
-        uint4* dst = reinterpret_cast<uint4*>((half ? p.dk : p.dv) + orow);
-        const float sc = half ? p.scale : 1.f;
+      const float sc = half ? p.scale : 1.f;
+      uint4 w[8];
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          dst[c] = make_uint4(
-              pack_bf16x2(__uint_as_float(gr[8 * c + 0]) * sc, __uint_as_float(gr[8 * c + 1]) * sc),
-              pack_bf16x2(__uint_as_float(gr[8 * c + 2]) * sc, __uint_as_float(gr[8 * c + 3]) * sc),
-              pack_bf16x2(__uint_as_float(gr[8 * c + 4]) * sc, __uint_as_float(gr[8 * c + 5]) * sc),
-              pack_bf16x2(__uint_as_float(gr[8 * c + 6]) * sc, __uint_as_float(gr[8 * c + 7]) * sc));
+      for (int c = 0; c < 8; ++c)
+        w[c] = make_uint4(
+            pack_bf16x2(__uint_as_float(gr[8 * c + 0]) * sc, __uint_as_float(gr[8 * c + 1]) * sc),
+            pack_bf16x2(__uint_as_float(gr[8 * c + 2]) * sc, __uint_as_float(gr[8 * c + 3]) * sc),
+            pack_bf16x2(__uint_as_float(gr[8 * c + 4]) * sc, __uint_as_float(gr[8 * c + 5]) * sc),
+            pack_bf16x2(__uint_as_float(gr[8 * c + 6]) * sc, __uint_as_float(gr[8 * c + 7]) * sc));
+      if (full_tile) {
+        // Row r into the swizzled [128 x 64] bf16 tile `half` of the dS^T
+        // buffer; one thread stores both tiles with TMA (whole 128-byte rows,
+        // instead of 16-byte pieces of 128 rows per warp instruction).
+        uint8_t* tile = sDST + half * kTileBytes;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(tile + sw128_offset(r, c)) = w[c];
+        fence_proxy_async_smem();
+        mbar_arrive(&bars[B_EPI_FULL]);  // warp 15, lane 1 stores the tiles
+      } else {
+        // The sequence's last, partial key tile: rows past its end belong to
+        // the next sequence (or lie past the tensor), so only rows inside it
+        // are written, one row per thread.  The dS^T buffer is not used, but
+        // the unit still completes both epilogue phases.
+        if (kpos < u.len) {
+          const long long orow = (static_cast<long long>(u.start + kpos) * p.pb.H + u.h) * kHD;
+          uint4* dst = reinterpret_cast<uint4*>((half ? p.dk : p.dv) + orow);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) dst[c] = w[c];
+        }
+        mbar_arrive(&bars[B_EPI_FULL]);
       }
       g += u.n_it;
+      ++nu;
     }
   }
 #undef NE_FOR_EACH_UNIT
@@ -728,11 +869,13 @@ __global__ void __launch_bounds__(kPostThreads)
     ne_attn_dq_postprocess_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq,
                                   __nv_bfloat16* __restrict__ dk, const Problem pb, RopeTable rope,
                                   float scale) {
+  pdl_wait();  // the main kernel's dQ' reduce-adds and dK stores have completed
   const int seq = blockIdx.y;
   int start, len;
   if (!seq_bounds(pb, seq, start, len, nullptr)) return;
   if (blockIdx.z == 1) {
     dk_rotate_item(dk, pb, rope, start, len);
+    pdl_launch_dependents();
     return;
   }
   const int H = pb.H;
@@ -761,11 +904,13 @@ __global__ void __launch_bounds__(kPostThreads)
   *reinterpret_cast<uint2*>(d + part * 4) = make_uint2(pack_bf16x2(go[0], go[1]), pack_bf16x2(go[2], go[3]));
   *reinterpret_cast<uint2*>(d + 32 + part * 4) =
       make_uint2(pack_bf16x2(gh[0], gh[1]), pack_bf16x2(gh[2], gh[3]));
+  pdl_launch_dependents();
 }
 
 cudaError_t launch_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                       const CUtensorMap& tmDO, const CUtensorMap& tmDQ, const BwdParams& p,
-                       int n_tiles, cudaStream_t stream, cudaEvent_t ev_pre, cudaEvent_t ev_main) {
+                       const CUtensorMap& tmDO, const CUtensorMap& tmDQ, const CUtensorMap& tmDV,
+                       const CUtensorMap& tmDK, const BwdParams& p, int n_tiles,
+                       cudaStream_t stream, cudaEvent_t ev_pre, cudaEvent_t ev_main) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(ne_attn_bwd_kernel,
@@ -775,9 +920,8 @@ cudaError_t launch_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
     attr_set = true;
   }
   dim3 pre_grid((n_tiles * kBM + bwd::kPreRows - 1) / bwd::kPreRows, p.pb.nseq);
-  ne_attn_bwd_preprocess_kernel<<<pre_grid, 256, 0, stream>>>(
-      p.q, p.k, p.out, p.dout, p.qr, p.kr, p.delta, p.dq_acc, p.pb, p.rope);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(ne_attn_bwd_preprocess_kernel, pre_grid, dim3(256), 0, stream, p.q,
+                             p.k, p.out, p.dout, p.qr, p.kr, p.delta, p.dq_acc, p.pb, p.rope);
   if (e != cudaSuccess) return e;
   if (ev_pre && (e = cudaEventRecord(ev_pre, stream)) != cudaSuccess) return e;
   // One persistent CTA per SM (at most one per unit).
@@ -790,17 +934,15 @@ cudaError_t launch_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
     return e;
   const long long n_units = static_cast<long long>(n_tiles) * p.pb.nseq * p.pb.H;
   const int G = static_cast<int>(n_units < sm_count[dev] ? n_units : sm_count[dev]);
-  ne_attn_bwd_kernel<<<G, bwd::kThreads, bwd::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, tmDO, tmDQ, p,
-                                                                    n_tiles);
-  e = cudaGetLastError();
+  e = launch_pdl(ne_attn_bwd_kernel, dim3(G), dim3(bwd::kThreads), bwd::SMEM_BYTES, stream, tmQ,
+                 tmK, tmV, tmDO, tmDQ, tmDV, tmDK, p, n_tiles);
   if (e != cudaSuccess) return e;
   if (ev_main && (e = cudaEventRecord(ev_main, stream)) != cudaSuccess) return e;
   const long long post_items = static_cast<long long>(n_tiles) * kBM * p.pb.H * kPostParts;
   // Layer z = 0: dQ from the accumulator; z = 1: dK rotated in place.
   dim3 pgrid(static_cast<unsigned>((post_items + kPostThreads - 1) / kPostThreads), p.pb.nseq, 2);
-  ne_attn_dq_postprocess_kernel<<<pgrid, kPostThreads, 0, stream>>>(p.dq_acc, p.dq, p.dk, p.pb,
-                                                                    p.rope, p.scale);
-  return cudaGetLastError();
+  return launch_pdl(ne_attn_dq_postprocess_kernel, pgrid, dim3(kPostThreads), 0, stream,
+                    static_cast<const float*>(p.dq_acc), p.dq, p.dk, p.pb, p.rope, p.scale);
 }
 
 }  // namespace ne

@@ -175,6 +175,8 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // whatever the stream ran before (e.g. the kernel that wrote q, k, v) has completed
+  pdl_launch_dependents();
 
   uint8_t* sQ = smem + OFF_Q;  // buffer b: Q_A at 2b tiles, Q_B at 2b + 1
   uint8_t* sK = smem + OFF_K;
@@ -574,8 +576,8 @@ cudaError_t launch_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
   const int nblk = (n_qtiles + 1) / 2;
   const long long n_items = static_cast<long long>(nblk) * p.pb.nseq * p.pb.H;
   const int G = static_cast<int>(n_items < sm_count[dev] ? n_items : sm_count[dev]);
-  ne_attn_fwd_kernel<<<G, fwd::kThreads, fwd::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, p, nblk);
-  return cudaGetLastError();
+  return launch_pdl(ne_attn_fwd_kernel, dim3(G), dim3(fwd::kThreads), fwd::SMEM_BYTES, stream,
+                    tmQ, tmK, tmV, p, nblk);
 }
 
 }  // namespace ne

@@ -12,8 +12,9 @@
 
 namespace ne {
 cudaError_t launch_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                       const CUtensorMap& tmDO, const CUtensorMap& tmDQ, const BwdParams& p,
-                       int n_tiles, cudaStream_t stream, cudaEvent_t ev_pre, cudaEvent_t ev_main);
+                       const CUtensorMap& tmDO, const CUtensorMap& tmDQ, const CUtensorMap& tmDV,
+                       const CUtensorMap& tmDK, const BwdParams& p, int n_tiles,
+                       cudaStream_t stream, cudaEvent_t ev_pre, cudaEvent_t ev_main);
 ne_status internal_prepare(int** status_word);
 ne_status internal_encode_rows(CUtensorMap* map, const void* base, int n_rows, int H);
 ne_status internal_encode_rows_f32(CUtensorMap* map, void* base, int n_rows, int H);
@@ -152,7 +153,10 @@ extern "C" ne_status ne_attn_bwd_noalloc(const ne_bf16* q, const ne_bf16* k, con
   if ((rc = ne::internal_encode_rows(&tv, v, n_tot, H)) != NE_OK) return rc;
   if ((rc = ne::internal_encode_rows(&tdo, dout, n_tot, H)) != NE_OK) return rc;
   if ((rc = ne::internal_encode_rows_f32(&tdq, p.dq_acc, n_tot, H)) != NE_OK) return rc;
-  const cudaError_t e = ne::launch_bwd(tq, tk, tv, tdo, tdq, p, n_tiles,
+  CUtensorMap tdv, tdk;
+  if ((rc = ne::internal_encode_rows(&tdv, dv, n_tot, H)) != NE_OK) return rc;
+  if ((rc = ne::internal_encode_rows(&tdk, dk, n_tot, H)) != NE_OK) return rc;
+  const cudaError_t e = ne::launch_bwd(tq, tk, tv, tdo, tdq, tdv, tdk, p, n_tiles,
                                        static_cast<cudaStream_t>(stream), nullptr, nullptr);
   if (e == cudaSuccess) return NE_OK;
   return e == cudaErrorMemoryAllocation ? NE_ERR_OOM : NE_ERR_CUDA;

@@ -32,6 +32,16 @@ __device__ __forceinline__ void rope_load_row(const RopeTable& rt, int pos, Rope
   for (int i = 0; i < 16; ++i) r.t[i] = __ldg(cs + 32 * i);
 }
 
+// The same registers from the row layout of the table (cs: one 256-byte row
+// per position; for a thread that loads its rows rarely, off the critical
+// path, where the warp-interleaved copy buys nothing).
+__device__ __forceinline__ void rope_load_row_flat(const RopeTable& rt, int pos, RopeRow& r) {
+  if (pos >= rt.capacity) pos = rt.capacity - 1;  // only rows past the sequence end
+  const float4* cs = reinterpret_cast<const float4*>(rt.cs + static_cast<long long>(pos) * 32);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) r.t[i] = __ldg(cs + i);
+}
+
 // Rotate one row (64 elements = 8 swizzled 16-byte chunks) of `tile` with the
 // table row `cs` of its position.
 __device__ __forceinline__ void rope_rotate_row(uint8_t* tile, int row, const RopeRow& cs) {

@@ -135,6 +135,37 @@ constexpr bool valid_reg_split(uint32_t softmax, uint32_t rotate, uint32_t mma) 
          softmax % 8 == 0 && rotate % 8 == 0 && mma % 8 == 0 && mma >= 24;
 }
 
+// Programmatic dependent launch (kernels launched with launch_pdl below).
+// pdl_wait: block until the grids this one depends on in stream order have
+// completed and their memory is visible (a no-op for a kernel launched
+// without the attribute); every kernel calls it before its first access to
+// global memory that an earlier kernel on the stream may write or read.
+// pdl_launch_dependents: let the next kernel on the stream be scheduled once
+// every CTA of this grid has called it or exited (its CTAs then run their
+// set-up and wait in pdl_wait; correctness never depends on where this is).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch `kernel` on `stream` with programmatic stream serialization allowed,
+// so that its CTAs may start while the previous kernel on the stream drains.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Named barrier among `nthreads` threads (a warpgroup) with id `id` (1..15).
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -176,6 +207,18 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// 3-d tiled store of a shared-memory tile into global memory, tracked by this
+// thread's bulk async-group (the box must lie inside the tensor: a store
+// never starts at a negative coordinate here).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0, int c1,
+                                             int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group"
+      " [%0, {%1, %2, %3}], [%4];" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(src))
       : "memory");
 }
 
