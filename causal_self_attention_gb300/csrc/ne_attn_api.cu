@@ -17,7 +17,10 @@
 
 namespace ne {
 cudaError_t launch_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                       const FwdParams& p, int n_qtiles, cudaStream_t stream);
+                       const CUtensorMap& tmO, const FwdParams& p, int n_qtiles,
+                       cudaStream_t stream);
+cudaError_t launch_rope_rows(const __nv_bfloat16* x, __nv_bfloat16* xr, const Problem& pb,
+                             const RopeTable& rope, cudaStream_t stream);
 cudaError_t launch_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                        const CUtensorMap& tmDO, const CUtensorMap& tmDQ, const CUtensorMap& tmDV,
                        const CUtensorMap& tmDK, const BwdParams& p, int n_tiles,
@@ -51,13 +54,49 @@ struct RopeEntry {
   float2* dev = nullptr;
 };
 
+// A temporary the forward keeps per stream (the rotated keys k'): allocated
+// on that stream the first time, grown (stream-ordered) when a larger problem
+// comes, reused by every later call on the stream, whose kernels it orders.
+struct StreamScratch {
+  cudaStream_t stream = nullptr;
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+
 struct DeviceState {
   bool ready = false;
   int* status = nullptr;  // device address of g_device_status on this device
   bool supported = false;
   std::vector<RopeEntry> tables;
   std::vector<float2*> retired;  // replaced tables, freed by ne_attn_release
+  std::vector<StreamScratch> scratch;
 };
+
+// The forward's per-stream temporary of at least `bytes` (caller holds g_mutex).
+ne_status stream_scratch(DeviceState& st, cudaStream_t stream, size_t bytes, void** out) {
+  for (auto& e : st.scratch)
+    if (e.stream == stream) {
+      if (e.bytes < bytes) {
+        // Enqueued after every earlier use of the old buffer on this stream.
+        if (cudaFreeAsync(e.ptr, stream) != cudaSuccess) return NE_ERR_CUDA;
+        e.ptr = nullptr;
+        e.bytes = 0;
+        cudaError_t r = cudaMallocAsync(&e.ptr, bytes, stream);
+        if (r != cudaSuccess) return r == cudaErrorMemoryAllocation ? NE_ERR_OOM : NE_ERR_CUDA;
+        e.bytes = bytes;
+      }
+      *out = e.ptr;
+      return NE_OK;
+    }
+  StreamScratch e;
+  e.stream = stream;
+  cudaError_t r = cudaMallocAsync(&e.ptr, bytes, stream);
+  if (r != cudaSuccess) return r == cudaErrorMemoryAllocation ? NE_ERR_OOM : NE_ERR_CUDA;
+  e.bytes = bytes;
+  st.scratch.push_back(e);
+  *out = e.ptr;
+  return NE_OK;
+}
 
 std::mutex g_mutex;
 DeviceState g_dev[kMaxDevices];
@@ -231,6 +270,11 @@ ne::Problem make_problem(const Shape& s) {
   return pb;
 }
 
+// Sequence length from which the forward rotates the keys once per call in a
+// pass of its own instead of in every item that uses a key tile (measured on
+// GB300: below it the extra pass costs more than the kernel saves).
+constexpr int kPreRotateLen = 2048;
+
 ne_status run_fwd(const Shape& s, const void* q, const void* k, const void* v, float rope_base,
                   float scale, void* out, int out_f32, float* lse, void* stream) {
   if (!q || !k || !v || !out || !lse) return NE_ERR_INVALID_ARG;
@@ -253,11 +297,48 @@ ne_status run_fwd(const Shape& s, const void* q, const void* k, const void* v, f
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = st->status;
   if ((rc = rope_table(*st, rope_base, n_qtiles * 128, &p.rope)) != NE_OK) return rc;
-  CUtensorMap tq, tk, tv;
-  if ((rc = encode_rows(&tq, q, s.n_tot, s.H)) != NE_OK) return rc;
-  if ((rc = encode_rows(&tk, k, s.n_tot, s.H)) != NE_OK) return rc;
-  if ((rc = encode_rows(&tv, v, s.n_tot, s.H)) != NE_OK) return rc;
-  return cuda_status(ne::launch_fwd(tq, tk, tv, p, n_qtiles, static_cast<cudaStream_t>(stream)));
+  // Keys: for short sequences each item rotates the key tiles it uses in
+  // shared memory; from kPreRotateLen positions on, the rotated keys
+  // k' = R(n) k are written once per call by a small pass into the library's
+  // temporary for this stream, or, while the stream is being captured into a
+  // graph, into a stream-ordered allocation of the call's own (a graph must
+  // not bake in a buffer that later calls outside it would also use).
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  p.rotate_k = s.max_len < kPreRotateLen ? 1 : 0;
+  CUtensorMap tq, tk, tv, to;
+  const void* keys = k;
+  bool own = false;
+  void* kr = nullptr;
+  cudaError_t e = cudaSuccess;
+  if (!p.rotate_k) {
+    const size_t kr_bytes = static_cast<size_t>(s.n_tot) * s.H * 64 * 2;
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(cs, &capture) != cudaSuccess) return NE_ERR_CUDA;
+    own = capture != cudaStreamCaptureStatusNone;
+    if (own) {
+      if ((e = cudaMallocAsync(&kr, kr_bytes, cs)) != cudaSuccess) return cuda_status(e);
+    } else if ((rc = stream_scratch(*st, cs, kr_bytes, &kr)) != NE_OK) {
+      return rc;
+    }
+    keys = kr;
+  }
+  rc = encode_rows(&tq, q, s.n_tot, s.H);
+  if (rc == NE_OK) rc = encode_rows(&tk, keys, s.n_tot, s.H);
+  if (rc == NE_OK) rc = encode_rows(&tv, v, s.n_tot, s.H);
+  // O tile stores (bf16 output only; the fp32 output is written per row).
+  if (rc == NE_OK) rc = encode_rows(&to, out_f32 ? q : out, s.n_tot, s.H);
+  if (rc == NE_OK) {
+    if (!p.rotate_k)
+      e = ne::launch_rope_rows(static_cast<const __nv_bfloat16*>(k),
+                               static_cast<__nv_bfloat16*>(kr), p.pb, p.rope, cs);
+    if (e == cudaSuccess) e = ne::launch_fwd(tq, tk, tv, to, p, n_qtiles, cs);
+  }
+  if (own) {
+    const cudaError_t e2 = cudaFreeAsync(kr, cs);
+    if (e == cudaSuccess) e = e2;
+  }
+  if (rc != NE_OK) return rc;
+  return cuda_status(e);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -555,12 +636,15 @@ void ne_attn_release(void) {
   cudaGetDevice(&cur);
   for (int d = 0; d < kMaxDevices; ++d) {
     DeviceState& st = g_dev[d];
-    if (st.tables.empty() && st.retired.empty()) continue;
+    if (st.tables.empty() && st.retired.empty() && st.scratch.empty()) continue;
     cudaSetDevice(d);
     for (auto& t : st.tables) cudaFree(t.dev);
     for (auto* p : st.retired) cudaFree(p);
+    for (auto& e : st.scratch) cudaFreeAsync(e.ptr, e.stream);
+    if (!st.scratch.empty()) cudaDeviceSynchronize();
     st.tables.clear();
     st.retired.clear();
+    st.scratch.clear();
   }
   cudaSetDevice(cur);
 }

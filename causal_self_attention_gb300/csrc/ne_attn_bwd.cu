@@ -78,8 +78,6 @@ enum Bar {
   B_K_EMPTY = B_K_FULL + 2,              // 2: both issuing warps done with the buffer's K'
   B_V_FULL = B_K_EMPTY + 2,              // per unit: V landed
   B_V_EMPTY,                             // per unit: the unit's last dP^T completed
-  B_STG_FREE,                            // per tile: the dQ' staging may be written
-  B_STG_FULL,                            // per tile: all 128 rows of dQ' staged
   B_EPI_FULL,                            // per unit: dV, scale dK' staged in the dS^T buffer
   B_EPI_READ,                            // per unit: their tile stores have read the buffer
   B_QDO_FULL,                            // kQStages
@@ -273,8 +271,6 @@ __global__ void __launch_bounds__(512, 1)
     }
     mbar_init(&bars[B_V_FULL], 1);
     mbar_init(&bars[B_V_EMPTY], 1);
-    mbar_init(&bars[B_STG_FREE], 1);
-    mbar_init(&bars[B_STG_FULL], 128);
     mbar_init(&bars[B_EPI_FULL], 256);
     mbar_init(&bars[B_EPI_READ], 1);
     for (int s = 0; s < kQStages; ++s) {
@@ -594,42 +590,34 @@ __global__ void __launch_bounds__(512, 1)
       return true;
     };
     float l2, dl;
-    for (int j = 0; ok && j < kRowSlots - 1 && ka >= 0; ++j) {
+    for (int j = 0; j < kRowSlots - 1 && ka >= 0; ++j) {  // no waits: slots not yet used
       load_rowstats(l2, dl);
-      ok = stage_rowstats(l2, dl);
+      stage_rowstats(l2, dl);
     }
     int g = 0;  // query tiles over all units
     NE_FOR_EACH_UNIT(u) {
-      if (!ok) break;
-      for (int it = 0; ok && it < u.n_it; ++it) {
+      for (int it = 0; it < u.n_it; ++it) {
         const int gq = g + it;
         const bool ahead = ka >= 0;  // tile gq + kRowSlots - 1 exists: its row terms are next
         if (ahead) load_rowstats(l2, dl);  // loads in flight during the drain
         // dQ'_it: TMEM -> swizzled fp32 staging (columns 0-31 and 32-63) ->
-        // two bulk tensor reduce-adds, issued by thread 0.
-        if (!mbar_wait_warp(&bars[B_DQ_FULL], gq & 1, abort_flag, p.status, 43)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+        // two bulk tensor reduce-adds, issued by thread 0.  The four warps
+        // meet at named barriers; a warp whose bounded wait gave up carries
+        // that into the first barrier's vote, and all four leave together.
         uint32_t v0[32], v1[32];
-        tmem_ld_x32(tmem + lane_base + kColDQ, v0);
-        tmem_ld_x32(tmem + lane_base + kColDQ + 32, v1);
-        tmem_ld_wait(v0);
-        tmem_ld_wait(v1);
-        tc_fence_before();
-        mbar_arrive(&bars[B_DQ_FREE]);
-        // The staging buffers are free once the previous tile's reductions
-        // have read them (thread 0 issued those and waits for it).  Bounded
-        // mbarrier waits rather than named barriers: every wait can give up.
-        if (r == 0) {
-          bulk_wait_group_read0();
-          mbar_arrive(&bars[B_STG_FREE]);
+        bool wok = mbar_wait_warp(&bars[B_DQ_FULL], gq & 1, abort_flag, p.status, 43);
+        if (wok) {
+          tc_fence_after();
+          tmem_ld_x32(tmem + lane_base + kColDQ, v0);
+          tmem_ld_x32(tmem + lane_base + kColDQ + 32, v1);
+          tmem_ld_wait(v0);
+          tmem_ld_wait(v1);
+          tc_fence_before();
+          mbar_arrive(&bars[B_DQ_FREE]);
         }
-        if (!mbar_wait_warp(&bars[B_STG_FREE], gq & 1, abort_flag, p.status, 47)) {
-          ok = false;
-          break;
-        }
+        // The staging buffers are free once the previous reductions have read them.
+        if (r == 0) bulk_wait_group_read0();
+        if (!(ok = named_bar_and(1, 128, ok && wok))) break;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           *reinterpret_cast<uint4*>(sDQ + sw128_offset(r, c)) =
@@ -638,20 +626,18 @@ __global__ void __launch_bounds__(512, 1)
               make_uint4(v1[4 * c], v1[4 * c + 1], v1[4 * c + 2], v1[4 * c + 3]);
         }
         fence_proxy_async_smem();
-        mbar_arrive(&bars[B_STG_FULL]);
+        named_bar_sync(1, 128);
         if (r == 0) {
-          if (mbar_wait(&bars[B_STG_FULL], gq & 1, abort_flag, p.status, 48)) {
-            const int qrow = u.start + (u.kt + it) * kBM;
-            tma_reduce_add_3d(&tmDQ, sDQ, 0, u.h, qrow);
-            tma_reduce_add_3d(&tmDQ, sDQ + kTileBytes, 32, u.h, qrow);
-            bulk_commit_group();
-          } else {
-            ok = false;
-          }
+          const int qrow = u.start + (u.kt + it) * kBM;
+          tma_reduce_add_3d(&tmDQ, sDQ, 0, u.h, qrow);
+          tma_reduce_add_3d(&tmDQ, sDQ + kTileBytes, 32, u.h, qrow);
+          bulk_commit_group();
         }
-        if (!__all_sync(0xffffffffu, ok)) break;
-        if (ahead && !(ok = stage_rowstats(l2, dl))) break;
+        // A failure here is carried into the next tile's vote.
+        if (ahead) ok = stage_rowstats(l2, dl);
       }
+      // (No exit here: a failure reaches the next tile's vote, or the loops
+      // simply end after the CTA's last tile.)
       g += u.n_it;
     }
     // Every reduce-add has completed (not only read its source) before the

@@ -6,8 +6,16 @@
 // with q' = R(m) q, k' = R(n) k (RoPE), the scores never leaving the SM
 // (tiled online softmax, as in the hand-written FlashAttention of the
 // NanoEuler Show HN page, paragraph 2; causality as in "Tiny Hackable CUDA",
-// section 3).  Both tiles share every rotated K/V tile, and while one tile's
+// section 3).  Both tiles share every K'/V tile, and while one tile's
 // softmax runs the tensor core works on the other tile's MMAs.
+//
+// RoPE: each query tile is used by one item only and is rotated in shared
+// memory right after its TMA load.  A key tile is used by every query tile at
+// or after it; the keys are rotated either in shared memory by every item
+// that uses them (kRotateK = 1, short sequences: no extra pass), or once
+// per call by a small pass that runs first (ne_attn_rope_rows_kernel,
+// k' = R(n) k, bf16; kRotateK = 0, long sequences, where rotating each key
+// tile several times -- its table loads -- paces the kernel).
 //
 // The kernel is persistent: one CTA per SM walks the items (longest first,
 // dealt out in a snake order over the CTAs), keeping its TMEM, barriers and
@@ -17,10 +25,10 @@
 // Warp roles (512 threads, registers re-split per warpgroup with setmaxnreg):
 //   warps 0-3   softmax A: thread t owns row t of tile A (TMEM lane t), 176 regs
 //   warps 4-7   softmax B: same for tile B
-//   warps 8-11  rotate: RoPE on each item's Q_A, Q_B and on every K tile in
-//               smem, 104 regs
+//   warps 8-11  rotate: RoPE on each item's Q_A, Q_B in smem (and, with
+//               rotate_k, on every K tile it uses), 104 regs
 //   warp 12     MMA: allocates TMEM; one elected lane issues S_X = Q_X K^T
-//   warp 13     TMA: lane 0 loads each item's Q_A, Q_B and the K ring (5 stages)
+//   warp 13     TMA: lane 0 loads each item's Q_A, Q_B and the K' ring (5 stages)
 //   warp 14     TMA: lane 0 loads the V ring (5 stages)
 //   warp 15     MMA: one elected lane issues O_X += P_X V; warps 12-15 run at
 //               56 regs
@@ -60,7 +68,7 @@ enum Bar {
   B_Q_ROT = B_Q_FULL + 2,
   B_Q_EMPTY = B_Q_ROT + 2,
   B_K_FULL = B_Q_EMPTY + 2,           // kStages
-  B_K_ROT = B_K_FULL + kStages,       // kStages
+  B_K_ROT = B_K_FULL + kStages,       // kStages (rotate_k only)
   B_K_EMPTY = B_K_ROT + kStages,      // kStages
   B_V_FULL = B_K_EMPTY + kStages,     // kStages
   B_V_EMPTY = B_V_FULL + kStages,     // kStages
@@ -70,7 +78,8 @@ enum Bar {
   B_PV_DONE = B_P_FULL + 2,
   B_O_FINAL = B_PV_DONE + 2,          // per tile: the item's last P V completed
   B_O_FREE = B_O_FINAL + 2,           // per tile: the epilogue has read O_X
-  B_MMA_DONE = B_O_FREE + 2,         // per issuing warp (S, P V)
+  B_OST_FULL = B_O_FREE + 2,          // per tile: O_X (bf16) staged in its Q slot
+  B_MMA_DONE = B_OST_FULL + 2,        // per issuing warp (S, P V)
   B_COUNT = B_MMA_DONE + 2
 };
 static_assert(8 * B_COUNT + 8 <= kBarBytes, "barrier region overflow");
@@ -123,10 +132,16 @@ __device__ __forceinline__ int item_index(int k, int c, int G) {
 }  // namespace fwd
 
 // Grid: G persistent CTAs; nblk = 256-row blocks of the longest sequence.
+// kRotateK: the K tiles are rotated in smem by the rotate warps (short
+// sequences); otherwise they come pre-rotated and the O tiles are written by
+// TMA from the Q buffer (long sequences).  Two instantiations, so that each
+// compiles only its own epilogue (registers are tight in the softmax warps).
+template <bool kRotateK>
 __global__ void __launch_bounds__(fwd::kThreads, 1)
     ne_attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV, const FwdParams p, int nblk) {
+                       const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ CUtensorMap tmO, const FwdParams p, int nblk) {
   using namespace fwd;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -145,7 +160,9 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars[B_Q_FULL + b], 1);
       mbar_init(&bars[B_Q_ROT + b], 128);
-      mbar_init(&bars[B_Q_EMPTY + b], 1);
+      // The item's last S MMA and, when O tiles are staged in the Q buffer
+      // (pre-rotated keys), its O tile stores.
+      mbar_init(&bars[B_Q_EMPTY + b], kRotateK ? 1 : 2);
     }
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars[B_K_FULL + s], 1);
@@ -161,6 +178,7 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
       mbar_init(&bars[B_PV_DONE + x], 1);
       mbar_init(&bars[B_O_FINAL + x], 1);
       mbar_init(&bars[B_O_FREE + x], 128);
+      mbar_init(&bars[B_OST_FULL + x], 128);
     }
     mbar_init(&bars[B_MMA_DONE], 1);
     mbar_init(&bars[B_MMA_DONE + 1], 1);
@@ -248,6 +266,35 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
             }
           }
       }
+    } else if (!kRotateK && warp == 14 && lane == 1) {
+      // O tile stores (pre-rotated keys only): once a tile's softmax threads
+      // have staged its bf16 O in the tile's own Q slot (no S MMA reads it any
+      // more), store it with TMA; when both tiles of the item are stored
+      // (their smem read), hand the Q buffer back to the loader.  Partial
+      // tiles (rows past the sequence) and fp32 output are written by the
+      // softmax threads.  With in-kernel key rotation the Q buffer goes back
+      // at the item's last S MMA (the rotate warps need the next items' Q
+      // early) and every row is written by its softmax thread.
+      tma_prefetch_desc(&tmO);
+      int nq = 0, nst[2] = {0, 0};
+      NE_FOR_EACH_ITEM(it) {
+        const int b = nq & 1;
+        bool ok = true;
+        for (int x = 0; x < 2 && ok; ++x) {
+          if (x == 1 && !it.hasB) continue;
+          if (!(ok = mbar_wait(&bars[B_OST_FULL + x], nst[x] & 1, abort_flag, p.status, 16))) break;
+          ++nst[x];
+          const int row0 = it.rowA + x * kBM;
+          if (!p.out_f32 && row0 + kBM <= it.len)
+            tma_store_3d(&tmO, sQ + (2 * b + x) * kTileBytes, 0, it.h, it.start + row0);
+        }
+        if (!ok) break;
+        bulk_commit_group();
+        bulk_wait_group_read0();
+        mbar_arrive(&bars[B_Q_EMPTY + b]);
+        ++nq;
+      }
+      bulk_wait_group0();  // the stores have completed before the kernel ends
     }
   } else if (warp == 12 || warp == 15) {
     // ------------------------------------------------------------ MMA issuers
@@ -277,7 +324,8 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
         ok = mbar_wait_warp(&bars[B_Q_ROT + b], (nq >> 1) & 1, abort_flag, p.status, 2);
         for (int j = 0; ok && j < it.nkv; ++j) {
           const int gj = g0 + j, s = gj % kStages;
-          if (!mbar_wait_warp(&bars[B_K_ROT + s], (gj / kStages) & 1, abort_flag, p.status, 3)) {
+          if (!mbar_wait_warp(&bars[(kRotateK ? B_K_ROT : B_K_FULL) + s], (gj / kStages) & 1,
+                              abort_flag, p.status, 3)) {
             ok = false;
             break;
           }
@@ -378,6 +426,7 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
       fence_proxy_async_smem();
       mbar_arrive(&bars[B_Q_ROT + b]);
       ++nq;
+      if (!kRotateK) continue;  // the keys come pre-rotated
       rope_load_row(p.rope, r, tab);
       for (int j = 0; j < it.nkv; ++j, ++g) {
         const int s = g % kStages;
@@ -403,9 +452,11 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
     bool ok = true;
     int cnt = 0;  // steps of this tile over all items
     int nit = 0;  // items in which this tile took part
+    int nq = 0;   // items (the Q buffer of item nq is nq & 1)
     NE_FOR_EACH_ITEM(it) {
       if (!ok) break;
       const int nkv_x = x ? it.nkvB : it.nkvA;
+      if constexpr (!kRotateK) ++nq;
       if (nkv_x == 0) continue;  // tile B outside the sequence
       const int diag = x ? 2 * it.blk + 1 : 2 * it.blk;
       float m_ref = 0.f;  // reference max (log2 units) the P values are taken against
@@ -513,18 +564,55 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
       tmem_ld_wait(o + 32);
       tc_fence_before();
       mbar_arrive(&bars[B_O_FREE + x]);  // the next item's first P V may overwrite O_X
-      if (erow < e.len) {
+      if constexpr (kRotateK) {
+        // Every row written by its own thread.
+        if (erow < e.len) {
+          const float inv_l = 1.f / l_sum;
+          const long long orow = (static_cast<long long>(e.start + erow) * p.pb.H + e.h) * kHD;
+          if (p.out_f32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow);
+#pragma unroll
+            for (int cc = 0; cc < 16; ++cc)
+              dst[cc] = make_float4(__uint_as_float(o[4 * cc + 0]) * inv_l,
+                                    __uint_as_float(o[4 * cc + 1]) * inv_l,
+                                    __uint_as_float(o[4 * cc + 2]) * inv_l,
+                                    __uint_as_float(o[4 * cc + 3]) * inv_l);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow);
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(o[8 * cc + 0]) * inv_l, __uint_as_float(o[8 * cc + 1]) * inv_l);
+              w.y = pack_bf16x2(__uint_as_float(o[8 * cc + 2]) * inv_l, __uint_as_float(o[8 * cc + 3]) * inv_l);
+              w.z = pack_bf16x2(__uint_as_float(o[8 * cc + 4]) * inv_l, __uint_as_float(o[8 * cc + 5]) * inv_l);
+              w.w = pack_bf16x2(__uint_as_float(o[8 * cc + 6]) * inv_l, __uint_as_float(o[8 * cc + 7]) * inv_l);
+              dst[cc] = w;
+            }
+          }
+          // LSE in natural-log units: (m_ref + log2 l) * ln 2.
+          p.lse[lse_index(p.pb, e.h, e.seq, e.start, erow)] =
+              (m_ref + __log2f(l_sum)) * 0.69314718055994531f;
+        }
+      } else {
         const float inv_l = 1.f / l_sum;
         const long long orow = (static_cast<long long>(e.start + erow) * p.pb.H + e.h) * kHD;
         if (p.out_f32) {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow);
+          if (erow < e.len) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow);
 #pragma unroll
-          for (int cc = 0; cc < 16; ++cc)
-            dst[cc] = make_float4(__uint_as_float(o[4 * cc + 0]) * inv_l,
-                                  __uint_as_float(o[4 * cc + 1]) * inv_l,
-                                  __uint_as_float(o[4 * cc + 2]) * inv_l,
-                                  __uint_as_float(o[4 * cc + 3]) * inv_l);
+            for (int cc = 0; cc < 16; ++cc)
+              dst[cc] = make_float4(__uint_as_float(o[4 * cc + 0]) * inv_l,
+                                    __uint_as_float(o[4 * cc + 1]) * inv_l,
+                                    __uint_as_float(o[4 * cc + 2]) * inv_l,
+                                    __uint_as_float(o[4 * cc + 3]) * inv_l);
+          }
         } else {
+          // A whole tile goes, row r in bf16, into the swizzled Q slot of this
+          // tile (item nq - 1's buffer), and warp 14, lane 1 stores it with
+          // TMA; the sequence's last, partial tile is written one row per
+          // thread.
+          const bool whole = e.rowA + x * kBM + kBM <= e.len;
+          uint8_t* slot = sQ + (2 * (opaque_int(nq - 1) & 1) + x) * kTileBytes;
           uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow);
 #pragma unroll
           for (int cc = 0; cc < 8; ++cc) {
@@ -533,12 +621,18 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
             w.y = pack_bf16x2(__uint_as_float(o[8 * cc + 2]) * inv_l, __uint_as_float(o[8 * cc + 3]) * inv_l);
             w.z = pack_bf16x2(__uint_as_float(o[8 * cc + 4]) * inv_l, __uint_as_float(o[8 * cc + 5]) * inv_l);
             w.w = pack_bf16x2(__uint_as_float(o[8 * cc + 6]) * inv_l, __uint_as_float(o[8 * cc + 7]) * inv_l);
-            dst[cc] = w;
+            if (whole)
+              *reinterpret_cast<uint4*>(slot + sw128_offset(r, cc)) = w;
+            else if (erow < e.len)
+              dst[cc] = w;
           }
+          if (whole) fence_proxy_async_smem();
         }
+        mbar_arrive(&bars[B_OST_FULL + x]);
         // LSE in natural-log units: (m_ref + log2 l) * ln 2.
-        p.lse[lse_index(p.pb, e.h, e.seq, e.start, erow)] =
-            (m_ref + __log2f(l_sum)) * 0.69314718055994531f;
+        if (erow < e.len)
+          p.lse[lse_index(p.pb, e.h, e.seq, e.start, erow)] =
+              (m_ref + __log2f(l_sum)) * 0.69314718055994531f;
       }
     }
   }
@@ -553,13 +647,75 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Key rotation pass: kr = R(n) k for every row n of every sequence (positions
+// restart at 0 per sequence), bf16 in and out, with the fp32 rule of the
+// in-tile rotation (lo = fma(x_i, c, -(x_{i+32} s)), hi = fma(x_{i+32}, c,
+// x_i s), round to nearest even) and the same table, so the attention kernel
+// multiplies bitwise the operands an in-tile rotation would have produced.
+// Grid (blocks of 256 items, sequences); an item is (row, head, part): part c
+// rotates the 16-byte chunk c (dims 8c..8c+7) against chunk c + 4 (dims
+// 32+8c..32+8c+7), so a warp moves eight whole 128-byte rows.
+// ---------------------------------------------------------------------------
+constexpr int kRopeThreads = 256, kRopeParts = 4;
+
+__global__ void __launch_bounds__(kRopeThreads)
+    ne_attn_rope_rows_kernel(const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ xr,
+                             const Problem pb, RopeTable rope) {
+  pdl_wait();  // the kernel that wrote k (and anything before it) has completed
+  const int seq = blockIdx.y;
+  int start, len;
+  if (!seq_bounds(pb, seq, start, len, nullptr)) return;
+  const int H = pb.H;
+  const long long w = static_cast<long long>(blockIdx.x) * kRopeThreads + threadIdx.x;
+  if (w < static_cast<long long>(len) * H * kRopeParts) {
+    const int c = static_cast<int>(w % kRopeParts);
+    const long long rh = w / kRopeParts;
+    const int pos = static_cast<int>(rh / H), h = static_cast<int>(rh - static_cast<long long>(pos) * H);
+    const long long row = (static_cast<long long>(start + pos) * H + h) * kHD;
+    const uint4 lo = __ldg(reinterpret_cast<const uint4*>(x + row) + c);
+    const uint4 hi = __ldg(reinterpret_cast<const uint4*>(x + row) + c + 4);
+    const float4* cs =
+        reinterpret_cast<const float4*>(rope.cs + static_cast<long long>(pos) * 32 + 8 * c);
+    uint32_t wl[4] = {lo.x, lo.y, lo.z, lo.w};
+    uint32_t wh[4] = {hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float4 t = __ldg(cs + u);  // (cos, sin) of dims 8c + 2u and 8c + 2u + 1
+      const float a0 = bf16lo_to_f32(wl[u]), a1 = bf16hi_to_f32(wl[u]);
+      const float b0 = bf16lo_to_f32(wh[u]), b1 = bf16hi_to_f32(wh[u]);
+      const float lo0 = __fmaf_rn(a0, t.x, -__fmul_rn(b0, t.y));
+      const float hi0 = __fmaf_rn(b0, t.x, __fmul_rn(a0, t.y));
+      const float lo1 = __fmaf_rn(a1, t.z, -__fmul_rn(b1, t.w));
+      const float hi1 = __fmaf_rn(b1, t.z, __fmul_rn(a1, t.w));
+      wl[u] = pack_bf16x2(lo0, lo1);
+      wh[u] = pack_bf16x2(hi0, hi1);
+    }
+    reinterpret_cast<uint4*>(xr + row)[c] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+    reinterpret_cast<uint4*>(xr + row)[c + 4] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+  }
+  pdl_launch_dependents();
+}
+
+cudaError_t launch_rope_rows(const __nv_bfloat16* x, __nv_bfloat16* xr, const Problem& pb,
+                             const RopeTable& rope, cudaStream_t stream) {
+  const long long items = static_cast<long long>(pb.max_len) * pb.H * kRopeParts;
+  dim3 grid(static_cast<unsigned>((items + kRopeThreads - 1) / kRopeThreads), pb.nseq);
+  return launch_pdl(ne_attn_rope_rows_kernel, grid, dim3(kRopeThreads), 0, stream, x, xr, pb,
+                    rope);
+}
+
 cudaError_t launch_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                       const FwdParams& p, int n_qtiles, cudaStream_t stream) {
+                       const CUtensorMap& tmO, const FwdParams& p, int n_qtiles,
+                       cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(ne_attn_fwd_kernel,
+    cudaError_t e = cudaFuncSetAttribute(ne_attn_fwd_kernel<true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          fwd::SMEM_BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(ne_attn_fwd_kernel<false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, fwd::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -576,8 +732,10 @@ cudaError_t launch_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
   const int nblk = (n_qtiles + 1) / 2;
   const long long n_items = static_cast<long long>(nblk) * p.pb.nseq * p.pb.H;
   const int G = static_cast<int>(n_items < sm_count[dev] ? n_items : sm_count[dev]);
-  return launch_pdl(ne_attn_fwd_kernel, dim3(G), dim3(fwd::kThreads), fwd::SMEM_BYTES, stream,
-                    tmQ, tmK, tmV, p, nblk);
+  return p.rotate_k ? launch_pdl(ne_attn_fwd_kernel<true>, dim3(G), dim3(fwd::kThreads),
+                                fwd::SMEM_BYTES, stream, tmQ, tmK, tmV, tmO, p, nblk)
+                    : launch_pdl(ne_attn_fwd_kernel<false>, dim3(G), dim3(fwd::kThreads),
+                                fwd::SMEM_BYTES, stream, tmQ, tmK, tmV, tmO, p, nblk);
 }
 
 }  // namespace ne

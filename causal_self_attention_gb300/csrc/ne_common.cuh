@@ -53,6 +53,8 @@ struct FwdParams {
   float scale_log2;  // softmax scale * log2(e)
   RopeTable rope;
   int* status;
+  int rotate_k;      // 1: K tiles are loaded un-rotated and rotated in smem;
+                     // 0: the keys come pre-rotated (k')
 };
 
 struct BwdParams {

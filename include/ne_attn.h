@@ -30,8 +30,12 @@
  *    aligned.
  *  - Every pointer is DEVICE memory owned by the caller; the library keeps no
  *    reference to it after the call returns.  The library owns only its RoPE
- *    cos/sin tables (released by ne_attn_release) and, when a backward is
- *    given no workspace, a stream-ordered temporary it frees itself.
+ *    cos/sin tables, one temporary per stream for the forward's rotated keys
+ *    (k' = R(n) k, 128 bytes per token and head, allocated stream-ordered on
+ *    the first call on that stream outside graph capture and grown when
+ *    needed; inside a capture each call allocates and frees its own) -- all
+ *    released by ne_attn_release -- and, when a backward is given no
+ *    workspace, a stream-ordered temporary it frees itself.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
  *    enqueued asynchronously on it; the call returns after the launch.
  *  - Argument errors are detected on the host before anything is launched
@@ -204,8 +208,9 @@ int ne_attn_last_device_code(void);
 /* Human-readable name of a status code (static string). */
 const char* ne_status_string(ne_status s);
 
-/* Free the RoPE tables cached for every device.  Call only when no launch
- * that may read them is still pending. */
+/* Free the RoPE tables and the per-stream temporaries kept for every
+ * device.  Call only when no launch that may read them is still pending, and
+ * before destroying a stream the library was given. */
 void ne_attn_release(void);
 
 #ifdef __cplusplus

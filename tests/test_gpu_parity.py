@@ -187,3 +187,19 @@ def test_repeated_calls_are_deterministic():
                 assert torch.equal(a, b)
             assert torch.allclose(cur[4].float(), ref[4].float(), atol=1e-2, rtol=1e-2)
         assert na.ne_attn_get_device_status() == 0
+
+
+def test_key_rotation_paths_agree_bitwise():
+    """The forward rotates the keys either inside every item that uses them
+    (short sequences) or once per call in a pass of its own (from 2048
+    positions on); a packed batch called with a small and with a large
+    max_seqlen takes the two paths and must give bitwise the same O and LSE."""
+    from causal_self_attention_gb300 import ne_attn as na
+    inp = make_custom(0, 0, 3, seed=51, lengths=[300, 129, 200])
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    cu = inp["cu_seqlens"].cuda()
+    outs = [na.ne_attn_varlen_fwd(q, k, v, cu, mx, out_f32=f) for mx in (300, 4096)
+            for f in (False, True)]
+    assert na.ne_attn_get_device_status() == 0
+    for a, b in zip(outs[:2], outs[2:]):
+        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
