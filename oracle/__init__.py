@@ -1,4 +1,6 @@
-"""CPU oracle for causal self-attention with RoPE, forward and backward.
+"""CPU oracle for causal self-attention with RoPE, forward and backward, and
+for the projections around it (RMSNorm + QKV projection with RoPE; output
+projection + residual).
 
 TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline leg import this package.  The product library never
@@ -65,6 +67,16 @@ def _load():
         lib.ne_oracle_probs.argtypes = [dp, dp, ctypes.c_longlong, ctypes.c_int, ctypes.c_int,
                                         ctypes.c_double, ctypes.c_double, ctypes.c_int, dp]
         lib.ne_oracle_probs.restype = ctypes.c_int
+        lib.ne_oracle_rmsnorm.argtypes = [dp, dp, ctypes.c_int, ctypes.c_int, ctypes.c_double, dp]
+        lib.ne_oracle_rmsnorm.restype = ctypes.c_int
+        lib.ne_oracle_linear.argtypes = [dp, dp, ctypes.c_int, ctypes.c_int, ctypes.c_int, dp]
+        lib.ne_oracle_linear.restype = ctypes.c_int
+        lib.ne_oracle_qkv_rope.argtypes = [dp, dp, dp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_double, ctypes.c_double,
+                                           dp, dp, dp]
+        lib.ne_oracle_qkv_rope.restype = ctypes.c_int
+        lib.ne_oracle_out_proj_residual.argtypes = [dp, dp, dp, ctypes.c_int, ctypes.c_int, dp]
+        lib.ne_oracle_out_proj_residual.restype = ctypes.c_int
         lib.ne_oracle_num_threads.argtypes = []
         lib.ne_oracle_num_threads.restype = ctypes.c_int
         _lib = lib
@@ -217,3 +229,49 @@ def attention_sampled(q, k, v, dout, cu_seqlens, picks, base: float = 10000.0,
         res.append(head(q, k, v, dout, (t0 * H + h) * D, L, D, H * D, base, scale, mode, qrows,
                         krows if dout is not None else []))
     return res
+
+
+# ---------------------------------------------------------------- projections
+
+def rmsnorm(x, g, eps: float = 1e-5) -> np.ndarray:
+    """RMSNorm of the rows of ``x`` ``[N, C]`` with weight ``g`` ``[C]``."""
+    x, g = as_f64(x), as_f64(g)
+    N, C = x.shape
+    out = np.empty_like(x)
+    if _load().ne_oracle_rmsnorm(_dptr(x), _dptr(g), N, C, float(eps), _dptr(out)) != 0:
+        raise ValueError("ne_oracle_rmsnorm: bad arguments")
+    return out
+
+
+def linear(a, w) -> np.ndarray:
+    """``a [N, K] . w[M, K]^T`` (weights in the [out, in] convention)."""
+    a, w = as_f64(a), as_f64(w)
+    N, K = a.shape
+    M = w.shape[0]
+    y = np.empty((N, M))
+    if _load().ne_oracle_linear(_dptr(a), _dptr(w), N, K, M, _dptr(y)) != 0:
+        raise ValueError("ne_oracle_linear: bad arguments")
+    return y
+
+
+def qkv_rope(x, g, w, B: int, T: int, H: int, D: int = 64, base: float = 10000.0,
+             eps: float = 1e-5):
+    """QKV projection with RoPE of a fixed-length batch: ``x [B*T, H*D]``,
+    ``g [H*D]``, ``w [3*H*D, H*D]``.  Returns ``(q', k', v)``, each ``[B*T, H*D]``."""
+    x, g, w = as_f64(x), as_f64(g), as_f64(w)
+    C = H * D
+    outs = [np.empty((B * T, C)) for _ in range(3)]
+    if _load().ne_oracle_qkv_rope(_dptr(x), _dptr(g), _dptr(w), B, T, H, D, float(base),
+                                  float(eps), *(_dptr(o) for o in outs)) != 0:
+        raise ValueError("ne_oracle_qkv_rope: bad arguments")
+    return tuple(outs)
+
+
+def out_proj_residual(o, w, r) -> np.ndarray:
+    """``r + o . w^T`` for ``o``, ``r`` ``[N, C]``, ``w`` ``[C, C]``."""
+    o, w, r = as_f64(o), as_f64(w), as_f64(r)
+    N, C = o.shape
+    y = np.empty((N, C))
+    if _load().ne_oracle_out_proj_residual(_dptr(o), _dptr(w), _dptr(r), N, C, _dptr(y)) != 0:
+        raise ValueError("ne_oracle_out_proj_residual: bad arguments")
+    return y

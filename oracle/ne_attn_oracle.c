@@ -366,3 +366,99 @@ int ne_oracle_num_threads(void)
     return 1;
 #endif
 }
+
+/*
+ * ---- The projections around the attention (the step before and the step
+ * after it in a transformer layer).  NanoEuler Show HN page, paragraph 2: the
+ * CUDA engine has RMSNorm and RoPE kernels and computes the matrix products of
+ * the layer; "Tiny Hackable CUDA", section 3: the projections are computed,
+ * RoPE is applied to them to encode relative position, and the attention is
+ * wrapped in a residual connection.  The pages print no equations; the
+ * standard definitions are used (RMSNorm: Zhang and Sennrich 2019; linear
+ * maps in the nn.Linear convention, weights [out, in], no bias):
+ *
+ *   RMSNorm:   xn[n][c] = x[n][c] / sqrt(mean_c' x[n][c']^2 + eps) * g[c]
+ *   linear:    y[n][m]  = sum_k a[n][k] w[m][k]
+ *   QKV:       [q | k | v] = linear(RMSNorm(x), w_qkv), w_qkv [3C, C];
+ *              q', k' = R(t) q, R(t) k per head of D columns, at the token's
+ *              position t within its sequence (rotate-half, as above)
+ *   out proj:  y = r + linear(o, w_o), w_o [C, C]   (residual r)
+ * Everything in double.
+ */
+
+/* Exported: RMSNorm of N rows of C.  Returns 0, or -1 on bad arguments. */
+int ne_oracle_rmsnorm(const double *x, const double *g, int N, int C, double eps, double *out)
+{
+    if (!x || !g || !out || N < 0 || C <= 0 || !(eps >= 0.0))
+        return -1;
+#pragma omp parallel for schedule(static)
+    for (int n = 0; n < N; n++) {
+        const double *xr = x + (long long)n * C;
+        double ss = 0.0;
+        for (int c = 0; c < C; c++)
+            ss += xr[c] * xr[c];
+        double inv = 1.0 / sqrt(ss / C + eps);
+        for (int c = 0; c < C; c++)
+            out[(long long)n * C + c] = xr[c] * inv * g[c];
+    }
+    return 0;
+}
+
+/* Exported: y[N][M] = a[N][K] . w[M][K]^T.  Returns 0, or -1 on bad arguments. */
+int ne_oracle_linear(const double *a, const double *w, int N, int K, int M, double *y)
+{
+    if (!a || !w || !y || N < 0 || K <= 0 || M <= 0)
+        return -1;
+#pragma omp parallel for schedule(static)
+    for (int n = 0; n < N; n++)
+        for (int m = 0; m < M; m++)
+            y[(long long)n * M + m] = dot(a + (long long)n * K, w + (long long)m * K, K);
+    return 0;
+}
+
+/* Exported: the QKV projection with RoPE of a fixed-length batch of B
+ * sequences of T tokens: x [B*T][C] (C = H*D), g [C], w [3C][C].  Writes
+ * q', k', v [B*T][C] (head h in columns h*D .. h*D+D-1).  Returns 0, or -1. */
+int ne_oracle_qkv_rope(const double *x, const double *g, const double *w, int B, int T, int H,
+                       int D, double base, double eps, double *qr, double *kr, double *v)
+{
+    if (!x || !g || !w || !qr || !kr || !v || B <= 0 || T <= 0 || H <= 0 || D <= 0 || (D % 2))
+        return -1;
+    const int C = H * D;
+    const long long N = (long long)B * T;
+    double *xn = malloc(sizeof(double) * (size_t)N * C);
+    double *y = malloc(sizeof(double) * (size_t)N * 3 * C);
+    if (!xn || !y) {
+        free(xn); free(y);
+        return -1;
+    }
+    ne_oracle_rmsnorm(x, g, (int)N, C, eps, xn);
+    ne_oracle_linear(xn, w, (int)N, C, 3 * C, y);
+#pragma omp parallel for schedule(static)
+    for (long long n = 0; n < N; n++) {
+        const int t = (int)(n % T);
+        const double *yr = y + n * 3 * C;
+        for (int h = 0; h < H; h++) {
+            rope_vector(yr + h * D, D, t, base, 0, qr + n * C + h * D);
+            rope_vector(yr + C + h * D, D, t, base, 0, kr + n * C + h * D);
+            for (int d = 0; d < D; d++)
+                v[n * C + h * D + d] = yr[2 * C + h * D + d];
+        }
+    }
+    free(xn);
+    free(y);
+    return 0;
+}
+
+/* Exported: y = r + o . w^T for N rows of C (w [C][C]).  Returns 0, or -1. */
+int ne_oracle_out_proj_residual(const double *o, const double *w, const double *r, int N, int C,
+                                double *y)
+{
+    if (!o || !w || !r || !y || N < 0 || C <= 0)
+        return -1;
+    if (ne_oracle_linear(o, w, N, C, C, y) != 0)
+        return -1;
+    for (long long i = 0; i < (long long)N * C; i++)
+        y[i] += r[i];
+    return 0;
+}
