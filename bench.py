@@ -341,6 +341,71 @@ def bench_workloads(args, dev, stream, flush, peak_tf):
     return res
 
 
+def proj_summary(args, dev, stream, flush, peak_tf):
+    """The projections around the attention at the GPT-2-small shape (B=8,
+    T=1024, C=768): RMSNorm + QKV projection with RoPE in the epilogue, and
+    the output projection + residual; each timed with CUDA events, the L2
+    flushed before every step, beside the same products by torch.matmul
+    (cuBLAS) for context."""
+    import torch
+
+    from causal_self_attention_gb300 import ne_attn as na
+    B, T, H = 8, 1024, 12
+    C, M = H * 64, B * T
+    g = torch.Generator().manual_seed(77)
+    x = torch.randn((M, C), generator=g).to(torch.bfloat16).to(dev)
+    gw = (torch.randn((C,), generator=g) * 0.1 + 1.0).to(torch.bfloat16).to(dev)
+    wq = (torch.randn((3 * C, C), generator=g) / C ** 0.5).to(torch.bfloat16).to(dev)
+    wo = (torch.randn((C, C), generator=g) / C ** 0.5).to(torch.bfloat16).to(dev)
+    res = torch.randn((M, C), generator=g).to(torch.bfloat16).to(dev)
+    xn = torch.empty_like(x)
+    rstd = torch.empty(M, dtype=torch.float32, device=dev)
+    q, k, v = (torch.empty((B, T, H, 64), dtype=torch.bfloat16, device=dev) for _ in range(3))
+    y = torch.empty_like(x)
+
+    def qkv():
+        na.ne_rmsnorm_qkv_rope(x, gw, wq, T, x_norm=xn, rstd=rstd, q=q, k=k, v=v, stream=stream)
+
+    def outp():
+        na.ne_out_proj_residual(x, wo, res, y=y, stream=stream)
+
+    def cublas_qkv():
+        torch.matmul(xn, wq.t())
+
+    def cublas_out():
+        torch.addmm(res, x, wo.t())
+
+    n = max(args.extra_steps, 3)
+    res_ms = {}
+    for name, fn in (("qkv", qkv), ("out", outp), ("cublas_qkv", cublas_qkv),
+                     ("cublas_out", cublas_out)):
+        for _ in range(3):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        res_ms[name] = statistics.median(a.elapsed_time(b) for a, b in ev)
+    assert na.ne_attn_get_device_status() == 0
+    fq, fo = 2.0 * M * 3 * C * C, 2.0 * M * C * C
+    return {
+        "shape": f"M={M} (B={B} T={T}), C={C}: QKV [M,{C}]x[{3 * C},{C}]^T, out [M,{C}]x[{C},{C}]^T",
+        "steps": n,
+        "rmsnorm_qkv_rope": {"ms_median": res_ms["qkv"],
+                             "tflops": fq / (res_ms["qkv"] * 1e-3) / 1e12,
+                             "frac_bf16_peak": fq / (res_ms["qkv"] * 1e-3) / 1e12 / peak_tf,
+                             "cublas_gemm_only_ms_median": res_ms["cublas_qkv"]},
+        "out_proj_residual": {"ms_median": res_ms["out"],
+                              "tflops": fo / (res_ms["out"] * 1e-3) / 1e12,
+                              "frac_bf16_peak": fo / (res_ms["out"] * 1e-3) / 1e12 / peak_tf,
+                              "cublas_addmm_ms_median": res_ms["cublas_out"]},
+    }
+
+
 def decode_summary(args, dev, stream, peaks):
     """One decode step over a KV cache (decode16k), timed with CUDA events:
     GB/s of K and V read, against the measured HBM bandwidth."""
@@ -621,6 +686,7 @@ def run_ours(args):
     if not args.no_extras:
         line["workloads"] = bench_workloads(args, dev, stream, flush, peak_tf)
         line["decode"] = decode_summary(args, dev, stream, peaks)
+        line["projections"] = proj_summary(args, dev, stream, flush, peak_tf)
     if not args.no_cpu_baseline and (world == 1 or rank == 0):
         import oracle
         oracle.build()

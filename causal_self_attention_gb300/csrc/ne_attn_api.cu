@@ -38,6 +38,21 @@ cudaError_t launch_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, const 
                           const RopeTable& rope, float scale_log2, float* part,
                           __nv_bfloat16* out, float* lse, int* status, cudaStream_t stream);
 constexpr unsigned kDecodeBoxRows = 32;  // keys per pipeline stage of the decode kernel
+namespace gemm {
+struct Params {
+  int M, N, K;
+  int n_tiles_m, n_tiles_n;
+  int C;
+  int T;
+  RopeTable rope;
+  int* status;
+};
+}  // namespace gemm
+cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* g, __nv_bfloat16* xn,
+                           float* rstd, int M, int C, float eps, cudaStream_t stream);
+cudaError_t launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmW,
+                        const CUtensorMap& tmO0, const CUtensorMap& tmO1, const CUtensorMap& tmO2,
+                        const gemm::Params& p, cudaStream_t stream);
 }  // namespace ne
 
 namespace {
@@ -235,6 +250,21 @@ ne_status encode_table(CUtensorMap* map, const float2* cs, int positions, unsign
                         const_cast<void*>(static_cast<const void*>(cs)), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NE_OK : NE_ERR_CUDA;
+}
+
+// 2-d tensor map over a row-major [rows, cols] bf16 matrix, box 64 x box_rows,
+// 128-byte swizzle (the operand and output tiles of the projection GEMM).
+ne_status encode_mat(CUtensorMap* map, const void* base, long long rows, int cols,
+                     unsigned box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? NE_OK : NE_ERR_CUDA;
 }
 
@@ -597,6 +627,83 @@ ne_status ne_attn_decode(const ne_bf16* q, const ne_bf16* k_cache, const ne_bf16
     if (e == cudaSuccess) e = e2;
   }
   return cuda_status(e);
+}
+
+ne_status ne_rmsnorm_qkv_rope(const ne_bf16* x, const ne_bf16* g, const ne_bf16* w_qkv, int B,
+                              int T, int H, int D, float eps, float rope_base, ne_bf16* x_norm,
+                              float* rstd, ne_bf16* q, ne_bf16* k, ne_bf16* v, void* stream) {
+  if (!x || !g || !w_qkv || !x_norm || !q || !k || !v) return NE_ERR_INVALID_ARG;
+  if (D != 64) return NE_ERR_UNSUPPORTED;
+  if (B <= 0 || T <= 0 || H <= 0) return NE_ERR_INVALID_ARG;
+  const long long M = static_cast<long long>(B) * T;
+  const long long C = static_cast<long long>(H) * 64;
+  if (C % 256 != 0) return NE_ERR_UNSUPPORTED;  // H a multiple of 4
+  if (M > (1LL << 31) - 1 || M * 3 * C > (1LL << 40)) return NE_ERR_INVALID_ARG;
+  if (!std::isfinite(eps) || eps < 0.f || !std::isfinite(rope_base) || rope_base <= 0.f)
+    return NE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(g) || !aligned16(w_qkv) || !aligned16(x_norm) ||
+      !aligned16(q) || !aligned16(k) || !aligned16(v) || (reinterpret_cast<uintptr_t>(rstd) & 3u))
+    return NE_ERR_MISALIGNED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState* st = nullptr;
+  ne_status rc = device_state(&st);
+  if (rc != NE_OK) return rc;
+  if ((rc = get_encoder()) != NE_OK) return rc;
+  ne::gemm::Params p;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(3 * C);
+  p.K = static_cast<int>(C);
+  p.n_tiles_m = static_cast<int>((M + 127) / 128);
+  p.n_tiles_n = p.N / 256;
+  p.C = static_cast<int>(C);
+  p.T = T;
+  p.status = st->status;
+  if ((rc = rope_table(*st, rope_base, T, &p.rope)) != NE_OK) return rc;
+  CUtensorMap ta, tw, tq, tk, tv;
+  if ((rc = encode_mat(&ta, x_norm, M, p.K, 128)) != NE_OK) return rc;
+  if ((rc = encode_mat(&tw, w_qkv, p.N, p.K, 256)) != NE_OK) return rc;
+  if ((rc = encode_mat(&tq, q, M, p.C, 128)) != NE_OK) return rc;
+  if ((rc = encode_mat(&tk, k, M, p.C, 128)) != NE_OK) return rc;
+  if ((rc = encode_mat(&tv, v, M, p.C, 128)) != NE_OK) return rc;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t e = ne::launch_rmsnorm(reinterpret_cast<const __nv_bfloat16*>(x),
+                                     reinterpret_cast<const __nv_bfloat16*>(g),
+                                     reinterpret_cast<__nv_bfloat16*>(x_norm), rstd, p.M, p.C,
+                                     eps, cs);
+  if (e == cudaSuccess) e = ne::launch_gemm(0, ta, tw, tq, tk, tv, p, cs);
+  return cuda_status(e);
+}
+
+ne_status ne_out_proj_residual(const ne_bf16* o, const ne_bf16* w_o, const ne_bf16* residual,
+                               int N, int C, ne_bf16* y, void* stream) {
+  if (!o || !w_o || !residual || !y) return NE_ERR_INVALID_ARG;
+  if (N <= 0 || C <= 0) return NE_ERR_INVALID_ARG;
+  if (C % 256 != 0) return NE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(N) * C > (1LL << 40)) return NE_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(w_o) || !aligned16(residual) || !aligned16(y))
+    return NE_ERR_MISALIGNED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState* st = nullptr;
+  ne_status rc = device_state(&st);
+  if (rc != NE_OK) return rc;
+  if ((rc = get_encoder()) != NE_OK) return rc;
+  ne::gemm::Params p;
+  p.M = N;
+  p.N = C;
+  p.K = C;
+  p.n_tiles_m = (N + 127) / 128;
+  p.n_tiles_n = C / 256;
+  p.C = C;
+  p.T = 1;
+  p.rope = RopeTable{nullptr, nullptr, 0};
+  p.status = st->status;
+  CUtensorMap ta, tw, ty, tr;
+  if ((rc = encode_mat(&ta, o, N, C, 128)) != NE_OK) return rc;
+  if ((rc = encode_mat(&tw, w_o, C, C, 256)) != NE_OK) return rc;
+  if ((rc = encode_mat(&ty, y, N, C, 128)) != NE_OK) return rc;
+  if ((rc = encode_mat(&tr, residual, N, C, 128)) != NE_OK) return rc;
+  return cuda_status(
+      ne::launch_gemm(1, ta, tw, ty, tr, tr, p, static_cast<cudaStream_t>(stream)));
 }
 
 ne_status ne_attn_set_bwd_phase_events(void* ev_after_preprocess, void* ev_after_main) {

@@ -29,7 +29,7 @@ EXPORTED = ("ne_attn_fwd", "ne_attn_fwd_f32out", "ne_attn_bwd", "ne_attn_bwd_wor
             "ne_attn_set_bwd_phase_events", "ne_attn_get_device_status",
             "ne_attn_last_device_code", "ne_status_string",
             "ne_attn_release", "ne_debug_tma_tile", "ne_debug_rope_tile", "ne_debug_umma",
-            "ne_debug_pipeline")
+            "ne_debug_pipeline", "ne_rmsnorm_qkv_rope", "ne_out_proj_residual")
 
 
 class NeAttnError(RuntimeError):
@@ -70,6 +70,8 @@ def lib():
         "ne_debug_rope_tile": [P, I, I, I, I, I, F, P, P],
         "ne_debug_umma": [I, P, P, P, P],
         "ne_debug_pipeline": [P, I, I, I, I, ctypes.c_longlong, P, P],
+        "ne_rmsnorm_qkv_rope": [P, P, P, I, I, I, I, F, F, P, P, P, P, P, P],
+        "ne_out_proj_residual": [P, P, P, I, I, P, P],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -214,6 +216,46 @@ def ne_attn_varlen_bwd(q, k, v, out, dout, lse, cu_seqlens, max_seqlen, rope_bas
         cu_seqlens.numel() - 1, N, int(max_seqlen), H, D, float(rope_base), float(scale),
         _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), ws_bytes, _stream(stream)))
     return dq, dk, dv
+
+
+def ne_rmsnorm_qkv_rope(x, g, w_qkv, T, eps=1e-5, rope_base=10000.0, x_norm=None, rstd=None,
+                        q=None, k=None, v=None, stream=None):
+    """RMSNorm of ``x`` (``[B*T, C]`` bf16, rows of B sequences of T tokens,
+    C = H*64) with weight ``g`` (``[C]`` bf16), then the QKV projection with
+    ``w_qkv`` (``[3C, C]`` bf16, [out, in]) and RoPE on q and k in the GEMM's
+    epilogue.  Returns ``(q', k', v, x_norm, rstd)``: q', k', v ``[B, T, H, 64]``
+    bf16 (the attention's layout), ``x_norm`` ``[B*T, C]`` bf16, ``rstd``
+    ``[B*T]`` fp32."""
+    for t, n in ((x, "x"), (g, "g"), (w_qkv, "w_qkv")):
+        _need(t, torch.bfloat16, n)
+    M, C = x.shape
+    B, H = M // T, C // 64
+    if B * T != M or H * 64 != C or tuple(w_qkv.shape) != (3 * C, C) or g.numel() != C:
+        raise ValueError("shapes: x [B*T, H*64], g [H*64], w_qkv [3*H*64, H*64]")
+    dev = x.device
+    x_norm = torch.empty_like(x) if x_norm is None else x_norm
+    rstd = torch.empty(M, dtype=torch.float32, device=dev) if rstd is None else rstd
+    q = torch.empty((B, T, H, 64), dtype=torch.bfloat16, device=dev) if q is None else q
+    k = torch.empty((B, T, H, 64), dtype=torch.bfloat16, device=dev) if k is None else k
+    v = torch.empty((B, T, H, 64), dtype=torch.bfloat16, device=dev) if v is None else v
+    _check("ne_rmsnorm_qkv_rope", lib().ne_rmsnorm_qkv_rope(
+        _ptr(x), _ptr(g), _ptr(w_qkv), B, T, H, 64, float(eps), float(rope_base), _ptr(x_norm),
+        _ptr(rstd), _ptr(q), _ptr(k), _ptr(v), _stream(stream)))
+    return q, k, v, x_norm, rstd
+
+
+def ne_out_proj_residual(o, w_o, residual, y=None, stream=None):
+    """``y = residual + o . w_o^T`` for ``o``, ``residual`` ``[N, C]`` bf16 and
+    ``w_o`` ``[C, C]`` bf16 ([out, in]).  Returns ``y`` ``[N, C]`` bf16."""
+    for t, n in ((o, "o"), (w_o, "w_o"), (residual, "residual")):
+        _need(t, torch.bfloat16, n)
+    N, C = o.shape
+    if tuple(w_o.shape) != (C, C) or tuple(residual.shape) != (N, C):
+        raise ValueError("shapes: o, residual [N, C], w_o [C, C]")
+    y = torch.empty_like(residual) if y is None else y
+    _check("ne_out_proj_residual", lib().ne_out_proj_residual(
+        _ptr(o), _ptr(w_o), _ptr(residual), N, C, _ptr(y), _stream(stream)))
+    return y
 
 
 def ne_attn_decode_workspace_bytes(B: int, H: int, Tmax: int) -> int:

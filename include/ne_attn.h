@@ -196,6 +196,39 @@ ne_status ne_attn_decode(const ne_bf16* q, const ne_bf16* k_cache, const ne_bf16
                          float scale, ne_bf16* out, float* lse, void* workspace,
                          size_t workspace_bytes, void* stream);
 
+/* The step before the attention in a transformer layer: RMSNorm, then the
+ * QKV projection, with RoPE applied to q and k in the projection's epilogue
+ * (NanoEuler Show HN page, paragraph 2: the CUDA engine has RMSNorm and RoPE
+ * kernels and computes the layer's matrix products; "Tiny Hackable CUDA",
+ * section 3: the projections are computed, then RoPE encodes relative
+ * position).  For a fixed-length batch of B sequences of T tokens, C = H*64
+ * with H a multiple of 4 (C a multiple of 256; NE_ERR_UNSUPPORTED otherwise),
+ * D = 64:
+ *   x_norm[n][c] = x[n][c] / sqrt(mean_c' x[n][c']^2 + eps) * g[c]   (rstd[n]
+ *                  = 1 / sqrt(mean + eps) in fp32; the bf16 x_norm is what the
+ *                  projection multiplies)
+ *   [q | k | v]  = x_norm . w_qkv^T             (w_qkv [3C, C], no bias)
+ *   q' = R(t) q, k' = R(t) k per head of 64, t = n mod T, in fp32 from the
+ *   fp32 accumulators with the library's RoPE table for rope_base, then bf16.
+ *   x:      [B*T, C] bf16 (input);  g: [C] bf16;  w_qkv: [3C, C] bf16
+ *   x_norm: [B*T, C] bf16 (written);  rstd: [B*T] fp32 (written; may be NULL)
+ *   q, k, v: [B, T, H, 64] bf16 (written) -- the attention's input layout.
+ * All pointers are device memory owned by the caller, 16-byte aligned (rstd:
+ * 4-byte).  eps finite and >= 0; rope_base finite and > 0.  Asynchronous on
+ * `stream`; argument errors return before anything is launched. */
+ne_status ne_rmsnorm_qkv_rope(const ne_bf16* x, const ne_bf16* g, const ne_bf16* w_qkv, int B,
+                              int T, int H, int D, float eps, float rope_base, ne_bf16* x_norm,
+                              float* rstd, ne_bf16* q, ne_bf16* k, ne_bf16* v, void* stream);
+
+/* The step after the attention: the output projection with the residual
+ * added in its epilogue ("Tiny Hackable CUDA", section 3: the attention is
+ * wrapped in a residual connection):  y = residual + o . w_o^T  in fp32, then
+ * bf16.  o (the attention output [N, H, 64] viewed as [N, C]), residual, y:
+ * [N, C] bf16; w_o: [C, C] bf16 ([out, in], no bias); C a multiple of 256.
+ * Conventions as above. */
+ne_status ne_out_proj_residual(const ne_bf16* o, const ne_bf16* w_o, const ne_bf16* residual,
+                               int N, int C, ne_bf16* y, void* stream);
+
 /* Synchronize `stream`, then return and clear the device status word of the
  * current device: NE_OK, NE_ERR_TIMEOUT or NE_ERR_BAD_SEQLEN (or NE_ERR_CUDA
  * if the synchronization itself failed). */
