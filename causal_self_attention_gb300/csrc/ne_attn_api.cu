@@ -305,12 +305,15 @@ ne::Problem make_problem(const Shape& s) {
 // GB300: below it the extra pass costs more than the kernel saves).
 constexpr int kPreRotateLen = 2048;
 
+// pre_rotated: q, k are q' = R(m) q, k' = R(n) k already (rope_base unused).
 ne_status run_fwd(const Shape& s, const void* q, const void* k, const void* v, float rope_base,
-                  float scale, void* out, int out_f32, float* lse, void* stream) {
+                  float scale, void* out, int out_f32, float* lse, void* stream,
+                  bool pre_rotated = false) {
   if (!q || !k || !v || !out || !lse) return NE_ERR_INVALID_ARG;
   ne_status rc = check_shape(s);
   if (rc != NE_OK) return rc;
-  if (!std::isfinite(scale) || scale <= 0.f || !std::isfinite(rope_base) || rope_base <= 0.f)
+  if (!std::isfinite(scale) || scale <= 0.f ||
+      (!pre_rotated && (!std::isfinite(rope_base) || rope_base <= 0.f)))
     return NE_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned4(lse))
     return NE_ERR_MISALIGNED;
@@ -326,7 +329,9 @@ ne_status run_fwd(const Shape& s, const void* q, const void* k, const void* v, f
   p.lse = lse;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = st->status;
-  if ((rc = rope_table(*st, rope_base, n_qtiles * 128, &p.rope)) != NE_OK) return rc;
+  p.rope = RopeTable{nullptr, nullptr, 0};
+  if (!pre_rotated && (rc = rope_table(*st, rope_base, n_qtiles * 128, &p.rope)) != NE_OK)
+    return rc;
   // Keys: for short sequences each item rotates the key tiles it uses in
   // shared memory; from kPreRotateLen positions on, the rotated keys
   // k' = R(n) k are written once per call by a small pass into the library's
@@ -334,13 +339,14 @@ ne_status run_fwd(const Shape& s, const void* q, const void* k, const void* v, f
   // graph, into a stream-ordered allocation of the call's own (a graph must
   // not bake in a buffer that later calls outside it would also use).
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  p.rotate_k = s.max_len < kPreRotateLen ? 1 : 0;
+  p.rotate_k = (!pre_rotated && s.max_len < kPreRotateLen) ? 1 : 0;
+  p.rotate_q = pre_rotated ? 0 : 1;
   CUtensorMap tq, tk, tv, to;
   const void* keys = k;
   bool own = false;
   void* kr = nullptr;
   cudaError_t e = cudaSuccess;
-  if (!p.rotate_k) {
+  if (!p.rotate_k && !pre_rotated) {
     const size_t kr_bytes = static_cast<size_t>(s.n_tot) * s.H * 64 * 2;
     cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(cs, &capture) != cudaSuccess) return NE_ERR_CUDA;
@@ -358,7 +364,7 @@ ne_status run_fwd(const Shape& s, const void* q, const void* k, const void* v, f
   // O tile stores (bf16 output only; the fp32 output is written per row).
   if (rc == NE_OK) rc = encode_rows(&to, out_f32 ? q : out, s.n_tot, s.H);
   if (rc == NE_OK) {
-    if (!p.rotate_k)
+    if (!p.rotate_k && !pre_rotated)
       e = ne::launch_rope_rows(static_cast<const __nv_bfloat16*>(k),
                                static_cast<__nv_bfloat16*>(kr), p.pb, p.rope, cs);
     if (e == cudaSuccess) e = ne::launch_fwd(tq, tk, tv, to, p, n_qtiles, cs);
@@ -373,13 +379,16 @@ ne_status run_fwd(const Shape& s, const void* q, const void* k, const void* v, f
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// pre_rotated: q, k are q', k' already; the gradients returned are w.r.t. them.
 ne_status run_bwd(const Shape& s, const void* q, const void* k, const void* v, const void* out,
                   const void* dout, const float* lse, float rope_base, float scale, void* dq,
-                  void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream) {
+                  void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream,
+                  bool pre_rotated = false) {
   if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return NE_ERR_INVALID_ARG;
   ne_status rc = check_shape(s);
   if (rc != NE_OK) return rc;
-  if (!std::isfinite(scale) || scale <= 0.f || !std::isfinite(rope_base) || rope_base <= 0.f)
+  if (!std::isfinite(scale) || scale <= 0.f ||
+      (!pre_rotated && (!std::isfinite(rope_base) || rope_base <= 0.f)))
     return NE_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
       !aligned4(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
@@ -404,7 +413,10 @@ ne_status run_bwd(const Shape& s, const void* q, const void* k, const void* v, c
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = st->status;
-  if ((rc = rope_table(*st, rope_base, n_tiles * 128, &p.rope)) != NE_OK) return rc;
+  p.pre_rotated = pre_rotated ? 1 : 0;
+  p.rope = RopeTable{nullptr, nullptr, 0};
+  if (!pre_rotated && (rc = rope_table(*st, rope_base, n_tiles * 128, &p.rope)) != NE_OK)
+    return rc;
   CUtensorMap tq, tk, tv, tdo;
   if ((rc = encode_rows(&tv, v, s.n_tot, s.H)) != NE_OK) return rc;
   if ((rc = encode_rows(&tdo, dout, s.n_tot, s.H)) != NE_OK) return rc;
@@ -426,6 +438,10 @@ ne_status run_bwd(const Shape& s, const void* q, const void* k, const void* v, c
   p.kr = reinterpret_cast<__nv_bfloat16*>(wsb + acc_bytes + del_bytes + rot_bytes);
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k = static_cast<const __nv_bfloat16*>(k);
+  if (pre_rotated) {  // the main kernel reads q', k' where the caller keeps them
+    p.qr = const_cast<__nv_bfloat16*>(p.q);
+    p.kr = const_cast<__nv_bfloat16*>(p.k);
+  }
   CUtensorMap tdq, tdv, tdk;
   rc = encode_rows(&tq, p.qr, s.n_tot, s.H);
   if (rc == NE_OK) rc = encode_rows(&tk, p.kr, s.n_tot, s.H);
@@ -558,6 +574,34 @@ ne_status ne_attn_bwd(const ne_bf16* q, const ne_bf16* k, const ne_bf16* v, cons
   if (B > 0 && T > 0 && static_cast<long long>(B) * T > (1LL << 31) - 1) return NE_ERR_INVALID_ARG;
   return run_bwd(s, q, k, v, out, dout, lse, rope_base, scale, dq, dk, dv, workspace,
                  workspace_bytes, stream);
+}
+
+ne_status ne_attn_fwd_rotated(const ne_bf16* qr, const ne_bf16* kr, const ne_bf16* v, int B,
+                              int H, int T, int D, float scale, ne_bf16* out, float* lse,
+                              void* stream) {
+  Shape s;
+  s.nseq = B;
+  s.max_len = T;
+  s.n_tot = (B > 0 && T > 0) ? B * T : 0;
+  s.H = H;
+  s.D = D;
+  if (B > 0 && T > 0 && static_cast<long long>(B) * T > (1LL << 31) - 1) return NE_ERR_INVALID_ARG;
+  return run_fwd(s, qr, kr, v, 0.f, scale, out, 0, lse, stream, true);
+}
+
+ne_status ne_attn_bwd_rotated(const ne_bf16* qr, const ne_bf16* kr, const ne_bf16* v,
+                              const ne_bf16* out, const ne_bf16* dout, const float* lse, int B,
+                              int H, int T, int D, float scale, ne_bf16* dqr, ne_bf16* dkr,
+                              ne_bf16* dv, void* workspace, size_t workspace_bytes, void* stream) {
+  Shape s;
+  s.nseq = B;
+  s.max_len = T;
+  s.n_tot = (B > 0 && T > 0) ? B * T : 0;
+  s.H = H;
+  s.D = D;
+  if (B > 0 && T > 0 && static_cast<long long>(B) * T > (1LL << 31) - 1) return NE_ERR_INVALID_ARG;
+  return run_bwd(s, qr, kr, v, out, dout, lse, 0.f, scale, dqr, dkr, dv, workspace,
+                 workspace_bytes, stream, true);
 }
 
 ne_status ne_attn_varlen_bwd(const ne_bf16* q, const ne_bf16* k, const ne_bf16* v,

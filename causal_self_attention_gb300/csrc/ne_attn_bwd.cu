@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(256)
                                   const __nv_bfloat16* __restrict__ dout,
                                   __nv_bfloat16* __restrict__ qr, __nv_bfloat16* __restrict__ kr,
                                   float* __restrict__ delta, float* __restrict__ dq_acc,
-                                  const Problem pb, RopeTable rope) {
+                                  const Problem pb, RopeTable rope, int pre_rotated) {
   pdl_wait();  // the forward that wrote O (and anything before it) has completed
   const int seq = blockIdx.y;
   int start, len;
@@ -159,8 +159,10 @@ __global__ void __launch_bounds__(256)
       float4* z = reinterpret_cast<float4*>(dq_acc + pair * kHD) + part * 2;
       z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
       z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-      // RoPE of one chunk pair of q (parts 0-3) or k (parts 4-7).
+      // RoPE of one chunk pair of q (parts 0-3) or k (parts 4-7); nothing to
+      // do when the caller passed q', k' already rotated.
       const int c = part & 3;
+      if (!pre_rotated) {
       const __nv_bfloat16* src = (part < 4 ? q : k) + pair * kHD;
       __nv_bfloat16* dst = (part < 4 ? qr : kr) + pair * kHD;
       const uint4 lo = __ldg(reinterpret_cast<const uint4*>(src) + c);
@@ -182,6 +184,7 @@ __global__ void __launch_bounds__(256)
       }
       reinterpret_cast<uint4*>(dst)[c] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
       reinterpret_cast<uint4*>(dst)[c + 4] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+      }
     }
     acc += __shfl_xor_sync(0xffffffffu, acc, 1);
     acc += __shfl_xor_sync(0xffffffffu, acc, 2);
@@ -854,7 +857,7 @@ __device__ __forceinline__ void dk_rotate_item(__nv_bfloat16* __restrict__ dk, c
 __global__ void __launch_bounds__(kPostThreads)
     ne_attn_dq_postprocess_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq,
                                   __nv_bfloat16* __restrict__ dk, const Problem pb, RopeTable rope,
-                                  float scale) {
+                                  float scale, int pre_rotated) {
   pdl_wait();  // the main kernel's dQ' reduce-adds and dK stores have completed
   const int seq = blockIdx.y;
   int start, len;
@@ -873,18 +876,26 @@ __global__ void __launch_bounds__(kPostThreads)
   const long long row_off = (static_cast<long long>(start + pos) * H + h) * kHD;
   const float4 lo = *reinterpret_cast<const float4*>(dq_acc + row_off + part * 4);
   const float4 hi = *reinterpret_cast<const float4*>(dq_acc + row_off + 32 + part * 4);
-  const float4* cs4 =
-      reinterpret_cast<const float4*>(rope.cs + static_cast<long long>(pos) * 32 + part * 4);
-  const float4 t0 = __ldg(cs4), t1 = __ldg(cs4 + 1);  // (cos, sin) of dims 4c .. 4c + 3
   const float a[4] = {lo.x * scale, lo.y * scale, lo.z * scale, lo.w * scale};
   const float b[4] = {hi.x * scale, hi.y * scale, hi.z * scale, hi.w * scale};
-  const float cz[4] = {t0.x, t0.z, t1.x, t1.z};
-  const float sz[4] = {t0.y, t0.w, t1.y, t1.w};
   float go[4], gh[4];
+  if (pre_rotated) {  // the gradient w.r.t. q' itself
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    go[i] = a[i] * cz[i] + b[i] * sz[i];
-    gh[i] = b[i] * cz[i] - a[i] * sz[i];
+    for (int i = 0; i < 4; ++i) {
+      go[i] = a[i];
+      gh[i] = b[i];
+    }
+  } else {
+    const float4* cs4 =
+        reinterpret_cast<const float4*>(rope.cs + static_cast<long long>(pos) * 32 + part * 4);
+    const float4 t0 = __ldg(cs4), t1 = __ldg(cs4 + 1);  // (cos, sin) of dims 4c .. 4c + 3
+    const float cz[4] = {t0.x, t0.z, t1.x, t1.z};
+    const float sz[4] = {t0.y, t0.w, t1.y, t1.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      go[i] = a[i] * cz[i] + b[i] * sz[i];
+      gh[i] = b[i] * cz[i] - a[i] * sz[i];
+    }
   }
   __nv_bfloat16* d = dq + row_off;
   *reinterpret_cast<uint2*>(d + part * 4) = make_uint2(pack_bf16x2(go[0], go[1]), pack_bf16x2(go[2], go[3]));
@@ -907,7 +918,8 @@ cudaError_t launch_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
   }
   dim3 pre_grid((n_tiles * kBM + bwd::kPreRows - 1) / bwd::kPreRows, p.pb.nseq);
   cudaError_t e = launch_pdl(ne_attn_bwd_preprocess_kernel, pre_grid, dim3(256), 0, stream, p.q,
-                             p.k, p.out, p.dout, p.qr, p.kr, p.delta, p.dq_acc, p.pb, p.rope);
+                             p.k, p.out, p.dout, p.qr, p.kr, p.delta, p.dq_acc, p.pb, p.rope,
+                             p.pre_rotated);
   if (e != cudaSuccess) return e;
   if (ev_pre && (e = cudaEventRecord(ev_pre, stream)) != cudaSuccess) return e;
   // One persistent CTA per SM (at most one per unit).
@@ -925,10 +937,13 @@ cudaError_t launch_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
   if (e != cudaSuccess) return e;
   if (ev_main && (e = cudaEventRecord(ev_main, stream)) != cudaSuccess) return e;
   const long long post_items = static_cast<long long>(n_tiles) * kBM * p.pb.H * kPostParts;
-  // Layer z = 0: dQ from the accumulator; z = 1: dK rotated in place.
-  dim3 pgrid(static_cast<unsigned>((post_items + kPostThreads - 1) / kPostThreads), p.pb.nseq, 2);
+  // Layer z = 0: dQ from the accumulator; z = 1: dK rotated in place (not
+  // for pre-rotated inputs, whose dK' the main kernel already wrote).
+  dim3 pgrid(static_cast<unsigned>((post_items + kPostThreads - 1) / kPostThreads), p.pb.nseq,
+             p.pre_rotated ? 1 : 2);
   return launch_pdl(ne_attn_dq_postprocess_kernel, pgrid, dim3(kPostThreads), 0, stream,
-                    static_cast<const float*>(p.dq_acc), p.dq, p.dk, p.pb, p.rope, p.scale);
+                    static_cast<const float*>(p.dq_acc), p.dq, p.dk, p.pb, p.rope, p.scale,
+                    p.pre_rotated);
 }
 
 }  // namespace ne

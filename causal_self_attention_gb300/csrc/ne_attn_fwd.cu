@@ -134,9 +134,12 @@ __device__ __forceinline__ int item_index(int k, int c, int G) {
 // Grid: G persistent CTAs; nblk = 256-row blocks of the longest sequence.
 // kRotateK: the K tiles are rotated in smem by the rotate warps (short
 // sequences); otherwise they come pre-rotated and the O tiles are written by
-// TMA from the Q buffer (long sequences).  Two instantiations, so that each
-// compiles only its own epilogue (registers are tight in the softmax warps).
-template <bool kRotateK>
+// TMA from the Q buffer (long sequences).  kRotateQ: the Q tiles are rotated
+// in smem (always, except for callers that pass q' = R(m) q already rotated,
+// e.g. by the QKV projection's epilogue).  Separate instantiations, so that
+// each compiles only its own epilogue (registers are tight in the softmax
+// warps).
+template <bool kRotateK, bool kRotateQ>
 __global__ void __launch_bounds__(fwd::kThreads, 1)
     ne_attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
@@ -418,12 +421,14 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
     NE_FOR_EACH_ITEM(it) {
       if (!ok) break;
       const int b = nq & 1;
-      rope_load_row(p.rope, it.rowA + r, tab);
+      if constexpr (kRotateQ) rope_load_row(p.rope, it.rowA + r, tab);
       if (!(ok = mbar_wait(&bars[B_Q_FULL + b], (nq >> 1) & 1, abort_flag, p.status, 6))) break;
-      rope_rotate_row(sQ + 2 * b * kTileBytes, r, tab);
-      rope_load_row(p.rope, it.rowA + kBM + r, tab);
-      rope_rotate_row(sQ + (2 * b + 1) * kTileBytes, r, tab);
-      fence_proxy_async_smem();
+      if constexpr (kRotateQ) {
+        rope_rotate_row(sQ + 2 * b * kTileBytes, r, tab);
+        rope_load_row(p.rope, it.rowA + kBM + r, tab);
+        rope_rotate_row(sQ + (2 * b + 1) * kTileBytes, r, tab);
+        fence_proxy_async_smem();
+      }
       mbar_arrive(&bars[B_Q_ROT + b]);
       ++nq;
       if (!kRotateK) continue;  // the keys come pre-rotated
@@ -710,11 +715,14 @@ cudaError_t launch_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
                        cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(ne_attn_fwd_kernel<true>,
+    cudaError_t e = cudaFuncSetAttribute(ne_attn_fwd_kernel<true, true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          fwd::SMEM_BYTES);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(ne_attn_fwd_kernel<false>,
+      e = cudaFuncSetAttribute(ne_attn_fwd_kernel<false, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, fwd::SMEM_BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(ne_attn_fwd_kernel<false, false>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, fwd::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
@@ -732,10 +740,14 @@ cudaError_t launch_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
   const int nblk = (n_qtiles + 1) / 2;
   const long long n_items = static_cast<long long>(nblk) * p.pb.nseq * p.pb.H;
   const int G = static_cast<int>(n_items < sm_count[dev] ? n_items : sm_count[dev]);
-  return p.rotate_k ? launch_pdl(ne_attn_fwd_kernel<true>, dim3(G), dim3(fwd::kThreads),
-                                fwd::SMEM_BYTES, stream, tmQ, tmK, tmV, tmO, p, nblk)
-                    : launch_pdl(ne_attn_fwd_kernel<false>, dim3(G), dim3(fwd::kThreads),
-                                fwd::SMEM_BYTES, stream, tmQ, tmK, tmV, tmO, p, nblk);
+  if (p.rotate_k)
+    return launch_pdl(ne_attn_fwd_kernel<true, true>, dim3(G), dim3(fwd::kThreads),
+                      fwd::SMEM_BYTES, stream, tmQ, tmK, tmV, tmO, p, nblk);
+  if (p.rotate_q)
+    return launch_pdl(ne_attn_fwd_kernel<false, true>, dim3(G), dim3(fwd::kThreads),
+                      fwd::SMEM_BYTES, stream, tmQ, tmK, tmV, tmO, p, nblk);
+  return launch_pdl(ne_attn_fwd_kernel<false, false>, dim3(G), dim3(fwd::kThreads),
+                    fwd::SMEM_BYTES, stream, tmQ, tmK, tmV, tmO, p, nblk);
 }
 
 }  // namespace ne

@@ -55,6 +55,7 @@ struct FwdParams {
   int* status;
   int rotate_k;      // 1: K tiles are loaded un-rotated and rotated in smem;
                      // 0: the keys come pre-rotated (k')
+  int rotate_q;      // 1: Q tiles are rotated in smem; 0: the caller passed q'
 };
 
 struct BwdParams {
@@ -75,6 +76,8 @@ struct BwdParams {
   float scale_log2;
   RopeTable rope;
   int* status;
+  int pre_rotated;  // 1: q, k are q', k' already; no rotation anywhere, and the
+                    // gradients returned are those w.r.t. q', k'
 };
 
 // Sequence bounds of sequence s.  Returns false (and raises the device status)

@@ -29,7 +29,8 @@ EXPORTED = ("ne_attn_fwd", "ne_attn_fwd_f32out", "ne_attn_bwd", "ne_attn_bwd_wor
             "ne_attn_set_bwd_phase_events", "ne_attn_get_device_status",
             "ne_attn_last_device_code", "ne_status_string",
             "ne_attn_release", "ne_debug_tma_tile", "ne_debug_rope_tile", "ne_debug_umma",
-            "ne_debug_pipeline", "ne_rmsnorm_qkv_rope", "ne_out_proj_residual")
+            "ne_debug_pipeline", "ne_rmsnorm_qkv_rope", "ne_out_proj_residual",
+            "ne_attn_fwd_rotated", "ne_attn_bwd_rotated")
 
 
 class NeAttnError(RuntimeError):
@@ -72,6 +73,8 @@ def lib():
         "ne_debug_pipeline": [P, I, I, I, I, ctypes.c_longlong, P, P],
         "ne_rmsnorm_qkv_rope": [P, P, P, I, I, I, I, F, F, P, P, P, P, P, P],
         "ne_out_proj_residual": [P, P, P, I, I, P, P],
+        "ne_attn_fwd_rotated": [P, P, P, I, I, I, I, F, P, P, P],
+        "ne_attn_bwd_rotated": [P, P, P, P, P, P, I, I, I, I, F, P, P, P, P, Z, P],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -216,6 +219,40 @@ def ne_attn_varlen_bwd(q, k, v, out, dout, lse, cu_seqlens, max_seqlen, rope_bas
         cu_seqlens.numel() - 1, N, int(max_seqlen), H, D, float(rope_base), float(scale),
         _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), ws_bytes, _stream(stream)))
     return dq, dk, dv
+
+
+def ne_attn_fwd_rotated(qr, kr, v, scale=None, out=None, lse=None, stream=None):
+    """Forward on pre-rotated ``q' = R(m) q``, ``k' = R(n) k`` (``[B, T, H, 64]``
+    bf16).  Returns ``(out, lse)``."""
+    for t, n in ((qr, "qr"), (kr, "kr"), (v, "v")):
+        _need(t, torch.bfloat16, n)
+    B, T, H, D = qr.shape
+    scale = D ** -0.5 if scale is None else scale
+    out = torch.empty_like(qr) if out is None else out
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=qr.device) if lse is None else lse
+    _check("ne_attn_fwd_rotated", lib().ne_attn_fwd_rotated(
+        _ptr(qr), _ptr(kr), _ptr(v), B, H, T, D, float(scale), _ptr(out), _ptr(lse),
+        _stream(stream)))
+    return out, lse
+
+
+def ne_attn_bwd_rotated(qr, kr, v, out, dout, lse, scale=None, dqr=None, dkr=None, dv=None,
+                        workspace=None, stream=None):
+    """Backward of :func:`ne_attn_fwd_rotated`.  Returns ``(dqr, dkr, dv)``: the
+    gradients w.r.t. q', k' (the rotated frame) and v."""
+    for t, n in ((qr, "qr"), (kr, "kr"), (v, "v"), (out, "out"), (dout, "dout")):
+        _need(t, torch.bfloat16, n)
+    _need(lse, torch.float32, "lse")
+    B, T, H, D = qr.shape
+    scale = D ** -0.5 if scale is None else scale
+    dqr = torch.empty_like(qr) if dqr is None else dqr
+    dkr = torch.empty_like(kr) if dkr is None else dkr
+    dv = torch.empty_like(v) if dv is None else dv
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("ne_attn_bwd_rotated", lib().ne_attn_bwd_rotated(
+        _ptr(qr), _ptr(kr), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), B, H, T, D, float(scale),
+        _ptr(dqr), _ptr(dkr), _ptr(dv), _ptr(workspace), ws_bytes, _stream(stream)))
+    return dqr, dkr, dv
 
 
 def ne_rmsnorm_qkv_rope(x, g, w_qkv, T, eps=1e-5, rope_base=10000.0, x_norm=None, rstd=None,

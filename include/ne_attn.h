@@ -101,6 +101,22 @@ ne_status ne_attn_bwd(const ne_bf16* q, const ne_bf16* k, const ne_bf16* v, cons
                       float rope_base, float scale, ne_bf16* dq, ne_bf16* dk, ne_bf16* dv,
                       void* workspace, size_t workspace_bytes, void* stream);
 
+/* Forward and backward on inputs already rotated: q' = R(m) q and k' = R(n) k
+ * as ne_rmsnorm_qkv_rope writes them (the projection applied RoPE in its
+ * epilogue), so nothing is rotated here.  Fixed length, arguments as in
+ * ne_attn_fwd / ne_attn_bwd without rope_base; qr, kr replace q, k.  The
+ * backward returns dqr, dkr -- the gradients with respect to q' and k' (the
+ * rotated frame; dq = R(m)^T dqr, dk = R(n)^T dkr) -- and dv.  With q', k'
+ * equal to the bf16 rotation ne_attn_fwd performs internally, O and LSE are
+ * bitwise those of ne_attn_fwd on q, k. */
+ne_status ne_attn_fwd_rotated(const ne_bf16* qr, const ne_bf16* kr, const ne_bf16* v, int B,
+                              int H, int T, int D, float scale, ne_bf16* out, float* lse,
+                              void* stream);
+ne_status ne_attn_bwd_rotated(const ne_bf16* qr, const ne_bf16* kr, const ne_bf16* v,
+                              const ne_bf16* out, const ne_bf16* dout, const float* lse, int B,
+                              int H, int T, int D, float scale, ne_bf16* dqr, ne_bf16* dkr,
+                              ne_bf16* dv, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Forward, packed variable-length batch.  Sequence s occupies rows
  * cu_seqlens[s] .. cu_seqlens[s+1]-1 of q, k, v, out ([n_tot, H, 64] bf16);
  * cu_seqlens is DEVICE int32 [nseq + 1], nondecreasing, cu_seqlens[0] = 0,

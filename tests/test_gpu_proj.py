@@ -90,3 +90,70 @@ def test_zero_weight_gives_the_residual_bitwise(na):
     o = torch.randn((N, C)).to(torch.bfloat16).cuda()
     y = na.ne_out_proj_residual(o, torch.zeros((C, C), dtype=torch.bfloat16).cuda(), r)
     assert torch.equal(y, r)
+
+
+def _rotate_bf16(x, T, H):
+    """The bf16 operands RoPE produces in the attention kernels (oracle mode 1),
+    per head, positions 0..T-1 in each sequence: [B, T, H, 64] bf16."""
+    B = x.shape[0]
+    out = np.empty(tuple(x.shape))
+    for b in range(B):
+        for h in range(H):
+            out[b, :, h] = oracle.rope(x[b, :, h].double().numpy(), base=10000.0, mode=1)
+    return torch.from_numpy(out).to(torch.bfloat16)
+
+
+def test_rotated_attention_matches_the_rotating_one(na):
+    """ne_attn_fwd_rotated on q', k' = the bf16 rotations gives bitwise the O,
+    LSE of ne_attn_fwd on q, k; ne_attn_bwd_rotated gives dv bitwise and dq',
+    dk' whose un-rotation matches the oracle's dq, dk."""
+    from causal_self_attention_gb300.inputs import make_custom
+    from parity import GRAD_TOL, packed_view
+    inp = make_custom(2, 300, 3, seed=61)
+    B, T, H = 2, 300, 3
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "dout"))
+    qr, kr = _rotate_bf16(inp["q"], T, H).cuda(), _rotate_bf16(inp["k"], T, H).cuda()
+    o, lse = na.ne_attn_fwd(q, k, v)
+    o2, lse2 = na.ne_attn_fwd_rotated(qr, kr, v)
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    dq, dk, dv = na.ne_attn_bwd(q, k, v, o, do, lse)
+    dqr, dkr, dv2 = na.ne_attn_bwd_rotated(qr, kr, v, o2, do, lse2)
+    assert na.ne_attn_get_device_status() == 0
+    assert torch.equal(dv, dv2)
+    (cq, ck, cv, cdo), cu = packed_view(inp)
+    ref = oracle.attention(cq, ck, cv, cdo, cu, base=10000.0, scale=inp["scale"], mode=0)
+    for name, g in (("dq", dqr), ("dk", dkr)):
+        gr = g.double().cpu().numpy()
+        back = np.empty_like(gr)
+        for b in range(B):
+            for h in range(H):
+                back[b, :, h] = oracle.rope_transpose(gr[b, :, h], base=10000.0)
+        err = rel_l2(back.reshape(B * T, H, 64), ref[name])
+        assert err <= GRAD_TOL, (name, err)
+
+
+def test_attention_block_chain(na):
+    """RMSNorm + QKV + RoPE -> attention on q', k' -> output projection +
+    residual, against the oracle's composition of the same steps (one layer's
+    attention block, as the pages' transformer layer runs it)."""
+    B, T, H = 1, 256, 4
+    C = H * 64
+    x, g, w = _inputs(B, T, H, 71)
+    gen = torch.Generator().manual_seed(72)
+    wo = (torch.randn((C, C), generator=gen) / C ** 0.5).to(torch.bfloat16)
+    q, k, v, _, _ = na.ne_rmsnorm_qkv_rope(x.cuda(), g.cuda(), w.cuda(), T)
+    o, _ = na.ne_attn_fwd_rotated(q, k, v)
+    y = na.ne_out_proj_residual(o.reshape(B * T, C), wo.cuda(), x.cuda())
+    assert na.ne_attn_get_device_status() == 0
+    rq, rk, rv = oracle.qkv_rope(x, g, w, B, T, H, 64)
+    # attention on the (double) rotated operands: base irrelevant at mode 0 with
+    # rotation already applied -- express it as attention with RoPE undone:
+    # the oracle's attention takes un-rotated q, k, so un-rotate q', k' first.
+    uq = np.stack([oracle.rope_transpose(rq[:, h * 64:(h + 1) * 64]) for h in range(H)], axis=1)
+    uk = np.stack([oracle.rope_transpose(rk[:, h * 64:(h + 1) * 64]) for h in range(H)], axis=1)
+    att = oracle.attention(uq, uk, rv.reshape(T, H, 64), None, [0, T], base=10000.0,
+                           scale=0.125, mode=0)
+    ref = oracle.out_proj_residual(att["o"].reshape(T, C), wo, x)
+    err = rel_l2(y.double().cpu().numpy(), ref)
+    print(f"\n[proj] attention block chain rel_l2={err:.2e}")
+    assert err <= TOL, err
