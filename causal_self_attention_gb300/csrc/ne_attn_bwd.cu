@@ -672,44 +672,50 @@ __global__ void __launch_bounds__(512, 1)
           break;
         }
         tc_fence_after();
-        uint32_t sv[64], dv[64];
+        // The thread's 64 query columns in two halves of 32, one after the
+        // other: each half's S^T and dP^T words come in one TMEM round trip.
+        // Holding 32 columns instead of 64 leaves the compiler registers to
+        // overlap the exponentials' latency (the accumulator columns are
+        // released once the second half is in registers).
         const uint32_t cs = kColS + 64 * half, cd = kColDP + 64 * half;
-        tmem_ld_x32(tmem + lane_base + cs, sv);
-        tmem_ld_x32(tmem + lane_base + cs + 32, sv + 32);
-        tmem_ld_x32(tmem + lane_base + cd, dv);
-        tmem_ld_x32(tmem + lane_base + cd + 32, dv + 32);
-        tmem_ld_wait(sv);
-        tmem_ld_wait(sv + 32);
-        tmem_ld_wait(dv);
-        tmem_ld_wait(dv + 32);
-        tc_fence_before();
-        mbar_arrive(&bars[B_S_FREE]);  // S^T/dP^T may be overwritten now
-        if (it == 0) {  // query tile == key tile: queries before the key get no weight
-#pragma unroll
-          for (int col = 0; col < 64; ++col)
-            if (64 * half + col < r) sv[col] = 0xff800000u;  // -inf: P = 0, dS = 0
-        }
         const float4* nl4 = reinterpret_cast<const float4*>(sLSE + sl * 128 + 64 * half);
         const float4* nd4 = reinterpret_cast<const float4*>(sDEL + sl * 128 + 64 * half);
         const uint64_t sl2x2 = f2_pack(sl2, sl2);
         uint32_t pw[32], dw[32];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const float4 nl = nl4[q], nd = nd4[q];
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t sv[32], dv[32];
+          tmem_ld_x32(tmem + lane_base + cs + 32 * hh, sv);
+          tmem_ld_x32(tmem + lane_base + cd + 32 * hh, dv);
+          tmem_ld_wait(sv);
+          tmem_ld_wait(dv);
+          if (hh == 1) {
+            tc_fence_before();
+            mbar_arrive(&bars[B_S_FREE]);  // S^T/dP^T may be overwritten now
+          }
+          if (it == 0) {
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int col = 4 * q + 2 * e;
-            const uint64_t t = f2_fma(f2_pack(__uint_as_float(sv[col]), __uint_as_float(sv[col + 1])),
-                                      sl2x2, e ? f2_pack(nl.z, nl.w) : f2_pack(nl.x, nl.y));
-            float t0, t1;
-            f2_unpack(t, t0, t1);
-            const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
-            const uint64_t dd = f2_add(f2_pack(__uint_as_float(dv[col]), __uint_as_float(dv[col + 1])),
-                                       e ? f2_pack(nd.z, nd.w) : f2_pack(nd.x, nd.y));
-            float d0, d1;
-            f2_unpack(f2_mul(f2_pack(p0, p1), dd), d0, d1);
-            pw[col / 2] = pack_bf16x2(p0, p1);
-            dw[col / 2] = pack_bf16x2(d0, d1);
+            for (int col = 0; col < 32; ++col)
+              if (64 * half + 32 * hh + col < r) sv[col] = 0xff800000u;
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 nl = nl4[8 * hh + q], nd = nd4[8 * hh + q];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int col = 4 * q + 2 * e;
+              const uint64_t t = f2_fma(f2_pack(__uint_as_float(sv[col]), __uint_as_float(sv[col + 1])),
+                                        sl2x2, e ? f2_pack(nl.z, nl.w) : f2_pack(nl.x, nl.y));
+              float t0, t1;
+              f2_unpack(t, t0, t1);
+              const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+              const uint64_t dd = f2_add(f2_pack(__uint_as_float(dv[col]), __uint_as_float(dv[col + 1])),
+                                         e ? f2_pack(nd.z, nd.w) : f2_pack(nd.x, nd.y));
+              float d0, d1;
+              f2_unpack(f2_mul(f2_pack(p0, p1), dd), d0, d1);
+              pw[16 * hh + col / 2] = pack_bf16x2(p0, p1);
+              dw[16 * hh + col / 2] = pack_bf16x2(d0, d1);
+            }
           }
         }
         // This warp is done with the slot's row terms.
