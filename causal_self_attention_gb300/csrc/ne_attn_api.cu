@@ -19,7 +19,8 @@ namespace ne {
 cudaError_t launch_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                        const CUtensorMap& tmO, const FwdParams& p, int n_qtiles,
                        cudaStream_t stream);
-cudaError_t launch_rope_rows(const __nv_bfloat16* x, __nv_bfloat16* xr, const Problem& pb,
+cudaError_t launch_rope_rows(const __nv_bfloat16* x0, __nv_bfloat16* xr0,
+                             const __nv_bfloat16* x1, __nv_bfloat16* xr1, const Problem& pb,
                              const RopeTable& rope, cudaStream_t stream);
 cudaError_t launch_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                        const CUtensorMap& tmDO, const CUtensorMap& tmDQ, const CUtensorMap& tmDV,
@@ -116,7 +117,7 @@ ne_status stream_scratch(DeviceState& st, cudaStream_t stream, size_t bytes, voi
 std::mutex g_mutex;
 DeviceState g_dev[kMaxDevices];
 int g_last_code = 0;
-cudaEvent_t g_ev_pre = nullptr, g_ev_main = nullptr;
+cudaEvent_t g_ev_pre = nullptr, g_ev_main = nullptr, g_ev_rot = nullptr;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 ne_status cuda_status(cudaError_t e) {
@@ -305,11 +306,19 @@ ne::Problem make_problem(const Shape& s) {
 // GB300: below it the extra pass costs more than the kernel saves).
 constexpr int kPreRotateLen = 2048;
 
-// pre_rotated: q, k are q' = R(m) q, k' = R(n) k already (rope_base unused).
+// How the operands are rotated.  kRotate: q, k as given, rotated inside;
+// kPreRotated: q, k are q' = R(m) q, k' = R(n) k already (rope_base unused);
+// kTrain: q, k as given, rotated by one pass into the caller's qr, kr, which
+// the attention kernel then reads (and the backward later reuses).
+enum class Rot { kRotate, kPreRotated, kTrain };
+
 ne_status run_fwd(const Shape& s, const void* q, const void* k, const void* v, float rope_base,
                   float scale, void* out, int out_f32, float* lse, void* stream,
-                  bool pre_rotated = false) {
+                  Rot mode = Rot::kRotate, void* qr_out = nullptr, void* kr_out = nullptr) {
+  const bool pre_rotated = mode == Rot::kPreRotated;
   if (!q || !k || !v || !out || !lse) return NE_ERR_INVALID_ARG;
+  if (mode == Rot::kTrain && (!qr_out || !kr_out)) return NE_ERR_INVALID_ARG;
+  if (mode == Rot::kTrain && (!aligned16(qr_out) || !aligned16(kr_out))) return NE_ERR_MISALIGNED;
   ne_status rc = check_shape(s);
   if (rc != NE_OK) return rc;
   if (!std::isfinite(scale) || scale <= 0.f ||
@@ -339,14 +348,15 @@ ne_status run_fwd(const Shape& s, const void* q, const void* k, const void* v, f
   // graph, into a stream-ordered allocation of the call's own (a graph must
   // not bake in a buffer that later calls outside it would also use).
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  p.rotate_k = (!pre_rotated && s.max_len < kPreRotateLen) ? 1 : 0;
-  p.rotate_q = pre_rotated ? 0 : 1;
+  p.rotate_k = (mode == Rot::kRotate && s.max_len < kPreRotateLen) ? 1 : 0;
+  p.rotate_q = mode == Rot::kRotate ? 1 : 0;
   CUtensorMap tq, tk, tv, to;
-  const void* keys = k;
+  const void* queries = mode == Rot::kTrain ? qr_out : q;
+  const void* keys = mode == Rot::kTrain ? kr_out : k;
   bool own = false;
   void* kr = nullptr;
   cudaError_t e = cudaSuccess;
-  if (!p.rotate_k && !pre_rotated) {
+  if (mode == Rot::kRotate && !p.rotate_k) {
     const size_t kr_bytes = static_cast<size_t>(s.n_tot) * s.H * 64 * 2;
     cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(cs, &capture) != cudaSuccess) return NE_ERR_CUDA;
@@ -358,15 +368,23 @@ ne_status run_fwd(const Shape& s, const void* q, const void* k, const void* v, f
     }
     keys = kr;
   }
-  rc = encode_rows(&tq, q, s.n_tot, s.H);
+  rc = encode_rows(&tq, queries, s.n_tot, s.H);
   if (rc == NE_OK) rc = encode_rows(&tk, keys, s.n_tot, s.H);
   if (rc == NE_OK) rc = encode_rows(&tv, v, s.n_tot, s.H);
   // O tile stores (bf16 output only; the fp32 output is written per row).
   if (rc == NE_OK) rc = encode_rows(&to, out_f32 ? q : out, s.n_tot, s.H);
   if (rc == NE_OK) {
-    if (!p.rotate_k && !pre_rotated)
+    if (mode == Rot::kRotate && !p.rotate_k)
       e = ne::launch_rope_rows(static_cast<const __nv_bfloat16*>(k),
-                               static_cast<__nv_bfloat16*>(kr), p.pb, p.rope, cs);
+                               static_cast<__nv_bfloat16*>(kr), nullptr, nullptr, p.pb, p.rope,
+                               cs);
+    else if (mode == Rot::kTrain)
+      e = ne::launch_rope_rows(static_cast<const __nv_bfloat16*>(q),
+                               static_cast<__nv_bfloat16*>(qr_out),
+                               static_cast<const __nv_bfloat16*>(k),
+                               static_cast<__nv_bfloat16*>(kr_out), p.pb, p.rope, cs);
+    const bool pass = (mode == Rot::kRotate && !p.rotate_k) || mode == Rot::kTrain;
+    if (e == cudaSuccess && g_ev_rot && pass) e = cudaEventRecord(g_ev_rot, cs);
     if (e == cudaSuccess) e = ne::launch_fwd(tq, tk, tv, to, p, n_qtiles, cs);
   }
   if (own) {
@@ -379,11 +397,14 @@ ne_status run_fwd(const Shape& s, const void* q, const void* k, const void* v, f
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// pre_rotated: q, k are q', k' already; the gradients returned are w.r.t. them.
+// kRotate: q, k as given; kPreRotated: q, k are q', k' and the gradients
+// returned are w.r.t. them; kTrain: q, k are q', k' (from the training
+// forward) and the gradients returned are w.r.t. the un-rotated q, k.
 ne_status run_bwd(const Shape& s, const void* q, const void* k, const void* v, const void* out,
                   const void* dout, const float* lse, float rope_base, float scale, void* dq,
                   void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream,
-                  bool pre_rotated = false) {
+                  Rot mode = Rot::kRotate) {
+  const bool pre_rotated = mode == Rot::kPreRotated;
   if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return NE_ERR_INVALID_ARG;
   ne_status rc = check_shape(s);
   if (rc != NE_OK) return rc;
@@ -413,7 +434,8 @@ ne_status run_bwd(const Shape& s, const void* q, const void* k, const void* v, c
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = st->status;
-  p.pre_rotated = pre_rotated ? 1 : 0;
+  p.rotate_in = mode == Rot::kRotate ? 1 : 0;
+  p.rotate_out = pre_rotated ? 0 : 1;
   p.rope = RopeTable{nullptr, nullptr, 0};
   if (!pre_rotated && (rc = rope_table(*st, rope_base, n_tiles * 128, &p.rope)) != NE_OK)
     return rc;
@@ -438,7 +460,7 @@ ne_status run_bwd(const Shape& s, const void* q, const void* k, const void* v, c
   p.kr = reinterpret_cast<__nv_bfloat16*>(wsb + acc_bytes + del_bytes + rot_bytes);
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k = static_cast<const __nv_bfloat16*>(k);
-  if (pre_rotated) {  // the main kernel reads q', k' where the caller keeps them
+  if (!p.rotate_in) {  // the main kernel reads q', k' where the caller keeps them
     p.qr = const_cast<__nv_bfloat16*>(p.q);
     p.kr = const_cast<__nv_bfloat16*>(p.k);
   }
@@ -586,7 +608,7 @@ ne_status ne_attn_fwd_rotated(const ne_bf16* qr, const ne_bf16* kr, const ne_bf1
   s.H = H;
   s.D = D;
   if (B > 0 && T > 0 && static_cast<long long>(B) * T > (1LL << 31) - 1) return NE_ERR_INVALID_ARG;
-  return run_fwd(s, qr, kr, v, 0.f, scale, out, 0, lse, stream, true);
+  return run_fwd(s, qr, kr, v, 0.f, scale, out, 0, lse, stream, Rot::kPreRotated);
 }
 
 ne_status ne_attn_bwd_rotated(const ne_bf16* qr, const ne_bf16* kr, const ne_bf16* v,
@@ -601,7 +623,69 @@ ne_status ne_attn_bwd_rotated(const ne_bf16* qr, const ne_bf16* kr, const ne_bf1
   s.D = D;
   if (B > 0 && T > 0 && static_cast<long long>(B) * T > (1LL << 31) - 1) return NE_ERR_INVALID_ARG;
   return run_bwd(s, qr, kr, v, out, dout, lse, 0.f, scale, dqr, dkr, dv, workspace,
-                 workspace_bytes, stream, true);
+                 workspace_bytes, stream, Rot::kPreRotated);
+}
+
+ne_status ne_attn_fwd_train(const ne_bf16* q, const ne_bf16* k, const ne_bf16* v, int B, int H,
+                            int T, int D, float rope_base, float scale, ne_bf16* out, float* lse,
+                            ne_bf16* qr, ne_bf16* kr, void* stream) {
+  Shape s;
+  s.nseq = B;
+  s.max_len = T;
+  s.n_tot = (B > 0 && T > 0) ? B * T : 0;
+  s.H = H;
+  s.D = D;
+  if (B > 0 && T > 0 && static_cast<long long>(B) * T > (1LL << 31) - 1) return NE_ERR_INVALID_ARG;
+  return run_fwd(s, q, k, v, rope_base, scale, out, 0, lse, stream, Rot::kTrain, qr, kr);
+}
+
+ne_status ne_attn_bwd_train(const ne_bf16* qr, const ne_bf16* kr, const ne_bf16* v,
+                            const ne_bf16* out, const ne_bf16* dout, const float* lse, int B,
+                            int H, int T, int D, float rope_base, float scale, ne_bf16* dq,
+                            ne_bf16* dk, ne_bf16* dv, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  Shape s;
+  s.nseq = B;
+  s.max_len = T;
+  s.n_tot = (B > 0 && T > 0) ? B * T : 0;
+  s.H = H;
+  s.D = D;
+  if (B > 0 && T > 0 && static_cast<long long>(B) * T > (1LL << 31) - 1) return NE_ERR_INVALID_ARG;
+  return run_bwd(s, qr, kr, v, out, dout, lse, rope_base, scale, dq, dk, dv, workspace,
+                 workspace_bytes, stream, Rot::kTrain);
+}
+
+ne_status ne_attn_varlen_fwd_train(const ne_bf16* q, const ne_bf16* k, const ne_bf16* v,
+                                   const int* cu_seqlens, int nseq, int n_tot, int max_seqlen,
+                                   int H, int D, float rope_base, float scale, ne_bf16* out,
+                                   float* lse, ne_bf16* qr, ne_bf16* kr, void* stream) {
+  Shape s;
+  s.cu = cu_seqlens;
+  s.fixed = false;
+  s.nseq = nseq;
+  s.n_tot = n_tot;
+  s.max_len = max_seqlen;
+  s.H = H;
+  s.D = D;
+  return run_fwd(s, q, k, v, rope_base, scale, out, 0, lse, stream, Rot::kTrain, qr, kr);
+}
+
+ne_status ne_attn_varlen_bwd_train(const ne_bf16* qr, const ne_bf16* kr, const ne_bf16* v,
+                                   const ne_bf16* out, const ne_bf16* dout, const float* lse,
+                                   const int* cu_seqlens, int nseq, int n_tot, int max_seqlen,
+                                   int H, int D, float rope_base, float scale, ne_bf16* dq,
+                                   ne_bf16* dk, ne_bf16* dv, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  Shape s;
+  s.cu = cu_seqlens;
+  s.fixed = false;
+  s.nseq = nseq;
+  s.n_tot = n_tot;
+  s.max_len = max_seqlen;
+  s.H = H;
+  s.D = D;
+  return run_bwd(s, qr, kr, v, out, dout, lse, rope_base, scale, dq, dk, dv, workspace,
+                 workspace_bytes, stream, Rot::kTrain);
 }
 
 ne_status ne_attn_varlen_bwd(const ne_bf16* q, const ne_bf16* k, const ne_bf16* v,
@@ -755,6 +839,12 @@ ne_status ne_attn_set_bwd_phase_events(void* ev_after_preprocess, void* ev_after
   if ((ev_after_preprocess == nullptr) != (ev_after_main == nullptr)) return NE_ERR_INVALID_ARG;
   g_ev_pre = static_cast<cudaEvent_t>(ev_after_preprocess);
   g_ev_main = static_cast<cudaEvent_t>(ev_after_main);
+  return NE_OK;
+}
+
+ne_status ne_attn_set_fwd_phase_event(void* ev_after_rotation) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  g_ev_rot = static_cast<cudaEvent_t>(ev_after_rotation);
   return NE_OK;
 }
 

@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(256)
                                   const __nv_bfloat16* __restrict__ dout,
                                   __nv_bfloat16* __restrict__ qr, __nv_bfloat16* __restrict__ kr,
                                   float* __restrict__ delta, float* __restrict__ dq_acc,
-                                  const Problem pb, RopeTable rope, int pre_rotated) {
+                                  const Problem pb, RopeTable rope, int rotate_in) {
   pdl_wait();  // the forward that wrote O (and anything before it) has completed
   const int seq = blockIdx.y;
   int start, len;
@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(256)
       // RoPE of one chunk pair of q (parts 0-3) or k (parts 4-7); nothing to
       // do when the caller passed q', k' already rotated.
       const int c = part & 3;
-      if (!pre_rotated) {
+      if (rotate_in) {
       const __nv_bfloat16* src = (part < 4 ? q : k) + pair * kHD;
       __nv_bfloat16* dst = (part < 4 ? qr : kr) + pair * kHD;
       const uint4 lo = __ldg(reinterpret_cast<const uint4*>(src) + c);
@@ -863,7 +863,7 @@ __device__ __forceinline__ void dk_rotate_item(__nv_bfloat16* __restrict__ dk, c
 __global__ void __launch_bounds__(kPostThreads)
     ne_attn_dq_postprocess_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq,
                                   __nv_bfloat16* __restrict__ dk, const Problem pb, RopeTable rope,
-                                  float scale, int pre_rotated) {
+                                  float scale, int rotate_out) {
   pdl_wait();  // the main kernel's dQ' reduce-adds and dK stores have completed
   const int seq = blockIdx.y;
   int start, len;
@@ -885,7 +885,7 @@ __global__ void __launch_bounds__(kPostThreads)
   const float a[4] = {lo.x * scale, lo.y * scale, lo.z * scale, lo.w * scale};
   const float b[4] = {hi.x * scale, hi.y * scale, hi.z * scale, hi.w * scale};
   float go[4], gh[4];
-  if (pre_rotated) {  // the gradient w.r.t. q' itself
+  if (!rotate_out) {  // the gradient w.r.t. q' itself
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       go[i] = a[i];
@@ -925,7 +925,7 @@ cudaError_t launch_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
   dim3 pre_grid((n_tiles * kBM + bwd::kPreRows - 1) / bwd::kPreRows, p.pb.nseq);
   cudaError_t e = launch_pdl(ne_attn_bwd_preprocess_kernel, pre_grid, dim3(256), 0, stream, p.q,
                              p.k, p.out, p.dout, p.qr, p.kr, p.delta, p.dq_acc, p.pb, p.rope,
-                             p.pre_rotated);
+                             p.rotate_in);
   if (e != cudaSuccess) return e;
   if (ev_pre && (e = cudaEventRecord(ev_pre, stream)) != cudaSuccess) return e;
   // One persistent CTA per SM (at most one per unit).
@@ -944,12 +944,12 @@ cudaError_t launch_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
   if (ev_main && (e = cudaEventRecord(ev_main, stream)) != cudaSuccess) return e;
   const long long post_items = static_cast<long long>(n_tiles) * kBM * p.pb.H * kPostParts;
   // Layer z = 0: dQ from the accumulator; z = 1: dK rotated in place (not
-  // for pre-rotated inputs, whose dK' the main kernel already wrote).
+  // when the gradient w.r.t. k' is asked for: the main kernel wrote it).
   dim3 pgrid(static_cast<unsigned>((post_items + kPostThreads - 1) / kPostThreads), p.pb.nseq,
-             p.pre_rotated ? 1 : 2);
+             p.rotate_out ? 2 : 1);
   return launch_pdl(ne_attn_dq_postprocess_kernel, pgrid, dim3(kPostThreads), 0, stream,
                     static_cast<const float*>(p.dq_acc), p.dq, p.dk, p.pb, p.rope, p.scale,
-                    p.pre_rotated);
+                    p.rotate_out);
 }
 
 }  // namespace ne

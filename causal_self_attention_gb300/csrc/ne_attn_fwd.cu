@@ -15,7 +15,9 @@
 // that uses them (kRotateK = 1, short sequences: no extra pass), or once
 // per call by a small pass that runs first (ne_attn_rope_rows_kernel,
 // k' = R(n) k, bf16; kRotateK = 0, long sequences, where rotating each key
-// tile several times -- its table loads -- paces the kernel).
+// tile several times -- its table loads -- paces the kernel).  The training
+// forward rotates queries and keys in that pass, into buffers the caller
+// keeps for the backward, and the kernel then rotates nothing (kRotateQ = 0).
 //
 // The kernel is persistent: one CTA per SM walks the items (longest first,
 // dealt out in a snake order over the CTAs), keeping its TMEM, barriers and
@@ -653,21 +655,26 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Key rotation pass: kr = R(n) k for every row n of every sequence (positions
-// restart at 0 per sequence), bf16 in and out, with the fp32 rule of the
-// in-tile rotation (lo = fma(x_i, c, -(x_{i+32} s)), hi = fma(x_{i+32}, c,
-// x_i s), round to nearest even) and the same table, so the attention kernel
-// multiplies bitwise the operands an in-tile rotation would have produced.
-// Grid (blocks of 256 items, sequences); an item is (row, head, part): part c
+// Rotation pass: xr = R(n) x for every row n of every sequence (positions
+// restart at 0 per sequence), for the keys alone (k' of a long-sequence
+// forward) or for queries and keys together (q', k' of the training forward),
+// bf16 in and out, with the fp32 rule of the in-tile rotation (lo = fma(x_i,
+// c, -(x_{i+32} s)), hi = fma(x_{i+32}, c, x_i s), round to nearest even) and
+// the same table, so the attention kernel multiplies bitwise the operands an
+// in-tile rotation would have produced.
+// Grid (blocks of 256 items, sequences, tensors); an item is (row, head, part): part c
 // rotates the 16-byte chunk c (dims 8c..8c+7) against chunk c + 4 (dims
 // 32+8c..32+8c+7), so a warp moves eight whole 128-byte rows.
 // ---------------------------------------------------------------------------
 constexpr int kRopeThreads = 256, kRopeParts = 4;
 
 __global__ void __launch_bounds__(kRopeThreads)
-    ne_attn_rope_rows_kernel(const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ xr,
+    ne_attn_rope_rows_kernel(const __nv_bfloat16* __restrict__ x0, __nv_bfloat16* __restrict__ xr0,
+                             const __nv_bfloat16* __restrict__ x1, __nv_bfloat16* __restrict__ xr1,
                              const Problem pb, RopeTable rope) {
-  pdl_wait();  // the kernel that wrote k (and anything before it) has completed
+  pdl_wait();  // the kernel that wrote q, k (and anything before it) has completed
+  const __nv_bfloat16* __restrict__ x = blockIdx.z ? x1 : x0;
+  __nv_bfloat16* __restrict__ xr = blockIdx.z ? xr1 : xr0;
   const int seq = blockIdx.y;
   int start, len;
   if (!seq_bounds(pb, seq, start, len, nullptr)) return;
@@ -702,12 +709,15 @@ __global__ void __launch_bounds__(kRopeThreads)
   pdl_launch_dependents();
 }
 
-cudaError_t launch_rope_rows(const __nv_bfloat16* x, __nv_bfloat16* xr, const Problem& pb,
+// x1, xr1: a second tensor rotated by the same launch, or null.
+cudaError_t launch_rope_rows(const __nv_bfloat16* x0, __nv_bfloat16* xr0,
+                             const __nv_bfloat16* x1, __nv_bfloat16* xr1, const Problem& pb,
                              const RopeTable& rope, cudaStream_t stream) {
   const long long items = static_cast<long long>(pb.max_len) * pb.H * kRopeParts;
-  dim3 grid(static_cast<unsigned>((items + kRopeThreads - 1) / kRopeThreads), pb.nseq);
-  return launch_pdl(ne_attn_rope_rows_kernel, grid, dim3(kRopeThreads), 0, stream, x, xr, pb,
-                    rope);
+  dim3 grid(static_cast<unsigned>((items + kRopeThreads - 1) / kRopeThreads), pb.nseq,
+            x1 ? 2 : 1);
+  return launch_pdl(ne_attn_rope_rows_kernel, grid, dim3(kRopeThreads), 0, stream, x0, xr0, x1,
+                    xr1, pb, rope);
 }
 
 cudaError_t launch_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,

@@ -134,7 +134,8 @@ extern "C" ne_status ne_attn_bwd_noalloc(const ne_bf16* q, const ne_bf16* k, con
   p.rope.cs = reinterpret_cast<const float2*>(nd.scratch);
   p.rope.csw = nullptr;  // the backward reads the row layout only
   p.rope.capacity = kMaxPositions;
-  p.pre_rotated = 0;
+  p.rotate_in = 1;
+  p.rotate_out = 1;
   // The preprocess kernel of every call zeroes the dQ' accumulator and
   // overwrites D_m, q' and k', so nothing left by an earlier call is read.
   const size_t acc_bytes = align256(static_cast<size_t>(rows) * 64 * sizeof(float));

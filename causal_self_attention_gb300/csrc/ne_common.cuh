@@ -76,8 +76,10 @@ struct BwdParams {
   float scale_log2;
   RopeTable rope;
   int* status;
-  int pre_rotated;  // 1: q, k are q', k' already; no rotation anywhere, and the
-                    // gradients returned are those w.r.t. q', k'
+  int rotate_in;   // 1: the preprocess writes q' = R(m) q, k' = R(n) k into the
+                   // workspace; 0: q, k are q', k' already (the caller's)
+  int rotate_out;  // 1: the postprocess returns dq = R(m)^T dq', dk = R(n)^T dk';
+                   // 0: the gradients w.r.t. q', k' themselves
 };
 
 // Sequence bounds of sequence s.  Returns false (and raises the device status)

@@ -30,7 +30,9 @@ EXPORTED = ("ne_attn_fwd", "ne_attn_fwd_f32out", "ne_attn_bwd", "ne_attn_bwd_wor
             "ne_attn_last_device_code", "ne_status_string",
             "ne_attn_release", "ne_debug_tma_tile", "ne_debug_rope_tile", "ne_debug_umma",
             "ne_debug_pipeline", "ne_rmsnorm_qkv_rope", "ne_out_proj_residual",
-            "ne_attn_fwd_rotated", "ne_attn_bwd_rotated")
+            "ne_attn_fwd_rotated", "ne_attn_bwd_rotated", "ne_attn_fwd_train",
+            "ne_attn_bwd_train", "ne_attn_varlen_fwd_train", "ne_attn_varlen_bwd_train",
+            "ne_attn_set_fwd_phase_event")
 
 
 class NeAttnError(RuntimeError):
@@ -75,6 +77,12 @@ def lib():
         "ne_out_proj_residual": [P, P, P, I, I, P, P],
         "ne_attn_fwd_rotated": [P, P, P, I, I, I, I, F, P, P, P],
         "ne_attn_bwd_rotated": [P, P, P, P, P, P, I, I, I, I, F, P, P, P, P, Z, P],
+        "ne_attn_fwd_train": [P, P, P, I, I, I, I, F, F, P, P, P, P, P],
+        "ne_attn_bwd_train": [P, P, P, P, P, P, I, I, I, I, F, F, P, P, P, P, Z, P],
+        "ne_attn_varlen_fwd_train": [P, P, P, P, I, I, I, I, I, F, F, P, P, P, P, P],
+        "ne_attn_varlen_bwd_train": [P, P, P, P, P, P, P, I, I, I, I, I, F, F, P, P, P, P, Z,
+                                     P],
+        "ne_attn_set_fwd_phase_event": [P],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -322,6 +330,93 @@ def ne_attn_decode(q, k_cache, v_cache, pos, rope_base=10000.0, scale=None, out=
                                 float(rope_base), float(scale), _ptr(out), _ptr(lse),
                                 _ptr(workspace), ws_bytes, _stream(stream)))
     return out, lse
+
+
+def ne_attn_fwd_train(q, k, v, rope_base=10000.0, scale=None, out=None, lse=None, qr=None,
+                      kr=None, stream=None):
+    """Training forward on ``[B, T, H, 64]`` bf16 tensors: as :func:`ne_attn_fwd`,
+    and also returns the rotated operands it computed once, for the backward.
+    Returns ``(out, lse, qr, kr)``."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, torch.bfloat16, n)
+    B, T, H, D = q.shape
+    scale = D ** -0.5 if scale is None else scale
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    qr = torch.empty_like(q) if qr is None else qr
+    kr = torch.empty_like(k) if kr is None else kr
+    _check("ne_attn_fwd_train", lib().ne_attn_fwd_train(
+        _ptr(q), _ptr(k), _ptr(v), B, H, T, D, float(rope_base), float(scale), _ptr(out),
+        _ptr(lse), _ptr(qr), _ptr(kr), _stream(stream)))
+    return out, lse, qr, kr
+
+
+def ne_attn_bwd_train(qr, kr, v, out, dout, lse, rope_base=10000.0, scale=None, dq=None,
+                      dk=None, dv=None, workspace=None, stream=None):
+    """Backward of :func:`ne_attn_fwd_train` from its ``qr``, ``kr``.  Returns
+    ``(dq, dk, dv)``: gradients w.r.t. the un-rotated q, k and v."""
+    for t, n in ((qr, "qr"), (kr, "kr"), (v, "v"), (out, "out"), (dout, "dout")):
+        _need(t, torch.bfloat16, n)
+    _need(lse, torch.float32, "lse")
+    B, T, H, D = qr.shape
+    scale = D ** -0.5 if scale is None else scale
+    dq = torch.empty_like(qr) if dq is None else dq
+    dk = torch.empty_like(kr) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("ne_attn_bwd_train", lib().ne_attn_bwd_train(
+        _ptr(qr), _ptr(kr), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), B, H, T, D,
+        float(rope_base), float(scale), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+        ws_bytes, _stream(stream)))
+    return dq, dk, dv
+
+
+def ne_attn_varlen_fwd_train(q, k, v, cu_seqlens, max_seqlen, rope_base=10000.0, scale=None,
+                             out=None, lse=None, qr=None, kr=None, stream=None):
+    """Training forward on packed ``[N_tot, H, 64]`` tensors.  Returns
+    ``(out, lse, qr, kr)`` with ``lse`` ``[H, N_tot]``."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, torch.bfloat16, n)
+    _need(cu_seqlens, torch.int32, "cu_seqlens")
+    N, H, D = q.shape
+    scale = D ** -0.5 if scale is None else scale
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    qr = torch.empty_like(q) if qr is None else qr
+    kr = torch.empty_like(k) if kr is None else kr
+    _check("ne_attn_varlen_fwd_train", lib().ne_attn_varlen_fwd_train(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), cu_seqlens.numel() - 1, N, int(max_seqlen),
+        H, D, float(rope_base), float(scale), _ptr(out), _ptr(lse), _ptr(qr), _ptr(kr),
+        _stream(stream)))
+    return out, lse, qr, kr
+
+
+def ne_attn_varlen_bwd_train(qr, kr, v, out, dout, lse, cu_seqlens, max_seqlen,
+                             rope_base=10000.0, scale=None, dq=None, dk=None, dv=None,
+                             workspace=None, stream=None):
+    """Backward of :func:`ne_attn_varlen_fwd_train`.  Returns ``(dq, dk, dv)``."""
+    for t, n in ((qr, "qr"), (kr, "kr"), (v, "v"), (out, "out"), (dout, "dout")):
+        _need(t, torch.bfloat16, n)
+    _need(lse, torch.float32, "lse")
+    _need(cu_seqlens, torch.int32, "cu_seqlens")
+    N, H, D = qr.shape
+    scale = D ** -0.5 if scale is None else scale
+    dq = torch.empty_like(qr) if dq is None else dq
+    dk = torch.empty_like(kr) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("ne_attn_varlen_bwd_train", lib().ne_attn_varlen_bwd_train(
+        _ptr(qr), _ptr(kr), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(cu_seqlens),
+        cu_seqlens.numel() - 1, N, int(max_seqlen), H, D, float(rope_base), float(scale),
+        _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), ws_bytes, _stream(stream)))
+    return dq, dk, dv
+
+
+def ne_attn_set_fwd_phase_event(ev_after_rotation=None) -> None:
+    """Record the given torch.cuda.Event between the rotation pass and the
+    attention kernel of every following forward that runs such a pass (None: off)."""
+    a = ctypes.c_void_p(ev_after_rotation.cuda_event) if ev_after_rotation else None
+    _check("ne_attn_set_fwd_phase_event", lib().ne_attn_set_fwd_phase_event(a))
 
 
 def ne_attn_set_bwd_phase_events(ev_after_preprocess=None, ev_after_main=None) -> None:

@@ -117,6 +117,28 @@ ne_status ne_attn_bwd_rotated(const ne_bf16* qr, const ne_bf16* kr, const ne_bf1
                               int H, int T, int D, float scale, ne_bf16* dqr, ne_bf16* dkr,
                               ne_bf16* dv, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Training pair: the forward keeps the rotated operands for the backward, so
+ * RoPE is applied to q and k once per training step instead of once in the
+ * forward and again in the backward.  ne_attn_fwd_train takes the un-rotated
+ * q, k, v (arguments as in ne_attn_fwd) and also writes qr = R(m) q and
+ * kr = R(n) k (bf16 [B, T, H, 64], 16-byte aligned, caller-owned; the same
+ * bf16 values ne_attn_fwd forms internally); O and LSE are bitwise those of
+ * ne_attn_fwd.  ne_attn_bwd_train takes those qr, kr in place of q, k (q, k
+ * themselves are not needed) with the other arguments as in ne_attn_bwd, and
+ * returns dq, dk w.r.t. the UN-rotated q, k and dv -- bitwise what
+ * ne_attn_bwd returns on q, k (dq up to its fp32 accumulation order).  The
+ * workspace of ne_attn_bwd_workspace_bytes is enough (its q', k' part goes
+ * unused).  qr, kr must be left as the forward wrote them; the gradients are
+ * computed from them as they are. */
+ne_status ne_attn_fwd_train(const ne_bf16* q, const ne_bf16* k, const ne_bf16* v, int B, int H,
+                            int T, int D, float rope_base, float scale, ne_bf16* out, float* lse,
+                            ne_bf16* qr, ne_bf16* kr, void* stream);
+ne_status ne_attn_bwd_train(const ne_bf16* qr, const ne_bf16* kr, const ne_bf16* v,
+                            const ne_bf16* out, const ne_bf16* dout, const float* lse, int B,
+                            int H, int T, int D, float rope_base, float scale, ne_bf16* dq,
+                            ne_bf16* dk, ne_bf16* dv, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
 /* Forward, packed variable-length batch.  Sequence s occupies rows
  * cu_seqlens[s] .. cu_seqlens[s+1]-1 of q, k, v, out ([n_tot, H, 64] bf16);
  * cu_seqlens is DEVICE int32 [nseq + 1], nondecreasing, cu_seqlens[0] = 0,
@@ -145,13 +167,34 @@ ne_status ne_attn_varlen_bwd(const ne_bf16* q, const ne_bf16* k, const ne_bf16* 
                              int D, float rope_base, float scale, ne_bf16* dq, ne_bf16* dk,
                              ne_bf16* dv, void* workspace, size_t workspace_bytes, void* stream);
 
+/* The training pair (see ne_attn_fwd_train) for packed variable-length
+ * batches; qr, kr: [n_tot, H, 64] bf16, positions restarting at 0 in every
+ * sequence; other arguments as in ne_attn_varlen_fwd / ne_attn_varlen_bwd. */
+ne_status ne_attn_varlen_fwd_train(const ne_bf16* q, const ne_bf16* k, const ne_bf16* v,
+                                   const int* cu_seqlens, int nseq, int n_tot, int max_seqlen,
+                                   int H, int D, float rope_base, float scale, ne_bf16* out,
+                                   float* lse, ne_bf16* qr, ne_bf16* kr, void* stream);
+ne_status ne_attn_varlen_bwd_train(const ne_bf16* qr, const ne_bf16* kr, const ne_bf16* v,
+                                   const ne_bf16* out, const ne_bf16* dout, const float* lse,
+                                   const int* cu_seqlens, int nseq, int n_tot, int max_seqlen,
+                                   int H, int D, float rope_base, float scale, ne_bf16* dq,
+                                   ne_bf16* dk, ne_bf16* dv, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
 /* Timing hook for profilers and benchmarks.  When set (non-NULL cudaEvent_t
  * handles created by the caller on the current device), every following
- * ne_attn_bwd / ne_attn_varlen_bwd call records ev_after_preprocess right
- * after its preprocess kernel and ev_after_main right after its main kernel,
- * on the call's stream, so the three backward kernels can be timed apart.
- * Pass NULL, NULL to turn it off.  Process-wide; not for concurrent callers. */
+ * backward call (ne_attn_bwd, ne_attn_varlen_bwd and their _rotated / _train
+ * forms) records ev_after_preprocess right after its preprocess kernel and
+ * ev_after_main right after its main kernel, on the call's stream, so the
+ * three backward kernels can be timed apart.  Pass NULL, NULL to turn it off.
+ * Process-wide; not for concurrent callers. */
 ne_status ne_attn_set_bwd_phase_events(void* ev_after_preprocess, void* ev_after_main);
+
+/* The same for the forward: every following forward call that runs a
+ * rotation pass before its attention kernel (the _train forms; ne_attn_fwd
+ * from 2048 positions on) records ev_after_rotation between the two.  NULL
+ * turns it off. */
+ne_status ne_attn_set_fwd_phase_event(void* ev_after_rotation);
 
 /* Backward that allocates no device memory at all, for callers that cannot
  * call cudaMalloc (or let a library do it for them): for example code running

@@ -74,6 +74,30 @@ def test_argument_errors_return_before_any_launch(lib):
     assert lib.ne_attn_fwd(fake, fake, fake, 1, 1, 64, 64, -1.0, 0.125, fake, fake, None) == 1
 
 
+def test_training_pair_argument_errors_return_before_any_launch(lib):
+    P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.ne_attn_fwd_train.argtypes = [P, P, P, I, I, I, I, F, F, P, P, P, P, P]
+    lib.ne_attn_bwd_train.argtypes = [P, P, P, P, P, P, I, I, I, I, F, F, P, P, P, P, Z, P]
+    fake = P(0x10000)  # never dereferenced: every case below fails its host check first
+
+    def fwd(qr=fake, kr=fake, base=10000.0):
+        return lib.ne_attn_fwd_train(fake, fake, fake, 1, 1, 64, 64, base, 0.125, fake, fake, qr,
+                                     kr, None)
+
+    assert fwd(qr=None) == 1          # the rotated outputs are required
+    assert fwd(kr=None) == 1
+    assert fwd(kr=P(0x10004)) == 3    # and 16-byte aligned
+    assert fwd(base=0.0) == 1         # the pass needs a valid rope base
+
+    def bwd(qr=fake, base=10000.0, ws=None, ws_bytes=0):
+        return lib.ne_attn_bwd_train(qr, fake, fake, fake, fake, fake, 1, 1, 64, 64, base, 0.125,
+                                     fake, fake, fake, ws, ws_bytes, None)
+
+    assert bwd(qr=None) == 1
+    assert bwd(base=float("nan")) == 1  # dq, dk are returned un-rotated: the base is used
+    assert bwd(ws=fake, ws_bytes=16) == 1
+
+
 def test_decode_argument_errors_return_before_any_launch(lib):
     P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.ne_attn_decode.argtypes = [P, P, P, P, I, I, I, I, F, F, P, P, P, Z, P]
