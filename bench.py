@@ -1,9 +1,12 @@
 #!/usr/bin/env python
 """Benchmark of causal RoPE self-attention forward + backward on GB300.
 
-One step = ne_attn_fwd + ne_attn_bwd (all kernels of the path) over one batch
-of the GPT-2-small training shape, B=8, H=12, T=1024, D=64, bf16 inputs drawn
-N(0,1) from a fixed seed, inputs resident in HBM.  The L2 is flushed (a 512 MiB
+One step = the training pair ne_attn_fwd_train + ne_attn_bwd_train (all
+kernels of the path: the q, k rotation pass, the forward, the backward's
+preprocess, main kernel and postprocess) over one batch of the GPT-2-small
+training shape, B=8, H=12, T=1024, D=64, bf16 inputs drawn N(0,1) from a fixed
+seed, inputs resident in HBM.  The plain pair ne_attn_fwd + ne_attn_bwd (same
+results, RoPE applied in both directions) is timed beside it.  The L2 is flushed (a 512 MiB
 write) between timed steps, outside the timed region.  Throughput counts the
 causal FLOPs: 2*B*H*T^2*D forward plus 2.5x that backward.
 
@@ -281,42 +284,41 @@ def bench_workloads(args, dev, stream, flush, peak_tf):
         ws = torch.empty(na.ne_attn_bwd_workspace_bytes(N, H, D), dtype=torch.uint8, device=dev)
         out = torch.empty_like(q)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        qr, kr = torch.empty_like(q), torch.empty_like(k)
         if "cu_seqlens" in inp:
             cu, mx = inp["cu_seqlens"].to(dev), inp["max_seqlen"]
             lse = torch.empty((H, N), dtype=torch.float32, device=dev)
 
-            def step():
-                na.ne_attn_varlen_fwd(q, k, v, cu, mx, base, scale, out=out, lse=lse,
-                                      stream=stream)
-                na.ne_attn_varlen_bwd(q, k, v, out, do, lse, cu, mx, base, scale, dq=dq, dk=dk,
-                                      dv=dv, workspace=ws, stream=stream)
+            def fwd():
+                na.ne_attn_varlen_fwd_train(q, k, v, cu, mx, base, scale, out=out, lse=lse,
+                                            qr=qr, kr=kr, stream=stream)
+
+            def bwd():
+                na.ne_attn_varlen_bwd_train(qr, kr, v, out, do, lse, cu, mx, base, scale,
+                                            dq=dq, dk=dk, dv=dv, workspace=ws, stream=stream)
         else:
             B, T = inp["B"], inp["T"]
             lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
 
-            def step():
-                na.ne_attn_fwd(q, k, v, base, scale, out=out, lse=lse, stream=stream)
-                na.ne_attn_bwd(q, k, v, out, do, lse, base, scale, dq=dq, dk=dk, dv=dv,
-                               workspace=ws, stream=stream)
+            def fwd():
+                na.ne_attn_fwd_train(q, k, v, base, scale, out=out, lse=lse, qr=qr, kr=kr,
+                                     stream=stream)
+
+            def bwd():
+                na.ne_attn_bwd_train(qr, kr, v, out, do, lse, base, scale, dq=dq, dk=dk, dv=dv,
+                                     workspace=ws, stream=stream)
         for _ in range(3):
             flush.zero_()
-            step()
+            fwd()
+            bwd()
         n = max(args.extra_steps, 3)
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
         for e in ev:
             flush.zero_()
             e[0].record(stream)
-            if "cu_seqlens" in inp:
-                na.ne_attn_varlen_fwd(q, k, v, cu, mx, base, scale, out=out, lse=lse,
-                                      stream=stream)
-                e[1].record(stream)
-                na.ne_attn_varlen_bwd(q, k, v, out, do, lse, cu, mx, base, scale, dq=dq, dk=dk,
-                                      dv=dv, workspace=ws, stream=stream)
-            else:
-                na.ne_attn_fwd(q, k, v, base, scale, out=out, lse=lse, stream=stream)
-                e[1].record(stream)
-                na.ne_attn_bwd(q, k, v, out, do, lse, base, scale, dq=dq, dk=dk, dv=dv,
-                               workspace=ws, stream=stream)
+            fwd()
+            e[1].record(stream)
+            bwd()
             e[2].record(stream)
         torch.cuda.synchronize()
         assert na.ne_attn_get_device_status() == 0
@@ -337,7 +339,7 @@ def bench_workloads(args, dev, stream, flush, peak_tf):
             "fwd_tflops_at_median": f_fwd / (statistics.median(t_f) * 1e-3) / 1e12,
             "bwd_tflops_at_median": f_bwd / (statistics.median(t_b) * 1e-3) / 1e12,
         }
-        del q, k, v, do, ws, out, dq, dk, dv, lse
+        del q, k, v, do, ws, out, dq, dk, dv, lse, qr, kr
     return res
 
 
@@ -468,18 +470,29 @@ def run_ours(args):
     out = torch.empty_like(q)
     lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    qr, kr = torch.empty_like(q), torch.empty_like(k)  # rotated operands kept for the backward
     ws = torch.empty(na.ne_attn_bwd_workspace_bytes(B * T, H, D), dtype=torch.uint8, device=dev)
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step():
+    def fwd():
+        na.ne_attn_fwd_train(q, k, v, base, scale, out=out, lse=lse, qr=qr, kr=kr, stream=stream)
+
+    def bwd():
+        na.ne_attn_bwd_train(qr, kr, v, out, do, lse, base, scale, dq=dq, dk=dk, dv=dv,
+                             workspace=ws, stream=stream)
+
+    def plain_step():
         na.ne_attn_fwd(q, k, v, base, scale, out=out, lse=lse, stream=stream)
         na.ne_attn_bwd(q, k, v, out, do, lse, base, scale, dq=dq, dk=dk, dv=dv, workspace=ws,
                        stream=stream)
 
     for _ in range(max(args.warmup, 3)):
         flush.zero_()
-        step()
+        fwd()
+        bwd()
+        flush.zero_()
+        plain_step()
     torch.cuda.synchronize()
     assert na.ne_attn_get_device_status() == 0
 
@@ -502,9 +515,8 @@ def run_ours(args):
         e = ev[i]
         flush.zero_()
         e[0].record(stream)
-        na.ne_attn_fwd(q, k, v, base, scale, out=out, lse=lse, stream=stream)
-        na.ne_attn_bwd(q, k, v, out, do, lse, base, scale, dq=dq, dk=dk, dv=dv, workspace=ws,
-                       stream=stream)
+        fwd()
+        bwd()
         e[1].record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -520,28 +532,42 @@ def run_ours(args):
     # Per-kernel breakdown (outside the timed region): the same steps with an
     # event between every two kernels, which times each kernel on its own.
     KB = min(K, 300)
-    evb = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(KB)]
-    for e in evb:  # the library records two of them: torch must have created them first
+    evb = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(KB)]
+    for e in evb:  # the library records three of them: torch must have created them first
         for x in e:
             x.record(stream)
     for i in range(KB):
         e = evb[i]
         flush.zero_()
-        na.ne_attn_set_bwd_phase_events(e[2], e[3])
+        na.ne_attn_set_fwd_phase_event(e[1])
+        na.ne_attn_set_bwd_phase_events(e[3], e[4])
         e[0].record(stream)
-        na.ne_attn_fwd(q, k, v, base, scale, out=out, lse=lse, stream=stream)
-        e[1].record(stream)
-        na.ne_attn_bwd(q, k, v, out, do, lse, base, scale, dq=dq, dk=dk, dv=dv, workspace=ws,
-                       stream=stream)
-        e[4].record(stream)
+        fwd()
+        e[2].record(stream)
+        bwd()
+        e[5].record(stream)
     torch.cuda.synchronize()
+    na.ne_attn_set_fwd_phase_event(None)
     na.ne_attn_set_bwd_phase_events(None, None)
     status = status or na.ne_attn_get_device_status()
-    t_fwd = [e[0].elapsed_time(e[1]) for e in evb]
-    t_pre = [e[1].elapsed_time(e[2]) for e in evb]
-    t_main = [e[2].elapsed_time(e[3]) for e in evb]
-    t_post = [e[3].elapsed_time(e[4]) for e in evb]
-    t_sep = [e[0].elapsed_time(e[4]) for e in evb]
+    t_rot = [e[0].elapsed_time(e[1]) for e in evb]
+    t_fwd = [e[1].elapsed_time(e[2]) for e in evb]
+    t_pre = [e[2].elapsed_time(e[3]) for e in evb]
+    t_main = [e[3].elapsed_time(e[4]) for e in evb]
+    t_post = [e[4].elapsed_time(e[5]) for e in evb]
+    t_sep = [e[0].elapsed_time(e[5]) for e in evb]
+
+    # The plain pair (RoPE inside both directions), for comparison.
+    KP = min(K, 300)
+    evp = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(KP)]
+    for e in evp:
+        flush.zero_()
+        e[0].record(stream)
+        plain_step()
+        e[1].record(stream)
+    torch.cuda.synchronize()
+    status = status or na.ne_attn_get_device_status()
+    t_plain = [e[0].elapsed_time(e[1]) for e in evp]
 
     # ---- end to end through the public API with host buffers ------------------
     # Every step uploads its q, k, v, dO from pinned host memory and downloads
@@ -563,7 +589,8 @@ def run_ours(args):
     s_comp = stream
     sets = []
     for _ in range(2):
-        d = {n: torch.empty_like(q) for n in ("q", "k", "v", "dout", "out", "dq", "dk", "dv")}
+        d = {n: torch.empty_like(q)
+             for n in ("q", "k", "v", "dout", "out", "dq", "dk", "dv", "qr", "kr")}
         d["lse"] = torch.empty_like(lse)
         sets.append(d)
 
@@ -587,10 +614,11 @@ def run_ours(args):
             if i >= 2:
                 for c in range(2):
                     s_comp.wait_event(ev_out[i - 2][c])  # step i-2's results have been read out
-            na.ne_attn_fwd(d["q"], d["k"], d["v"], base, scale, out=d["out"], lse=d["lse"],
-                           stream=s_comp)
-            na.ne_attn_bwd(d["q"], d["k"], d["v"], d["out"], d["dout"], d["lse"], base, scale,
-                           dq=d["dq"], dk=d["dk"], dv=d["dv"], workspace=ws, stream=s_comp)
+            na.ne_attn_fwd_train(d["q"], d["k"], d["v"], base, scale, out=d["out"],
+                                 lse=d["lse"], qr=d["qr"], kr=d["kr"], stream=s_comp)
+            na.ne_attn_bwd_train(d["qr"], d["kr"], d["v"], d["out"], d["dout"], d["lse"], base,
+                                 scale, dq=d["dq"], dk=d["dk"], dv=d["dv"], workspace=ws,
+                                 stream=s_comp)
             ev_comp[i].record(s_comp)
             outs = ((h_out, d["out"]), (h_lse, d["lse"]), (h_grads[0], d["dq"]),
                     (h_grads[1], d["dk"]), (h_grads[2], d["dv"]))
@@ -617,6 +645,7 @@ def run_ours(args):
     peaks, peak_kind = load_peaks()
     peak_tf = peaks["bf16_tflops"]
     per_kernel = {
+        "ne_attn_rope_rows_kernel": statistics.mean(t_rot),
         "ne_attn_fwd_kernel": statistics.mean(t_fwd),
         "ne_attn_bwd_preprocess_kernel": statistics.mean(t_pre),
         "ne_attn_bwd_kernel": statistics.mean(t_main),
@@ -632,14 +661,18 @@ def run_ours(args):
                 "traffic": recorded_traffic(dom)}
     # HBM-bound helpers: algorithmic bytes / time.
     n_el = B * T * H * D
-    # read O, dO, q, k; write D, zero dQ', write q', k'
-    pre_bytes = 4 * n_el * 2 + B * H * T * 4 + n_el * 4 + 2 * n_el * 2
+    rot_bytes = 4 * n_el * 2                                  # read q, k; write q', k'
+    pre_bytes = 2 * n_el * 2 + B * H * T * 4 + n_el * 4       # read O, dO; write D; zero dQ'
     post_bytes = n_el * 4 + n_el * 2 + 2 * n_el * 2       # read dQ', write dQ; dK in place
-    med = {"ne_attn_fwd_kernel": statistics.median(t_fwd),
+    med = {"ne_attn_rope_rows_kernel": statistics.median(t_rot),
+           "ne_attn_fwd_kernel": statistics.median(t_fwd),
            "ne_attn_bwd_preprocess_kernel": statistics.median(t_pre),
            "ne_attn_bwd_kernel": statistics.median(t_main),
            "ne_attn_dq_postprocess_kernel": statistics.median(t_post)}
     kernels = {
+        "ne_attn_rope_rows_kernel": {
+            "ms": per_kernel["ne_attn_rope_rows_kernel"],
+            "gbs": rot_bytes / (per_kernel["ne_attn_rope_rows_kernel"] * 1e-3) / 1e9},
         "ne_attn_fwd_kernel": {"ms": per_kernel["ne_attn_fwd_kernel"],
                                "tflops": f_fwd / (per_kernel["ne_attn_fwd_kernel"] * 1e-3) / 1e12},
         "ne_attn_bwd_kernel": {"ms": per_kernel["ne_attn_bwd_kernel"],
@@ -660,7 +693,7 @@ def run_ours(args):
         "value_at_median": job_tflops(f_step, 1, median_ms, world), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{WORKLOAD}: B={B} H={H} T={T} D={D}, causal, RoPE base 10000, "
-                               "fwd+bwd", "B": B, "H": H, "T": T, "D": D,
+                               "fwd+bwd (training pair)", "B": B, "H": H, "T": T, "D": D,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed (512 MiB write) between timed steps"},
         "pct_bf16_peak": 100.0 * value / (world * peak_tf),
@@ -678,7 +711,12 @@ def run_ours(args):
                       "how": "events between the kernels (outside the timed region): each "
                              "kernel timed on its own, without the overlap of one kernel's "
                              "start with the previous one's drain"},
-        "gpu_launches": 4 * K,
+        "plain_pair": {"steps": KP, "ms_per_step_median": statistics.median(t_plain),
+                       "tflops_at_median": f_step / (statistics.median(t_plain) * 1e-3) / 1e12,
+                       "how": "ne_attn_fwd + ne_attn_bwd (RoPE applied inside the forward and "
+                              "again in the backward's preprocess), L2 flushed, outside the "
+                              "timed region"},
+        "gpu_launches": 5 * K,
         "clocks": clk,
         "wall_s": wall,
         "device_status": status,

@@ -37,9 +37,10 @@ def packed_view(inp):
     return ts, [i * T for i in range(B + 1)]
 
 
-def run_gpu(inp, device="cuda", bwd=True):
+def run_gpu(inp, device="cuda", bwd=True, train=False):
     """Run the library on ``inp``; returns CPU tensors in the packed layout
-    ([N, H, D] and LSE [H, N])."""
+    ([N, H, D] and LSE [H, N]).  ``train``: the bf16 forward and the backward
+    are the training pair (rotated operands kept from forward to backward)."""
     from causal_self_attention_gb300 import ne_attn as na
 
     q, k, v, do = (inp[n].to(device) for n in ("q", "k", "v", "dout"))
@@ -49,16 +50,27 @@ def run_gpu(inp, device="cuda", bwd=True):
         cu = inp["cu_seqlens"].to(device)
         mx = inp["max_seqlen"]
         o32, lse = na.ne_attn_varlen_fwd(q, k, v, cu, mx, base, scale, out_f32=True)
-        o16, lse16 = na.ne_attn_varlen_fwd(q, k, v, cu, mx, base, scale)
-        if bwd:
-            dq, dk, dv = na.ne_attn_varlen_bwd(q, k, v, o16, do, lse16, cu, mx, base, scale)
+        if train:
+            o16, lse16, qr, kr = na.ne_attn_varlen_fwd_train(q, k, v, cu, mx, base, scale)
+            if bwd:
+                dq, dk, dv = na.ne_attn_varlen_bwd_train(qr, kr, v, o16, do, lse16, cu, mx, base,
+                                                         scale)
+        else:
+            o16, lse16 = na.ne_attn_varlen_fwd(q, k, v, cu, mx, base, scale)
+            if bwd:
+                dq, dk, dv = na.ne_attn_varlen_bwd(q, k, v, o16, do, lse16, cu, mx, base, scale)
         res["lse"] = lse.cpu()
         res["lse_bf16call"] = lse16.cpu()
     else:
         o32, lse = na.ne_attn_fwd(q, k, v, base, scale, out_f32=True)
-        o16, lse16 = na.ne_attn_fwd(q, k, v, base, scale)
-        if bwd:
-            dq, dk, dv = na.ne_attn_bwd(q, k, v, o16, do, lse16, base, scale)
+        if train:
+            o16, lse16, qr, kr = na.ne_attn_fwd_train(q, k, v, base, scale)
+            if bwd:
+                dq, dk, dv = na.ne_attn_bwd_train(qr, kr, v, o16, do, lse16, base, scale)
+        else:
+            o16, lse16 = na.ne_attn_fwd(q, k, v, base, scale)
+            if bwd:
+                dq, dk, dv = na.ne_attn_bwd(q, k, v, o16, do, lse16, base, scale)
         B, H, T = lse.shape
         res["lse"] = lse.permute(1, 0, 2).reshape(H, B * T).cpu()
         res["lse_bf16call"] = lse16.permute(1, 0, 2).reshape(H, B * T).cpu()
