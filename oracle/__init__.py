@@ -1,6 +1,7 @@
-"""CPU oracle for causal self-attention with RoPE, forward and backward, and
-for the projections around it (RMSNorm + QKV projection with RoPE; output
-projection + residual).
+"""CPU oracle for causal self-attention with RoPE, forward and backward, for
+the projections around it (RMSNorm + QKV projection with RoPE; output
+projection + residual), and for a multi-token prediction head with its
+softmax cross-entropy loss and analytic gradients.
 
 TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline leg import this package.  The product library never
@@ -77,6 +78,9 @@ def _load():
         lib.ne_oracle_qkv_rope.restype = ctypes.c_int
         lib.ne_oracle_out_proj_residual.argtypes = [dp, dp, dp, ctypes.c_int, ctypes.c_int, dp]
         lib.ne_oracle_out_proj_residual.restype = ctypes.c_int
+        lib.ne_oracle_mtp_head.argtypes = [dp, dp, ip, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, dp, dp, dp, dp]
+        lib.ne_oracle_mtp_head.restype = ctypes.c_int
         lib.ne_oracle_num_threads.argtypes = []
         lib.ne_oracle_num_threads.restype = ctypes.c_int
         _lib = lib
@@ -275,3 +279,23 @@ def out_proj_residual(o, w, r) -> np.ndarray:
     if _load().ne_oracle_out_proj_residual(_dptr(o), _dptr(w), _dptr(r), N, C, _dptr(y)) != 0:
         raise ValueError("ne_oracle_out_proj_residual: bad arguments")
     return y
+
+
+def mtp_head(h, w, targets, K: int):
+    """Multi-token prediction head with softmax cross-entropy: ``h [M, C]``,
+    ``w [K*V, C]`` (head j in rows j*V .. j*V+V-1), ``targets [M, K]`` int
+    (-1: no target).  Returns ``(loss, row_loss [M, K], dh [M, C], dw [K*V, C])``."""
+    h, w = as_f64(h), as_f64(w)
+    tg = np.ascontiguousarray(np.asarray(targets, dtype=np.int32))
+    M, C = h.shape
+    V = w.shape[0] // K
+    assert w.shape == (K * V, C) and tg.shape == (M, K)
+    loss = np.zeros(1)
+    row_loss = np.empty((M, K))
+    dh = np.empty((M, C))
+    dw = np.empty((K * V, C))
+    if _load().ne_oracle_mtp_head(_dptr(h), _dptr(w), _iptr(tg), M, C, K, V, _dptr(loss),
+                                  _dptr(row_loss), _dptr(dh), _dptr(dw)) != 0:
+        raise ValueError("ne_oracle_mtp_head: bad arguments")
+    return float(loss[0]), row_loss, dh, dw
+

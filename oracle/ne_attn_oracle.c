@@ -1,6 +1,8 @@
 /*
  * ne_attn_oracle.c -- plain, slow CPU oracle for causal self-attention with
- * rotary position embedding (RoPE), forward and backward, in double precision.
+ * rotary position embedding (RoPE), forward and backward, in double precision;
+ * also for the projections around it and for a multi-token prediction head
+ * with its loss and gradients (each at the end of this file).
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, loads or
  * calls this file; only the tests, the smoke check and the benchmark's CPU
@@ -462,3 +464,80 @@ int ne_oracle_out_proj_residual(const double *o, const double *w, const double *
         y[i] += r[i];
     return 0;
 }
+
+/*
+ * Multi-token prediction (MTP) head with its softmax cross-entropy loss and
+ * analytic gradients (NanoEuler Show HN page, paragraph 2: the engine's
+ * analytic gradients, "including the RoPE and MTP layers", are checked against
+ * double-precision centred finite differences).  The page names the layers and
+ * nothing more; the plainest reading is taken: K linear heads on the trunk's
+ * hidden state h_t, head j (0-based) predicting the token j + 1 positions
+ * ahead, each scored by softmax cross-entropy, the loss the mean over the
+ * (t, j) with a target:
+ *     logit_j(t)[v] = h_t . w_{jV+v}
+ *     lse_j(t)      = log sum_v exp(logit_j(t)[v])
+ *     loss          = (1/n) sum_{(t,j) with target} (lse_j(t) - logit_j(t)[y_tj])
+ *     dlogit_j(t)   = (softmax(logit_j(t)) - onehot(y_tj)) / n
+ *     dh_t          = sum_j sum_v dlogit_j(t)[v] w_{jV+v}
+ *     dw_{jV+v}     = sum_t dlogit_j(t)[v] h_t
+ * h [M][C], w [K*V][C], targets [M][K] (token id, or -1: no target there).
+ * Writes loss (scalar; 0 when no (t, j) has a target), row_loss [M][K] (0
+ * where there is no target), dh [M][C] and dw [K*V][C].  Returns 0, or -1.
+ */
+int ne_oracle_mtp_head(const double *h, const double *w, const int *targets, int M, int C, int K,
+                       int V, double *loss, double *row_loss, double *dh, double *dw)
+{
+    if (!h || !w || !targets || !loss || !row_loss || !dh || !dw || M < 0 || C <= 0 || K <= 0 ||
+        V <= 0)
+        return -1;
+    long long n = 0;
+    for (long long i = 0; i < (long long)M * K; i++) {
+        if (targets[i] >= V)
+            return -1;
+        if (targets[i] >= 0)
+            n++;
+    }
+    for (long long i = 0; i < (long long)M * C; i++)
+        dh[i] = 0.0;
+    for (long long i = 0; i < (long long)K * V * C; i++)
+        dw[i] = 0.0;
+    double *logit = malloc(sizeof(double) * (size_t)V);
+    if (!logit)
+        return -1;
+    double sum = 0.0;
+    for (int t = 0; t < M; t++) {
+        const double *ht = h + (long long)t * C;
+        for (int j = 0; j < K; j++) {
+            const int y = targets[(long long)t * K + j];
+            row_loss[(long long)t * K + j] = 0.0;
+            if (y < 0)
+                continue;
+            const double *wj = w + (long long)j * V * C;
+            double mx = -INFINITY;
+            for (int v = 0; v < V; v++) {
+                logit[v] = dot(ht, wj + (long long)v * C, C);
+                if (logit[v] > mx)
+                    mx = logit[v];
+            }
+            double se = 0.0;
+            for (int v = 0; v < V; v++)
+                se += exp(logit[v] - mx);
+            const double lse = mx + log(se);
+            row_loss[(long long)t * K + j] = lse - logit[y];
+            sum += lse - logit[y];
+            for (int v = 0; v < V; v++) {
+                const double g = (exp(logit[v] - lse) - (v == y ? 1.0 : 0.0)) / (double)n;
+                const double *wv = wj + (long long)v * C;
+                double *dwv = dw + ((long long)j * V + v) * C;
+                for (int c = 0; c < C; c++) {
+                    dh[(long long)t * C + c] += g * wv[c];
+                    dwv[c] += g * ht[c];
+                }
+            }
+        }
+    }
+    free(logit);
+    *loss = n > 0 ? sum / (double)n : 0.0;
+    return 0;
+}
+
