@@ -39,16 +39,6 @@ cudaError_t launch_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, const 
                           const RopeTable& rope, float scale_log2, float* part,
                           __nv_bfloat16* out, float* lse, int* status, cudaStream_t stream);
 constexpr unsigned kDecodeBoxRows = 32;  // keys per pipeline stage of the decode kernel
-namespace gemm {
-struct Params {
-  int M, N, K;
-  int n_tiles_m, n_tiles_n;
-  int C;
-  int T;
-  RopeTable rope;
-  int* status;
-};
-}  // namespace gemm
 cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* g, __nv_bfloat16* xn,
                            float* rstd, int M, int C, float eps, cudaStream_t stream);
 cudaError_t launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmW,
@@ -266,6 +256,19 @@ ne_status encode_mat(CUtensorMap* map, const void* base, long long rows, int col
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NE_OK : NE_ERR_CUDA;
+}
+
+// fp32 [rows, cols] matrix, boxes of 32 columns (128 bytes) x box_rows.
+ne_status encode_mat_f32(CUtensorMap* map, void* base, long long rows, int cols,
+                         unsigned box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4};
+  cuuint32_t box[2] = {32, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? NE_OK : NE_ERR_CUDA;
 }
 
@@ -798,7 +801,7 @@ ne_status ne_rmsnorm_qkv_rope(const ne_bf16* x, const ne_bf16* g, const ne_bf16*
                                      reinterpret_cast<const __nv_bfloat16*>(g),
                                      reinterpret_cast<__nv_bfloat16*>(x_norm), rstd, p.M, p.C,
                                      eps, cs);
-  if (e == cudaSuccess) e = ne::launch_gemm(0, ta, tw, tq, tk, tv, p, cs);
+  if (e == cudaSuccess) e = ne::launch_gemm(ne::gemm::kQkvRope, ta, tw, tq, tk, tv, p, cs);
   return cuda_status(e);
 }
 
@@ -831,7 +834,116 @@ ne_status ne_out_proj_residual(const ne_bf16* o, const ne_bf16* w_o, const ne_bf
   if ((rc = encode_mat(&ty, y, N, C, 128)) != NE_OK) return rc;
   if ((rc = encode_mat(&tr, residual, N, C, 128)) != NE_OK) return rc;
   return cuda_status(
-      ne::launch_gemm(1, ta, tw, ty, tr, tr, p, static_cast<cudaStream_t>(stream)));
+      ne::launch_gemm(ne::gemm::kResidual, ta, tw, ty, tr, tr, p, static_cast<cudaStream_t>(stream)));
+}
+
+size_t ne_mtp_head_workspace_bytes(int M, int K, int V) {
+  if (M <= 0 || K <= 0 || V <= 0) return 0;
+  const size_t dl = (static_cast<size_t>(M) * K * V * 2 + 255) & ~static_cast<size_t>(255);
+  return dl + 256;  // dlogits bf16 [M, K*V], then the two fp32 accumulators
+}
+
+ne_status ne_mtp_head(const ne_bf16* h, const ne_bf16* w, const int* targets, int M, int C, int K,
+                      int V, float* loss, float* row_loss, ne_bf16* dh, float* dw,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  if (!h || !w || !targets || !loss || !row_loss || !dh || !dw) return NE_ERR_INVALID_ARG;
+  if (M <= 0 || C <= 0 || K <= 0 || V <= 0) return NE_ERR_INVALID_ARG;
+  if (V != 256 || C % 8 != 0) return NE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(M) * K * V > (1LL << 40) || static_cast<long long>(M) * C > (1LL << 40) ||
+      static_cast<long long>(K) * V * C > (1LL << 31))
+    return NE_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(w) || !aligned16(dh) || !aligned16(dw) || !aligned4(targets) ||
+      !aligned4(loss) || !aligned4(row_loss))
+    return NE_ERR_MISALIGNED;
+  const size_t need = ne_mtp_head_workspace_bytes(M, K, V);
+  if (workspace && workspace_bytes < need) return NE_ERR_INVALID_ARG;
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return NE_ERR_MISALIGNED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState* st = nullptr;
+  ne_status rc = device_state(&st);
+  if (rc != NE_OK) return rc;
+  if ((rc = get_encoder()) != NE_OK) return rc;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  void* ws = workspace;
+  bool owned = false;
+  if (!ws) {
+    const cudaError_t e = cudaMallocAsync(&ws, need, cs);
+    if (e != cudaSuccess) return cuda_status(e);
+    owned = true;
+  }
+  const int N = K * V;
+  ne_bf16* dlogits = static_cast<ne_bf16*>(ws);
+  float* acc = reinterpret_cast<float*>(static_cast<char*>(ws) + need - 256);
+  // 1. logits = h . W^T with the cross-entropy epilogue -> dlogits, row losses, sums
+  ne::gemm::Params p1;
+  p1.M = M;
+  p1.N = N;
+  p1.K = C;
+  p1.n_tiles_m = (M + 127) / 128;
+  p1.n_tiles_n = K;
+  p1.targets = targets;
+  p1.heads = K;
+  p1.row_loss = row_loss;
+  p1.acc = acc;
+  p1.status = st->status;
+  // 2. dh = dlogits . W / n (W read MN-major: its rows are the contraction)
+  ne::gemm::Params p2;
+  p2.M = M;
+  p2.N = C;
+  p2.K = N;
+  p2.n_tiles_m = (M + 127) / 128;
+  p2.n_tiles_n = (C + 255) / 256;
+  p2.acc = acc;
+  p2.loss = loss;
+  p2.status = st->status;
+  // 3. dW = dlogits^T . h / n, both read MN-major, the tokens split over the
+  // CTAs (partial tiles reduce-added in fp32)
+  ne::gemm::Params p3;
+  p3.M = N;
+  p3.N = C;
+  p3.K = M;
+  p3.n_tiles_m = (N + 127) / 128;
+  p3.n_tiles_n = (C + 255) / 256;
+  {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      sms = 148;
+    const int k_chunks = (M + 63) / 64;
+    const int n_mn = p3.n_tiles_m * p3.n_tiles_n;
+    int splits = sms / n_mn;
+    splits = splits < 1 ? 1 : (splits > k_chunks ? k_chunks : splits);
+    p3.chunks_per_split = (k_chunks + splits - 1) / splits;
+    p3.k_splits = (k_chunks + p3.chunks_per_split - 1) / p3.chunks_per_split;  // none empty
+  }
+  p3.acc = acc;
+  p3.status = st->status;
+  CUtensorMap th_k, tw_k, tdl_k, tw_mn, tdh, tdl_mn, th_mn, tdw;
+  if ((rc = encode_mat(&th_k, h, M, C, 128)) == NE_OK &&
+      (rc = encode_mat(&tw_k, w, N, C, 256)) == NE_OK &&
+      (rc = encode_mat(&tdl_k, dlogits, M, N, 128)) == NE_OK &&
+      (rc = encode_mat(&tw_mn, w, N, C, 64)) == NE_OK &&
+      (rc = encode_mat(&tdh, dh, M, C, 128)) == NE_OK &&
+      (rc = encode_mat(&tdl_mn, dlogits, M, N, 64)) == NE_OK &&
+      (rc = encode_mat(&th_mn, h, M, C, 64)) == NE_OK)
+    rc = encode_mat_f32(&tdw, dw, N, C, 128);
+  cudaError_t e = cudaSuccess;
+  if (rc == NE_OK) {
+    e = cudaMemsetAsync(acc, 0, 2 * sizeof(float), cs);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dw, 0, static_cast<size_t>(N) * C * sizeof(float), cs);
+    if (e == cudaSuccess)
+      e = ne::launch_gemm(ne::gemm::kMtpCe, th_k, tw_k, tdl_k, tdl_k, tdl_k, p1, cs);
+    if (e == cudaSuccess)
+      e = ne::launch_gemm(ne::gemm::kScale, tdl_k, tw_mn, tdh, tdh, tdh, p2, cs);
+    if (e == cudaSuccess)
+      e = ne::launch_gemm(ne::gemm::kReduceF32, tdl_mn, th_mn, tdw, tdw, tdw, p3, cs);
+  }
+  if (owned) {
+    const cudaError_t e2 = cudaFreeAsync(ws, cs);
+    if (e == cudaSuccess) e = e2;
+  }
+  if (rc != NE_OK) return rc;
+  return cuda_status(e);
 }
 
 ne_status ne_attn_set_bwd_phase_events(void* ev_after_preprocess, void* ev_after_main) {

@@ -102,6 +102,28 @@ __device__ __forceinline__ bool seq_bounds(const Problem& pb, int s, int& start,
   return true;
 }
 
+// Parameters of the projection GEMM (ne_proj.cu), shared by the launches in
+// the API file.
+namespace gemm {
+enum Epilogue { kQkvRope = 0, kResidual = 1, kMtpCe = 2, kScale = 3, kReduceF32 = 4 };
+struct Params {
+  int M = 0, N = 0, K = 0;
+  int n_tiles_m = 0, n_tiles_n = 0;
+  int k_splits = 1;               // K ranges per output tile (more than 1: kReduceF32 only)
+  int chunks_per_split = 1 << 20;  // 64-wide K chunks per range
+  int C = 0;  // kQkvRope: width of each of q, k, v (N = 3C)
+  int T = 1;  // kQkvRope: tokens per sequence (position = row mod T)
+  RopeTable rope{nullptr, nullptr, 0};
+  // Multi-token prediction head
+  const int* targets = nullptr;  // [M, heads] (kMtpCe): token id, or -1 for no target
+  int heads = 1;                 // kMtpCe: heads of 256 logits (N = 256 * heads)
+  float* row_loss = nullptr;     // [M, heads] (kMtpCe)
+  float* acc = nullptr;          // [2]: sum of the row losses, count of targets (kMtpCe adds)
+  float* loss = nullptr;         // [1]: acc[0] / acc[1], written by kScale
+  int* status = nullptr;
+};
+}  // namespace gemm
+
 // Index of LSE / delta element (head h, sequence s starting at row `start`,
 // position t within the sequence).
 __device__ __forceinline__ long long lse_index(const Problem& pb, int h, int s, int start, int t) {

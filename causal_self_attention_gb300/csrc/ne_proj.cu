@@ -24,7 +24,26 @@
 // Epilogues: kQkvRope -- the tile lies in q, k or v (C is a multiple of 256);
 // q and k columns are rotated per head of 64 at the token's position
 // (row mod T) in fp32 before the bf16 rounding; kResidual -- the residual
-// block, TMA-loaded into the staging buffer one block ahead, is added.
+// block, TMA-loaded into the staging buffer one block ahead, is added;
+// kMtpCe -- the tile's 256 columns are one head's logits over a 256-way
+// vocabulary: softmax cross-entropy against the row's target, the row's loss
+// out, and softmax - onehot (bf16) stored as dlogits; kScale -- the tile
+// times 1/n (n: the cross-entropy's target count), bf16; kReduceF32 -- the
+// same in fp32, added into the output by bulk tensor reduce-adds (split-K
+// partial tiles).
+//
+// Operand layouts: A and W are K-major by default (A [M, K], W [N, K],
+// 64-column chunks); with kAMn / kBMn the operand is read MN-major from a
+// [K, M] (or [K, N]) row-major matrix, each 64-row chunk as 64 x 64 boxes
+// (8 KiB apart), so that A^T B and A B products need no transposed copies.
+// Split-K: a tile list entry is (output tile, K range); its partial result
+// is reduced into the output (kReduceF32 only).
+//
+// Multi-token prediction head (NanoEuler Show HN page, paragraph 2: the MTP
+// layers' analytic gradients are checked against double-precision finite
+// differences): logits = h . W^T with kMtpCe, then dh = dlogits . W (A
+// K-major, W MN-major, kScale) and dW = dlogits^T . h (both MN-major,
+// split-K, kReduceF32).
 #include "ne_rope.cuh"
 #include "ne_sm100.cuh"
 
@@ -57,37 +76,32 @@ enum Bar {
 };
 static_assert(8 * B_COUNT + 8 <= kBarBytes, "barrier region overflow");
 
-constexpr uint32_t kIdesc = make_idesc_bf16(kTM, kTN, false, false);  // A, W both K-major
 
-enum Epilogue { kQkvRope = 0, kResidual = 1 };
-
-struct Params {
-  int M, N, K;
-  int n_tiles_m, n_tiles_n;
-  int C;          // kQkvRope: width of each of q, k, v (N = 3C)
-  int T;          // kQkvRope: tokens per sequence (position = row mod T)
-  RopeTable rope;
-  int* status;
-};
-
-// Tile `t` of the output: m fastest, so the CTAs working at the same time
-// share the weight tile (3.5 MB of weights stay in L2 either way).
-__device__ __forceinline__ void tile_coords(const Params& p, int t, int& m0, int& n0) {
-  m0 = (t % p.n_tiles_m) * kTM;
-  n0 = (t / p.n_tiles_m) * kTN;
+// Entry `t` of the tile list: output tile m fastest (the CTAs working at the
+// same time share the weight tile), then n, then the K range.
+__device__ __forceinline__ void tile_coords(const Params& p, int t, int& m0, int& n0, int& kc0,
+                                            int& kc1) {
+  const int n_mn = p.n_tiles_m * p.n_tiles_n;
+  const int mn = t % n_mn, sp = t / n_mn;
+  m0 = (mn % p.n_tiles_m) * kTM;
+  n0 = (mn / p.n_tiles_m) * kTN;
+  const int k_chunks = (p.K + kBK - 1) / kBK;
+  kc0 = sp * p.chunks_per_split;
+  kc1 = min(k_chunks, kc0 + p.chunks_per_split);
 }
 
 }  // namespace gemm
 
-template <int kEpi>
+template <int kEpi, bool kAMn, bool kBMn>
 __global__ void __launch_bounds__(gemm::kThreads, 1)
     ne_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmW,
-                   const __grid_constant__ CUtensorMap tmO0,   // q' | y
+                   const __grid_constant__ CUtensorMap tmO0,   // q' | y | dlogits | dh | dW (fp32)
                    const __grid_constant__ CUtensorMap tmO1,   // k' | residual
                    const __grid_constant__ CUtensorMap tmO2,   // v
                    const gemm::Params p) {
   using namespace gemm;
+  constexpr uint32_t kIdesc = make_idesc_bf16(kTM, kTN, kAMn, kBMn);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -95,9 +109,8 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + 8 * B_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_BAR + 8 * B_COUNT + 4);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int n_tiles = p.n_tiles_m * p.n_tiles_n;
+  const int n_tiles = p.n_tiles_m * p.n_tiles_n * p.k_splits;
   const int G = gridDim.x, cta = blockIdx.x;
-  const int k_chunks = (p.K + kBK - 1) / kBK;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -133,9 +146,9 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
       int last[kStages] = {-1, -1, -1, -1};
       bool ok = true;
       for (int t = cta; ok && t < n_tiles; t += G) {
-        int m0, n0;
-        tile_coords(p, t, m0, n0);
-        for (int kb = 0; kb < k_chunks; ++kb, ++it) {
+        int m0, n0, kc0, kc1;
+        tile_coords(p, t, m0, n0, kc0, kc1);
+        for (int kb = kc0; kb < kc1; ++kb, ++it) {
           const int s = it % kStages;
           if (it >= kStages &&
               !mbar_wait(&bars[B_EMPTY + s], ((it - kStages) / kStages) & 1, abort_flag, p.status,
@@ -145,8 +158,20 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
           }
           uint8_t* st = smem + OFF_STAGE + s * kStageBytes;
           mbar_arrive_expect_tx(&bars[B_FULL + s], kStageBytes);
-          tma_load_2d(st, &tmA, &bars[B_FULL + s], kb * kBK, m0);
-          tma_load_2d(st + kABytes, &tmW, &bars[B_FULL + s], kb * kBK, n0);
+          if constexpr (kAMn) {  // A^T chunk: rows kb*64.., columns m0.. of the [K, M] matrix
+            tma_load_2d(st, &tmA, &bars[B_FULL + s], m0, kb * kBK);
+            tma_load_2d(st + kABytes / 2, &tmA, &bars[B_FULL + s], m0 + 64, kb * kBK);
+          } else {
+            tma_load_2d(st, &tmA, &bars[B_FULL + s], kb * kBK, m0);
+          }
+          if constexpr (kBMn) {  // W^T chunk: rows kb*64.., columns n0.. of the [K, N] matrix
+#pragma unroll
+            for (int i = 0; i < kTN / 64; ++i)
+              tma_load_2d(st + kABytes + i * (kWBytes / 4), &tmW, &bars[B_FULL + s], n0 + 64 * i,
+                          kb * kBK);
+          } else {
+            tma_load_2d(st + kABytes, &tmW, &bars[B_FULL + s], kb * kBK, n0);
+          }
           last[s] = it;
         }
       }
@@ -161,11 +186,18 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMAs
-    const uint64_t d0 = make_sdesc_sw128(smem_u32(smem + OFF_STAGE), 16, 1024);
-    constexpr uint64_t kStageD = kStageBytes >> 4, kAD = kABytes >> 4;
+    // K-major operand: a K16 step adds 32 bytes; MN-major (64 x 64 boxes 8 KiB
+    // apart, 128-byte rows along K): a K16 step adds 16 rows = 2048 bytes.
+    const uint64_t dA0 = make_sdesc_sw128(smem_u32(smem + OFF_STAGE), kAMn ? kABytes / 2 : 16, 1024);
+    const uint64_t dW0 =
+        make_sdesc_sw128(smem_u32(smem + OFF_STAGE + kABytes), kBMn ? kWBytes / 4 : 16, 1024);
+    constexpr uint64_t kStageD = kStageBytes >> 4;
+    constexpr uint64_t kStepA = kAMn ? 128 : 2, kStepW = kBMn ? 128 : 2;
     int it = 0, lt = 0;
     bool ok = true;
     for (int t = cta; ok && t < n_tiles; t += G, ++lt) {
+      int m0, n0, kc0, kc1;
+      tile_coords(p, t, m0, n0, kc0, kc1);
       const int acc = lt & 1;
       if (lt >= 2 &&
           !mbar_wait_warp(&bars[B_ACC_EMPTY + acc], ((lt - 2) >> 1) & 1, abort_flag, p.status, 61)) {
@@ -173,7 +205,7 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
         break;
       }
       tc_fence_after();
-      for (int kb = 0; kb < k_chunks; ++kb, ++it) {
+      for (int kb = kc0; kb < kc1; ++kb, ++it) {
         const int s = it % kStages;
         if (!mbar_wait_warp(&bars[B_FULL + s], (it / kStages) & 1, abort_flag, p.status, 62)) {
           ok = false;
@@ -181,13 +213,13 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
         }
         tc_fence_after();
         if (elect_one()) {
-          const uint64_t dA = opaque_u64(d0) + kStageD * s, dW = dA + kAD;
+          const uint64_t dA = opaque_u64(dA0) + kStageD * s, dW = opaque_u64(dW0) + kStageD * s;
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)  // 16 elements = 32 bytes per step
-            umma_bf16_ss(tmem + acc * kTN, dA + 2 * kk, dW + 2 * kk, kIdesc,
-                         (kb > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            umma_bf16_ss(tmem + acc * kTN, dA + kStepA * kk, dW + kStepW * kk, kIdesc,
+                         (kb > kc0 || kk > 0) ? 1u : 0u);
           umma_commit(&bars[B_EMPTY + s]);
-          if (kb == k_chunks - 1) umma_commit(&bars[B_ACC_FULL + acc]);
+          if (kb == kc1 - 1) umma_commit(&bars[B_ACC_FULL + acc]);
         }
         __syncwarp();
       }
@@ -207,7 +239,7 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
     uint8_t* stage_out = smem + OFF_OUT;
     if (leader) {
       tma_prefetch_desc(&tmO0);
-      tma_prefetch_desc(&tmO1);
+      if (kEpi == kQkvRope || kEpi == kResidual) tma_prefetch_desc(&tmO1);
       if (kEpi == kQkvRope) tma_prefetch_desc(&tmO2);
     }
     // Residual block b (over the CTA's tiles x 4 blocks) into staging buffer
@@ -215,18 +247,28 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
     auto issue_residual = [&](int b) {
       const int t = cta + (b >> 2) * G;
       if (t >= n_tiles) return;
-      int m0, n0;
-      tile_coords(p, t, m0, n0);
+      int m0, n0, kc0, kc1;
+      tile_coords(p, t, m0, n0, kc0, kc1);
       mbar_arrive_expect_tx(&bars[B_RES_FULL + (b & 1)], kOutBlock);
       tma_load_2d(stage_out + (b & 1) * kOutBlock, &tmO1, &bars[B_RES_FULL + (b & 1)],
                   n0 + (b & 3) * 64, m0);
     };
     if (kEpi == kResidual && leader) issue_residual(0);
+    // kScale / kReduceF32: the products are the gradients of the mean
+    // cross-entropy, 1/n times the sums (n from the cross-entropy kernel,
+    // which completed before this grid started).
+    float inv_n = 1.f;
+    if constexpr (kEpi == kScale || kEpi == kReduceF32) {
+      const float cnt = p.acc[1];
+      inv_n = cnt > 0.f ? 1.f / cnt : 0.f;
+      if (kEpi == kScale && cta == 0 && leader) p.loss[0] = cnt > 0.f ? p.acc[0] / cnt : 0.f;
+    }
+    constexpr float kLog2e = 1.4426950408889634f;
     bool ok = true;
     int lt = 0, gb = 0;  // tiles, 64-column blocks of this CTA
     for (int t = cta; ok && t < n_tiles; t += G, ++lt) {
-      int m0, n0;
-      tile_coords(p, t, m0, n0);
+      int m0, n0, kc0, kc1;
+      tile_coords(p, t, m0, n0, kc0, kc1);
       const int acc = lt & 1;
       bool wok = mbar_wait_warp(&bars[B_ACC_FULL + acc], (lt >> 1) & 1, abort_flag, p.status, 63);
       // The token's position (q, k rotation) and its table row, loaded once per tile.
@@ -235,6 +277,43 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
       if (kEpi == kQkvRope && which < 2) {
         const int row = m0 + r < p.M ? m0 + r : p.M - 1;
         rope_load_row_flat(p.rope, row % p.T, tab);
+      }
+      // kMtpCe, first pass over the row's 256 logits: max, sum of exponentials
+      // (online over the four blocks), the target's logit.
+      const int head = (kEpi == kMtpCe) ? n0 / kTN : 0;
+      const bool in_rows = m0 + r < p.M;
+      int y = -1;
+      float lse = 0.f, y_logit = 0.f;
+      if constexpr (kEpi == kMtpCe) {
+        if (in_rows) y = __ldg(p.targets + static_cast<long long>(m0 + r) * p.heads + head);
+        if (wok) {
+          tc_fence_after();
+          float mx = -INFINITY, se = 0.f;
+#pragma unroll 1
+          for (int cb = 0; cb < kTN / 64; ++cb) {
+            uint32_t v0[32], v1[32];
+            tmem_ld_x32(tmem + lane_base + acc * kTN + cb * 64, v0);
+            tmem_ld_x32(tmem + lane_base + acc * kTN + cb * 64 + 32, v1);
+            tmem_ld_wait(v0);
+            tmem_ld_wait(v1);
+            float bm = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              bm = fmaxf(bm, fmaxf(__uint_as_float(v0[i]), __uint_as_float(v1[i])));
+            const float nm = fmaxf(mx, bm);
+            float bs = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              bs += ex2_approx((__uint_as_float(v0[i]) - nm) * kLog2e);
+              bs += ex2_approx((__uint_as_float(v1[i]) - nm) * kLog2e);
+              y_logit = (cb * 64 + i == y) ? __uint_as_float(v0[i]) : y_logit;
+              y_logit = (cb * 64 + 32 + i == y) ? __uint_as_float(v1[i]) : y_logit;
+            }
+            se = se * ex2_approx((mx - nm) * kLog2e) + bs;
+            mx = nm;
+          }
+          lse = mx + logf(se);
+        }
       }
       tc_fence_after();
       for (int cb = 0; cb < kTN / 64; ++cb, ++gb) {
@@ -257,6 +336,29 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
           tc_fence_before();
           mbar_arrive(&bars[B_ACC_EMPTY + acc]);
         }
+        if constexpr (kEpi == kReduceF32) {
+          // Both staging buffers hold this block as fp32 columns 0-31 and
+          // 32-63 ([128][32], 128-byte swizzle); they are free once the
+          // previous block's reduce-adds have read them.
+          if (leader) bulk_wait_group_read0();
+          if (!(ok = named_bar_and(1, 128, ok && wok))) break;
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<float4*>(stage_out + h * kOutBlock + sw128_offset(r, c)) =
+                  make_float4(a[32 * h + 4 * c] * inv_n, a[32 * h + 4 * c + 1] * inv_n,
+                              a[32 * h + 4 * c + 2] * inv_n, a[32 * h + 4 * c + 3] * inv_n);
+          fence_proxy_async_smem();
+          named_bar_sync(1, 128);
+          if (leader) {  // no box starts past the output's last column
+            if (n0 + cb * 64 < p.N) tma_reduce_add_2d(&tmO0, stage_out, n0 + cb * 64, m0);
+            if (n0 + cb * 64 + 32 < p.N)
+              tma_reduce_add_2d(&tmO0, stage_out + kOutBlock, n0 + cb * 64 + 32, m0);
+            bulk_commit_group();
+          }
+          continue;
+        }
         if (kEpi == kQkvRope) {
           if (which < 2) {
             // RoPE, rotate-half within the head: element i pairs with i + 32,
@@ -273,11 +375,17 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
               a[i + 33] = __fmaf_rn(y1, cs.z, __fmul_rn(x1, cs.w));
             }
           }
-          // The staging buffer's previous store has read it (the leader waits,
-          // all four warps meet; a failed wait above is voted out here).
-          if (leader) bulk_wait_group_read1();
-          if (!(ok = named_bar_and(1, 128, ok && wok))) break;
-        } else {
+        } else if (kEpi == kMtpCe) {
+          // dlogits = softmax - onehot(target); 0 without a target.
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            a[i] = y >= 0 ? ex2_approx((a[i] - lse) * kLog2e) - (cb * 64 + i == y ? 1.f : 0.f)
+                          : 0.f;
+        } else if (kEpi == kScale) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) a[i] *= inv_n;
+        }
+        if (kEpi == kResidual) {
           // The residual block was loaded into this buffer one block ahead.
           wok = wok && mbar_wait_warp(&bars[B_RES_FULL + sb], (gb >> 1) & 1, abort_flag,
                                       p.status, 64);
@@ -294,6 +402,11 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
             a[8 * c + 6] += bf16lo_to_f32(rv.w);
             a[8 * c + 7] += bf16hi_to_f32(rv.w);
           }
+        } else {
+          // The staging buffer's previous store has read it (the leader waits,
+          // all four warps meet; a failed wait above is voted out here).
+          if (leader) bulk_wait_group_read1();
+          if (!(ok = named_bar_and(1, 128, ok && wok))) break;
         }
         // Row r of the block, bf16, into the swizzled staging buffer.
 #pragma unroll
@@ -307,7 +420,7 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
           if (kEpi == kQkvRope) {
             const CUtensorMap* out = which == 0 ? &tmO0 : (which == 1 ? &tmO1 : &tmO2);
             tma_store_2d(out, buf, n0 - which * p.C + cb * 64, m0);
-          } else {
+          } else if (n0 + cb * 64 < p.N) {  // no box starts past the output's last column
             tma_store_2d(&tmO0, buf, n0 + cb * 64, m0);
           }
           bulk_commit_group();
@@ -319,12 +432,24 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
           }
         }
       }
+      if constexpr (kEpi == kMtpCe) {
+        // The row's loss (0 without a target); the CTA-wide sums go to acc.
+        const bool has = ok && wok && in_rows && y >= 0;
+        const float rl = has ? lse - y_logit : 0.f;
+        if (ok && wok && in_rows) p.row_loss[static_cast<long long>(m0 + r) * p.heads + head] = rl;
+        float sum = rl, cnt = has ? 1.f : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          sum += __shfl_xor_sync(0xffffffffu, sum, o);
+          cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+        }
+        if (lane == 0 && cnt > 0.f) {
+          atomicAdd(p.acc, sum);
+          atomicAdd(p.acc + 1, cnt);
+        }
+      }
     }
     if (leader) bulk_wait_group0();  // the stores have completed before the kernel ends
-    if (kEpi == kResidual && leader) {
-      // A residual load issued for a block past the CTA's last tile is never
-      // issued (issue_residual skips it); nothing else can be in flight.
-    }
   }
 
   tc_fence_before();
@@ -386,20 +511,30 @@ cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* g, __nv_
                     C, eps);
 }
 
-cudaError_t launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmW,
-                        const CUtensorMap& tmO0, const CUtensorMap& tmO1, const CUtensorMap& tmO2,
-                        const gemm::Params& p, cudaStream_t stream) {
+namespace {
+template <int kEpi, bool kAMn, bool kBMn>
+cudaError_t launch_gemm_inst(const CUtensorMap& tmA, const CUtensorMap& tmW,
+                             const CUtensorMap& tmO0, const CUtensorMap& tmO1,
+                             const CUtensorMap& tmO2, const gemm::Params& p, int G,
+                             cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(ne_gemm_kernel<gemm::kQkvRope>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         gemm::SMEM_BYTES);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(ne_gemm_kernel<gemm::kResidual>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, gemm::SMEM_BYTES);
+    const cudaError_t e = cudaFuncSetAttribute(ne_gemm_kernel<kEpi, kAMn, kBMn>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               gemm::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  return launch_pdl(ne_gemm_kernel<kEpi, kAMn, kBMn>, dim3(G), dim3(gemm::kThreads),
+                    gemm::SMEM_BYTES, stream, tmA, tmW, tmO0, tmO1, tmO2, p);
+}
+}  // namespace
+
+// epi: gemm::Epilogue.  kScale reads A K-major and W MN-major (dlogits . W);
+// kReduceF32 reads both MN-major (dlogits^T . h); the others both K-major.
+cudaError_t launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmW,
+                        const CUtensorMap& tmO0, const CUtensorMap& tmO1, const CUtensorMap& tmO2,
+                        const gemm::Params& p, cudaStream_t stream) {
   static int sm_count[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -408,13 +543,22 @@ cudaError_t launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmW,
   if (!sm_count[dev] &&
       (e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return e;
-  const int n_tiles = p.n_tiles_m * p.n_tiles_n;
-  const int G = n_tiles < sm_count[dev] ? n_tiles : sm_count[dev];
-  if (epi == gemm::kQkvRope)
-    return launch_pdl(ne_gemm_kernel<gemm::kQkvRope>, dim3(G), dim3(gemm::kThreads),
-                      gemm::SMEM_BYTES, stream, tmA, tmW, tmO0, tmO1, tmO2, p);
-  return launch_pdl(ne_gemm_kernel<gemm::kResidual>, dim3(G), dim3(gemm::kThreads),
-                    gemm::SMEM_BYTES, stream, tmA, tmW, tmO0, tmO1, tmO2, p);
+  const long long n_tiles = static_cast<long long>(p.n_tiles_m) * p.n_tiles_n * p.k_splits;
+  const int G = static_cast<int>(n_tiles < sm_count[dev] ? n_tiles : sm_count[dev]);
+  switch (epi) {
+    case gemm::kQkvRope:
+      return launch_gemm_inst<gemm::kQkvRope, false, false>(tmA, tmW, tmO0, tmO1, tmO2, p, G, stream);
+    case gemm::kResidual:
+      return launch_gemm_inst<gemm::kResidual, false, false>(tmA, tmW, tmO0, tmO1, tmO2, p, G, stream);
+    case gemm::kMtpCe:
+      return launch_gemm_inst<gemm::kMtpCe, false, false>(tmA, tmW, tmO0, tmO1, tmO2, p, G, stream);
+    case gemm::kScale:
+      return launch_gemm_inst<gemm::kScale, false, true>(tmA, tmW, tmO0, tmO1, tmO2, p, G, stream);
+    case gemm::kReduceF32:
+      return launch_gemm_inst<gemm::kReduceF32, true, true>(tmA, tmW, tmO0, tmO1, tmO2, p, G, stream);
+    default:
+      return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace ne

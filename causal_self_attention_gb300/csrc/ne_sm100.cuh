@@ -259,6 +259,17 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const 
       "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(src))
       : "memory");
 }
+// 2-d tiled bulk reduction (add) of a shared-memory tile into global memory,
+// tracked by this thread's bulk async-group (parts past the tensor's end are
+// not written; the box never starts at a negative coordinate here).
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const void* src, int c0,
+                                                  int c1) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%1, %2}], [%3];" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(c0), "r"(c1), "r"(smem_u32(src))
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

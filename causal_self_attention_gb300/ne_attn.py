@@ -32,7 +32,7 @@ EXPORTED = ("ne_attn_fwd", "ne_attn_fwd_f32out", "ne_attn_bwd", "ne_attn_bwd_wor
             "ne_debug_pipeline", "ne_rmsnorm_qkv_rope", "ne_out_proj_residual",
             "ne_attn_fwd_rotated", "ne_attn_bwd_rotated", "ne_attn_fwd_train",
             "ne_attn_bwd_train", "ne_attn_varlen_fwd_train", "ne_attn_varlen_bwd_train",
-            "ne_attn_set_fwd_phase_event")
+            "ne_attn_set_fwd_phase_event", "ne_mtp_head", "ne_mtp_head_workspace_bytes")
 
 
 class NeAttnError(RuntimeError):
@@ -83,6 +83,7 @@ def lib():
         "ne_attn_varlen_bwd_train": [P, P, P, P, P, P, P, I, I, I, I, I, F, F, P, P, P, P, Z,
                                      P],
         "ne_attn_set_fwd_phase_event": [P],
+        "ne_mtp_head": [P, P, P, I, I, I, I, P, P, P, P, P, Z, P],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -90,6 +91,8 @@ def lib():
         fn.restype = None if name == "ne_attn_release" else I
     L.ne_attn_bwd_workspace_bytes.argtypes = [I, I, I]
     L.ne_attn_bwd_workspace_bytes.restype = Z
+    L.ne_mtp_head_workspace_bytes.argtypes = [I, I, I]
+    L.ne_mtp_head_workspace_bytes.restype = Z
     L.ne_attn_decode_workspace_bytes.argtypes = [I, I, I]
     L.ne_attn_decode_workspace_bytes.restype = Z
     L.ne_status_string.argtypes = [I]
@@ -301,6 +304,32 @@ def ne_out_proj_residual(o, w_o, residual, y=None, stream=None):
     _check("ne_out_proj_residual", lib().ne_out_proj_residual(
         _ptr(o), _ptr(w_o), _ptr(residual), N, C, _ptr(y), _stream(stream)))
     return y
+
+
+def ne_mtp_head_workspace_bytes(M: int, K: int, V: int = 256) -> int:
+    return int(lib().ne_mtp_head_workspace_bytes(M, K, V))
+
+
+def ne_mtp_head(h, w, targets, K, loss=None, row_loss=None, dh=None, dw=None, workspace=None,
+                stream=None):
+    """Multi-token prediction head with softmax cross-entropy: ``h [M, C]``
+    bf16, ``w [K*256, C]`` bf16, ``targets [M, K]`` int32 (-1: no target).
+    Returns ``(loss [1], row_loss [M, K], dh [M, C] bf16, dw [K*256, C] fp32)``."""
+    _need(h, torch.bfloat16, "h")
+    _need(w, torch.bfloat16, "w")
+    _need(targets, torch.int32, "targets")
+    M, C = h.shape
+    V = w.shape[0] // K
+    loss = torch.empty(1, dtype=torch.float32, device=h.device) if loss is None else loss
+    row_loss = (torch.empty((M, K), dtype=torch.float32, device=h.device) if row_loss is None
+                else row_loss)
+    dh = torch.empty_like(h) if dh is None else dh
+    dw = torch.empty((K * V, C), dtype=torch.float32, device=h.device) if dw is None else dw
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("ne_mtp_head", lib().ne_mtp_head(
+        _ptr(h), _ptr(w), _ptr(targets), M, C, K, V, _ptr(loss), _ptr(row_loss), _ptr(dh),
+        _ptr(dw), _ptr(workspace), ws_bytes, _stream(stream)))
+    return loss, row_loss, dh, dw
 
 
 def ne_attn_decode_workspace_bytes(B: int, H: int, Tmax: int) -> int:

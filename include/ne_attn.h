@@ -288,6 +288,32 @@ ne_status ne_rmsnorm_qkv_rope(const ne_bf16* x, const ne_bf16* g, const ne_bf16*
 ne_status ne_out_proj_residual(const ne_bf16* o, const ne_bf16* w_o, const ne_bf16* residual,
                                int N, int C, ne_bf16* y, void* stream);
 
+/* Multi-token prediction (MTP) head with its softmax cross-entropy loss and
+ * analytic gradients, the loss-side layer whose gradients the NanoEuler Show
+ * HN page (paragraph 2) checks against double-precision finite differences
+ * "including the RoPE and MTP layers".  K linear heads on the hidden states,
+ * head j (0-based) predicting the token j + 1 positions ahead:
+ *   logit_j(t) = h_t . W_j^T,   W_j = rows j*V .. j*V+V-1 of w
+ *   loss = (1/n) sum over (t, j) with a target y_tj of (lse_j(t) - logit_j(t)[y_tj])
+ *   dh = sum_j dlogit_j W_j,  dW_j = dlogit_j^T h,  dlogit_j(t) = (softmax - onehot(y_tj)) / n
+ * (n: the number of (t, j) with a target; all zero when n = 0).
+ * h: [M, C] bf16; w: [K*V, C] bf16 ([out, in], no bias); targets: [M, K]
+ * int32 DEVICE array, each in [0, V) or -1 (no target there; a value outside
+ * [-1, V) gives an unspecified loss for that row).  V must be 256 (a
+ * byte-level vocabulary: one 256-wide GEMM tile per head), C a multiple of 8.
+ * Writes loss [1] fp32 (the mean), row_loss [M, K] fp32 (each (t, j)'s term,
+ * 0 where there is no target), dh [M, C] bf16 and dw [K*V, C] fp32.
+ * workspace: ne_mtp_head_workspace_bytes(M, K, V) bytes of device memory,
+ * 256-byte aligned (it holds dlogits [M, K*V] bf16), or NULL to let the
+ * library allocate a stream-ordered temporary.  The loss sums are fp32
+ * atomics, so the loss's last bits may differ from run to run.  Pointers
+ * 16-byte aligned (targets, loss, row_loss 4-byte).  Asynchronous on
+ * `stream`; argument errors return before anything is launched. */
+size_t ne_mtp_head_workspace_bytes(int M, int K, int V);
+ne_status ne_mtp_head(const ne_bf16* h, const ne_bf16* w, const int* targets, int M, int C, int K,
+                      int V, float* loss, float* row_loss, ne_bf16* dh, float* dw,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
 /* Synchronize `stream`, then return and clear the device status word of the
  * current device: NE_OK, NE_ERR_TIMEOUT or NE_ERR_BAD_SEQLEN (or NE_ERR_CUDA
  * if the synchronization itself failed). */

@@ -98,6 +98,28 @@ def test_training_pair_argument_errors_return_before_any_launch(lib):
     assert bwd(ws=fake, ws_bytes=16) == 1
 
 
+def test_mtp_head_argument_errors_return_before_any_launch(lib):
+    P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.ne_mtp_head.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P, Z, P]
+    lib.ne_mtp_head_workspace_bytes.argtypes = [I, I, I]
+    lib.ne_mtp_head_workspace_bytes.restype = Z
+    fake = P(0x10000)  # never dereferenced: every case below fails its host check first
+
+    def call(h=fake, M=300, C=192, K=2, V=256, ws=None, ws_bytes=0):
+        return lib.ne_mtp_head(h, fake, fake, M, C, K, V, fake, fake, fake, fake, ws, ws_bytes,
+                               None)
+
+    assert call(h=None) == 1
+    assert call(M=0) == 1
+    assert call(V=512) == 2       # one 256-wide tile per head
+    assert call(C=100) == 2       # rows must be 16-byte multiples
+    assert call(h=P(0x10008)) == 3
+    assert call(ws=fake, ws_bytes=16) == 1
+    # dlogits bf16 [M, K*V] rounded up to 256 bytes, then 256 bytes of accumulators
+    assert lib.ne_mtp_head_workspace_bytes(300, 2, 256) == 307200 + 256
+    assert lib.ne_mtp_head_workspace_bytes(0, 2, 256) == 0
+
+
 def test_decode_argument_errors_return_before_any_launch(lib):
     P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.ne_attn_decode.argtypes = [P, P, P, P, I, I, I, I, F, F, P, P, P, Z, P]
