@@ -408,6 +408,64 @@ def proj_summary(args, dev, stream, flush, peak_tf):
     }
 
 
+def mtp_summary(args, dev, stream, flush, peak_tf):
+    """The multi-token prediction head at the GPT-2-small shape (8192 tokens of
+    width 768, heads for the next token and the one after it, a 256-way byte
+    vocabulary): logits with the cross-entropy in the GEMM epilogue, dh and dW;
+    timed with CUDA events, the L2 flushed before every step, beside torch's
+    three bare products (cuBLAS) for context."""
+    import torch
+
+    from causal_self_attention_gb300 import ne_attn as na
+    M, C, K, V = 8192, 768, 2, 256
+    g = torch.Generator().manual_seed(91)
+    h = torch.randn((M, C), generator=g).to(torch.bfloat16).to(dev)
+    w = (torch.randn((K * V, C), generator=g) * (2.0 / C ** 0.5)).to(torch.bfloat16).to(dev)
+    tg = torch.randint(0, V, (M, K), generator=g, dtype=torch.int32)
+    tg[-1, 1] = -1  # the last token has no token two ahead
+    tg = tg.to(dev)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    row = torch.empty((M, K), dtype=torch.float32, device=dev)
+    dh = torch.empty_like(h)
+    dw = torch.empty((K * V, C), dtype=torch.float32, device=dev)
+    ws = torch.empty(na.ne_mtp_head_workspace_bytes(M, K, V), dtype=torch.uint8, device=dev)
+    dl = torch.empty((M, K * V), dtype=torch.bfloat16, device=dev)
+
+    def ours():
+        na.ne_mtp_head(h, w, tg, K, loss=loss, row_loss=row, dh=dh, dw=dw, workspace=ws,
+                       stream=stream)
+
+    def cublas():
+        torch.matmul(h, w.t())
+        torch.matmul(dl, w)
+        torch.matmul(dl.t(), h)
+
+    n = max(args.extra_steps, 3)
+    res_ms = {}
+    for name, fn in (("ours", ours), ("cublas", cublas)):
+        for _ in range(3):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        res_ms[name] = statistics.median(a.elapsed_time(b) for a, b in ev)
+    assert na.ne_attn_get_device_status() == 0
+    fl = 3 * 2.0 * M * C * K * V  # logits, dh, dW
+    return {
+        "shape": f"M={M} tokens, C={C}, K={K} heads (next token and the one after), V={V}",
+        "steps": n, "gflop": fl / 1e9,
+        "ms_median": res_ms["ours"], "tflops": fl / (res_ms["ours"] * 1e-3) / 1e12,
+        "frac_bf16_peak": fl / (res_ms["ours"] * 1e-3) / 1e12 / peak_tf,
+        "cublas_three_products_ms_median": res_ms["cublas"],
+        "loss": float(loss.cpu()[0]),
+    }
+
+
 def decode_summary(args, dev, stream, peaks):
     """One decode step over a KV cache (decode16k), timed with CUDA events:
     GB/s of K and V read, against the measured HBM bandwidth."""
@@ -725,6 +783,7 @@ def run_ours(args):
         line["workloads"] = bench_workloads(args, dev, stream, flush, peak_tf)
         line["decode"] = decode_summary(args, dev, stream, peaks)
         line["projections"] = proj_summary(args, dev, stream, flush, peak_tf)
+        line["mtp_head"] = mtp_summary(args, dev, stream, flush, peak_tf)
     if not args.no_cpu_baseline and (world == 1 or rank == 0):
         import oracle
         oracle.build()
