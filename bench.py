@@ -466,9 +466,24 @@ def mtp_summary(args, dev, stream, flush, peak_tf):
     }
 
 
+def _time_calls(fn, n, stream):
+    """Per-call device times (ms) of n calls of fn on stream, CUDA events."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    for a, b in ev:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
 def decode_summary(args, dev, stream, peaks):
     """One decode step over a KV cache (decode16k), timed with CUDA events:
-    GB/s of K and V read, against the measured HBM bandwidth."""
+    GB/s of K and V read, against the measured HBM bandwidth.  Also the same
+    step on a cache of rotated keys (ne_attn_decode_rotated: q' and k' given,
+    nothing rotated, no table read)."""
     import torch
 
     from causal_self_attention_gb300 import ne_attn as na
@@ -479,27 +494,36 @@ def decode_summary(args, dev, stream, peaks):
     out = torch.empty_like(q)
     lse = torch.empty((B, H), dtype=torch.float32, device=dev)
     ws = torch.empty(na.ne_attn_decode_workspace_bytes(B, H, Tmax), dtype=torch.uint8, device=dev)
-    for _ in range(5):
+
+    def rotating():
         na.ne_attn_decode(q, kc, vc, pos, inp["rope_base"], inp["scale"], out=out, lse=lse,
                           workspace=ws, stream=stream)
+
+    def rotated():  # timing only: the cache's contents do not change the work
+        na.ne_attn_decode_rotated(q, kc, vc, pos, inp["scale"], out=out, lse=lse, workspace=ws,
+                                  stream=stream)
+
     n = max(4 * args.extra_steps, 3)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(n)]
-    for a, b in ev:  # the cache (2 x 403 MB) is larger than L2: no flush needed
-        a.record(stream)
-        na.ne_attn_decode(q, kc, vc, pos, inp["rope_base"], inp["scale"], out=out, lse=lse,
-                          workspace=ws, stream=stream)
-        b.record(stream)
-    torch.cuda.synchronize()
-    assert na.ne_attn_get_device_status() == 0
-    t = [a.elapsed_time(b) for a, b in ev]
     kv = decode_kv_bytes(inp)
+    res = {}
+    for name, fn in (("rotating", rotating), ("rotated", rotated)):
+        for _ in range(5):
+            fn()
+        # the cache (2 x 403 MB) is larger than L2: no flush needed
+        res[name] = _time_calls(fn, n, stream)
+    assert na.ne_attn_get_device_status() == 0
+    t = res["rotating"]
     medi = statistics.median(t)
+    medr = statistics.median(res["rotated"])
     return {"workload": f"{DECODE_WORKLOAD}: B={B} H={H} Tmax={Tmax} D=64, one new token per "
                         "sequence at the last cache row", "steps": n,
             "ms_per_step": statistics.mean(t), "ms_per_step_median": medi,
             "gbs_at_median": kv / (medi * 1e-3) / 1e9, "kv_bytes_per_step": kv,
-            "frac_hbm": kv / (medi * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+            "frac_hbm": kv / (medi * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "rotated_cache": {"how": "ne_attn_decode_rotated: cache of k' = R(n) k, q' given",
+                              "ms_per_step_median": medr,
+                              "gbs_at_median": kv / (medr * 1e-3) / 1e9,
+                              "frac_hbm": kv / (medr * 1e-3) / 1e9 / peaks["hbm_gbs"]}}
 
 
 def run_ours(args):
@@ -886,6 +910,15 @@ def run_decode(args):
     torch.cuda.synchronize()
     e2e_ms = t0.elapsed_time(t1) / KE
 
+    # The same step on a cache of rotated keys (outside the timed region).
+    def step_rot(s=stream):
+        na.ne_attn_decode_rotated(q, kc, vc, pos, scale, out=out, lse=lse, workspace=ws, stream=s)
+
+    for _ in range(3):
+        step_rot()
+    t_rot = statistics.median(_time_calls(step_rot, max(K, 3), stream))
+    assert na.ne_attn_get_device_status() == 0
+
     peaks, peak_kind = load_peaks()
     line = {
         "metric": DECODE_METRIC, "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": K,
@@ -904,6 +937,11 @@ def run_decode(args):
         "gpu_launches": 2 * K,
         "clocks": clk,
         "device_status": status,
+        "rotated_cache": {"how": "ne_attn_decode_rotated on a cache of k' = R(n) k with q' "
+                                 "given (nothing rotated, no table read); outside the timed "
+                                 "region", "ms_per_step_median": t_rot,
+                          "gbs_at_median": kv_bytes / (t_rot * 1e-3) / 1e9,
+                          "frac_hbm": kv_bytes / (t_rot * 1e-3) / 1e9 / peaks["hbm_gbs"]},
     }
     if not args.no_cpu_baseline:
         import oracle

@@ -37,7 +37,8 @@ size_t decode_part_bytes(int B, int H, int Tmax);
 cudaError_t launch_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmT,
                           const __nv_bfloat16* q, const int* pos, int B, int H, int Tmax,
                           const RopeTable& rope, float scale_log2, float* part,
-                          __nv_bfloat16* out, float* lse, int* status, cudaStream_t stream);
+                          __nv_bfloat16* out, float* lse, int* status, cudaStream_t stream,
+                          bool rot);
 constexpr unsigned kDecodeBoxRows = 32;  // keys per pipeline stage of the decode kernel
 cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* g, __nv_bfloat16* xn,
                            float* rstd, int M, int C, float eps, cudaStream_t stream);
@@ -713,16 +714,20 @@ size_t ne_attn_decode_workspace_bytes(int B, int H, int Tmax) {
   return ne::decode_part_bytes(B, H, Tmax);
 }
 
-ne_status ne_attn_decode(const ne_bf16* q, const ne_bf16* k_cache, const ne_bf16* v_cache,
-                         const int* pos, int B, int H, int Tmax, int D, float rope_base,
-                         float scale, ne_bf16* out, float* lse, void* workspace,
-                         size_t workspace_bytes, void* stream) {
+namespace {
+
+// Shared body of the two decode entry points.  rot: q and the cached keys are
+// un-rotated and rotated in the kernel; otherwise both arrive rotated (q', k').
+ne_status run_decode(const ne_bf16* q, const ne_bf16* k_cache, const ne_bf16* v_cache,
+                     const int* pos, int B, int H, int Tmax, int D, bool rot, float rope_base,
+                     float scale, ne_bf16* out, float* lse, void* workspace,
+                     size_t workspace_bytes, void* stream) {
   if (!q || !k_cache || !v_cache || !pos || !out || !lse) return NE_ERR_INVALID_ARG;
   if (D != 64) return NE_ERR_UNSUPPORTED;
   if (B <= 0 || H <= 0 || Tmax <= 0) return NE_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * Tmax > 0x7fffffffLL) return NE_ERR_UNSUPPORTED;
-  if (!std::isfinite(scale) || scale <= 0.f || !std::isfinite(rope_base) || rope_base <= 0.f)
-    return NE_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale <= 0.f) return NE_ERR_INVALID_ARG;
+  if (rot && (!std::isfinite(rope_base) || rope_base <= 0.f)) return NE_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned4(pos) ||
       !aligned4(out) || !aligned4(lse))
     return NE_ERR_MISALIGNED;
@@ -734,13 +739,15 @@ ne_status ne_attn_decode(const ne_bf16* q, const ne_bf16* k_cache, const ne_bf16
   ne_status rc = device_state(&st);
   if (rc != NE_OK) return rc;
   if ((rc = get_encoder()) != NE_OK) return rc;
-  RopeTable rope;
-  if ((rc = rope_table(*st, rope_base, Tmax, &rope)) != NE_OK) return rc;
+  RopeTable rope{};
+  CUtensorMap tt{};  // the RoPE table, 32-row boxes of half rows (unused without rotation)
+  if (rot) {
+    if ((rc = rope_table(*st, rope_base, Tmax, &rope)) != NE_OK) return rc;
+    if ((rc = encode_table(&tt, rope.cs, rope.capacity, ne::kDecodeBoxRows)) != NE_OK) return rc;
+  }
   CUtensorMap tk, tv;  // the caches as [B * Tmax, H, 64], 32-row boxes
   if ((rc = encode_rows(&tk, k_cache, B * Tmax, H, ne::kDecodeBoxRows)) != NE_OK) return rc;
   if ((rc = encode_rows(&tv, v_cache, B * Tmax, H, ne::kDecodeBoxRows)) != NE_OK) return rc;
-  CUtensorMap tt;  // the RoPE table, 32-row boxes of half rows
-  if ((rc = encode_table(&tt, rope.cs, rope.capacity, ne::kDecodeBoxRows)) != NE_OK) return rc;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   void* ws = workspace;
   bool owned = false;
@@ -752,12 +759,30 @@ ne_status ne_attn_decode(const ne_bf16* q, const ne_bf16* k_cache, const ne_bf16
   cudaError_t e = ne::launch_decode(
       tk, tv, tt, reinterpret_cast<const __nv_bfloat16*>(q), pos, B, H, Tmax, rope,
       scale * 1.4426950408889634f, static_cast<float*>(ws), reinterpret_cast<__nv_bfloat16*>(out),
-      lse, st->status, cs);
+      lse, st->status, cs, rot);
   if (owned) {
     cudaError_t e2 = cudaFreeAsync(ws, cs);
     if (e == cudaSuccess) e = e2;
   }
   return cuda_status(e);
+}
+
+}  // namespace
+
+ne_status ne_attn_decode(const ne_bf16* q, const ne_bf16* k_cache, const ne_bf16* v_cache,
+                         const int* pos, int B, int H, int Tmax, int D, float rope_base,
+                         float scale, ne_bf16* out, float* lse, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  return run_decode(q, k_cache, v_cache, pos, B, H, Tmax, D, true, rope_base, scale, out, lse,
+                    workspace, workspace_bytes, stream);
+}
+
+ne_status ne_attn_decode_rotated(const ne_bf16* qr, const ne_bf16* kr_cache,
+                                 const ne_bf16* v_cache, const int* pos, int B, int H, int Tmax,
+                                 int D, float scale, ne_bf16* out, float* lse, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  return run_decode(qr, kr_cache, v_cache, pos, B, H, Tmax, D, false, 0.f, scale, out, lse,
+                    workspace, workspace_bytes, stream);
 }
 
 ne_status ne_rmsnorm_qkv_rope(const ne_bf16* x, const ne_bf16* g, const ne_bf16* w_qkv, int B,

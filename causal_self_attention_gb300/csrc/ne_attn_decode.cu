@@ -30,7 +30,10 @@
 //      their log-sum-exp weights into o (bf16) and LSE (fp32, natural log).
 // Keys are rotated with the fp32 rule of the training kernels and rounded to
 // bf16, so a decode at position T-1 sees exactly the operands the training
-// forward multiplies.
+// forward multiplies.  kRot = false: the caller passes q' and a cache of
+// rotated keys k' (as the training forward or the QKV projection with RoPE
+// writes them); nothing is rotated, no table rows are loaded, and a stage
+// holds only the K and V boxes.
 #include "ne_sm100.cuh"
 
 namespace ne {
@@ -43,10 +46,15 @@ constexpr int kKeys = 32;            // keys per stage (the TMA box height)
 constexpr int kStages = 3;
 constexpr int kKvBytes = kKeys * 128;                  // one K or V box
 constexpr int kTabBytes = kKeys * 256;                 // 16 table rows
-constexpr int kStageBytes = 2 * kKvBytes + kTabBytes;  // 8 KiB
-constexpr int OFF_BAR = kStages * kStageBytes;
-constexpr int OFF_RED = OFF_BAR + 2 * kStages * 8 + 16;
-constexpr int SMEM_BYTES = OFF_RED + kWarps * 66 * 4 + 1024;  // + slack for 1024-byte alignment
+// Shared memory of each instantiation: the ring (K, V and, when keys are
+// rotated here, the table rows), barriers, the warps' partial states.
+template <bool kRot>
+struct Smem {
+  static constexpr int kStageBytes = 2 * kKvBytes + (kRot ? kTabBytes : 0);  // 16 / 8 KiB
+  static constexpr int OFF_BAR = kStages * kStageBytes;
+  static constexpr int OFF_RED = OFF_BAR + 2 * kStages * 8 + 16;
+  static constexpr int BYTES = OFF_RED + kWarps * 66 * 4 + 1024;  // + slack for 1024-byte alignment
+};
 constexpr int kPartFloats = 68;      // m, l, 2 pad, o[64] (16-byte multiple)
 }  // namespace dec
 
@@ -104,6 +112,7 @@ __device__ __forceinline__ void merge_state(float& m, float& l, float (&o)[8], f
   m = mn;
 }
 
+template <bool kRot>
 __global__ void __launch_bounds__(dec::kThreads)
     ne_attn_decode_split_kernel(const __grid_constant__ CUtensorMap tmK,
                                 const __grid_constant__ CUtensorMap tmV,
@@ -112,13 +121,15 @@ __global__ void __launch_bounds__(dec::kThreads)
                                 int H, int Tmax, RopeTable rope, float scale_log2,
                                 float* __restrict__ part, int chunk, int n_chunks, int* status) {
   using namespace dec;
+  using L = Smem<kRot>;
+  constexpr int kStageBytes = L::kStageBytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
   uint64_t* empty = full + kStages;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_BAR + 2 * kStages * 8);
-  float (*red)[66] = reinterpret_cast<float (*)[66]>(smem + OFF_RED);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_BAR + 2 * kStages * 8);
+  float (*red)[66] = reinterpret_cast<float (*)[66]>(smem + L::OFF_RED);
 
   // Heads vary fastest over the grid: the CTAs running together read the
   // 12 neighbouring 128-byte pieces of the same cache rows.
@@ -150,7 +161,7 @@ __global__ void __launch_bounds__(dec::kThreads)
     if (lane == 0) {
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      tma_prefetch_desc(&tmT);
+      if (kRot) tma_prefetch_desc(&tmT);
       int i = 0;
       for (; i < n_st; ++i) {
         const int s = i % kStages;
@@ -164,8 +175,10 @@ __global__ void __launch_bounds__(dec::kThreads)
         // table) are filled with zeros by the TMA unit.
         tma_load_3d(st, &tmK, &full[s], 0, h, b * Tmax + key0);
         tma_load_3d(st + kKvBytes, &tmV, &full[s], 0, h, b * Tmax + key0);
-        tma_load_2d(st + 2 * kKvBytes, &tmT, &full[s], 0, key0);
-        tma_load_2d(st + 3 * kKvBytes, &tmT, &full[s], 32, key0);
+        if constexpr (kRot) {
+          tma_load_2d(st + 2 * kKvBytes, &tmT, &full[s], 0, key0);
+          tma_load_2d(st + 3 * kKvBytes, &tmT, &full[s], 32, key0);
+        }
       }
       // Every copy issued has landed before this warp exits (on the normal
       // path the consumers have already waited for them; after an abort they
@@ -186,12 +199,16 @@ __global__ void __launch_bounds__(dec::kThreads)
   {
     const uint4* qrow = reinterpret_cast<const uint4*>(q + (static_cast<long long>(b) * H + h) * 64);
     const uint4 w = __ldg(qrow + cl);
-    float x[8], y[8];
-    float4 t[4];
-    load_pairs(rope.cs + static_cast<long long>(bad ? 0 : m_pos) * 32, cl, t);
-    unpack8(w, x);
-    unpack8(shfl_xor_u4(w, 4), y);
-    rope_chunk(x, y, cl, t, qr);
+    if constexpr (kRot) {
+      float x[8], y[8];
+      float4 t[4];
+      load_pairs(rope.cs + static_cast<long long>(bad ? 0 : m_pos) * 32, cl, t);
+      unpack8(w, x);
+      unpack8(shfl_xor_u4(w, 4), y);
+      rope_chunk(x, y, cl, t, qr);
+    } else {
+      unpack8(w, qr);
+    }
   }
 
   float m = -INFINITY, l = 0.f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -203,20 +220,23 @@ __global__ void __launch_bounds__(dec::kThreads)
     const uint8_t* st = smem + s * kStageBytes;
     const uint4 wk = *reinterpret_cast<const uint4*>(st + sw128_offset(row, cl));
     const uint4 wv = *reinterpret_cast<const uint4*>(st + kKvBytes + sw128_offset(row, cl));
-    float4 tb[4];
-    {
+    const bool live = kbeg + kKeys * i + row < k_end;
+    float kr[8];
+    if constexpr (kRot) {
+      float4 tb[4];
       // Pairs 8q .. 8q + 7 (q = cl & 3): half q >> 1 of the row, 16-byte
       // units 4 (q & 1) .. + 3 of that half, swizzled like K and V.
       const uint8_t* half = st + (2 + ((cl & 3) >> 1)) * kKvBytes;
 #pragma unroll
       for (int u = 0; u < 4; ++u)
         tb[u] = *reinterpret_cast<const float4*>(half + sw128_offset(row, 4 * (cl & 1) + u));
+      float x[8], y[8];
+      unpack8(wk, x);
+      unpack8(shfl_xor_u4(wk, 4), y);
+      rope_chunk(x, y, cl, tb, kr);
+    } else {
+      unpack8(wk, kr);
     }
-    const bool live = kbeg + kKeys * i + row < k_end;
-    float x[8], y[8], kr[8];
-    unpack8(wk, x);
-    unpack8(shfl_xor_u4(wk, 4), y);
-    rope_chunk(x, y, cl, tb, kr);
     float dot = 0.f;
 #pragma unroll
     for (int e = 0; e < 8; ++e) dot = __fmaf_rn(qr[e], kr[e], dot);
@@ -325,15 +345,21 @@ size_t decode_part_bytes(int B, int H, int Tmax) {
   return static_cast<size_t>(B) * H * decode_chunks(Tmax) * dec::kPartFloats * sizeof(float);
 }
 
+// rot: q and the cached keys are rotated here (tmT: the table); otherwise the
+// caller passed q' and a cache of k' (tmT unused).
 cudaError_t launch_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmT,
                           const __nv_bfloat16* q, const int* pos, int B, int H, int Tmax,
                           const RopeTable& rope, float scale_log2, float* part,
-                          __nv_bfloat16* out, float* lse, int* status, cudaStream_t stream) {
+                          __nv_bfloat16* out, float* lse, int* status, cudaStream_t stream,
+                          bool rot) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(ne_attn_decode_split_kernel,
+    cudaError_t e = cudaFuncSetAttribute(ne_attn_decode_split_kernel<true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         dec::SMEM_BYTES);
+                                         dec::Smem<true>::BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(ne_attn_decode_split_kernel<false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, dec::Smem<false>::BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -343,8 +369,12 @@ cudaError_t launch_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, const 
   const int chunk = big >= 1024 ? 1024 : dec::kChunkUnit;
   const int n_chunks = (Tmax + chunk - 1) / chunk;
   dim3 grid(H, n_chunks, B);
-  ne_attn_decode_split_kernel<<<grid, dec::kThreads, dec::SMEM_BYTES, stream>>>(
-      tmK, tmV, tmT, q, pos, H, Tmax, rope, scale_log2, part, chunk, n_chunks, status);
+  if (rot)
+    ne_attn_decode_split_kernel<true><<<grid, dec::kThreads, dec::Smem<true>::BYTES, stream>>>(
+        tmK, tmV, tmT, q, pos, H, Tmax, rope, scale_log2, part, chunk, n_chunks, status);
+  else
+    ne_attn_decode_split_kernel<false><<<grid, dec::kThreads, dec::Smem<false>::BYTES, stream>>>(
+        tmK, tmV, tmT, q, pos, H, Tmax, rope, scale_log2, part, chunk, n_chunks, status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ne_attn_decode_merge_kernel<<<B * H, 32, 0, stream>>>(part, n_chunks, out, lse);

@@ -24,7 +24,8 @@ STATUS_NAMES = {0: "NE_OK", 1: "NE_ERR_INVALID_ARG", 2: "NE_ERR_UNSUPPORTED",
                 7: "NE_ERR_BAD_SEQLEN", 8: "NE_ERR_TOO_LARGE"}
 
 EXPORTED = ("ne_attn_fwd", "ne_attn_fwd_f32out", "ne_attn_bwd", "ne_attn_bwd_workspace_bytes",
-            "ne_attn_bwd_noalloc", "ne_attn_decode", "ne_attn_decode_workspace_bytes",
+            "ne_attn_bwd_noalloc", "ne_attn_decode", "ne_attn_decode_rotated",
+            "ne_attn_decode_workspace_bytes",
             "ne_attn_varlen_fwd", "ne_attn_varlen_fwd_f32out", "ne_attn_varlen_bwd",
             "ne_attn_set_bwd_phase_events", "ne_attn_get_device_status",
             "ne_attn_last_device_code", "ne_status_string",
@@ -65,6 +66,7 @@ def lib():
         "ne_attn_varlen_fwd_f32out": [P, P, P, P, I, I, I, I, I, F, F, P, P, P],
         "ne_attn_varlen_bwd": [P, P, P, P, P, P, P, I, I, I, I, I, F, F, P, P, P, P, Z, P],
         "ne_attn_decode": [P, P, P, P, I, I, I, I, F, F, P, P, P, Z, P],
+        "ne_attn_decode_rotated": [P, P, P, P, I, I, I, I, F, P, P, P, Z, P],
         "ne_attn_set_bwd_phase_events": [P, P],
         "ne_attn_get_device_status": [P],
         "ne_attn_last_device_code": [],
@@ -358,6 +360,31 @@ def ne_attn_decode(q, k_cache, v_cache, pos, rope_base=10000.0, scale=None, out=
            lib().ne_attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(pos), B, H, Tmax, D,
                                 float(rope_base), float(scale), _ptr(out), _ptr(lse),
                                 _ptr(workspace), ws_bytes, _stream(stream)))
+    return out, lse
+
+
+def ne_attn_decode_rotated(qr, kr_cache, v_cache, pos, scale=None, out=None, lse=None,
+                           workspace=None, stream=None):
+    """Decode over a cache of rotated keys: ``qr`` ``[B, H, 64]`` bf16 (the new
+    tokens' ``q' = R(pos) q``), ``kr_cache`` ``[B, Tmax, H, 64]`` bf16 holding
+    ``k'_n = R(n) k_n``, ``v_cache`` likewise, ``pos`` int32 ``[B]`` on the
+    device.  Returns ``(out [B, H, 64] bf16, lse [B, H] fp32)``."""
+    _need(qr, torch.bfloat16, "qr")
+    _need(kr_cache, torch.bfloat16, "kr_cache")
+    _need(v_cache, torch.bfloat16, "v_cache")
+    _need(pos, torch.int32, "pos")
+    B, H, D = qr.shape
+    Tmax = kr_cache.shape[1]
+    if tuple(kr_cache.shape) != (B, Tmax, H, D) or tuple(v_cache.shape) != (B, Tmax, H, D):
+        raise ValueError("kr_cache / v_cache must be [B, Tmax, H, D] matching qr")
+    scale = D ** -0.5 if scale is None else scale
+    out = torch.empty_like(qr) if out is None else out
+    lse = torch.empty((B, H), dtype=torch.float32, device=qr.device) if lse is None else lse
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("ne_attn_decode_rotated",
+           lib().ne_attn_decode_rotated(_ptr(qr), _ptr(kr_cache), _ptr(v_cache), _ptr(pos), B, H,
+                                        Tmax, D, float(scale), _ptr(out), _ptr(lse),
+                                        _ptr(workspace), ws_bytes, _stream(stream)))
     return out, lse
 
 

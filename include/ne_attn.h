@@ -255,6 +255,18 @@ ne_status ne_attn_decode(const ne_bf16* q, const ne_bf16* k_cache, const ne_bf16
                          float scale, ne_bf16* out, float* lse, void* workspace,
                          size_t workspace_bytes, void* stream);
 
+/* Decode over a cache of ROTATED keys: kr_cache holds k'_n = R(n) k_n (as
+ * ne_attn_fwd_train's kr or ne_rmsnorm_qkv_rope's k write them) and qr is the
+ * new token's q' = R(pos[b]) q, so nothing is rotated and no table is read;
+ * the cache traffic is the K' and V rows alone.  Arguments, layouts, status
+ * and workspace as in ne_attn_decode (no rope_base).  With the rotation of
+ * ne_attn_decode (fp32 products, one bf16 rounding) applied to q and the
+ * keys, the results equal ne_attn_decode's bit for bit. */
+ne_status ne_attn_decode_rotated(const ne_bf16* qr, const ne_bf16* kr_cache,
+                                 const ne_bf16* v_cache, const int* pos, int B, int H, int Tmax,
+                                 int D, float scale, ne_bf16* out, float* lse, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
 /* The step before the attention in a transformer layer: RMSNorm, then the
  * QKV projection, with RoPE applied to q and k in the projection's epilogue
  * (NanoEuler Show HN page, paragraph 2: the CUDA engine has RMSNorm and RoPE

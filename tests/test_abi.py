@@ -142,3 +142,23 @@ def test_decode_argument_errors_return_before_any_launch(lib):
     # workspace: one (m, l, o[64]) partial of 68 floats per 256-key chunk per (b, h)
     assert lib.ne_attn_decode_workspace_bytes(2, 3, 1000) == 2 * 3 * 4 * 68 * 4
     assert lib.ne_attn_decode_workspace_bytes(0, 3, 1000) == 0
+
+
+def test_rotated_decode_argument_errors_return_before_any_launch(lib):
+    P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.ne_attn_decode_rotated.argtypes = [P, P, P, P, I, I, I, I, F, P, P, P, Z, P]
+    fake = P(0x10000)  # never dereferenced: every case below fails its host check first
+
+    def call(qr=fake, kr=fake, B=2, H=3, Tmax=100, D=64, scale=0.125, out=fake, ws=None,
+             ws_bytes=0):
+        return lib.ne_attn_decode_rotated(qr, kr, fake, fake, B, H, Tmax, D, scale, out, fake,
+                                          ws, ws_bytes, None)
+
+    assert call(qr=None) == 1
+    assert call(kr=None) == 1
+    assert call(out=None) == 1
+    assert call(D=32) == 2
+    assert call(B=0) == 1
+    assert call(scale=float("nan")) == 1
+    assert call(kr=P(0x10004)) == 3
+    assert call(ws=fake, ws_bytes=16) == 1

@@ -7,7 +7,10 @@ over the cached keys and values.  Bars: O max abs error <= 1e-2 (the kernel
 writes bf16), LSE abs error <= 1e-3.  Cases: ragged positions including 0 and
 the last cache row, the two named decode workloads (every sequence and head),
 agreement with the training forward's last row, and a position outside the
-cache (reported, never read)."""
+cache (reported, never read).  ne_attn_decode_rotated on a cache of rotated
+keys (rotated by the oracle's mode-1 rule, the bf16 values the kernels
+multiply) gives bit for bit the results of ne_attn_decode on the un-rotated
+cache, and meets the oracle's bars."""
 import numpy as np
 import pytest
 import torch
@@ -95,3 +98,52 @@ def test_decode_position_outside_the_cache_is_reported(na):
     assert torch.all(out[1] == 0) and torch.all(torch.isinf(lse[1]))
     ro, rl = _oracle_decode(dict(inp, B=1, pos=inp["pos"][:1]))
     assert np.max(np.abs(out[0].float().cpu().numpy() - ro[0])) <= O_TOL
+
+
+def _rotate_cache(kc):
+    """Oracle mode-1 rotation of a cache ``[B, Tmax, H, 64]``: row n at
+    position n."""
+    B, _, H, _ = kc.shape
+    out = np.empty(kc.shape, dtype=np.float64)
+    for b in range(B):
+        for h in range(H):
+            out[b, :, h] = oracle.rope(kc[b, :, h].double().numpy(), base=10000.0, mode=1)
+    return torch.from_numpy(out).to(torch.bfloat16)
+
+
+def _rotate_queries(q, pos):
+    """Oracle mode-1 rotation of ``q`` ``[B, H, 64]``, row b at position pos[b]."""
+    B, H, D = q.shape
+    out = np.empty((B, H, D))
+    for b in range(B):
+        m = int(pos[b])
+        x = np.zeros((m + 1, D))
+        for h in range(H):
+            x[m] = q[b, h].double().numpy()
+            out[b, h] = oracle.rope(x, base=10000.0, mode=1)[m]
+    return torch.from_numpy(out).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("case", ["ragged", "decode1k", "decode16k"])
+def test_rotated_cache_decode_equals_the_rotating_one(na, case):
+    inp = (make_decode(B=5, H=3, Tmax=600, positions=[0, 1, 255, 256, 599], seed=21)
+           if case == "ragged" else make_decode(case))
+    q, kc, vc, pos = (inp[n].cuda() for n in ("q", "k_cache", "v_cache", "pos"))
+    qr = _rotate_queries(inp["q"], inp["pos"]).cuda()
+    krc = _rotate_cache(inp["k_cache"]).cuda()
+    o1, l1 = na.ne_attn_decode(q, kc, vc, pos, inp["rope_base"], inp["scale"])
+    o2, l2 = na.ne_attn_decode_rotated(qr, krc, vc, pos, inp["scale"])
+    assert na.ne_attn_get_device_status() == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    if case == "ragged":
+        ro, rl = _oracle_decode(inp)
+        assert np.max(np.abs(o2.float().cpu().numpy() - ro)) <= O_TOL
+        assert np.max(np.abs(l2.cpu().numpy() - rl)) <= LSE_TOL
+
+
+def test_rotated_cache_decode_reports_a_position_outside_the_cache(na):
+    inp = make_decode(B=2, H=2, Tmax=64, positions=[10, 64], seed=23)
+    qr, kc, vc, pos = (inp[n].cuda() for n in ("q", "k_cache", "v_cache", "pos"))
+    out, lse = na.ne_attn_decode_rotated(qr, kc, vc, pos)
+    assert na.ne_attn_get_device_status() == 7  # NE_ERR_BAD_SEQLEN
+    assert torch.all(out[1] == 0) and torch.all(torch.isinf(lse[1]))
