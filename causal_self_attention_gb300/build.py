@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libne_attn.so")
 SOURCES = ["ne_attn_api.cu", "ne_attn_fwd.cu", "ne_attn_bwd.cu", "ne_attn_noalloc.cu",
-           "ne_attn_decode.cu", "ne_debug.cu", "ne_proj.cu"]
+           "ne_attn_decode.cu", "ne_debug.cu", "ne_proj.cu", "ne_sched.cu"]
 GENCODE = "-gencode=arch=compute_103a,code=sm_103a"
 
 

@@ -3,6 +3,7 @@
 // cos/sin table cache, the device status word, backward workspace handling,
 // and the launches.  No arithmetic of the method runs here except building the
 // RoPE table (on the host, in double).
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -33,6 +34,8 @@ cudaError_t launch_debug_umma(int form, const __nv_bfloat16* a, const __nv_bfloa
                               int* status, cudaStream_t stream);
 cudaError_t launch_debug_pipeline(const CUtensorMap& tm, int n_items, int drop_item,
                                   long long limit, float* d, int* status, cudaStream_t stream);
+std::vector<int> unit_steps(int nseq, int H, int T);
+std::vector<int> pack_schedule(const std::vector<int>& w, int G, double c_lo, double c_hi);
 size_t decode_part_bytes(int B, int H, int Tmax);
 cudaError_t launch_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmT,
                           const __nv_bfloat16* q, const int* pos, int B, int H, int Tmax,
@@ -70,13 +73,22 @@ struct StreamScratch {
   size_t bytes = 0;
 };
 
+// A work schedule of the persistent backward for one fixed-length shape
+// (ne_sched.cu); dev == nullptr where the snake order is kept.
+struct SchedEntry {
+  int nseq = 0, H = 0, T = 0, G = 0;
+  int* dev = nullptr;
+};
+
 struct DeviceState {
   bool ready = false;
   int* status = nullptr;  // device address of g_device_status on this device
   bool supported = false;
+  int sm_count = 0;
   std::vector<RopeEntry> tables;
   std::vector<float2*> retired;  // replaced tables, freed by ne_attn_release
   std::vector<StreamScratch> scratch;
+  std::vector<SchedEntry> scheds;
 };
 
 // The forward's per-stream temporary of at least `bytes` (caller holds g_mutex).
@@ -129,6 +141,8 @@ ne_status device_state(DeviceState** out) {
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
       return NE_ERR_CUDA;
     st.supported = (major == 10 && minor == 3);
+    if (cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return NE_ERR_CUDA;
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return NE_ERR_CUDA;
     st.status = static_cast<int*>(p);
@@ -200,6 +214,56 @@ ne_status rope_table(DeviceState& st, float base, int positions, RopeTable* out)
     }
   st.tables.push_back(RopeEntry{base, cap, dev});
   *out = table_view(dev, cap);
+  return NE_OK;
+}
+
+// Per-unit overhead range of the persistent backward, in query-tile steps:
+// fits of unit duration = overhead + steps x step time to globaltimer stamps
+// of every CTA on GB300 give 1.2-1.8 steps (the unit's K', V loads and its
+// dV/dK epilogue) at the GPT-2-small, 4096 and 16384-byte shapes.
+constexpr double kBwdOverhead[2] = {1.0, 2.0};
+constexpr size_t kMaxSchedules = 256;
+
+// The work schedule of the persistent backward (its units over n_tiles x nseq
+// x H) for a fixed-length batch of length T: packed on the host on first use
+// of the shape and kept on the device.  *sched = nullptr keeps the kernel's
+// snake order: when it is as good, for a packed (varlen) batch, or when a
+// table cannot be made now (the stream is being captured, or the cache is
+// full).
+ne_status work_schedule(DeviceState& st, bool fixed, int nseq, int H, int T, cudaStream_t stream,
+                        const int** sched, int* G) {
+  *sched = nullptr;
+  *G = 0;
+  if (!fixed) return NE_OK;
+  const long long n = static_cast<long long>((T + 127) / 128) * nseq * H;
+  *G = static_cast<int>(n < st.sm_count ? n : st.sm_count);
+  for (const auto& e : st.scheds)
+    if (e.nseq == nseq && e.H == H && e.T == T && e.G == *G) {
+      *sched = e.dev;
+      return NE_OK;
+    }
+  if (st.scheds.size() >= kMaxSchedules) return NE_OK;
+  cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &capture) != cudaSuccess) return NE_ERR_CUDA;
+  if (capture != cudaStreamCaptureStatusNone) return NE_OK;
+  const std::vector<int> tab =
+      ne::pack_schedule(ne::unit_steps(nseq, H, T), *G, kBwdOverhead[0], kBwdOverhead[1]);
+  SchedEntry e;
+  e.nseq = nseq;
+  e.H = H;
+  e.T = T;
+  e.G = *G;
+  if (!tab.empty()) {
+    cudaError_t r = cudaMalloc(&e.dev, tab.size() * sizeof(int));
+    if (r == cudaSuccess)
+      r = cudaMemcpy(e.dev, tab.data(), tab.size() * sizeof(int), cudaMemcpyHostToDevice);
+    if (r != cudaSuccess) {
+      if (e.dev) cudaFree(e.dev);
+      return cuda_status(r);
+    }
+  }
+  st.scheds.push_back(e);
+  *sched = e.dev;
   return NE_OK;
 }
 
@@ -442,6 +506,9 @@ ne_status run_bwd(const Shape& s, const void* q, const void* k, const void* v, c
   p.rotate_out = pre_rotated ? 0 : 1;
   p.rope = RopeTable{nullptr, nullptr, 0};
   if (!pre_rotated && (rc = rope_table(*st, rope_base, n_tiles * 128, &p.rope)) != NE_OK)
+    return rc;
+  if ((rc = work_schedule(*st, s.fixed, s.nseq, s.H, s.max_len, cs, &p.sched, &p.sched_ctas)) !=
+      NE_OK)
     return rc;
   CUtensorMap tq, tk, tv, tdo;
   if ((rc = encode_rows(&tv, v, s.n_tot, s.H)) != NE_OK) return rc;
@@ -1014,9 +1081,13 @@ void ne_attn_release(void) {
   cudaGetDevice(&cur);
   for (int d = 0; d < kMaxDevices; ++d) {
     DeviceState& st = g_dev[d];
-    if (st.tables.empty() && st.retired.empty() && st.scratch.empty()) continue;
+    if (st.tables.empty() && st.retired.empty() && st.scratch.empty() && st.scheds.empty())
+      continue;
     cudaSetDevice(d);
     for (auto& t : st.tables) cudaFree(t.dev);
+    for (auto& e : st.scheds)
+      if (e.dev) cudaFree(e.dev);
+    st.scheds.clear();
     for (auto* p : st.retired) cudaFree(p);
     for (auto& e : st.scratch) cudaFreeAsync(e.ptr, e.stream);
     if (!st.scratch.empty()) cudaDeviceSynchronize();
@@ -1028,6 +1099,17 @@ void ne_attn_release(void) {
 }
 
 // ------------------------------------------------------------ debug entries --
+
+int ne_debug_schedule(int nseq, int H, int T, int G, int* out, int out_len) {
+  if (nseq <= 0 || H <= 0 || T <= 0 || G <= 0 || !out || out_len < 0 ||
+      static_cast<long long>(nseq) * H * ((T + 127) / 128) > (1 << 24))
+    return -1;
+  const std::vector<int> tab =
+      ne::pack_schedule(ne::unit_steps(nseq, H, T), G, kBwdOverhead[0], kBwdOverhead[1]);
+  if (tab.size() > static_cast<size_t>(out_len)) return -1;
+  std::copy(tab.begin(), tab.end(), out);
+  return static_cast<int>(tab.size());
+}
 
 ne_status ne_debug_tma_tile(const ne_bf16* src, int n_rows, int H, int h, int row0,
                             void* dst_raw, void* stream) {

@@ -198,7 +198,8 @@ __global__ void __launch_bounds__(256)
 // 2. main kernel: persistent.  A unit is one 128-key tile kt of one (sequence,
 //    head); the CTAs (one per SM) walk the units longest first (key tile 0,
 //    whose query tiles are the most, for every (sequence, head), then tile 1,
-//    ...), dealt in a snake order.  TMEM, barriers and the Q'/dO ring persist
+//    ...), dealt in a snake order -- or, for a fixed-length batch, by a
+//    schedule packed on the host.  TMEM, barriers and the Q'/dO ring persist
 //    across units, so a unit's start (its K', V loads, first S^T/dP^T) overlaps
 //    the previous unit's tail (last dQ' drain, dV/dK epilogue) instead of
 //    waiting for a new CTA.  Barrier phases count query tiles over all of the
@@ -227,17 +228,11 @@ __device__ __forceinline__ bool get_unit(const BwdParams& p, int r, Unit& u) {
   return true;
 }
 
-// The k-th unit of CTA c among G: rounds of G units, dealt c = 0..G-1 in even
-// rounds and G-1..0 in odd rounds (increasing in k).
-__device__ __forceinline__ int unit_index(int k, int c, int G) {
-  return k * G + ((k & 1) ? (G - 1 - c) : c);
-}
-
 // The first k' >= k whose unit is not empty (its description in u), or -1.
 __device__ __forceinline__ int next_unit(const BwdParams& p, int n_units, int c, int G, int k,
                                          Unit& u) {
   for (;; ++k) {
-    const int r = unit_index(k, c, G);
+    const int r = dealt_item(p.sched, k, c, G, n_units);
     if (r >= n_units) return -1;
     if (get_unit(p, r, u)) return k;
   }
@@ -316,7 +311,8 @@ __global__ void __launch_bounds__(512, 1)
   float* sDEL = reinterpret_cast<float*>(smem + OFF_DEL);
   // The units of this CTA, in order (the same sequence in every role).
 #define NE_FOR_EACH_UNIT(u)                                                                   \
-  for (int k_ = 0, r_ = unit_index(0, cta, G); r_ < n_units; ++k_, r_ = unit_index(k_, cta, G)) \
+  for (int k_ = 0, r_ = dealt_item(p.sched, 0, cta, G, n_units); r_ < n_units;                \
+       ++k_, r_ = dealt_item(p.sched, k_, cta, G, n_units))                                      \
     if (Unit u; get_unit(p, r_, u))
 
   if (warp == 13 || warp == 15) {
@@ -922,24 +918,26 @@ cudaError_t launch_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 pre_grid((n_tiles * kBM + bwd::kPreRows - 1) / bwd::kPreRows, p.pb.nseq);
-  cudaError_t e = launch_pdl(ne_attn_bwd_preprocess_kernel, pre_grid, dim3(256), 0, stream, p.q,
-                             p.k, p.out, p.dout, p.qr, p.kr, p.delta, p.dq_acc, p.pb, p.rope,
-                             p.rotate_in);
-  if (e != cudaSuccess) return e;
-  if (ev_pre && (e = cudaEventRecord(ev_pre, stream)) != cudaSuccess) return e;
   // One persistent CTA per SM (at most one per unit).
   static int sm_count[64] = {0};
   int dev = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!sm_count[dev] &&
       (e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return e;
   const long long n_units = static_cast<long long>(n_tiles) * p.pb.nseq * p.pb.H;
   const int G = static_cast<int>(n_units < sm_count[dev] ? n_units : sm_count[dev]);
+  BwdParams pm = p;
+  if (pm.sched && pm.sched_ctas != G) pm.sched = nullptr;  // made for another grid: snake order
+  dim3 pre_grid((n_tiles * kBM + bwd::kPreRows - 1) / bwd::kPreRows, p.pb.nseq);
+  e = launch_pdl(ne_attn_bwd_preprocess_kernel, pre_grid, dim3(256), 0, stream, p.q, p.k, p.out,
+                 p.dout, p.qr, p.kr, p.delta, p.dq_acc, p.pb, p.rope, p.rotate_in);
+  if (e != cudaSuccess) return e;
+  if (ev_pre && (e = cudaEventRecord(ev_pre, stream)) != cudaSuccess) return e;
   e = launch_pdl(ne_attn_bwd_kernel, dim3(G), dim3(bwd::kThreads), bwd::SMEM_BYTES, stream, tmQ,
-                 tmK, tmV, tmDO, tmDQ, tmDV, tmDK, p, n_tiles);
+                 tmK, tmV, tmDO, tmDQ, tmDV, tmDK, pm, n_tiles);
   if (e != cudaSuccess) return e;
   if (ev_main && (e = cudaEventRecord(ev_main, stream)) != cudaSuccess) return e;
   const long long post_items = static_cast<long long>(n_tiles) * kBM * p.pb.H * kPostParts;

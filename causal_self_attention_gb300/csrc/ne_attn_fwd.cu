@@ -125,12 +125,6 @@ __device__ __forceinline__ bool get_item(const FwdParams& p, int nblk, int r, It
   return true;
 }
 
-// The k-th item of CTA c among G: rounds of G items, dealt c = 0..G-1 in even
-// rounds and G-1..0 in odd rounds, so that long and short items mix.
-__device__ __forceinline__ int item_index(int k, int c, int G) {
-  return k * G + ((k & 1) ? (G - 1 - c) : c);
-}
-
 }  // namespace fwd
 
 // Grid: G persistent CTAs; nblk = 256-row blocks of the longest sequence.
@@ -206,7 +200,8 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
   uint8_t* sV = smem + OFF_V;
   // The items of this CTA, in order (the same sequence in every role).
 #define NE_FOR_EACH_ITEM(it)                                                        \
-  for (int k_ = 0, r_ = item_index(0, cta, G); r_ < n_items; ++k_, r_ = item_index(k_, cta, G)) \
+  for (int k_ = 0, r_ = dealt_item(nullptr, 0, cta, G, n_items); r_ < n_items;                 \
+       ++k_, r_ = dealt_item(nullptr, k_, cta, G, n_items))                                       \
     if (Item it; get_item(p, nblk, r_, it, threadIdx.x == 0))
 
   if (warp == 13 || warp == 14) {

@@ -80,6 +80,8 @@ struct BwdParams {
                    // workspace; 0: q, k are q', k' already (the caller's)
   int rotate_out;  // 1: the postprocess returns dq = R(m)^T dq', dk = R(n)^T dk';
                    // 0: the gradients w.r.t. q', k' themselves
+  const int* sched = nullptr;  // work schedule of the persistent main kernel, or
+  int sched_ctas = 0;          // nullptr for the snake order; the grid it was made for
 };
 
 // Sequence bounds of sequence s.  Returns false (and raises the device status)
@@ -100,6 +102,22 @@ __device__ __forceinline__ bool seq_bounds(const Problem& pb, int s, int& start,
     len = pb.max_len;
   }
   return true;
+}
+
+// Work dealing of the persistent kernels: the index r (in the longest-first
+// order of work items) of the k-th item of CTA c among G, or n when CTA c has
+// fewer than k + 1 items.  With a schedule -- offsets sched[0..G], then the
+// items of CTA c at sched[G + 1 + sched[c]] .. sched[G + 1 + sched[c + 1] - 1],
+// packed on the host -- its entries; without, rounds of G items dealt
+// c = 0..G-1 in even rounds and G-1..0 in odd rounds, so that long and short
+// items mix.
+__device__ __forceinline__ int dealt_item(const int* sched, int k, int c, int G, int n) {
+  if (sched) {
+    const int b = __ldg(sched + c), e = __ldg(sched + c + 1);
+    return b + k < e ? __ldg(sched + G + 1 + b + k) : n;
+  }
+  const int r = k * G + ((k & 1) ? (G - 1 - c) : c);
+  return r < n ? r : n;
 }
 
 // Parameters of the projection GEMM (ne_proj.cu), shared by the launches in

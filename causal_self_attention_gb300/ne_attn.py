@@ -33,7 +33,8 @@ EXPORTED = ("ne_attn_fwd", "ne_attn_fwd_f32out", "ne_attn_bwd", "ne_attn_bwd_wor
             "ne_debug_pipeline", "ne_rmsnorm_qkv_rope", "ne_out_proj_residual",
             "ne_attn_fwd_rotated", "ne_attn_bwd_rotated", "ne_attn_fwd_train",
             "ne_attn_bwd_train", "ne_attn_varlen_fwd_train", "ne_attn_varlen_bwd_train",
-            "ne_attn_set_fwd_phase_event", "ne_mtp_head", "ne_mtp_head_workspace_bytes")
+            "ne_attn_set_fwd_phase_event", "ne_mtp_head", "ne_mtp_head_workspace_bytes",
+            "ne_debug_schedule")
 
 
 class NeAttnError(RuntimeError):
@@ -86,6 +87,7 @@ def lib():
                                      P],
         "ne_attn_set_fwd_phase_event": [P],
         "ne_mtp_head": [P, P, P, I, I, I, I, P, P, P, P, P, Z, P],
+        "ne_debug_schedule": [I, I, I, I, P, I],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -527,6 +529,20 @@ def ne_debug_umma(form, a, b, stream=None):
     _check("ne_debug_umma", lib().ne_debug_umma(int(form), _ptr(a), _ptr(b), _ptr(d),
                                                 _stream(stream)))
     return d
+
+
+def ne_debug_schedule(nseq, H, T, G):
+    """The persistent backward's work schedule for a fixed-length batch (host
+    only): ``(offsets [G + 1], units)`` as lists, or None when the snake order
+    is kept."""
+    n = nseq * H * ((T + 127) // 128)
+    buf = (ctypes.c_int * (G + 1 + n))()
+    m = lib().ne_debug_schedule(int(nseq), int(H), int(T), int(G), buf, len(buf))
+    if m < 0:
+        raise NeAttnError("ne_debug_schedule", 1)
+    if m == 0:
+        return None
+    return list(buf[:G + 1]), list(buf[G + 1:m])
 
 
 def ne_debug_pipeline(src, n_items, drop_item=-1, wait_limit_cycles=2_000_000_000, stream=None):

@@ -2,7 +2,8 @@
  * ne_attn_debug.h -- bring-up entry points of the attention library, used by
  * its GPU tests to check each hardware primitive on its own against plain
  * host arithmetic: the TMA 128-byte-swizzled tile load, the in-smem RoPE of a
- * tile, and the three tcgen05 MMA operand forms the attention kernels use.
+ * tile, and the three tcgen05 MMA operand forms the attention kernels use;
+ * and, on the host alone, the work schedule of the persistent backward.
  * They follow the conventions of ne_attn.h (device pointers owned by the
  * caller, asynchronous on `stream`, host-side argument checks).  The paper
  * pages have no counterpart: these exist only to test the pieces.
@@ -59,6 +60,15 @@ ne_status ne_debug_umma(int form, const ne_bf16* a, const ne_bf16* b, float* d, 
  * 128 * n_items <= n_rows. */
 ne_status ne_debug_pipeline(const ne_bf16* src, int n_rows, int H, int n_items, int drop_item,
                             long long wait_limit_cycles, float* d, void* stream);
+
+/* The work schedule the fixed-length backward calls give their persistent
+ * main kernel (host only, no device needed): its units (one key tile of one
+ * sequence and head, longest first) for a batch of nseq sequences of length
+ * T with H heads, dealt to G CTAs.  Writes the table -- offsets [G + 1], then
+ * every CTA's units in the kernel's index order -- into out (HOST, out_len
+ * ints) and returns its length: 0 when the snake order is kept (no table),
+ * -1 on a bad argument or a table longer than out_len. */
+int ne_debug_schedule(int nseq, int H, int T, int G, int* out, int out_len);
 
 #ifdef __cplusplus
 }
