@@ -33,9 +33,11 @@
  *    cos/sin tables, one temporary per stream for the forward's rotated keys
  *    (k' = R(n) k, 128 bytes per token and head, allocated stream-ordered on
  *    the first call on that stream outside graph capture and grown when
- *    needed; inside a capture each call allocates and frees its own) -- all
- *    released by ne_attn_release -- and, when a backward is given no
- *    workspace, a stream-ordered temporary it frees itself.
+ *    needed; inside a capture each call allocates and frees its own), the
+ *    backward's work-schedule tables (one per fixed-length shape, a few KB,
+ *    made on first use outside graph capture) -- all released by
+ *    ne_attn_release -- and, when a backward is given no workspace, a
+ *    stream-ordered temporary it frees itself.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
  *    enqueued asynchronously on it; the call returns after the launch.
  *  - Argument errors are detected on the host before anything is launched
@@ -338,8 +340,8 @@ int ne_attn_last_device_code(void);
 /* Human-readable name of a status code (static string). */
 const char* ne_status_string(ne_status s);
 
-/* Free the RoPE tables and the per-stream temporaries kept for every
- * device.  Call only when no launch that may read them is still pending, and
+/* Free the RoPE tables, the work-schedule tables and the per-stream
+ * temporaries kept for every device.  Call only when no launch that may read them is still pending, and
  * before destroying a stream the library was given. */
 void ne_attn_release(void);
 
