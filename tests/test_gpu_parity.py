@@ -121,15 +121,24 @@ def test_varlen_config_sampled():
     assert "dk_long_rel_l2" in errs
 
 
-def test_varlen_equal_lengths_matches_fixed():
-    """A packed batch of equal lengths computes exactly the fixed-length call."""
-    fixed = make_custom(3, 200, 2, seed=21)
+@pytest.mark.parametrize("B,T,H", [(3, 200, 2), (8, 1024, 12)])
+def test_varlen_equal_lengths_matches_fixed(B, T, H):
+    """A packed batch of equal lengths computes exactly the fixed-length call.
+    At the GPT-2-small shape the fixed-length backward deals its units by the
+    schedule packed on the host while the packed batch keeps the kernel's
+    snake order: which CTA computes a unit must not change dK, dV."""
+    from causal_self_attention_gb300 import ne_attn as na
+    fixed = make_custom(B, T, H, seed=21)
     packed = dict(fixed)
-    H, D = fixed["H"], fixed["D"]
+    D = fixed["D"]
     for n in ("q", "k", "v", "dout"):
         packed[n] = fixed[n].reshape(-1, H, D)
-    packed["cu_seqlens"] = torch.tensor([0, 200, 400, 600], dtype=torch.int32)
-    packed["max_seqlen"] = 200
+    packed["cu_seqlens"] = torch.arange(0, (B + 1) * T, T, dtype=torch.int32)
+    packed["max_seqlen"] = T
+    if T == 1024:
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        n_units = B * H * (T // 128)
+        assert na.ne_debug_schedule(B, H, T, min(sms, n_units)) is not None
     a, b = run_gpu(fixed), run_gpu(packed)
     for n in ("o32", "o16", "lse", "dk", "dv"):
         assert torch.equal(a[n], b[n]), n
