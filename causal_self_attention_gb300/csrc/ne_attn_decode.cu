@@ -69,29 +69,30 @@ __device__ __forceinline__ void load_pairs(const float2* __restrict__ cs, int c,
   for (int u = 0; u < 4; ++u) t[u] = __ldg(p + u);
 }
 
-// Rotate the 8 dims of chunk c (dims 8c..8c+7 of a 64-dim row) given the 8
-// dims of its partner chunk c ^ 4 and the chunk's (cos, sin) pairs; the
-// result is rounded to bf16 and returned as fp32.
-__device__ __forceinline__ void rope_chunk(const float (&x)[8], const float (&y)[8], int c,
-                                           const float4 (&t)[4], float (&out)[8]) {
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const float cs_c = (e & 1) ? t[e >> 1].z : t[e >> 1].x;
-    const float cs_s = (e & 1) ? t[e >> 1].w : t[e >> 1].y;
-    // c < 4: x is element i, y element i + 32:  x' = fma(x, cos, -(y sin))
-    // c >= 4: x is element i + 32, y element i: x' = fma(x, cos, y sin)
-    const float r = (c < 4) ? __fmaf_rn(x[e], cs_c, -__fmul_rn(y[e], cs_s))
-                            : __fmaf_rn(x[e], cs_c, __fmul_rn(y[e], cs_s));
-    out[e] = __bfloat162float(__float2bfloat16_rn(r));
-  }
-}
-
-__device__ __forceinline__ void unpack8(const uint4 w, float (&x)[8]) {
+// The 8 bf16 dims of a 16-byte chunk as 4 packed fp32 pairs.
+__device__ __forceinline__ void unpack8x2(const uint4 w, uint64_t (&x)[4]) {
   const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    x[2 * e] = bf16lo_to_f32(u[e]);
-    x[2 * e + 1] = bf16hi_to_f32(u[e]);
+  for (int e = 0; e < 4; ++e) x[e] = f2_pack(bf16lo_to_f32(u[e]), bf16hi_to_f32(u[e]));
+}
+
+// Rotate the 8 dims of chunk c (dims 8c..8c+7 of a 64-dim row) given the 8
+// dims of its partner chunk c ^ 4 and the chunk's (cos, sin) pairs, two dims
+// per packed instruction; the result is rounded to bf16 and returned as fp32
+// pairs.  c < 4: x holds element i, y element i + 32, x' = fma(x, cos,
+// -(y sin)); c >= 4: x holds element i + 32, y element i, x' = fma(x, cos,
+// y sin).  The sign is folded into sin: y (-sin) is exactly -(y sin).
+__device__ __forceinline__ void rope_chunk2(const uint64_t (&x)[4], const uint64_t (&y)[4], int c,
+                                            const float4 (&t)[4], uint64_t (&out)[4]) {
+  const float sg = (c < 4) ? -1.f : 1.f;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const uint64_t cs = f2_pack(t[u].x, t[u].z);
+    const uint64_t sn = f2_pack(sg * t[u].y, sg * t[u].w);
+    float r0, r1;
+    f2_unpack(f2_fma(x[u], cs, f2_mul(y[u], sn)), r0, r1);
+    const uint32_t h = pack_bf16x2(r0, r1);  // round to nearest even
+    out[u] = f2_pack(bf16lo_to_f32(h), bf16hi_to_f32(h));
   }
 }
 
@@ -199,23 +200,28 @@ __global__ void __launch_bounds__(dec::kThreads)
 
   // ------------------------------------------------------------ consumers
   // q' = R(m) q, the 8 dims of chunk cl (every lane group holds a copy).
-  float qr[8];
+  uint64_t q2[4];
   {
     const uint4* qrow = reinterpret_cast<const uint4*>(q + (static_cast<long long>(b) * H + h) * 64);
     const uint4 w = __ldg(qrow + cl);
     if constexpr (kRot) {
-      float x[8], y[8];
+      uint64_t x[4], y[4];
       float4 t[4];
       load_pairs(rope.cs + static_cast<long long>(bad ? 0 : m_pos) * 32, cl, t);
-      unpack8(w, x);
-      unpack8(shfl_xor_u4(w, 4), y);
-      rope_chunk(x, y, cl, t, qr);
+      unpack8x2(w, x);
+      unpack8x2(shfl_xor_u4(w, 4), y);
+      rope_chunk2(x, y, cl, t, q2);
     } else {
-      unpack8(w, qr);
+      unpack8x2(w, q2);
     }
   }
 
-  float m = -INFINITY, l = 0.f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  // Online softmax of each lane group against a reference max m_ref (log2
+  // units) that moves only when a score exceeds it by more than 2^8 (exact:
+  // o and l keep a common reference, so the usual rescale of every key is
+  // skipped); o as 4 packed pairs.
+  float m_ref = -INFINITY, l = 0.f;
+  uint64_t o2[4] = {0, 0, 0, 0};
   const int row = 4 * warp + grp;  // this lane group's row of every stage
   bool ok = true;
   for (int i = 0; ok && i < n_st; ++i) {
@@ -225,7 +231,7 @@ __global__ void __launch_bounds__(dec::kThreads)
     const uint4 wk = *reinterpret_cast<const uint4*>(st + sw128_offset(row, cl));
     const uint4 wv = *reinterpret_cast<const uint4*>(st + kKvBytes + sw128_offset(row, cl));
     const bool live = kbeg + kKeys * i + row < k_end;
-    float kr[8];
+    uint64_t k2[4];
     if constexpr (kRot) {
       float4 tb[4];
       // Pairs 8q .. 8q + 7 (q = cl & 3): half q >> 1 of the row, 16-byte
@@ -234,35 +240,47 @@ __global__ void __launch_bounds__(dec::kThreads)
 #pragma unroll
       for (int u = 0; u < 4; ++u)
         tb[u] = *reinterpret_cast<const float4*>(half + sw128_offset(row, 4 * (cl & 1) + u));
-      float x[8], y[8];
-      unpack8(wk, x);
-      unpack8(shfl_xor_u4(wk, 4), y);
-      rope_chunk(x, y, cl, tb, kr);
+      uint64_t x[4], y[4];
+      unpack8x2(wk, x);
+      unpack8x2(shfl_xor_u4(wk, 4), y);
+      rope_chunk2(x, y, cl, tb, k2);
     } else {
-      unpack8(wk, kr);
+      unpack8x2(wk, k2);
     }
-    float dot = 0.f;
+    uint64_t d2 = f2_mul(q2[0], k2[0]);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) dot = __fmaf_rn(qr[e], kr[e], dot);
+    for (int u = 1; u < 4; ++u) d2 = f2_fma(q2[u], k2[u], d2);
+    float d0, d1;
+    f2_unpack(d2, d0, d1);
+    float dot = d0 + d1;
     dot += __shfl_xor_sync(0xffffffffu, dot, 1);
     dot += __shfl_xor_sync(0xffffffffu, dot, 2);
     dot += __shfl_xor_sync(0xffffffffu, dot, 4);
-    float vv[8];
-    unpack8(wv, vv);
+    uint64_t v2[4];
+    unpack8x2(wv, v2);
     // Every value read from the stage is in registers now: release it.
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
     if (live) {
       const float sc = dot * scale_log2;
-      const float mn = fmaxf(m, sc);
-      const float a = (m == -INFINITY) ? 0.f : ex2_approx(m - mn);
-      const float p = ex2_approx(sc - mn);
-      l = l * a + p;
+      if (sc > m_ref + 8.f) {  // also the group's first key (m_ref = -inf)
+        const float a = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - sc);
+        const uint64_t a2 = f2_pack(a, a);
+        l *= a;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = __fmaf_rn(p, vv[e], o[e] * a);
-      m = mn;
+        for (int u = 0; u < 4; ++u) o2[u] = f2_mul(o2[u], a2);
+        m_ref = sc;
+      }
+      const float pk = ex2_approx(sc - m_ref);
+      const uint64_t p2 = f2_pack(pk, pk);
+      l += pk;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) o2[u] = f2_fma(p2, v2[u], o2[u]);
     }
   }
+  float m = m_ref, o[8];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) f2_unpack(o2[u], o[2 * u], o[2 * u + 1]);
   // Merge the 4 lane groups (lanes cl, cl + 8, cl + 16, cl + 24).
 #pragma unroll
   for (int sh = 8; sh <= 16; sh <<= 1) {
