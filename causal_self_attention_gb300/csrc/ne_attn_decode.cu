@@ -17,11 +17,14 @@
 //      of the RoPE table as two boxes of half rows (4 KiB each), all with the
 //      128-byte swizzle, so that the warps' reads spread over the banks (the
 //      table rows read contiguously made 8-way bank conflicts).  Warps 0-7
-//      take 4 keys of each stage; eight lanes share one 128-byte key row
-//      (lane l: chunk l % 8, 16 bytes), its RoPE partner chunk comes from
-//      lane l ^ 4 by a shuffle.  A group of eight lanes keeps its own online
-//      softmax (max, sum, the 8 output dims of its chunk); groups, then
-//      warps, are merged and the CTA writes one partial (m, l, o[64]).
+//      take 4 keys of each stage; eight lanes share one 128-byte key row,
+//      lane c holding dims 4c .. 4c + 3 and their RoPE partners 32 + 4c ..
+//      32 + 4c + 3, so that it rotates its own dims with one read of the 4
+//      (cos, sin) pairs they share (an earlier layout, 16 contiguous bytes
+//      per lane, read every table pair twice and fetched the partner dims by
+//      shuffles: 3.99-4.16 TB/s).  A group of eight lanes keeps its own
+//      online softmax (max, sum, its 8 output dims); groups, then warps,
+//      are merged and the CTA writes one partial (m, l, o[64]).
 //      Three CTAs per SM (24 consumer warps) measured best: 3.86 TB/s at
 //      B8 H12 Tmax16384 against 2.69 with 4 warps and 8 stages -- the
 //      consumers' per-key chain (swizzled loads, RoPE, dot, shuffles, exp)
@@ -33,7 +36,7 @@
 // forward multiplies.  kRot = false: the caller passes q' and a cache of
 // rotated keys k' (as the training forward or the QKV projection with RoPE
 // writes them); nothing is rotated, no table rows are loaded, and a ring
-// of 4 stages holds only the K and V boxes (40 registers, 5 CTAs per SM).
+// of 4 stages holds only the K and V boxes (5 CTAs per SM).
 #include "ne_sm100.cuh"
 
 namespace ne {
@@ -61,47 +64,67 @@ struct Smem {
 constexpr int kPartFloats = 68;      // m, l, 2 pad, o[64] (16-byte multiple)
 }  // namespace dec
 
-// The 8 (cos, sin) pairs of the dims of chunk c (dims 8(c & 3) .. + 7 of the
-// 32 frequencies) of table row `cs` (one position), as 4 float4.
-__device__ __forceinline__ void load_pairs(const float2* __restrict__ cs, int c, float4 (&t)[4]) {
-  const float4* p = reinterpret_cast<const float4*>(cs + 8 * (c & 3));
-#pragma unroll
-  for (int u = 0; u < 4; ++u) t[u] = __ldg(p + u);
+// Lane c (0..7) of a key's lane group holds the 8 dims {4c .. 4c + 3} and
+// their RoPE partners {32 + 4c .. 32 + 4c + 3}, as 4 packed fp32 pairs: [0], [1]
+// the low quad, [2], [3] the high quad.  A lane then rotates its own dims
+// with the 4 (cos, sin) pairs of frequencies 4c .. 4c + 3 (two float4s) and
+// no partner exchange.
+
+// bf16 words (lo, hi quad: 8 bytes each) -> 4 packed fp32 pairs.
+__device__ __forceinline__ void unpack_quads(uint2 lo, uint2 hi, uint64_t (&x)[4]) {
+  x[0] = f2_pack(bf16lo_to_f32(lo.x), bf16hi_to_f32(lo.x));
+  x[1] = f2_pack(bf16lo_to_f32(lo.y), bf16hi_to_f32(lo.y));
+  x[2] = f2_pack(bf16lo_to_f32(hi.x), bf16hi_to_f32(hi.x));
+  x[3] = f2_pack(bf16lo_to_f32(hi.y), bf16hi_to_f32(hi.y));
 }
 
-// The 8 bf16 dims of a 16-byte chunk as 4 packed fp32 pairs.
-__device__ __forceinline__ void unpack8x2(const uint4 w, uint64_t (&x)[4]) {
-  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+// Rotate a lane's 8 dims with the fp32 rule of the training kernels: dim i of
+// the low half gets fma(x_i, cos, -(x_{i+32} sin)), dim i + 32 gets
+// fma(x_{i+32}, cos, x_i sin) (x (-sin) is exactly -(x sin)); each result is
+// rounded to bf16 and kept as fp32.  t[0], t[1]: (cos, sin, cos, sin) of
+// frequencies 4c, 4c + 1 and 4c + 2, 4c + 3.
+__device__ __forceinline__ void rope_quads(const uint64_t (&x)[4], const float4 (&t)[2],
+                                           uint64_t (&out)[4]) {
 #pragma unroll
-  for (int e = 0; e < 4; ++e) x[e] = f2_pack(bf16lo_to_f32(u[e]), bf16hi_to_f32(u[e]));
-}
-
-// Rotate the 8 dims of chunk c (dims 8c..8c+7 of a 64-dim row) given the 8
-// dims of its partner chunk c ^ 4 and the chunk's (cos, sin) pairs, two dims
-// per packed instruction; the result is rounded to bf16 and returned as fp32
-// pairs.  c < 4: x holds element i, y element i + 32, x' = fma(x, cos,
-// -(y sin)); c >= 4: x holds element i + 32, y element i, x' = fma(x, cos,
-// y sin).  The sign is folded into sin: y (-sin) is exactly -(y sin).
-__device__ __forceinline__ void rope_chunk2(const uint64_t (&x)[4], const uint64_t (&y)[4], int c,
-                                            const float4 (&t)[4], uint64_t (&out)[4]) {
-  const float sg = (c < 4) ? -1.f : 1.f;
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
+  for (int u = 0; u < 2; ++u) {
     const uint64_t cs = f2_pack(t[u].x, t[u].z);
-    const uint64_t sn = f2_pack(sg * t[u].y, sg * t[u].w);
-    float r0, r1;
-    f2_unpack(f2_fma(x[u], cs, f2_mul(y[u], sn)), r0, r1);
-    const uint32_t h = pack_bf16x2(r0, r1);  // round to nearest even
-    out[u] = f2_pack(bf16lo_to_f32(h), bf16hi_to_f32(h));
+    const uint64_t sn = f2_pack(t[u].y, t[u].w);
+    const uint64_t nsn = f2_pack(-t[u].y, -t[u].w);
+    float a0, a1, b0, b1;
+    f2_unpack(f2_fma(x[u], cs, f2_mul(x[u + 2], nsn)), a0, a1);
+    f2_unpack(f2_fma(x[u + 2], cs, f2_mul(x[u], sn)), b0, b1);
+    const uint32_t ha = pack_bf16x2(a0, a1), hb = pack_bf16x2(b0, b1);  // round to nearest even
+    out[u] = f2_pack(bf16lo_to_f32(ha), bf16hi_to_f32(ha));
+    out[u + 2] = f2_pack(bf16lo_to_f32(hb), bf16hi_to_f32(hb));
   }
 }
 
-__device__ __forceinline__ uint4 shfl_xor_u4(uint4 w, int m) {
-  w.x = __shfl_xor_sync(0xffffffffu, w.x, m);
-  w.y = __shfl_xor_sync(0xffffffffu, w.y, m);
-  w.z = __shfl_xor_sync(0xffffffffu, w.z, m);
-  w.w = __shfl_xor_sync(0xffffffffu, w.w, m);
-  return w;
+// A lane's two quads of a 128-byte-swizzled 64-dim bf16 row in shared memory.
+// Lane groups of odd index load the high quad first, so that the 4 rows one
+// warp instruction touches fall half on each half of the banks.
+__device__ __forceinline__ void load_quads(const uint8_t* base, int row, int c, int grp,
+                                           uint2& lo, uint2& hi) {
+  const int first = grp & 1;  // 0: low quad first
+  const uint32_t in = (c & 1) * 8;
+  const uint2 a = *reinterpret_cast<const uint2*>(base + sw128_offset(row, 4 * first + (c >> 1)) + in);
+  const uint2 b = *reinterpret_cast<const uint2*>(base + sw128_offset(row, 4 * (first ^ 1) + (c >> 1)) + in);
+  lo = first ? b : a;
+  hi = first ? a : b;
+}
+
+// The (cos, sin) pairs of frequencies 4c .. 4c + 3 of a stage's table row:
+// half c >> 2 of the row (pairs 16 (c >> 2) ..), 16-byte units 2 (c & 3) and
+// 2 (c & 3) + 1 of that half.  Lanes of the second half take their units in
+// the other order, so that one instruction reads even units of one half and
+// odd units of the other (no two lanes of a row on the same banks).
+__device__ __forceinline__ void load_table_quads(const uint8_t* halves, int row, int c,
+                                                 float4 (&t)[2]) {
+  const int sw = c >> 2;
+  const uint8_t* h = halves + sw * dec::kKvBytes;
+  const float4 a = *reinterpret_cast<const float4*>(h + sw128_offset(row, 2 * (c & 3) + sw));
+  const float4 b = *reinterpret_cast<const float4*>(h + sw128_offset(row, 2 * (c & 3) + 1 - sw));
+  t[0] = sw ? b : a;
+  t[1] = sw ? a : b;
 }
 
 // Merge online-softmax state (m, l, o[8]) with another (log2 units).
@@ -116,8 +139,12 @@ __device__ __forceinline__ void merge_state(float& m, float& l, float (&o)[8], f
   m = mn;
 }
 
+// Registers: the rotating instantiation is left free (70 per thread: its
+// per-key chain of table reads, rotation and dot keeps more values live; with
+// the compiler's default 52 it ran 8% slower on decode16k); the other is held
+// to 5 CTAs per SM (40 per thread).
 template <bool kRot>
-__global__ void __launch_bounds__(dec::kThreads)
+__global__ void __launch_bounds__(dec::kThreads, kRot ? 1 : 5)
     ne_attn_decode_split_kernel(const __grid_constant__ CUtensorMap tmK,
                                 const __grid_constant__ CUtensorMap tmV,
                                 const __grid_constant__ CUtensorMap tmT,
@@ -140,7 +167,7 @@ __global__ void __launch_bounds__(dec::kThreads)
   // 12 neighbouring 128-byte pieces of the same cache rows.
   const int h = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int cl = lane & 7;   // 16-byte chunk of the row this lane holds
+  const int cl = lane & 7;   // this lane's dims: 4cl..4cl+3 and 32+4cl..32+4cl+3
   const int grp = lane >> 3; // which of the warp's 4 keys per stage
 
   const int m_pos = __ldg(pos + b);
@@ -199,20 +226,20 @@ __global__ void __launch_bounds__(dec::kThreads)
   }
 
   // ------------------------------------------------------------ consumers
-  // q' = R(m) q, the 8 dims of chunk cl (every lane group holds a copy).
+  // q' = R(m) q, this lane's 8 dims (every lane group holds a copy).
   uint64_t q2[4];
   {
-    const uint4* qrow = reinterpret_cast<const uint4*>(q + (static_cast<long long>(b) * H + h) * 64);
-    const uint4 w = __ldg(qrow + cl);
+    const uint2* qrow = reinterpret_cast<const uint2*>(q + (static_cast<long long>(b) * H + h) * 64);
+    uint64_t x[4];
+    unpack_quads(__ldg(qrow + cl), __ldg(qrow + 8 + cl), x);
     if constexpr (kRot) {
-      uint64_t x[4], y[4];
-      float4 t[4];
-      load_pairs(rope.cs + static_cast<long long>(bad ? 0 : m_pos) * 32, cl, t);
-      unpack8x2(w, x);
-      unpack8x2(shfl_xor_u4(w, 4), y);
-      rope_chunk2(x, y, cl, t, q2);
+      const float4* tq = reinterpret_cast<const float4*>(
+          rope.cs + static_cast<long long>(bad ? 0 : m_pos) * 32 + 4 * cl);
+      const float4 t[2] = {__ldg(tq), __ldg(tq + 1)};
+      rope_quads(x, t, q2);
     } else {
-      unpack8x2(w, q2);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) q2[u] = x[u];
     }
   }
 
@@ -228,24 +255,19 @@ __global__ void __launch_bounds__(dec::kThreads)
     const int s = i % kStages;
     if (!(ok = mbar_wait_warp(&full[s], (i / kStages) & 1, abort_flag, status, 51))) break;
     const uint8_t* st = smem + s * kStageBytes;
-    const uint4 wk = *reinterpret_cast<const uint4*>(st + sw128_offset(row, cl));
-    const uint4 wv = *reinterpret_cast<const uint4*>(st + kKvBytes + sw128_offset(row, cl));
+    uint2 klo, khi, vlo, vhi;
+    load_quads(st, row, cl, grp, klo, khi);
+    load_quads(st + kKvBytes, row, cl, grp, vlo, vhi);
     const bool live = kbeg + kKeys * i + row < k_end;
     uint64_t k2[4];
     if constexpr (kRot) {
-      float4 tb[4];
-      // Pairs 8q .. 8q + 7 (q = cl & 3): half q >> 1 of the row, 16-byte
-      // units 4 (q & 1) .. + 3 of that half, swizzled like K and V.
-      const uint8_t* half = st + (2 + ((cl & 3) >> 1)) * kKvBytes;
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        tb[u] = *reinterpret_cast<const float4*>(half + sw128_offset(row, 4 * (cl & 1) + u));
-      uint64_t x[4], y[4];
-      unpack8x2(wk, x);
-      unpack8x2(shfl_xor_u4(wk, 4), y);
-      rope_chunk2(x, y, cl, tb, k2);
+      float4 tb[2];
+      load_table_quads(st + 2 * kKvBytes, row, cl, tb);
+      uint64_t x[4];
+      unpack_quads(klo, khi, x);
+      rope_quads(x, tb, k2);
     } else {
-      unpack8x2(wk, k2);
+      unpack_quads(klo, khi, k2);
     }
     uint64_t d2 = f2_mul(q2[0], k2[0]);
 #pragma unroll
@@ -257,7 +279,7 @@ __global__ void __launch_bounds__(dec::kThreads)
     dot += __shfl_xor_sync(0xffffffffu, dot, 2);
     dot += __shfl_xor_sync(0xffffffffu, dot, 4);
     uint64_t v2[4];
-    unpack8x2(wv, v2);
+    unpack_quads(vlo, vhi, v2);
     // Every value read from the stage is in registers now: release it.
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
@@ -293,7 +315,10 @@ __global__ void __launch_bounds__(dec::kThreads)
   }
   if (lane < 8) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) red[warp][2 + 8 * cl + e] = o[e];
+    for (int e = 0; e < 4; ++e) {
+      red[warp][2 + 4 * cl + e] = o[e];
+      red[warp][2 + 32 + 4 * cl + e] = o[4 + e];
+    }
     if (lane == 0) {
       red[warp][0] = m;
       red[warp][1] = l;
