@@ -35,6 +35,8 @@ cudaError_t launch_debug_umma(int form, const __nv_bfloat16* a, const __nv_bfloa
 cudaError_t launch_debug_pipeline(const CUtensorMap& tm, int n_items, int drop_item,
                                   long long limit, float* d, int* status, cudaStream_t stream);
 std::vector<int> unit_steps(int nseq, int H, int T);
+cudaError_t launch_compact_items(const Problem& pb, int kind, int n_blocks, int n_buckets,
+                                 int* out, cudaStream_t stream);
 std::vector<int> pack_schedule(const std::vector<int>& w, int G, double c_lo, double c_hi);
 size_t decode_part_bytes(int B, int H, int Tmax);
 cudaError_t launch_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmT,
@@ -369,6 +371,16 @@ ne::Problem make_problem(const Shape& s) {
   return pb;
 }
 
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Packed (varlen) batches: the persistent kernels deal the non-empty items of
+// their work lists, longest first, as sorted on the device by a one-CTA
+// kernel (ne_sched.cu) into a per-stream temporary, up to this many items
+// (beyond, that single CTA would take longer than the imbalance it removes
+// may save; the kernels then deal the whole list).
+constexpr long long kMaxCompactItems = 1 << 16;
+constexpr int kMaxBuckets = 8192;  // its counting sort's buckets (shared memory, 32 KB)
+
 // Sequence length from which the forward rotates the keys once per call in a
 // pass of its own instead of in every item that uses a key tile (measured on
 // GB300: below it the extra pass costs more than the kernel saves).
@@ -421,20 +433,34 @@ ne_status run_fwd(const Shape& s, const void* q, const void* k, const void* v, f
   CUtensorMap tq, tk, tv, to;
   const void* queries = mode == Rot::kTrain ? qr_out : q;
   const void* keys = mode == Rot::kTrain ? kr_out : k;
+  // Temporaries: the rotated keys (long sequences) and, for a packed batch,
+  // the compacted item list.
+  const int nblk = (n_qtiles + 1) / 2;
+  const long long n_items = static_cast<long long>(nblk) * s.nseq * s.H;
+  const bool compact = !s.fixed && n_items <= kMaxCompactItems && 2 * nblk + 1 <= kMaxBuckets;
+  const size_t kr_bytes =
+      (mode == Rot::kRotate && !p.rotate_k) ? static_cast<size_t>(s.n_tot) * s.H * 64 * 2 : 0;
+  const size_t tmp_bytes =
+      align256(kr_bytes) + (compact ? static_cast<size_t>(n_items + 1) * sizeof(int) : 0);
   bool own = false;
+  void* tmp = nullptr;
   void* kr = nullptr;
+  int* list = nullptr;
   cudaError_t e = cudaSuccess;
-  if (mode == Rot::kRotate && !p.rotate_k) {
-    const size_t kr_bytes = static_cast<size_t>(s.n_tot) * s.H * 64 * 2;
+  if (tmp_bytes) {
     cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(cs, &capture) != cudaSuccess) return NE_ERR_CUDA;
     own = capture != cudaStreamCaptureStatusNone;
     if (own) {
-      if ((e = cudaMallocAsync(&kr, kr_bytes, cs)) != cudaSuccess) return cuda_status(e);
-    } else if ((rc = stream_scratch(*st, cs, kr_bytes, &kr)) != NE_OK) {
+      if ((e = cudaMallocAsync(&tmp, tmp_bytes, cs)) != cudaSuccess) return cuda_status(e);
+    } else if ((rc = stream_scratch(*st, cs, tmp_bytes, &tmp)) != NE_OK) {
       return rc;
     }
-    keys = kr;
+    if (kr_bytes) {
+      kr = tmp;
+      keys = kr;
+    }
+    if (compact) list = reinterpret_cast<int*>(static_cast<char*>(tmp) + align256(kr_bytes));
   }
   rc = encode_rows(&tq, queries, s.n_tot, s.H);
   if (rc == NE_OK) rc = encode_rows(&tk, keys, s.n_tot, s.H);
@@ -453,17 +479,19 @@ ne_status run_fwd(const Shape& s, const void* q, const void* k, const void* v, f
                                static_cast<__nv_bfloat16*>(kr_out), p.pb, p.rope, cs);
     const bool pass = (mode == Rot::kRotate && !p.rotate_k) || mode == Rot::kTrain;
     if (e == cudaSuccess && g_ev_rot && pass) e = cudaEventRecord(g_ev_rot, cs);
+    if (e == cudaSuccess && compact) {
+      e = ne::launch_compact_items(p.pb, 0, nblk, 2 * nblk + 1, list, cs);
+      p.compact = list;
+    }
     if (e == cudaSuccess) e = ne::launch_fwd(tq, tk, tv, to, p, n_qtiles, cs);
   }
   if (own) {
-    const cudaError_t e2 = cudaFreeAsync(kr, cs);
+    const cudaError_t e2 = cudaFreeAsync(tmp, cs);
     if (e == cudaSuccess) e = e2;
   }
   if (rc != NE_OK) return rc;
   return cuda_status(e);
 }
-
-size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // kRotate: q, k as given; kPreRotated: q, k are q', k' and the gradients
 // returned are w.r.t. them; kTrain: q, k are q', k' (from the training
@@ -535,15 +563,48 @@ ne_status run_bwd(const Shape& s, const void* q, const void* k, const void* v, c
     p.qr = const_cast<__nv_bfloat16*>(p.q);
     p.kr = const_cast<__nv_bfloat16*>(p.k);
   }
+  // Packed batch: the compacted unit list in the library's temporary for this
+  // stream (a stream-ordered allocation of the call's own during capture).
+  const long long n_units = static_cast<long long>(n_tiles) * s.nseq * s.H;
+  const bool compact = !s.fixed && n_units <= kMaxCompactItems && n_tiles + 1 <= kMaxBuckets;
+  int* list = nullptr;
+  bool own_list = false;
+  if (compact) {
+    const size_t list_bytes = static_cast<size_t>(n_units + 1) * sizeof(int);
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(cs, &capture) != cudaSuccess) rc = NE_ERR_CUDA;
+    own_list = capture != cudaStreamCaptureStatusNone;
+    void* lp = nullptr;
+    if (rc == NE_OK) {
+      if (own_list) {
+        const cudaError_t e = cudaMallocAsync(&lp, list_bytes, cs);
+        if (e != cudaSuccess) rc = cuda_status(e);
+      } else {
+        rc = stream_scratch(*st, cs, list_bytes, &lp);
+      }
+    }
+    list = static_cast<int*>(lp);
+    if (rc != NE_OK) own_list = false;
+  }
   CUtensorMap tdq, tdv, tdk;
-  rc = encode_rows(&tq, p.qr, s.n_tot, s.H);
+  if (rc == NE_OK) rc = encode_rows(&tq, p.qr, s.n_tot, s.H);
   if (rc == NE_OK) rc = encode_rows(&tk, p.kr, s.n_tot, s.H);
   if (rc == NE_OK) rc = encode_rows_f32(&tdq, p.dq_acc, s.n_tot, s.H);
   if (rc == NE_OK) rc = encode_rows(&tdv, dv, s.n_tot, s.H);
   if (rc == NE_OK) rc = encode_rows(&tdk, dk, s.n_tot, s.H);
-  cudaError_t e = rc == NE_OK ? ne::launch_bwd(tq, tk, tv, tdo, tdq, tdv, tdk, p, n_tiles, cs,
-                                                g_ev_pre, g_ev_main)
-                              : cudaErrorInvalidValue;
+  cudaError_t e = cudaSuccess;
+  if (rc == NE_OK && compact) {
+    e = ne::launch_compact_items(p.pb, 1, n_tiles, n_tiles + 1, list, cs);
+    p.compact = list;
+  }
+  if (rc == NE_OK && e == cudaSuccess)
+    e = ne::launch_bwd(tq, tk, tv, tdo, tdq, tdv, tdk, p, n_tiles, cs, g_ev_pre, g_ev_main);
+  else if (rc != NE_OK)
+    e = cudaErrorInvalidValue;
+  if (own_list) {
+    const cudaError_t e2 = cudaFreeAsync(list, cs);
+    if (e == cudaSuccess) e = e2;
+  }
   if (owned) {
     cudaError_t e2 = cudaFreeAsync(ws, cs);
     if (e == cudaSuccess) e = e2;

@@ -125,11 +125,15 @@ __global__ void __launch_bounds__(256)
                                   const __nv_bfloat16* __restrict__ dout,
                                   __nv_bfloat16* __restrict__ qr, __nv_bfloat16* __restrict__ kr,
                                   float* __restrict__ delta, float* __restrict__ dq_acc,
-                                  const Problem pb, RopeTable rope, int rotate_in) {
+                                  const Problem pb, RopeTable rope, int rotate_in,
+                                  int* status) {
   pdl_wait();  // the forward that wrote O (and anything before it) has completed
   const int seq = blockIdx.y;
   int start, len;
-  if (!seq_bounds(pb, seq, start, len, nullptr)) return;
+  // A sequence whose cu_seqlens bounds are invalid is skipped by all three
+  // kernels; the first CTA of its row reports it.
+  if (!seq_bounds(pb, seq, start, len, (blockIdx.x == 0 && threadIdx.x == 0) ? status : nullptr))
+    return;
   const int t0 = blockIdx.x * bwd::kPreRows;
   if (t0 >= len) return;
   const int H = pb.H;
@@ -232,7 +236,7 @@ __device__ __forceinline__ bool get_unit(const BwdParams& p, int r, Unit& u) {
 __device__ __forceinline__ int next_unit(const BwdParams& p, int n_units, int c, int G, int k,
                                          Unit& u) {
   for (;; ++k) {
-    const int r = dealt_item(p.sched, k, c, G, n_units);
+    const int r = dealt_item(p.sched, p.compact, k, c, G, n_units);
     if (r >= n_units) return -1;
     if (get_unit(p, r, u)) return k;
   }
@@ -311,8 +315,8 @@ __global__ void __launch_bounds__(512, 1)
   float* sDEL = reinterpret_cast<float*>(smem + OFF_DEL);
   // The units of this CTA, in order (the same sequence in every role).
 #define NE_FOR_EACH_UNIT(u)                                                                   \
-  for (int k_ = 0, r_ = dealt_item(p.sched, 0, cta, G, n_units); r_ < n_units;                \
-       ++k_, r_ = dealt_item(p.sched, k_, cta, G, n_units))                                      \
+  for (int k_ = 0, r_ = dealt_item(p.sched, p.compact, 0, cta, G, n_units); r_ < n_units;     \
+       ++k_, r_ = dealt_item(p.sched, p.compact, k_, cta, G, n_units))                           \
     if (Unit u; get_unit(p, r_, u))
 
   if (warp == 13 || warp == 15) {
@@ -933,7 +937,7 @@ cudaError_t launch_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
   if (pm.sched && pm.sched_ctas != G) pm.sched = nullptr;  // made for another grid: snake order
   dim3 pre_grid((n_tiles * kBM + bwd::kPreRows - 1) / bwd::kPreRows, p.pb.nseq);
   e = launch_pdl(ne_attn_bwd_preprocess_kernel, pre_grid, dim3(256), 0, stream, p.q, p.k, p.out,
-                 p.dout, p.qr, p.kr, p.delta, p.dq_acc, p.pb, p.rope, p.rotate_in);
+                 p.dout, p.qr, p.kr, p.delta, p.dq_acc, p.pb, p.rope, p.rotate_in, p.status);
   if (e != cudaSuccess) return e;
   if (ev_pre && (e = cudaEventRecord(ev_pre, stream)) != cudaSuccess) return e;
   e = launch_pdl(ne_attn_bwd_kernel, dim3(G), dim3(bwd::kThreads), bwd::SMEM_BYTES, stream, tmQ,

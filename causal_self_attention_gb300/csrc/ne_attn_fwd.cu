@@ -200,8 +200,8 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
   uint8_t* sV = smem + OFF_V;
   // The items of this CTA, in order (the same sequence in every role).
 #define NE_FOR_EACH_ITEM(it)                                                        \
-  for (int k_ = 0, r_ = dealt_item(nullptr, 0, cta, G, n_items); r_ < n_items;                 \
-       ++k_, r_ = dealt_item(nullptr, k_, cta, G, n_items))                                       \
+  for (int k_ = 0, r_ = dealt_item(nullptr, p.compact, 0, cta, G, n_items); r_ < n_items;       \
+       ++k_, r_ = dealt_item(nullptr, p.compact, k_, cta, G, n_items))                             \
     if (Item it; get_item(p, nblk, r_, it, threadIdx.x == 0))
 
   if (warp == 13 || warp == 14) {

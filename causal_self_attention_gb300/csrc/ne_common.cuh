@@ -56,6 +56,7 @@ struct FwdParams {
   int rotate_k;      // 1: K tiles are loaded un-rotated and rotated in smem;
                      // 0: the keys come pre-rotated (k')
   int rotate_q;      // 1: Q tiles are rotated in smem; 0: the caller passed q'
+  const int* compact = nullptr;  // packed batch: the non-empty items (dealt_item), or nullptr
 };
 
 struct BwdParams {
@@ -82,6 +83,7 @@ struct BwdParams {
                    // 0: the gradients w.r.t. q', k' themselves
   const int* sched = nullptr;  // work schedule of the persistent main kernel, or
   int sched_ctas = 0;          // nullptr for the snake order; the grid it was made for
+  const int* compact = nullptr;  // packed batch: the non-empty units (dealt_item), or nullptr
 };
 
 // Sequence bounds of sequence s.  Returns false (and raises the device status)
@@ -108,16 +110,21 @@ __device__ __forceinline__ bool seq_bounds(const Problem& pb, int s, int& start,
 // order of work items) of the k-th item of CTA c among G, or n when CTA c has
 // fewer than k + 1 items.  With a schedule -- offsets sched[0..G], then the
 // items of CTA c at sched[G + 1 + sched[c]] .. sched[G + 1 + sched[c + 1] - 1],
-// packed on the host -- its entries; without, rounds of G items dealt
+// packed on the host -- its entries.  Otherwise rounds of G items dealt
 // c = 0..G-1 in even rounds and G-1..0 in odd rounds, so that long and short
-// items mix.
-__device__ __forceinline__ int dealt_item(const int* sched, int k, int c, int G, int n) {
+// items mix: over all n indices, or, for a packed (varlen) batch, over the
+// list compact[1 .. compact[0]] of the items that are not empty (a short
+// sequence has no items for the higher blocks; dealt with their holes, they
+// left some CTAs with far more work than others).
+__device__ __forceinline__ int dealt_item(const int* sched, const int* compact, int k, int c,
+                                          int G, int n) {
   if (sched) {
     const int b = __ldg(sched + c), e = __ldg(sched + c + 1);
     return b + k < e ? __ldg(sched + G + 1 + b + k) : n;
   }
-  const int r = k * G + ((k & 1) ? (G - 1 - c) : c);
-  return r < n ? r : n;
+  const int m = k * G + ((k & 1) ? (G - 1 - c) : c);
+  if (compact) return m < __ldg(compact) ? __ldg(compact + 1 + m) : n;
+  return m < n ? m : n;
 }
 
 // Parameters of the projection GEMM (ne_proj.cu), shared by the launches in

@@ -1,4 +1,6 @@
-// ne_sched.cu -- work schedule of the persistent attention backward (host code).
+// ne_sched.cu -- work dealing of the persistent attention kernels: the
+// backward's schedule packed on the host for a fixed-length batch, and the
+// compaction of a packed batch's work lists on the device.
 //
 // The backward main kernel runs one CTA per SM over a list of work units of
 // unequal length, indexed longest first: unit r is key tile j = r / (nseq H)
@@ -33,7 +35,103 @@
 #include <numeric>
 #include <vector>
 
+#include "ne_sm100.cuh"
+
 namespace ne {
+
+// ---------------------------------------------------------------------------
+// Packed (variable-length) batches: the work lists of both persistent kernels
+// enumerate every (block, sequence, head), and a sequence shorter than the
+// longest has no items for the higher blocks.  Dealt with those holes, the
+// snake order left the busiest forward CTA at 1.6 times the mean work on a
+// batch of lengths 64..2048; without the holes but in block order, the
+// backward's units (whose length also depends on their sequence's length)
+// were worse still.  The lengths are on the device, so one CTA builds the
+// list there before the kernel runs: the items that are not empty, sorted by
+// their number of steps, longest first (a counting sort: steps are small
+// integers), which the kernel then deals in the snake order.  out[0] = the
+// number of items, out[1 ..] their indices; items of equal length in no fixed
+// order (every item is computed the same way by whichever CTA gets it).
+// Items of a sequence whose bounds are invalid are kept, last, so that the
+// kernel reports them as before.
+//   kind 0: forward items, r -> block n_blocks - 1 - r / (nseq H) (pairs of
+//           128-row query tiles), steps = key tiles of its last query tile;
+//   kind 1: backward units, r -> key tile r / (nseq H), steps = query tiles
+//           from it to the end of its sequence.
+// Bucket b of the sort holds the items of b steps; bucket 0 the kept items of
+// invalid sequences; -1 marks an empty item.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int item_bucket(const Problem& pb, int kind, int n_blocks, int r) {
+  const int per = pb.nseq * pb.H;
+  const int blk = r / per;
+  const int seq = (r - blk * per) / pb.H;
+  int start, len;
+  if (!seq_bounds(pb, seq, start, len, nullptr)) return 0;
+  if (kind == 0) {
+    const int b = n_blocks - 1 - blk;  // the item's block of two query tiles
+    if (2 * b * kBM >= len) return -1;
+    return (2 * b + 1) * kBM < len ? 2 * b + 2 : 2 * b + 1;
+  }
+  if (blk * kBM >= len) return -1;
+  return (len + kBM - 1) / kBM - blk;
+}
+
+// Add 1 to ctr[key] for every active lane, one atomic per distinct key in the
+// warp; returns this lane's slot among the lanes that added (old value + rank).
+__device__ __forceinline__ int warp_counted_add(int* ctr, int key, bool active) {
+  const unsigned act = __ballot_sync(0xffffffffu, active);
+  if (!active) return 0;
+  const int lane = threadIdx.x & 31;
+  const unsigned peers = __match_any_sync(act, key);
+  const int leader = __ffs(peers) - 1;
+  int base = 0;
+  if (lane == leader) base = atomicAdd(ctr + key, __popc(peers));
+  base = __shfl_sync(peers, base, leader);
+  return base + __popc(peers & ((1u << lane) - 1u));
+}
+
+__global__ void __launch_bounds__(1024)
+    ne_compact_items_kernel(const Problem pb, int kind, int n_blocks, int n_buckets,
+                            int* __restrict__ out) {
+  pdl_wait();  // cu_seqlens may come from the kernel before
+  extern __shared__ int bucket[];  // counts, then the next free slot of each bucket
+  const int n = n_blocks * pb.nseq * pb.H;
+  for (int b = threadIdx.x; b < n_buckets; b += blockDim.x) bucket[b] = 0;
+  __syncthreads();
+  for (int r0 = 0; r0 < n; r0 += blockDim.x) {
+    const int r = r0 + threadIdx.x;
+    const int b = r < n ? item_bucket(pb, kind, n_blocks, r) : -1;
+    warp_counted_add(bucket, b < 0 ? 0 : b, b >= 0);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {  // first slots: the most steps first, bucket 0 last
+    int at = 0;
+    for (int b = n_buckets - 1; b >= 1; --b) {
+      const int c = bucket[b];
+      bucket[b] = at;
+      at += c;
+    }
+    const int c0 = bucket[0];
+    bucket[0] = at;
+    out[0] = at + c0;
+  }
+  __syncthreads();
+  for (int r0 = 0; r0 < n; r0 += blockDim.x) {
+    const int r = r0 + threadIdx.x;
+    const int b = r < n ? item_bucket(pb, kind, n_blocks, r) : -1;
+    const int slot = warp_counted_add(bucket, b < 0 ? 0 : b, b >= 0);
+    if (b >= 0) out[1 + slot] = r;
+  }
+  pdl_launch_dependents();
+}
+
+// n_buckets: the largest number of steps an item can have, plus one.
+cudaError_t launch_compact_items(const Problem& pb, int kind, int n_blocks, int n_buckets,
+                                 int* out, cudaStream_t stream) {
+  return launch_pdl(ne_compact_items_kernel, dim3(1), dim3(1024),
+                    static_cast<size_t>(n_buckets) * sizeof(int), stream, pb, kind, n_blocks,
+                    n_buckets, out);
+}
 
 namespace {
 

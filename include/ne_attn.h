@@ -146,8 +146,10 @@ ne_status ne_attn_bwd_train(const ne_bf16* qr, const ne_bf16* kr, const ne_bf16*
  * cu_seqlens is DEVICE int32 [nseq + 1], nondecreasing, cu_seqlens[0] = 0,
  * cu_seqlens[nseq] = n_tot.  RoPE positions restart at 0 in every sequence and
  * attention never crosses a sequence boundary.  max_seqlen must be >= every
- * sequence length (a longer sequence is reported as NE_ERR_BAD_SEQLEN by
- * ne_attn_get_device_status and its tail is not computed).  lse: [H, n_tot]
+ * sequence length: a longer sequence (or one that cu_seqlens puts outside
+ * [0, n_tot]) is reported as NE_ERR_BAD_SEQLEN by ne_attn_get_device_status
+ * and skipped -- its rows of out and lse (and, in the backward, of dq, dk,
+ * dv) are not written; the other sequences are computed as usual.  lse: [H, n_tot]
  * fp32.  With equal lengths T this computes exactly what ne_attn_fwd computes
  * on [B, T, H, 64] (LSE layout aside). */
 ne_status ne_attn_varlen_fwd(const ne_bf16* q, const ne_bf16* k, const ne_bf16* v,

@@ -212,3 +212,28 @@ def test_key_rotation_paths_agree_bitwise():
     assert na.ne_attn_get_device_status() == 0
     for a, b in zip(outs[:2], outs[2:]):
         assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_varlen_sequence_longer_than_max_is_reported():
+    """cu_seqlens puts a sequence above max_seqlen: both directions report
+    NE_ERR_BAD_SEQLEN, skip that sequence (it is never read past the limit)
+    and compute the others exactly as a valid call does -- through the work
+    lists compacted on the device, which keep the bad sequence's items so
+    that the kernels see and report it."""
+    from causal_self_attention_gb300 import ne_attn as na
+    inp = make_custom(0, 0, 2, seed=77, lengths=[100, 300, 50])
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "dout"))
+    cu = inp["cu_seqlens"].cuda()
+    o_ref, lse_ref = na.ne_attn_varlen_fwd(q, k, v, cu, 300)
+    dq_ref, dk_ref, dv_ref = na.ne_attn_varlen_bwd(q, k, v, o_ref, do, lse_ref, cu, 300)
+    assert na.ne_attn_get_device_status() == 0
+    o, lse = na.ne_attn_varlen_fwd(q, k, v, cu, 200)
+    assert na.ne_attn_get_device_status() == 7  # NE_ERR_BAD_SEQLEN
+    dq, dk, dv = na.ne_attn_varlen_bwd(q, k, v, o_ref, do, lse_ref, cu, 200)
+    assert na.ne_attn_get_device_status() == 7
+    keep = torch.cat([torch.arange(0, 100), torch.arange(400, 450)]).cuda()
+    assert torch.equal(o[keep], o_ref[keep])
+    assert torch.equal(lse[:, keep], lse_ref[:, keep])
+    assert torch.equal(dk[keep], dk_ref[keep]) and torch.equal(dv[keep], dv_ref[keep])
+    assert torch.allclose(dq[keep].float(), dq_ref[keep].float(), atol=1e-2, rtol=0)
+    assert na.ne_attn_get_device_status() == 0
