@@ -170,14 +170,6 @@ __global__ void __launch_bounds__(dec::kThreads, kRot ? 1 : 5)
   const int cl = lane & 7;   // this lane's dims: 4cl..4cl+3 and 32+4cl..32+4cl+3
   const int grp = lane >> 3; // which of the warp's 4 keys per stage
 
-  const int m_pos = __ldg(pos + b);
-  const bool bad = (m_pos < 0 || m_pos >= Tmax);
-  if (bad && c == 0 && h == 0 && threadIdx.x == 0 && status) atomicCAS(status, 0, NE_DEV_BAD_SEQLEN);
-  const int n_keys = bad ? 0 : m_pos + 1;
-  const int kbeg = c * chunk;
-  const int k_end = min(kbeg + chunk, n_keys);
-  const int n_st = k_end > kbeg ? (k_end - kbeg + kKeys - 1) / kKeys : 0;  // stages of this CTA
-
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -187,6 +179,18 @@ __global__ void __launch_bounds__(dec::kThreads, kRot ? 1 : 5)
     mbar_fence_init();
   }
   __syncthreads();
+  // Launched with programmatic dependent launch: the set-up above overlaps the
+  // previous kernel on the stream (e.g. the one that appended to the cache).
+  pdl_wait();
+  pdl_launch_dependents();
+
+  const int m_pos = __ldg(pos + b);
+  const bool bad = (m_pos < 0 || m_pos >= Tmax);
+  if (bad && c == 0 && h == 0 && threadIdx.x == 0 && status) atomicCAS(status, 0, NE_DEV_BAD_SEQLEN);
+  const int n_keys = bad ? 0 : m_pos + 1;
+  const int kbeg = c * chunk;
+  const int k_end = min(kbeg + chunk, n_keys);
+  const int n_st = k_end > kbeg ? (k_end - kbeg + kKeys - 1) / kKeys : 0;  // stages of this CTA
 
   if (warp == kWarps) {
     // ------------------------------------------------------- TMA producer
@@ -352,6 +356,8 @@ __global__ void __launch_bounds__(32)
     ne_attn_decode_merge_kernel(const float* __restrict__ part, int n_chunks,
                                 __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
   using namespace dec;
+  pdl_wait();  // the split kernel's partials are complete
+  pdl_launch_dependents();
   const long long bh = blockIdx.x;
   const int lane = threadIdx.x;
   const float* src = part + bh * n_chunks * kPartFloats;
@@ -416,16 +422,16 @@ cudaError_t launch_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, const 
   const int chunk = big >= 1024 ? 1024 : dec::kChunkUnit;
   const int n_chunks = (Tmax + chunk - 1) / chunk;
   dim3 grid(H, n_chunks, B);
-  if (rot)
-    ne_attn_decode_split_kernel<true><<<grid, dec::kThreads, dec::Smem<true>::BYTES, stream>>>(
-        tmK, tmV, tmT, q, pos, H, Tmax, rope, scale_log2, part, chunk, n_chunks, status);
-  else
-    ne_attn_decode_split_kernel<false><<<grid, dec::kThreads, dec::Smem<false>::BYTES, stream>>>(
-        tmK, tmV, tmT, q, pos, H, Tmax, rope, scale_log2, part, chunk, n_chunks, status);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e =
+      rot ? launch_pdl(ne_attn_decode_split_kernel<true>, grid, dim3(dec::kThreads),
+                       dec::Smem<true>::BYTES, stream, tmK, tmV, tmT, q, pos, H, Tmax, rope,
+                       scale_log2, part, chunk, n_chunks, status)
+          : launch_pdl(ne_attn_decode_split_kernel<false>, grid, dim3(dec::kThreads),
+                       dec::Smem<false>::BYTES, stream, tmK, tmV, tmT, q, pos, H, Tmax, rope,
+                       scale_log2, part, chunk, n_chunks, status);
   if (e != cudaSuccess) return e;
-  ne_attn_decode_merge_kernel<<<B * H, 32, 0, stream>>>(part, n_chunks, out, lse);
-  return cudaGetLastError();
+  return launch_pdl(ne_attn_decode_merge_kernel, dim3(B * H), dim3(32), 0, stream, part, n_chunks,
+                    out, lse);
 }
 
 }  // namespace ne
