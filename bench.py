@@ -878,31 +878,38 @@ def run_decode(args):
     ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     gbs = kv_bytes / (ms * 1e-3) / 1e9
 
-    # End to end: the new token's q, k, v rows uploaded into the cache, O and
-    # LSE read back, every step (the cache itself stays resident, as a KV
-    # cache does).
-    h_q = inp["q"].pin_memory()
-    h_k = inp["k_cache"][:, -1].contiguous().pin_memory()
-    h_v = inp["v_cache"][:, -1].contiguous().pin_memory()
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    d_k = torch.empty_like(h_k, device=dev)
-    d_v = torch.empty_like(h_v, device=dev)
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v))
-    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+    # End to end: the new token's q, k, v rows uploaded (one copy of one
+    # contiguous block) and written into the cache, O and LSE read back (one
+    # copy: both are views of one device block), every step, one step after
+    # the other as a generation loop runs (the cache itself stays resident,
+    # as a KV cache does).
+    h_in = torch.stack([inp["q"], inp["k_cache"][:, -1], inp["v_cache"][:, -1]]).pin_memory()
+    d_in = torch.empty_like(h_in, device=dev)
+    o_bytes = out.numel() * out.element_size()
+    d_res = torch.empty(o_bytes + lse.numel() * 4, dtype=torch.uint8, device=dev)
+    h_res = torch.empty(d_res.shape, dtype=torch.uint8).pin_memory()
+    e_out = d_res[:o_bytes].view(torch.bfloat16).view(out.shape)
+    e_lse = d_res[o_bytes:].view(torch.float32).view(lse.shape)
+    h2d = h_in.numel() * h_in.element_size()
+    d2h = h_res.numel()
     KE = max(args.e2e_steps, 2)
+    last = int(inp["pos"][0])
+
+    def e2e_step():
+        d_in.copy_(h_in, non_blocking=True)
+        kc[:, last].copy_(d_in[1])
+        vc[:, last].copy_(d_in[2])
+        na.ne_attn_decode(d_in[0], kc, vc, pos, base, scale, out=e_out, lse=e_lse, workspace=ws,
+                          stream=stream)
+        h_res.copy_(d_res, non_blocking=True)
+
+    for _ in range(3):  # warm-up: the first pass pays one-time set-up (~0.6 s measured)
+        e2e_step()
+    torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    last = int(inp["pos"][0])
     for _ in range(KE):
-        q.copy_(h_q, non_blocking=True)
-        d_k.copy_(h_k, non_blocking=True)
-        d_v.copy_(h_v, non_blocking=True)
-        kc[:, last].copy_(d_k)
-        vc[:, last].copy_(d_v)
-        step()
-        h_out.copy_(out, non_blocking=True)
-        h_lse.copy_(lse, non_blocking=True)
+        e2e_step()
     t1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = t0.elapsed_time(t1) / KE
