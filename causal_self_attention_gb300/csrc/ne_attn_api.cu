@@ -47,6 +47,7 @@ cudaError_t launch_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, const 
 constexpr unsigned kDecodeBoxRows = 32;  // keys per pipeline stage of the decode kernel
 cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* g, __nv_bfloat16* xn,
                            float* rstd, int M, int C, float eps, cudaStream_t stream);
+int gemm_tile_n(int epi, long long M, int N, int G);
 cudaError_t launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmW,
                         const CUtensorMap& tmO0, const CUtensorMap& tmO1, const CUtensorMap& tmO2,
                         const gemm::Params& p, cudaStream_t stream);
@@ -976,14 +977,15 @@ ne_status ne_out_proj_residual(const ne_bf16* o, const ne_bf16* w_o, const ne_bf
   p.N = C;
   p.K = C;
   p.n_tiles_m = (N + 127) / 128;
-  p.n_tiles_n = C / 256;
+  p.tile_n = ne::gemm_tile_n(ne::gemm::kResidual, N, C, st->sm_count);
+  p.n_tiles_n = (C + p.tile_n - 1) / p.tile_n;
   p.C = C;
   p.T = 1;
   p.rope = RopeTable{nullptr, nullptr, 0};
   p.status = st->status;
   CUtensorMap ta, tw, ty, tr;
   if ((rc = encode_mat(&ta, o, N, C, 128)) != NE_OK) return rc;
-  if ((rc = encode_mat(&tw, w_o, C, C, 256)) != NE_OK) return rc;
+  if ((rc = encode_mat(&tw, w_o, C, C, p.tile_n)) != NE_OK) return rc;
   if ((rc = encode_mat(&ty, y, N, C, 128)) != NE_OK) return rc;
   if ((rc = encode_mat(&tr, residual, N, C, 128)) != NE_OK) return rc;
   return cuda_status(
@@ -1045,7 +1047,8 @@ ne_status ne_mtp_head(const ne_bf16* h, const ne_bf16* w, const int* targets, in
   p2.N = C;
   p2.K = N;
   p2.n_tiles_m = (M + 127) / 128;
-  p2.n_tiles_n = (C + 255) / 256;
+  p2.tile_n = ne::gemm_tile_n(ne::gemm::kScale, M, C, st->sm_count);
+  p2.n_tiles_n = (C + p2.tile_n - 1) / p2.tile_n;
   p2.acc = acc;
   p2.loss = loss;
   p2.status = st->status;

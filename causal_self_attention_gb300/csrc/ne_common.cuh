@@ -134,6 +134,7 @@ enum Epilogue { kQkvRope = 0, kResidual = 1, kMtpCe = 2, kScale = 3, kReduceF32 
 struct Params {
   int M = 0, N = 0, K = 0;
   int n_tiles_m = 0, n_tiles_n = 0;
+  int tile_n = 256;               // output tile width (256; 192 for kResidual / kScale)
   int k_splits = 1;               // K ranges per output tile (more than 1: kReduceF32 only)
   int chunks_per_split = 1 << 20;  // 64-wide K chunks per range
   int C = 0;  // kQkvRope: width of each of q, k, v (N = 3C)

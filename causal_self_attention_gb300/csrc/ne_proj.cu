@@ -9,10 +9,13 @@
 //
 // GEMM: Y[M, N] = A[M, K] . W[N, K]^T, bf16 operands, fp32 accumulation,
 // weights in the [out, in] layout.  Persistent CTAs (one per SM) walk the
-// 128 x 256 output tiles; per tile the K dimension streams through a 4-stage
-// TMA ring of 64-column chunks (A 128 x 64, W 256 x 64, 128-byte swizzled).
-// Two TMEM accumulators of 256 columns let the epilogue of one tile overlap
-// the MMAs of the next.
+// 128 x 256 output tiles (128 x 192 for the output projection and dh where
+// that makes fewer, fuller rounds of tiles: a 768-wide output in 256-wide
+// tiles over 8192 rows is 192 tiles for 152 SMs, the second round a quarter
+// full); per tile the K dimension streams through a 4-stage TMA ring of
+// 64-column chunks (A 128 x 64, W 256 x 64, 128-byte swizzled).  Two TMEM
+// accumulators of 256 (192) columns let the epilogue of one tile overlap the
+// MMAs of the next.
 //   warp 0      TMA: lane 0 loads the A and W chunks
 //   warp 1      MMA: allocates TMEM; its elected lane issues the tcgen05 MMAs
 //               (M 128, N 256, K 16)
@@ -52,18 +55,25 @@ namespace ne {
 namespace gemm {
 
 constexpr int kThreads = 192;
-constexpr int kTM = 128, kTN = 256, kBK = 64;
+constexpr int kTM = 128, kBK = 64;
 constexpr int kStages = 4;
 constexpr int kABytes = kTM * kBK * 2;        // 16 KiB
-constexpr int kWBytes = kTN * kBK * 2;        // 32 KiB
-constexpr int kStageBytes = kABytes + kWBytes;
 constexpr int kOutBlock = kTM * 64 * 2;       // one 128 x 64 bf16 output block: 16 KiB
-constexpr int OFF_STAGE = 0;
-constexpr int OFF_OUT = OFF_STAGE + kStages * kStageBytes;  // 2 staging buffers
-constexpr int OFF_BAR = OFF_OUT + 2 * kOutBlock;
 constexpr int kBarBytes = 256;
-constexpr int SMEM_BYTES = OFF_BAR + kBarBytes + 1024;  // + slack for 1024-byte alignment
-static_assert(SMEM_BYTES <= 232448, "more shared memory than an sm_103 CTA may have");
+constexpr int kMnBox = 64 * kBK * 2;          // one 64 x 64 box of an MN-major operand: 8 KiB
+// Output tiles 128 x kTN: kTN = 256, or 192 where a wave of 128 x 256 tiles
+// would leave most SMs idle in its last round (a 768-wide output).
+template <int kTN>
+struct Tile {
+  static_assert(kTN % 64 == 0 && kTN <= 256, "tile width");
+  static constexpr int kWBytes = kTN * kBK * 2;  // 32 / 24 KiB
+  static constexpr int kStageBytes = kABytes + kWBytes;
+  static constexpr int OFF_STAGE = 0;
+  static constexpr int OFF_OUT = OFF_STAGE + kStages * kStageBytes;  // 2 staging buffers
+  static constexpr int OFF_BAR = OFF_OUT + 2 * kOutBlock;
+  static constexpr int SMEM_BYTES = OFF_BAR + kBarBytes + 1024;  // + slack for alignment
+  static_assert(SMEM_BYTES <= 232448, "more shared memory than an sm_103 CTA may have");
+};
 
 enum Bar {
   B_FULL = 0,                  // kStages
@@ -79,6 +89,7 @@ static_assert(8 * B_COUNT + 8 <= kBarBytes, "barrier region overflow");
 
 // Entry `t` of the tile list: output tile m fastest (the CTAs working at the
 // same time share the weight tile), then n, then the K range.
+template <int kTN>
 __device__ __forceinline__ void tile_coords(const Params& p, int t, int& m0, int& n0, int& kc0,
                                             int& kc1) {
   const int n_mn = p.n_tiles_m * p.n_tiles_n;
@@ -92,7 +103,7 @@ __device__ __forceinline__ void tile_coords(const Params& p, int t, int& m0, int
 
 }  // namespace gemm
 
-template <int kEpi, bool kAMn, bool kBMn>
+template <int kEpi, bool kAMn, bool kBMn, int kTN>
 __global__ void __launch_bounds__(gemm::kThreads, 1)
     ne_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmW,
@@ -101,6 +112,10 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
                    const __grid_constant__ CUtensorMap tmO2,   // v
                    const gemm::Params p) {
   using namespace gemm;
+  constexpr int kWBytes = Tile<kTN>::kWBytes, kStageBytes = Tile<kTN>::kStageBytes;
+  constexpr int OFF_STAGE = Tile<kTN>::OFF_STAGE, OFF_OUT = Tile<kTN>::OFF_OUT,
+                OFF_BAR = Tile<kTN>::OFF_BAR;
+  constexpr int kNB = kTN / 64;  // 64-column output blocks per tile
   constexpr uint32_t kIdesc = make_idesc_bf16(kTM, kTN, kAMn, kBMn);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -147,7 +162,7 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
       bool ok = true;
       for (int t = cta; ok && t < n_tiles; t += G) {
         int m0, n0, kc0, kc1;
-        tile_coords(p, t, m0, n0, kc0, kc1);
+        tile_coords<kTN>(p, t, m0, n0, kc0, kc1);
         for (int kb = kc0; kb < kc1; ++kb, ++it) {
           const int s = it % kStages;
           if (it >= kStages &&
@@ -167,7 +182,7 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
           if constexpr (kBMn) {  // W^T chunk: rows kb*64.., columns n0.. of the [K, N] matrix
 #pragma unroll
             for (int i = 0; i < kTN / 64; ++i)
-              tma_load_2d(st + kABytes + i * (kWBytes / 4), &tmW, &bars[B_FULL + s], n0 + 64 * i,
+              tma_load_2d(st + kABytes + i * kMnBox, &tmW, &bars[B_FULL + s], n0 + 64 * i,
                           kb * kBK);
           } else {
             tma_load_2d(st + kABytes, &tmW, &bars[B_FULL + s], kb * kBK, n0);
@@ -190,14 +205,14 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
     // apart, 128-byte rows along K): a K16 step adds 16 rows = 2048 bytes.
     const uint64_t dA0 = make_sdesc_sw128(smem_u32(smem + OFF_STAGE), kAMn ? kABytes / 2 : 16, 1024);
     const uint64_t dW0 =
-        make_sdesc_sw128(smem_u32(smem + OFF_STAGE + kABytes), kBMn ? kWBytes / 4 : 16, 1024);
+        make_sdesc_sw128(smem_u32(smem + OFF_STAGE + kABytes), kBMn ? kMnBox : 16, 1024);
     constexpr uint64_t kStageD = kStageBytes >> 4;
     constexpr uint64_t kStepA = kAMn ? 128 : 2, kStepW = kBMn ? 128 : 2;
     int it = 0, lt = 0;
     bool ok = true;
     for (int t = cta; ok && t < n_tiles; t += G, ++lt) {
       int m0, n0, kc0, kc1;
-      tile_coords(p, t, m0, n0, kc0, kc1);
+      tile_coords<kTN>(p, t, m0, n0, kc0, kc1);
       const int acc = lt & 1;
       if (lt >= 2 &&
           !mbar_wait_warp(&bars[B_ACC_EMPTY + acc], ((lt - 2) >> 1) & 1, abort_flag, p.status, 61)) {
@@ -242,16 +257,16 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
       if (kEpi == kQkvRope || kEpi == kResidual) tma_prefetch_desc(&tmO1);
       if (kEpi == kQkvRope) tma_prefetch_desc(&tmO2);
     }
-    // Residual block b (over the CTA's tiles x 4 blocks) into staging buffer
+    // Residual block b (over the CTA's tiles x kNB blocks) into staging buffer
     // b & 1: issued by the leader one block ahead.
     auto issue_residual = [&](int b) {
-      const int t = cta + (b >> 2) * G;
+      const int t = cta + (b / kNB) * G;
       if (t >= n_tiles) return;
       int m0, n0, kc0, kc1;
-      tile_coords(p, t, m0, n0, kc0, kc1);
+      tile_coords<kTN>(p, t, m0, n0, kc0, kc1);
       mbar_arrive_expect_tx(&bars[B_RES_FULL + (b & 1)], kOutBlock);
       tma_load_2d(stage_out + (b & 1) * kOutBlock, &tmO1, &bars[B_RES_FULL + (b & 1)],
-                  n0 + (b & 3) * 64, m0);
+                  n0 + (b % kNB) * 64, m0);
     };
     if (kEpi == kResidual && leader) issue_residual(0);
     // kScale / kReduceF32: the products are the gradients of the mean
@@ -268,7 +283,7 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
     int lt = 0, gb = 0;  // tiles, 64-column blocks of this CTA
     for (int t = cta; ok && t < n_tiles; t += G, ++lt) {
       int m0, n0, kc0, kc1;
-      tile_coords(p, t, m0, n0, kc0, kc1);
+      tile_coords<kTN>(p, t, m0, n0, kc0, kc1);
       const int acc = lt & 1;
       bool wok = mbar_wait_warp(&bars[B_ACC_FULL + acc], (lt >> 1) & 1, abort_flag, p.status, 63);
       // The token's position (q, k rotation) and its table row, loaded once per tile.
@@ -512,23 +527,33 @@ cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* g, __nv_
 }
 
 namespace {
-template <int kEpi, bool kAMn, bool kBMn>
+template <int kEpi, bool kAMn, bool kBMn, int kTN = 256>
 cudaError_t launch_gemm_inst(const CUtensorMap& tmA, const CUtensorMap& tmW,
                              const CUtensorMap& tmO0, const CUtensorMap& tmO1,
                              const CUtensorMap& tmO2, const gemm::Params& p, int G,
                              cudaStream_t stream) {
+  constexpr int kSmem = gemm::Tile<kTN>::SMEM_BYTES;
   static bool attr_set = false;
   if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(ne_gemm_kernel<kEpi, kAMn, kBMn>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               gemm::SMEM_BYTES);
+    const cudaError_t e = cudaFuncSetAttribute(ne_gemm_kernel<kEpi, kAMn, kBMn, kTN>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_pdl(ne_gemm_kernel<kEpi, kAMn, kBMn>, dim3(G), dim3(gemm::kThreads),
-                    gemm::SMEM_BYTES, stream, tmA, tmW, tmO0, tmO1, tmO2, p);
+  return launch_pdl(ne_gemm_kernel<kEpi, kAMn, kBMn, kTN>, dim3(G), dim3(gemm::kThreads), kSmem,
+                    stream, tmA, tmW, tmO0, tmO1, tmO2, p);
 }
 }  // namespace
+
+// The output tile width for a product of M x N: 192 instead of 256 where it
+// takes fewer tile-widths of work on the busiest of G CTAs (rounds of G tiles
+// x tile width), for the epilogues built with both (kResidual, kScale).
+int gemm_tile_n(int epi, long long M, int N, int G) {
+  if ((epi != gemm::kResidual && epi != gemm::kScale) || G <= 0) return 256;
+  const long long mt = (M + gemm::kTM - 1) / gemm::kTM;
+  auto cost = [&](int tn) { return ((mt * ((N + tn - 1) / tn) + G - 1) / G) * tn; };
+  return cost(192) < cost(256) ? 192 : 256;
+}
 
 // epi: gemm::Epilogue.  kScale reads A K-major and W MN-major (dlogits . W);
 // kReduceF32 reads both MN-major (dlogits^T . h); the others both K-major.
@@ -549,10 +574,16 @@ cudaError_t launch_gemm(int epi, const CUtensorMap& tmA, const CUtensorMap& tmW,
     case gemm::kQkvRope:
       return launch_gemm_inst<gemm::kQkvRope, false, false>(tmA, tmW, tmO0, tmO1, tmO2, p, G, stream);
     case gemm::kResidual:
+      if (p.tile_n == 192)
+        return launch_gemm_inst<gemm::kResidual, false, false, 192>(tmA, tmW, tmO0, tmO1, tmO2, p,
+                                                                    G, stream);
       return launch_gemm_inst<gemm::kResidual, false, false>(tmA, tmW, tmO0, tmO1, tmO2, p, G, stream);
     case gemm::kMtpCe:
       return launch_gemm_inst<gemm::kMtpCe, false, false>(tmA, tmW, tmO0, tmO1, tmO2, p, G, stream);
     case gemm::kScale:
+      if (p.tile_n == 192)
+        return launch_gemm_inst<gemm::kScale, false, true, 192>(tmA, tmW, tmO0, tmO1, tmO2, p, G,
+                                                                stream);
       return launch_gemm_inst<gemm::kScale, false, true>(tmA, tmW, tmO0, tmO1, tmO2, p, G, stream);
     case gemm::kReduceF32:
       return launch_gemm_inst<gemm::kReduceF32, true, true>(tmA, tmW, tmO0, tmO1, tmO2, p, G, stream);
