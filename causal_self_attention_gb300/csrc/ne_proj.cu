@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(gemm::kThreads, 1)
                    const __grid_constant__ CUtensorMap tmO2,   // v
                    const gemm::Params p) {
   using namespace gemm;
-  constexpr int kWBytes = Tile<kTN>::kWBytes, kStageBytes = Tile<kTN>::kStageBytes;
+  constexpr int kStageBytes = Tile<kTN>::kStageBytes;
   constexpr int OFF_STAGE = Tile<kTN>::OFF_STAGE, OFF_OUT = Tile<kTN>::OFF_OUT,
                 OFF_BAR = Tile<kTN>::OFF_BAR;
   constexpr int kNB = kTN / 64;  // 64-column output blocks per tile
