@@ -725,7 +725,7 @@ def run_ours(args):
     per_kernel = {
         "ne_attn_rope_rows_kernel": statistics.mean(t_rot),
         "ne_attn_fwd_kernel": statistics.mean(t_fwd),
-        "ne_attn_bwd_preprocess_kernel": statistics.mean(t_pre),
+        "ne_attn_bwd_prep_stream_kernel": statistics.mean(t_pre),
         "ne_attn_bwd_kernel": statistics.mean(t_main),
         "ne_attn_dq_postprocess_kernel": statistics.mean(t_post),
     }
@@ -744,7 +744,7 @@ def run_ours(args):
     post_bytes = n_el * 4 + n_el * 2 + 2 * n_el * 2       # read dQ', write dQ; dK in place
     med = {"ne_attn_rope_rows_kernel": statistics.median(t_rot),
            "ne_attn_fwd_kernel": statistics.median(t_fwd),
-           "ne_attn_bwd_preprocess_kernel": statistics.median(t_pre),
+           "ne_attn_bwd_prep_stream_kernel": statistics.median(t_pre),
            "ne_attn_bwd_kernel": statistics.median(t_main),
            "ne_attn_dq_postprocess_kernel": statistics.median(t_post)}
     kernels = {
@@ -755,9 +755,9 @@ def run_ours(args):
                                "tflops": f_fwd / (per_kernel["ne_attn_fwd_kernel"] * 1e-3) / 1e12},
         "ne_attn_bwd_kernel": {"ms": per_kernel["ne_attn_bwd_kernel"],
                                "tflops": f_bwd / (per_kernel["ne_attn_bwd_kernel"] * 1e-3) / 1e12},
-        "ne_attn_bwd_preprocess_kernel": {
-            "ms": per_kernel["ne_attn_bwd_preprocess_kernel"],
-            "gbs": pre_bytes / (per_kernel["ne_attn_bwd_preprocess_kernel"] * 1e-3) / 1e9},
+        "ne_attn_bwd_prep_stream_kernel": {
+            "ms": per_kernel["ne_attn_bwd_prep_stream_kernel"],
+            "gbs": pre_bytes / (per_kernel["ne_attn_bwd_prep_stream_kernel"] * 1e-3) / 1e9},
         "ne_attn_dq_postprocess_kernel": {
             "ms": per_kernel["ne_attn_dq_postprocess_kernel"],
             "gbs": post_bytes / (per_kernel["ne_attn_dq_postprocess_kernel"] * 1e-3) / 1e9},

@@ -357,7 +357,9 @@ ne_status check_shape(const Shape& s) {
   if (rows > (1LL << 31) - 1 - 256) return NE_ERR_INVALID_ARG;
   if (static_cast<long long>(s.nseq) * s.H > (1LL << 31) - 1) return NE_ERR_INVALID_ARG;
   if ((s.max_len + 127) / 128 > 65535) return NE_ERR_INVALID_ARG;
-  if (static_cast<long long>(rows) * s.H * 64 > (1LL << 40)) return NE_ERR_INVALID_ARG;
+  // Every (row, head) pair index fits in 32 bits (each tensor then stays under
+  // 256 GB, more than the device holds).
+  if (static_cast<long long>(rows) * s.H > (1LL << 31) - 1) return NE_ERR_INVALID_ARG;
   return NE_OK;
 }
 

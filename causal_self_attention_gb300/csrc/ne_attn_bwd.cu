@@ -9,7 +9,9 @@
 //      workspace buffers with the forward's fp32 rule, so the main kernel
 //      multiplies exactly the operands the forward did and rotates nothing
 //      (a query tile is used by every key tile at or before it: rotating it
-//      there would repeat the work once per key tile);
+//      there would repeat the work once per key tile).  When the caller
+//      passes q', k' (the training pair) nothing is rotated, and a
+//      persistent form streams O and dO through shared memory instead;
 //   2. main: persistent, one CTA per SM; each walks its units (128-key tile
 //      j of one (sequence, head)) and, per unit, the query tiles i >= j,
 //      recomputing P from the saved LSE:
@@ -109,8 +111,9 @@ constexpr int kPreRows = 16;   // rows per CTA of the preprocess
 }  // namespace bwd
 
 // ---------------------------------------------------------------------------
-// 1. preprocess.  Grid (row blocks of kPreRows, sequences); 8 threads per
-//    (row, head) pair.  Thread `part` (0..7) of a pair:
+// 1. preprocess of the plain pair (q, k un-rotated).  Grid (row blocks of
+//    kPreRows, sequences); 8 threads per (row, head) pair.  Thread `part`
+//    (0..7) of a pair:
 //      - multiplies its 8 of the 64 products dO . O (summed over the 8
 //        threads by shuffles) -> D_m;
 //      - zeroes its 8 floats of the dQ' accumulator row;
@@ -125,8 +128,7 @@ __global__ void __launch_bounds__(256)
                                   const __nv_bfloat16* __restrict__ dout,
                                   __nv_bfloat16* __restrict__ qr, __nv_bfloat16* __restrict__ kr,
                                   float* __restrict__ delta, float* __restrict__ dq_acc,
-                                  const Problem pb, RopeTable rope, int rotate_in,
-                                  int* status) {
+                                  const Problem pb, RopeTable rope, int* status) {
   pdl_wait();  // the forward that wrote O (and anything before it) has completed
   const int seq = blockIdx.y;
   int start, len;
@@ -163,10 +165,8 @@ __global__ void __launch_bounds__(256)
       float4* z = reinterpret_cast<float4*>(dq_acc + pair * kHD) + part * 2;
       z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
       z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-      // RoPE of one chunk pair of q (parts 0-3) or k (parts 4-7); nothing to
-      // do when the caller passed q', k' already rotated.
+      // RoPE of one chunk pair of q (parts 0-3) or k (parts 4-7).
       const int c = part & 3;
-      if (rotate_in) {
       const __nv_bfloat16* src = (part < 4 ? q : k) + pair * kHD;
       __nv_bfloat16* dst = (part < 4 ? qr : kr) + pair * kHD;
       const uint4 lo = __ldg(reinterpret_cast<const uint4*>(src) + c);
@@ -188,12 +188,134 @@ __global__ void __launch_bounds__(256)
       }
       reinterpret_cast<uint4*>(dst)[c] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
       reinterpret_cast<uint4*>(dst)[c + 4] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-      }
     }
     acc += __shfl_xor_sync(0xffffffffu, acc, 1);
     acc += __shfl_xor_sync(0xffffffffu, acc, 2);
     acc += __shfl_xor_sync(0xffffffffu, acc, 4);
     if (valid && part == 0) delta[static_cast<long long>(h) * pb.n_tot + start + pos] = acc;
+  }
+  pdl_launch_dependents();
+}
+
+// ---------------------------------------------------------------------------
+// 1'. preprocess when q', k' are the caller's (nothing to rotate): a
+//     persistent stream over the (row, head) pairs of the packed tensors.
+//     Each CTA (kPrepCtasPerSm per SM) takes an even share of the pairs in
+//     chunks of at most kPrepPairs.  Thread 0 bulk-copies the O and dO rows
+//     of a chunk into one of kPrepStages shared-memory stages, kPrepStages
+//     chunks ahead; all threads zero the chunk's dQ' rows, then form D_m from
+//     the staged rows with 8 threads per pair and the partial sums and
+//     shuffle tree of the kernel above, so that D is bitwise the same.  Rows
+//     outside every sequence (a packed batch with gaps, or a sequence with
+//     bad bounds) get D and zeroed dQ' rows too; nothing reads them.
+// ---------------------------------------------------------------------------
+namespace bwd {
+constexpr int kPrepPairs = 128;  // pairs per chunk
+constexpr int kPrepStages = 2;
+constexpr int kPrepCtasPerSm = 3;
+constexpr int kPrepRowBytes = kHD * 2;                           // one bf16 row of O or dO
+constexpr int kPrepStageBytes = 2 * kPrepPairs * kPrepRowBytes;  // O rows, then dO rows
+constexpr int PREP_SMEM_BYTES = kPrepStages * kPrepStageBytes + kPrepStages * 8 + 16;
+}  // namespace bwd
+
+__global__ void __launch_bounds__(256, bwd::kPrepCtasPerSm)
+    ne_attn_bwd_prep_stream_kernel(const __nv_bfloat16* __restrict__ out,
+                                   const __nv_bfloat16* __restrict__ dout,
+                                   float* __restrict__ delta, float* __restrict__ dq_acc,
+                                   const Problem pb, int* status) {
+  using namespace bwd;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kPrepStages * kPrepStageBytes);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + kPrepStages);
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    for (int s = 0; s < kPrepStages; ++s) mbar_init(&full[s], 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  pdl_wait();  // the forward that wrote O (and anything before it) has completed
+  // Bad cu_seqlens entries are reported here; the main kernel and the
+  // postprocess skip those sequences.
+  if (pb.cu_seqlens && blockIdx.x == 0) {
+    for (int s = tid; s < pb.nseq; s += 256) {
+      int a, l;
+      seq_bounds(pb, s, a, l, status);
+    }
+  }
+  const int H = pb.H;
+  const long long n_pairs = static_cast<long long>(pb.n_tot) * H;
+  const long long p0 = n_pairs * blockIdx.x / gridDim.x;
+  const int mine = static_cast<int>(n_pairs * (blockIdx.x + 1) / gridDim.x - p0);
+  const int n_ch = (mine + kPrepPairs - 1) / kPrepPairs;
+  // Chunk j: pairs p0 + first(j) .. p0 + first(j + 1) - 1 (at most kPrepPairs),
+  // split as evenly as the count allows (32-bit arithmetic from here on: the
+  // pair p0 + t is row m0 + (h0 + t) / H, head (h0 + t) % H).
+  const int per = n_ch ? mine / n_ch : 0, extra = n_ch ? mine - per * n_ch : 0;
+  auto first = [&](int j) { return j * per + min(j, extra); };
+  const long long m0 = p0 / H;
+  const int h0 = static_cast<int>(p0 - m0 * H);
+  auto issue = [&](int j) {
+    const int s = j % kPrepStages;
+    const long long b = p0 + first(j);
+    const uint32_t bytes = static_cast<uint32_t>(first(j + 1) - first(j)) * kPrepRowBytes;
+    uint8_t* st = smem + s * kPrepStageBytes;
+    mbar_arrive_expect_tx(&full[s], 2u * bytes);
+    bulk_load(st, out + b * kHD, bytes, &full[s]);
+    bulk_load(st + kPrepPairs * kPrepRowBytes, dout + b * kHD, bytes, &full[s]);
+  };
+  int issued = 0;  // thread 0 only
+  if (tid == 0)
+    for (; issued < n_ch && issued < kPrepStages; ++issued) issue(issued);
+  int j = 0;
+  for (; j < n_ch; ++j) {
+    const int s = j % kPrepStages;
+    const int t0 = first(j);
+    const long long b = p0 + t0;
+    const int np = first(j + 1) - t0;
+    // The chunk's dQ' rows (np x 64 fp32), while its O and dO rows land.
+    uint4* z = reinterpret_cast<uint4*>(dq_acc + b * kHD);
+    for (int i = tid; i < np * (kHD / 4); i += 256) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    const bool ok = mbar_wait(&full[s], (j / kPrepStages) & 1, abort_flag, status, 45);
+    if (!__syncthreads_and(ok)) break;
+    const uint8_t* so = smem + s * kPrepStageBytes;
+    const uint8_t* sg = so + kPrepPairs * kPrepRowBytes;
+    const int items = np * 8;
+    const int items_all = (items + 255) & ~255;  // every thread runs every round (shuffles)
+    for (int w = tid; w < items_all; w += 256) {
+      const bool valid = w < items;
+      const int part = w & 7;
+      const int pr = valid ? (w >> 3) : 0;  // a lane past the end reads pair 0, discarded
+      const uint4 o = *reinterpret_cast<const uint4*>(so + pr * kPrepRowBytes + part * 16);
+      const uint4 g = *reinterpret_cast<const uint4*>(sg + pr * kPrepRowBytes + part * 16);
+      const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+      const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+      float acc = 0.f;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        acc = __fmaf_rn(bf16lo_to_f32(ow[u]), bf16lo_to_f32(gw[u]), acc);
+        acc = __fmaf_rn(bf16hi_to_f32(ow[u]), bf16hi_to_f32(gw[u]), acc);
+      }
+      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+      if (valid && part == 0) {
+        const int t = h0 + t0 + pr;
+        const int dm = t / H;
+        delta[static_cast<long long>(t - dm * H) * pb.n_tot + m0 + dm] = acc;
+      }
+    }
+    __syncthreads();  // stage s has been read: refill it
+    if (tid == 0 && issued < n_ch) issue(issued++);
+  }
+  if (tid == 0) {
+    // After an abort, the loads still in flight land before the CTA exits.
+    for (; j < issued; ++j) {
+      const long long t0 = clock64();
+      while (!mbar_try_wait(&full[j % kPrepStages], (j / kPrepStages) & 1) &&
+             clock64() - t0 < NE_WAIT_LIMIT_CYCLES) {
+      }
+    }
   }
   pdl_launch_dependents();
 }
@@ -837,8 +959,8 @@ __device__ __forceinline__ void dk_rotate_item(__nv_bfloat16* __restrict__ dk, c
   const long long w = static_cast<long long>(blockIdx.x) * kPostThreads + threadIdx.x;
   if (w >= static_cast<long long>(len) * H * kPostParts) return;
   const int part = static_cast<int>(w % kPostParts);
-  const long long rh = w / kPostParts;
-  const int pos = static_cast<int>(rh / H), h = static_cast<int>(rh - static_cast<long long>(pos) * H);
+  const int rh = static_cast<int>(w / kPostParts);  // (row, head) pairs fit in 32 bits
+  const int pos = rh / H, h = rh - pos * H;
   __nv_bfloat16* row = dk + (static_cast<long long>(start + pos) * H + h) * kHD;
   const uint2 lo = *reinterpret_cast<const uint2*>(row + part * 4);
   const uint2 hi = *reinterpret_cast<const uint2*>(row + 32 + part * 4);
@@ -877,8 +999,8 @@ __global__ void __launch_bounds__(kPostThreads)
   const long long w = static_cast<long long>(blockIdx.x) * kPostThreads + threadIdx.x;
   if (w >= static_cast<long long>(len) * H * kPostParts) return;
   const int part = static_cast<int>(w % kPostParts);
-  const long long rh = w / kPostParts;
-  const int pos = static_cast<int>(rh / H), h = static_cast<int>(rh - static_cast<long long>(pos) * H);
+  const int rh = static_cast<int>(w / kPostParts);  // (row, head) pairs fit in 32 bits
+  const int pos = rh / H, h = rh - pos * H;
   const long long row_off = (static_cast<long long>(start + pos) * H + h) * kHD;
   const float4 lo = *reinterpret_cast<const float4*>(dq_acc + row_off + part * 4);
   const float4 hi = *reinterpret_cast<const float4*>(dq_acc + row_off + 32 + part * 4);
@@ -919,6 +1041,10 @@ cudaError_t launch_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
     cudaError_t e = cudaFuncSetAttribute(ne_attn_bwd_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          bwd::SMEM_BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(ne_attn_bwd_prep_stream_kernel,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               bwd::PREP_SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -935,9 +1061,19 @@ cudaError_t launch_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
   const int G = static_cast<int>(n_units < sm_count[dev] ? n_units : sm_count[dev]);
   BwdParams pm = p;
   if (pm.sched && pm.sched_ctas != G) pm.sched = nullptr;  // made for another grid: snake order
-  dim3 pre_grid((n_tiles * kBM + bwd::kPreRows - 1) / bwd::kPreRows, p.pb.nseq);
-  e = launch_pdl(ne_attn_bwd_preprocess_kernel, pre_grid, dim3(256), 0, stream, p.q, p.k, p.out,
-                 p.dout, p.qr, p.kr, p.delta, p.dq_acc, p.pb, p.rope, p.rotate_in, p.status);
+  if (p.rotate_in) {
+    dim3 pre_grid((n_tiles * kBM + bwd::kPreRows - 1) / bwd::kPreRows, p.pb.nseq);
+    e = launch_pdl(ne_attn_bwd_preprocess_kernel, pre_grid, dim3(256), 0, stream, p.q, p.k,
+                   p.out, p.dout, p.qr, p.kr, p.delta, p.dq_acc, p.pb, p.rope, p.status);
+  } else {
+    // kPrepCtasPerSm CTAs per SM, each streaming an even share of the pairs.
+    const long long chunks = (static_cast<long long>(p.pb.n_tot) * p.pb.H + bwd::kPrepPairs - 1) /
+                             bwd::kPrepPairs;
+    const long long slots = static_cast<long long>(bwd::kPrepCtasPerSm) * sm_count[dev];
+    const int pg = static_cast<int>(chunks < slots ? (chunks > 0 ? chunks : 1) : slots);
+    e = launch_pdl(ne_attn_bwd_prep_stream_kernel, dim3(pg), dim3(256), bwd::PREP_SMEM_BYTES,
+                   stream, p.out, p.dout, p.delta, p.dq_acc, p.pb, p.status);
+  }
   if (e != cudaSuccess) return e;
   if (ev_pre && (e = cudaEventRecord(ev_pre, stream)) != cudaSuccess) return e;
   e = launch_pdl(ne_attn_bwd_kernel, dim3(G), dim3(bwd::kThreads), bwd::SMEM_BYTES, stream, tmQ,

@@ -677,8 +677,8 @@ __global__ void __launch_bounds__(kRopeThreads)
   const long long w = static_cast<long long>(blockIdx.x) * kRopeThreads + threadIdx.x;
   if (w < static_cast<long long>(len) * H * kRopeParts) {
     const int c = static_cast<int>(w % kRopeParts);
-    const long long rh = w / kRopeParts;
-    const int pos = static_cast<int>(rh / H), h = static_cast<int>(rh - static_cast<long long>(pos) * H);
+    const int rh = static_cast<int>(w / kRopeParts);  // (row, head) pairs fit in 32 bits
+    const int pos = rh / H, h = rh - pos * H;
     const long long row = (static_cast<long long>(start + pos) * H + h) * kHD;
     const uint4 lo = __ldg(reinterpret_cast<const uint4*>(x + row) + c);
     const uint4 hi = __ldg(reinterpret_cast<const uint4*>(x + row) + c + 4);

@@ -28,6 +28,10 @@
  *    pointers must be 16-byte aligned (NE_ERR_MISALIGNED).
  *  - lse is fp32 [B, H, T] (fixed length) or [H, N_tot] (varlen), 4-byte
  *    aligned.
+ *  - Sizes: fewer than 2^31 rows (B * T or N_tot) and fewer than 2^31
+ *    (row, head) pairs (rows * H: each tensor then stays under 256 GB), at
+ *    most 65535 key tiles of 128 rows per sequence; a larger problem is
+ *    refused with NE_ERR_INVALID_ARG.
  *  - Every pointer is DEVICE memory owned by the caller; the library keeps no
  *    reference to it after the call returns.  The library owns only its RoPE
  *    cos/sin tables, one temporary per stream for the forward's rotated keys

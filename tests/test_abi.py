@@ -67,6 +67,9 @@ def test_argument_errors_return_before_any_launch(lib):
     assert lib.ne_attn_fwd(fake, fake, fake, 1, 1, 64, 128, 10000.0, 0.125, fake, fake, None) == 2
     # non-positive size
     assert lib.ne_attn_fwd(fake, fake, fake, 0, 1, 64, 64, 10000.0, 0.125, fake, fake, None) == 1
+    # 2^31 (row, head) pairs: beyond the 32-bit pair indexes of the kernels
+    assert lib.ne_attn_fwd(fake, fake, fake, 1, 4096, 1 << 19, 64, 10000.0, 0.125, fake, fake,
+                           None) == 1
     # misaligned tensor pointer
     assert lib.ne_attn_fwd(P(0x10002), fake, fake, 1, 1, 64, 64, 10000.0, 0.125, fake, fake,
                            None) == 3

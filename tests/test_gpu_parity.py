@@ -219,7 +219,9 @@ def test_varlen_sequence_longer_than_max_is_reported():
     NE_ERR_BAD_SEQLEN, skip that sequence (it is never read past the limit)
     and compute the others exactly as a valid call does -- through the work
     lists compacted on the device, which keep the bad sequence's items so
-    that the kernels see and report it."""
+    that the kernels see and report it.  The training pair's backward (whose
+    preprocess streams every packed row without looking at the sequences)
+    reports and skips it the same way."""
     from causal_self_attention_gb300 import ne_attn as na
     inp = make_custom(0, 0, 2, seed=77, lengths=[100, 300, 50])
     q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "dout"))
@@ -234,6 +236,13 @@ def test_varlen_sequence_longer_than_max_is_reported():
     keep = torch.cat([torch.arange(0, 100), torch.arange(400, 450)]).cuda()
     assert torch.equal(o[keep], o_ref[keep])
     assert torch.equal(lse[:, keep], lse_ref[:, keep])
+    assert torch.equal(dk[keep], dk_ref[keep]) and torch.equal(dv[keep], dv_ref[keep])
+    assert torch.allclose(dq[keep].float(), dq_ref[keep].float(), atol=1e-2, rtol=0)
+    assert na.ne_attn_get_device_status() == 0
+    _, _, qr, kr = na.ne_attn_varlen_fwd_train(q, k, v, cu, 300)
+    assert na.ne_attn_get_device_status() == 0
+    dq, dk, dv = na.ne_attn_varlen_bwd_train(qr, kr, v, o_ref, do, lse_ref, cu, 200)
+    assert na.ne_attn_get_device_status() == 7
     assert torch.equal(dk[keep], dk_ref[keep]) and torch.equal(dv[keep], dv_ref[keep])
     assert torch.allclose(dq[keep].float(), dq_ref[keep].float(), atol=1e-2, rtol=0)
     assert na.ne_attn_get_device_status() == 0
