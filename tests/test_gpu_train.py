@@ -7,7 +7,7 @@ ne_attn_fwd; the backward from q', k' returns the gradients w.r.t. the
 un-rotated q, k that ne_attn_bwd returns (dk, dv bitwise; dq to the order of
 its fp32 accumulation, relative L2 <= 1e-3, as between two calls of
 ne_attn_bwd) and meets the oracle's bar (relative L2 <= 2e-2).  Shapes: a
-ragged short case, a case from 2048 positions on (where ne_attn_fwd itself
+single row, short ragged sequences (T 63, 129, 300), a case from 2048 positions on (where ne_attn_fwd itself
 rotates the keys in a separate pass), the GPT-2-small training shape, and a
 packed variable-length batch.
 """
@@ -55,9 +55,14 @@ def _same_gradients(got, ref):
     return err
 
 
-@pytest.mark.parametrize("case", ["ragged", "long", "gpt2s"])
+@pytest.mark.parametrize("case", ["one_row", "t63", "t129", "ragged", "long", "gpt2s"])
 def test_training_pair_matches_the_plain_pair(na, case):
-    inp = {"ragged": lambda: make_custom(2, 300, 3, seed=91),
+    # one_row .. t129: fewer (row, head) pairs than the streamed preprocess
+    # has CTAs, chunks of a few pairs, and a last query tile of one row.
+    inp = {"one_row": lambda: make_custom(1, 1, 1, seed=88),
+           "t63": lambda: make_custom(3, 63, 5, seed=89),
+           "t129": lambda: make_custom(1, 129, 2, seed=90),
+           "ragged": lambda: make_custom(2, 300, 3, seed=91),
            "long": lambda: make_custom(1, 2300, 2, seed=92),
            "gpt2s": lambda: make_inputs("gpt2s")}[case]()
     q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "dout"))
