@@ -176,12 +176,19 @@ RopeTable table_view(float2* dev, int cap) {
 // cs[p * 32 + i] = ((float)cos(p * theta_i), (float)sin(p * theta_i)),
 // theta_i = base^(-(2i)/64), all in double before the final fp32 rounding;
 // followed by the same values in the warp-interleaved layout of RopeTable::csw.
-ne_status rope_table(DeviceState& st, float base, int positions, RopeTable* out) {
+ne_status rope_table(DeviceState& st, float base, int positions, cudaStream_t stream,
+                     RopeTable* out) {
   for (auto& e : st.tables)
     if (e.base == base && e.capacity >= positions) {
       *out = table_view(e.dev, e.capacity);
       return NE_OK;
     }
+  // A new table is built with a synchronous allocation and copy, which a
+  // stream capture does not allow: the first call for a base (or for more
+  // positions) must run outside the capture.
+  cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &capture) != cudaSuccess) return NE_ERR_CUDA;
+  if (capture != cudaStreamCaptureStatusNone) return NE_ERR_UNSUPPORTED;
   int cap = 4096;
   while (cap < positions) cap *= 2;
   std::vector<float2> host(static_cast<size_t>(cap) * 64);
@@ -422,7 +429,8 @@ ne_status run_fwd(const Shape& s, const void* q, const void* k, const void* v, f
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = st->status;
   p.rope = RopeTable{nullptr, nullptr, 0};
-  if (!pre_rotated && (rc = rope_table(*st, rope_base, n_qtiles * 128, &p.rope)) != NE_OK)
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (!pre_rotated && (rc = rope_table(*st, rope_base, n_qtiles * 128, cs, &p.rope)) != NE_OK)
     return rc;
   // Keys: for short sequences each item rotates the key tiles it uses in
   // shared memory; from kPreRotateLen positions on, the rotated keys
@@ -430,7 +438,6 @@ ne_status run_fwd(const Shape& s, const void* q, const void* k, const void* v, f
   // temporary for this stream, or, while the stream is being captured into a
   // graph, into a stream-ordered allocation of the call's own (a graph must
   // not bake in a buffer that later calls outside it would also use).
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
   p.rotate_k = (mode == Rot::kRotate && s.max_len < kPreRotateLen) ? 1 : 0;
   p.rotate_q = mode == Rot::kRotate ? 1 : 0;
   CUtensorMap tq, tk, tv, to;
@@ -536,7 +543,7 @@ ne_status run_bwd(const Shape& s, const void* q, const void* k, const void* v, c
   p.rotate_in = mode == Rot::kRotate ? 1 : 0;
   p.rotate_out = pre_rotated ? 0 : 1;
   p.rope = RopeTable{nullptr, nullptr, 0};
-  if (!pre_rotated && (rc = rope_table(*st, rope_base, n_tiles * 128, &p.rope)) != NE_OK)
+  if (!pre_rotated && (rc = rope_table(*st, rope_base, n_tiles * 128, cs, &p.rope)) != NE_OK)
     return rc;
   if ((rc = work_schedule(*st, s.fixed, s.nseq, s.H, s.max_len, cs, &p.sched, &p.sched_ctas)) !=
       NE_OK)
@@ -873,7 +880,9 @@ ne_status run_decode(const ne_bf16* q, const ne_bf16* k_cache, const ne_bf16* v_
   RopeTable rope{};
   CUtensorMap tt{};  // the RoPE table, 32-row boxes of half rows (unused without rotation)
   if (rot) {
-    if ((rc = rope_table(*st, rope_base, Tmax, &rope)) != NE_OK) return rc;
+    if ((rc = rope_table(*st, rope_base, Tmax, static_cast<cudaStream_t>(stream), &rope)) !=
+        NE_OK)
+      return rc;
     if ((rc = encode_table(&tt, rope.cs, rope.capacity, ne::kDecodeBoxRows)) != NE_OK) return rc;
   }
   CUtensorMap tk, tv;  // the caches as [B * Tmax, H, 64], 32-row boxes
@@ -945,7 +954,9 @@ ne_status ne_rmsnorm_qkv_rope(const ne_bf16* x, const ne_bf16* g, const ne_bf16*
   p.C = static_cast<int>(C);
   p.T = T;
   p.status = st->status;
-  if ((rc = rope_table(*st, rope_base, T, &p.rope)) != NE_OK) return rc;
+  if ((rc = rope_table(*st, rope_base, T, static_cast<cudaStream_t>(stream), &p.rope)) !=
+      NE_OK)
+    return rc;
   CUtensorMap ta, tw, tq, tk, tv;
   if ((rc = encode_mat(&ta, x_norm, M, p.K, 128)) != NE_OK) return rc;
   if ((rc = encode_mat(&tw, w_qkv, p.N, p.K, 256)) != NE_OK) return rc;
@@ -1205,7 +1216,9 @@ ne_status ne_debug_rope_tile(const ne_bf16* src, int n_rows, int H, int h, int r
   if (rc != NE_OK) return rc;
   if ((rc = get_encoder()) != NE_OK) return rc;
   RopeTable rt;
-  if ((rc = rope_table(*st, rope_base, pos0 + 128, &rt)) != NE_OK) return rc;
+  if ((rc = rope_table(*st, rope_base, pos0 + 128, static_cast<cudaStream_t>(stream), &rt)) !=
+      NE_OK)
+    return rc;
   CUtensorMap tm;
   if ((rc = encode_rows(&tm, src, n_rows, H)) != NE_OK) return rc;
   return cuda_status(ne::launch_debug_tile(tm, h, row0, 1, pos0, rt, nullptr,

@@ -44,6 +44,12 @@
  *    stream-ordered temporary it frees itself.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
  *    enqueued asynchronously on it; the call returns after the launch.
+ *  - Calls may be captured into a CUDA graph once a call with the same
+ *    rope_base and at least as many positions has run outside a capture:
+ *    that first call builds the RoPE table with a synchronous copy, which a
+ *    capture does not allow (inside one it returns NE_ERR_UNSUPPORTED and
+ *    enqueues nothing).  Workspaces, temporaries and work lists that a
+ *    captured call needs are allocated stream-ordered inside the graph.
  *  - Argument errors are detected on the host before anything is launched
  *    and return a nonzero ne_status.  Errors found on the device (a varlen
  *    sequence longer than max_seqlen, a pipeline wait that timed out) are
