@@ -107,6 +107,12 @@ extern "C" ne_status ne_attn_bwd_noalloc(const ne_bf16* q, const ne_bf16* k, con
     nd.scratch = static_cast<unsigned char*>(ptr);
   }
   if (nd.table_base != rope_base) {
+    // A copy captured into a graph would read the host image at replay time,
+    // when later calls may have rebuilt it for another base: refused.
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &capture) != cudaSuccess)
+      return NE_ERR_CUDA;
+    if (capture != cudaStreamCaptureStatusNone) return NE_ERR_UNSUPPORTED;
     nd.table_base = 0.f;
     if ((rc = upload_table(nd.scratch, rope_base, static_cast<cudaStream_t>(stream))) != NE_OK)
       return rc;

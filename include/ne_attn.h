@@ -230,7 +230,10 @@ ne_status ne_attn_set_fwd_phase_event(void* ev_after_rotation);
  * the previous call's, writes the RoPE table for that base into the array with
  * a copy from host memory enqueued on `stream`: it runs after the earlier work
  * of that stream (whose kernels may still read the old table) and before this
- * call's kernels.  Make the first call before any stream capture.  Every call
+ * call's kernels.  Make the first call, and any call with a new rope_base,
+ * outside a stream capture: inside one such a call returns NE_ERR_UNSUPPORTED
+ * and enqueues nothing (a captured copy would read the host image when the
+ * graph is replayed, after later calls may have rebuilt it).  Every call
  * shares the one array and leaves the last call's contents in it (the parts
  * that must start from zero are cleared on every call), so calls whose work
  * overlaps on the GPU -- on different streams, or on different host threads --

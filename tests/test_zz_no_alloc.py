@@ -9,8 +9,9 @@ results through that array are those of the ordinary backward (dK and dV
 bitwise, dQ up to the order of its fp32 additions) on calls in a row, so that
 what one call leaves in the shared array cannot leak into the next; that they
 meet the oracle's bar on their own; that a new RoPE base rewrites the table in
-stream order, behind earlier work on the caller's stream; and that problems
-larger than the array are refused on the host.
+stream order, behind earlier work on the caller's stream, and is refused inside
+a stream capture; and that problems larger than the array are refused on the
+host.
 
 This file is collected last on purpose: a run that stops at the first failure
 has then already run every other test.
@@ -123,3 +124,32 @@ def test_noalloc_table_rewrite_is_ordered_on_the_callers_stream():
         _compare(got, ref, f"base {b}")
     # The two bases give different gradients: the table really changed.
     assert not torch.equal(outs[0][1], outs[1][1])
+
+
+@pytest.mark.gpu
+def test_noalloc_base_change_inside_a_capture_is_refused():
+    """A new RoPE base inside a stream capture would capture a copy of a host
+    image that later calls rebuild: refused with NE_ERR_UNSUPPORTED, nothing
+    enqueued; a call at the base already in the table is captured and replays
+    to the eager results."""
+    na = _na()
+    inp = make_custom(1, 200, 2, seed=92)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "dout"))
+    o, lse = na.ne_attn_fwd(q, k, v, rope_base=10000.0)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    na.ne_attn_bwd_noalloc(q, k, v, o, do, lse, rope_base=10000.0, dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    ref = [t.clone() for t in (dq, dk, dv)]
+    for t in (dq, dk, dv):
+        t.zero_()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        with pytest.raises(RuntimeError, match="UNSUPPORTED"):
+            na.ne_attn_bwd_noalloc(q, k, v, o, do, lse, rope_base=20000.0, dq=dq, dk=dk, dv=dv)
+        na.ne_attn_bwd_noalloc(q, k, v, o, do, lse, rope_base=10000.0, dq=dq, dk=dk, dv=dv)
+    g.replay()
+    torch.cuda.synchronize()
+    assert na.ne_attn_get_device_status() == 0
+    _compare((dq, dk, dv), ref, "captured at base 10000")
