@@ -102,7 +102,17 @@ def check_full(inp, gpu, bwd=True):
     if bwd:
         ref0 = oracle.attention(q, k, v, do, cu, base=base, scale=scale, mode=0)
         for name in ("dq", "dk", "dv"):
-            errs[name + "_rel_l2"] = rel_l2(gpu[name].double().numpy(), ref0[name])
+            got = gpu[name].double().numpy()
+            if np.linalg.norm(ref0[name]) == 0.0:
+                # Every sequence has one row: its only softmax weight is 1, so
+                # O = V and D = dO . O equals dP exactly, and dS, hence dQ and
+                # dK, are exactly zero.  The kernels form dP - D from two fp32
+                # sums of the same 64 exact products, in different orders: the
+                # rounding residue is measured against the scale of dV.
+                errs[name + "_rel_l2"] = float(np.linalg.norm(got) /
+                                               max(np.linalg.norm(ref0["dv"]), 1e-300))
+            else:
+                errs[name + "_rel_l2"] = rel_l2(got, ref0[name])
         for name in ("dq", "dk", "dv"):
             assert errs[name + "_rel_l2"] <= GRAD_TOL, errs
     return errs

@@ -34,8 +34,8 @@ def test_tiny_config_full():
     _report("tiny", check_full(inp, run_gpu(inp)))
 
 
-@pytest.mark.parametrize("B,T,H", [(1, 1, 1), (1, 63, 2), (2, 65, 1), (1, 129, 3), (3, 200, 2),
-                                   (1, 384, 1)])
+@pytest.mark.parametrize("B,T,H", [(1, 1, 1), (2, 1, 3), (1, 63, 2), (2, 65, 1), (1, 129, 3),
+                                   (3, 200, 2), (1, 384, 1)])
 def test_edge_shapes_full(B, T, H):
     inp = make_custom(B, T, H, seed=100 + T)
     _report(f"B{B} T{T} H{H}", check_full(inp, run_gpu(inp)))
