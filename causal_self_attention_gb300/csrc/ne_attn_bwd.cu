@@ -234,6 +234,17 @@ __global__ void __launch_bounds__(256, bwd::kPrepCtasPerSm)
     mbar_fence_init();
   }
   __syncthreads();
+  // This CTA's share of dO into L2 while the forward finishes (dO is an input
+  // of the call, which the forward does not write; a prefetch is only a hint).
+  if (tid == 0) {
+    const long long all = static_cast<long long>(pb.n_tot) * pb.H;
+    const long long a = all * blockIdx.x / gridDim.x, e = all * (blockIdx.x + 1) / gridDim.x;
+    if (e > a)
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                       reinterpret_cast<uint64_t>(dout + a * kHD)),
+                   "r"(static_cast<uint32_t>((e - a) * kPrepRowBytes))
+                   : "memory");
+  }
   pdl_wait();  // the forward that wrote O (and anything before it) has completed
   // Bad cu_seqlens entries are reported here; the main kernel and the
   // postprocess skip those sequences.
